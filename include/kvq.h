@@ -1,0 +1,235 @@
+/*
+ * kvq.h -- C ABI of libkvq: a paged KV cache held in dynamic low-bit form on
+ * one GB300 (sm_103a), with the write path that fills it and the decode and
+ * chunked-prefill attention that read it.
+ *
+ * Sources the operations follow (web pages, cited by title and section):
+ *   [vLLM-INT4]  vLLM PR #40835 review summary, "INT4 per-token-head KV cache
+ *                for the Triton backend": sections 功能与动机 (motivation: RHT
+ *                plus asymmetric scale/zero point), 实现拆解 (implementation
+ *                breakdown, items 2-4), 关键源码片段 (key source snippets:
+ *                INT4_CONFIG range [-8, 7]; get_kv_cache_shape row size
+ *                head_size//2 + scale_pad, scale_pad = 4), 风险与影响 (causal only).
+ *   [FD-INT2]    FastDeploy PR #5173 "[Feature] support dynamic int2
+ *                quantization cache kv": Motivation, Modifications, Usage.
+ *   [FD-HEADWISE] FastDeploy PR #7718 "Optimize AppendAttention for discrete
+ *                head-wise block_idx": Motivation (block_tables_headwise
+ *                layout), Modifications "PR2-only delta" table (-1 sentinel,
+ *                sink_size), Correctness gates.
+ *   [ASCEND-INT8] vllm-ascend-quantized-kv-cache 0.2.0rc2 METADATA, "Ascend
+ *                INT8 KV Cache Plugin", section 运行机制 (dynamic symmetric
+ *                per-channel INT8, scales taken along tokens on the first K/V
+ *                a layer receives; prefill gathers and dequantises pages).
+ *   [FD-UINT8]   FastDeploy PR #7757 "fix cache_manager_v1 allocating kv cache
+ *                with wrong dtype when kv_cache_quant_type is set", section 修复
+ *                (every quantised cache is stored as 1-byte uint8).
+ *
+ * Conventions shared by every call
+ *   - Every pointer is a DEVICE pointer on the current CUDA device unless the
+ *     comment says "host".  The library allocates nothing and keeps no state
+ *     besides a per-device cache of the SM count.
+ *   - Calls enqueue work on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream) and never synchronise.  Outputs are valid
+ *     once the stream reaches the work.
+ *   - Host-detectable errors (NULL pointers, unsupported shapes, misaligned
+ *     pointers, a too-small workspace, Hq % Hkv != 0) return a status before
+ *     any launch and leave all device memory untouched.  A failed launch
+ *     returns KVQ_ERR_CUDA; kvq_last_error() then holds the CUDA message.
+ *   - Device-detectable contract violations (a block id >= num_blocks, a
+ *     position beyond the table row, more new tokens than seq_len) OR a bit
+ *     into *dev_error (KVQ_DEVERR_* below, nullable), and the offending row
+ *     is skipped: it is never read nor written.  Read *dev_error after the
+ *     stream synchronises.
+ *   - Inputs must be finite; NaN or Inf inputs give unspecified codes.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_ABI_VERSION 1
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, both/neither table, Hq % Hkv != 0 */
+  KVQ_ERR_UNSUPPORTED = 2, /* head_dim, block_size, mode, dtype or GQA group not built */
+  KVQ_ERR_CUDA = 3,        /* a kernel launch failed; see kvq_last_error() */
+  KVQ_ERR_WORKSPACE = 4    /* decode workspace NULL or smaller than required */
+} kvq_status;
+
+/* Quantisation modes.
+ * INT4 / INT2: per (token, kv_head) row: optional RHT, then asymmetric codes
+ *   u in [0, 2^b - 1] with an fp16 scale s and fp16 zero point m (the value of
+ *   code 0); the signed view q = u - 2^(b-1) covers [-8, 7] for INT4
+ *   ([vLLM-INT4] 关键源码片段, INT4_CONFIG) and [-2, 1] for INT2 ([FD-INT2]).
+ * INT8: dynamic symmetric per-channel codes in [-127, 127] with one fp32
+ *   scale per (K|V, kv_head, channel) ([ASCEND-INT8] 运行机制); no RHT. */
+typedef enum {
+  KVQ_INT4_TOKEN_HEAD = 0,
+  KVQ_INT2_TOKEN_HEAD = 1,
+  KVQ_INT8_CHANNEL = 2
+} kvq_mode;
+
+/* Element type of q / k / v inputs. */
+typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
+
+/* Bits OR-ed into *dev_error by the kernels. */
+#define KVQ_DEVERR_BLOCK_RANGE 1 /* table entry >= num_blocks: row skipped */
+#define KVQ_DEVERR_TABLE_RANGE 2 /* position / block_size >= max_blocks: row skipped */
+#define KVQ_DEVERR_SEQ_LEN 4     /* negative seq_len, or more new tokens than seq_len */
+
+/* One layer's paged cache (caller-allocated; store it as torch.uint8, cf.
+ * [FD-UINT8] 修复).
+ *
+ * Page layout ([vLLM-INT4] 关键源码片段 get_kv_cache_shape gives the row;
+ * K and V are kept in separate pools so that one (block, kv_head) page is
+ * contiguous):
+ *     k_pages, v_pages : uint8 [num_blocks][num_kv_heads][block_size][row_bytes]
+ *     row_bytes        : kvq_row_bytes(mode, head_dim)
+ *       INT4: head_dim/2 data bytes (element 2i in the low nibble of byte i),
+ *             then 4 pad bytes = fp16 scale s, fp16 zero point m (little endian)
+ *       INT2: head_dim/4 data bytes (element 4i+j in bits 2j..2j+1 of byte i),
+ *             then the same 4 pad bytes
+ *       INT8: head_dim bytes of two's-complement codes (no pad)
+ *   Both pools must be 16-byte aligned.
+ *
+ * rht_signs: int8 [head_dim] of +1/-1 (device).  Non-NULL turns the random
+ *   Hadamard transform on for INT4/INT2: y = H (signs * x), H the unnormalised
+ *   Sylvester Walsh-Hadamard matrix ([vLLM-INT4] 功能与动机, 实现拆解 2).  One
+ *   vector per layer, shared by K, V and every head.  Must be NULL for INT8.
+ *
+ * ch_amax / ch_amax_ready (INT8 only, else NULL):
+ *   ch_amax: fp32 [2][num_kv_heads][head_dim] (index 0 = K, 1 = V).  The scale
+ *   of a channel is ch_amax / 127 (IEEE fp32 division).  While
+ *   *ch_amax_ready == 0 the buffer must hold zeros: the next kvq_write takes
+ *   the per-channel max |x| over ALL tokens it is given (also tokens whose page
+ *   is -1), stores it here and sets *ch_amax_ready = 1 ([ASCEND-INT8] 运行机制:
+ *   scales come from the first K/V a layer receives).  Later writes reuse it
+ *   and saturate at +-127. */
+typedef struct {
+  uint8_t* k_pages;
+  uint8_t* v_pages;
+  int32_t num_blocks;
+  int32_t num_kv_heads;
+  int32_t block_size; /* 16, 32 or 64 */
+  int32_t head_dim;   /* 64 or 128 */
+  int32_t mode;       /* kvq_mode */
+  const int8_t* rht_signs;
+  float* ch_amax;
+  int32_t* ch_amax_ready;
+} kvq_cache;
+
+/* Paging state of one step.
+ * Exactly one of the two tables is non-NULL ([FD-HEADWISE] Motivation):
+ *   block_tables          int32 [batch][max_blocks]: row b serves every head
+ *   block_tables_headwise int32 [batch * num_kv_heads][max_blocks]: row
+ *                         b * num_kv_heads + h serves kv head h
+ *   Token position p of a row lives in page table[row][p / block_size], slot
+ *   p % block_size.  An entry < 0 (-1 sentinel) marks an evicted block: it is
+ *   never dereferenced, writes to it are dropped and its keys contribute
+ *   nothing ([FD-HEADWISE] PR2-only delta, Correctness gates).
+ * seq_lens int32 [batch]: tokens in the cache for each sequence AFTER this
+ *   step's write.  Decode queries sit at position seq_lens[b] - 1.
+ * window_per_kv_head int32 [num_kv_heads] or NULL (= all heads full):
+ *   0 = full attention; W > 0 = sliding window: a query at p sees key j iff
+ *   j <= p and (j < sink_size or j > p - W) ([FD-HEADWISE] sink_size).
+ */
+typedef struct {
+  const int32_t* block_tables;
+  const int32_t* block_tables_headwise;
+  int32_t max_blocks;
+  int32_t batch;
+  const int32_t* seq_lens;
+  const int32_t* window_per_kv_head;
+  int32_t sink_size;
+} kvq_paging;
+
+/* Bytes of one cache row for (mode, head_dim); 0 if unsupported. */
+int32_t kvq_row_bytes(int32_t mode, int32_t head_dim);
+
+/* kvq_write -- quantise new K/V tokens and scatter them into the pages.
+ * ([vLLM-INT4] 实现拆解 2 and 4: rotate, per-token-head scale and zero point,
+ * pack, scatter through the block table; [FD-INT2] Modifications: cache-write
+ * kernels for the 2-bit cache; [ASCEND-INT8] 运行机制 for INT8.)
+ *
+ * k, v          : [num_tokens][num_kv_heads][head_dim] of `dtype` (row-major,
+ *                 16-byte aligned).
+ * cu_new_tokens : int32 [batch + 1], cu[0] = 0, non-decreasing, cu[batch] =
+ *                 num_tokens.  Sequence b owns tokens cu[b] .. cu[b+1]-1, at
+ *                 positions seq_lens[b] - n_b .. seq_lens[b] - 1 (n_b = its count).
+ * Per row the codes are bit-exactly defined: fp32 sign flip and butterfly in
+ * stage order 1, 2, 4, ..., head_dim/2; min/max canonicalised with +0.0f;
+ * s = (max - min) / (2^b - 1) (IEEE); s, m rounded to fp16 (round to nearest
+ * even, saturating at +-65504); u = clamp(rne((y - m) / s), 0, 2^b - 1), u = 0
+ * when the fp16 scale is 0.  INT8: q = clamp(rne(x / (amax / 127)), -127, 127),
+ * 0 when the scale is 0.
+ * num_tokens == 0 is a no-op returning KVQ_OK. */
+kvq_status kvq_write(const kvq_cache* cache, const kvq_paging* paging,
+                     const void* k, const void* v, int32_t dtype,
+                     const int32_t* cu_new_tokens, int32_t num_tokens,
+                     int32_t* dev_error, void* stream);
+
+/* Workspace needed by kvq_decode_attn for `num_splits` (0 = the library's
+ * choice).  Writes the byte count to *bytes (host) and the split count that
+ * kvq_decode_attn will use to *splits_used (host, nullable). */
+kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_paging* paging,
+                                     int32_t num_q_heads, int32_t num_splits,
+                                     size_t* bytes, int32_t* splits_used);
+
+/* kvq_decode_attn -- one decode query per sequence over the paged cache.
+ * ([vLLM-INT4] 实现拆解 2: unpack, dequantise, attention; [FD-HEADWISE]
+ * per-head row walk with -1 sentinel; [ASCEND-INT8] 运行机制: decode
+ * dequantises inside the attention kernel.)
+ *
+ * q   : [batch][num_q_heads][head_dim] of `dtype`; q head hq reads kv head
+ *       hq / (num_q_heads / num_kv_heads).  GQA group size 1..8.
+ * out : fp32 [batch][num_q_heads][head_dim] = sum_j P_j v_j with
+ *       P = softmax_j(softmax_scale * q . k_j) over the visible keys, where k_j
+ *       and v_j are the dequantised rows mapped back through the inverse RHT.
+ *       A query with no visible key gets zeros.
+ * workspace : device scratch of >= kvq_decode_workspace_size() bytes, 256-byte
+ *       aligned, owned by the caller; its contents on entry do not matter.
+ * The work is split along the keys (split-KV); a second kernel merges the
+ * splits and applies the inverse RHT. */
+kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging,
+                           const void* q, int32_t dtype, int32_t num_q_heads,
+                           float softmax_scale, float* out,
+                           void* workspace, size_t workspace_bytes, int32_t num_splits,
+                           int32_t* dev_error, void* stream);
+
+/* kvq_prefill_attn -- causal chunked-prefill attention of a chunk of queries
+ * against everything in the cache, the chunk itself included (write the chunk
+ * with kvq_write first).  ([FD-INT2] Usage: chunked prefill; [vLLM-INT4]
+ * 风险与影响: causal attention only; [ASCEND-INT8] 运行机制: chunked prefill
+ * reads the paged cache.)
+ *
+ * q    : [total_q][num_q_heads][head_dim] of `dtype`.
+ * cu_q : int32 [batch + 1]; sequence b's queries are rows cu_q[b] .. cu_q[b+1]-1
+ *        at positions seq_lens[b] - n_b + i.
+ * max_q_per_seq : host upper bound on n_b (sizes the grid).
+ * out  : fp32 [total_q][num_q_heads][head_dim]. */
+kvq_status kvq_prefill_attn(const kvq_cache* cache, const kvq_paging* paging,
+                            const void* q, int32_t dtype, int32_t num_q_heads,
+                            const int32_t* cu_q, int32_t total_q, int32_t max_q_per_seq,
+                            float softmax_scale, float* out,
+                            int32_t* dev_error, void* stream);
+
+/* Human-readable name of a status. */
+const char* kvq_status_string(int32_t status);
+
+/* Message of the last KVQ_ERR_* returned on this host thread ("" if none). */
+const char* kvq_last_error(void);
+
+/* KVQ_ABI_VERSION of the loaded library. */
+int32_t kvq_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

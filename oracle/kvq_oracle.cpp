@@ -1,0 +1,529 @@
+// kvq_oracle.cpp -- plain, slow CPU oracle of the paged low-bit KV cache.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing in the library (sub_byte_quantized_write_gb300/)
+// includes, links or calls this file; only tests/, the smoke check and the
+// bench's CPU-baseline leg load it.  It shares no header, helper, table or
+// constant with the CUDA path: every step is written out here from the pages.
+//
+// What it computes (sources by page title and section):
+//   * Write, INT4 / INT2 per (token, kv_head) row -- vLLM PR #40835 review
+//     summary ("INT4 per-token-head KV cache for the Triton backend"),
+//     功能与动机 and 实现拆解 item 2: rotate with a random Hadamard transform,
+//     then an asymmetric scale and zero point per token-head, round, pack two
+//     4-bit codes per byte; 关键源码片段 INT4_CONFIG: signed range [-8, 7];
+//     get_kv_cache_shape: row = head_size/2 data bytes + 4 pad bytes.
+//     FastDeploy PR #5173 "support dynamic int2 quantization cache kv",
+//     Motivation / Modifications: the same dynamic scheme at 2 bits.
+//   * Write, INT8 per channel -- vllm-ascend-quantized-kv-cache METADATA
+//     ("Ascend INT8 KV Cache Plugin"), 运行机制: symmetric per-channel scales
+//     taken along the token axis on the first K/V a layer receives, separately
+//     for K and V.
+//   * Paging -- FastDeploy PR #7718 "Optimize AppendAttention for discrete
+//     head-wise block_idx", Motivation: uniform [batch, block] table or
+//     head-wise [batch * kv_heads, block] table; PR2-only delta table and
+//     Correctness gates: a -1 entry is an evicted sliding-window block whose
+//     keys contribute nothing and whose page is never addressed; sink_size.
+//   * Attention -- the textbook definition: softmax(scale * q . k_j) weights
+//     over the visible dequantised keys, output sum_j P_j v_j, in double.
+//
+// Readings taken where the pages are silent:
+//   RHT unnormalised forward y = H (d * x), inverse x = d * (H y) / D; butterfly
+//   stage order h = 1, 2, ..., D/2 in fp32; the zero point m is the value of
+//   code 0 (the row minimum); fp16 round-to-nearest-even saturating at 65504;
+//   codes by round-half-to-even; element 2i in the low nibble; element 4i+j in
+//   bits 2j; pad = fp16 s then fp16 m; INT8 range [-127, 127] with scale
+//   amax / 127; a query at p sees key j iff j <= p and (no window, or j < sink,
+//   or j > p - W) and its block entry is a valid id.
+//
+// Built with -O2 -ffp-contract=off -fno-fast-math so that the fp32 write path
+// is evaluated exactly in the order written.
+
+#include <algorithm>
+#include <atomic>
+#include <cfenv>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2 };
+enum { DT_F32 = 0, DT_BF16 = 1 };
+enum { ERR_BLOCK_RANGE = 1, ERR_TABLE_RANGE = 2, ERR_SEQ_LEN = 4 };
+
+// ---------------------------------------------------------------------------
+// IEEE-754 binary16 conversions, from the format's definition:
+// 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent 0 encodes
+// subnormals (fraction * 2^-24), exponent 31 encodes Inf/NaN.
+
+uint16_t f16_encode_exact(double v /* >= 0, exactly representable in binary16 */) {
+  if (v == 0.0) return 0;
+  if (v < std::ldexp(1.0, -14)) {  // subnormal: v = frac * 2^-24
+    return (uint16_t)(v / std::ldexp(1.0, -24));
+  }
+  int e2;
+  double fr = std::frexp(v, &e2);  // v = fr * 2^e2, fr in [0.5, 1)
+  int e = e2 - 1;                  // v = (2 fr) * 2^e, 2 fr in [1, 2)
+  if (e > 15) return 0x7C00;       // infinity
+  double frac = (2.0 * fr - 1.0) * 1024.0;  // exact integer 0..1023
+  return (uint16_t)(((e + 15) << 10) | (int)frac);
+}
+
+// Round a float to binary16, nearest representable value, ties to even;
+// magnitudes at or beyond 65520 (half an ulp above the largest finite 65504)
+// become infinity, as IEEE rounding prescribes.
+uint16_t f16_round_nearest_even(float x) {
+  uint32_t bits;
+  std::memcpy(&bits, &x, 4);
+  uint16_t sign = (uint16_t)((bits >> 31) << 15);
+  if (std::isnan(x)) return (uint16_t)(sign | 0x7E00);
+  double a = std::fabs((double)x);
+  if (std::isinf(x)) return (uint16_t)(sign | 0x7C00);
+  // spacing of binary16 values around a: 2^(e-10) in binade [2^e, 2^(e+1)),
+  // e >= -14; subnormal spacing 2^-24 below 2^-14.
+  double ulp;
+  if (a < std::ldexp(1.0, -14)) {
+    ulp = std::ldexp(1.0, -24);
+  } else {
+    int e2;
+    std::frexp(a, &e2);
+    ulp = std::ldexp(1.0, (e2 - 1) - 10);
+  }
+  double q = a / ulp;                 // exact: ulp is a power of two
+  double r = std::nearbyint(q);       // ties to even (default rounding mode)
+  double v = r * ulp;
+  if (v >= 65520.0) return (uint16_t)(sign | 0x7C00);
+  return (uint16_t)(sign | f16_encode_exact(v));
+}
+
+float f16_decode(uint16_t h) {
+  int s = h >> 15, e = (h >> 10) & 31, f = h & 1023;
+  double v;
+  if (e == 0) v = std::ldexp((double)f, -24);
+  else if (e == 31) v = f ? NAN : INFINITY;
+  else v = std::ldexp(1.0 + f / 1024.0, e - 15);
+  return (float)(s ? -v : v);
+}
+
+// Saturating variant used for the stored scale and zero point: values beyond
+// the largest finite binary16 are clamped to +-65504 before rounding.
+uint16_t f16_saturate(float x) {
+  if (x > 65504.0f) x = 65504.0f;
+  if (x < -65504.0f) x = -65504.0f;
+  return f16_round_nearest_even(x);
+}
+
+float widen(const void* base, int dtype, size_t idx) {
+  if (dtype == DT_F32) return ((const float*)base)[idx];
+  uint16_t b = ((const uint16_t*)base)[idx];
+  uint32_t u = (uint32_t)b << 16;  // bf16 -> fp32 is exact: append 16 zero bits
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+int code_bits(int mode) { return mode == MODE_INT4 ? 4 : (mode == MODE_INT2 ? 2 : 8); }
+
+int row_bytes(int mode, int D) {
+  if (D != 64 && D != 128) return 0;
+  if (mode == MODE_INT4) return D / 2 + 4;  // nibbles + fp16 s + fp16 m
+  if (mode == MODE_INT2) return D / 4 + 4;  // crumbs + fp16 s + fp16 m
+  if (mode == MODE_INT8) return D;
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Random Hadamard transform (forward), fp32, fixed order: sign flip, then the
+// Walsh-Hadamard butterfly with stride h = 1, 2, 4, ..., D/2; each pair
+// (j, j+h) with (j & h) == 0 becomes (x_j + x_{j+h}, x_j - x_{j+h}).
+void rht_forward_f32(float* x, int D, const int8_t* signs) {
+  if (signs) {
+    for (int i = 0; i < D; ++i)
+      if (signs[i] < 0) x[i] = -x[i];
+  }
+  for (int h = 1; h < D; h <<= 1) {
+    for (int j = 0; j < D; ++j) {
+      if (j & h) continue;
+      float a = x[j], b = x[j + h];
+      x[j] = a + b;
+      x[j + h] = a - b;
+    }
+  }
+}
+
+// Unnormalised Walsh-Hadamard product in double (used for the inverse).
+void wht_double(double* x, int D) {
+  for (int h = 1; h < D; h <<= 1)
+    for (int j = 0; j < D; ++j) {
+      if (j & h) continue;
+      double a = x[j], b = x[j + h];
+      x[j] = a + b;
+      x[j + h] = a - b;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Code packing.  INT4: byte i = u[2i] | u[2i+1] << 4.  INT2: byte i =
+// sum_j u[4i+j] << 2j.  INT8: byte i = two's complement of the signed code.
+void pack_codes(int mode, const uint8_t* u, int D, uint8_t* out) {
+  if (mode == MODE_INT4) {
+    for (int i = 0; i < D / 2; ++i) out[i] = (uint8_t)((u[2 * i] & 15) | ((u[2 * i + 1] & 15) << 4));
+  } else if (mode == MODE_INT2) {
+    for (int i = 0; i < D / 4; ++i) {
+      int b = 0;
+      for (int j = 0; j < 4; ++j) b |= (u[4 * i + j] & 3) << (2 * j);
+      out[i] = (uint8_t)b;
+    }
+  } else {
+    for (int i = 0; i < D; ++i) out[i] = u[i];
+  }
+}
+
+void unpack_codes(int mode, const uint8_t* bytes, int D, uint8_t* u) {
+  if (mode == MODE_INT4) {
+    for (int i = 0; i < D / 2; ++i) {
+      u[2 * i] = bytes[i] & 15;
+      u[2 * i + 1] = bytes[i] >> 4;
+    }
+  } else if (mode == MODE_INT2) {
+    for (int i = 0; i < D / 4; ++i)
+      for (int j = 0; j < 4; ++j) u[4 * i + j] = (bytes[i] >> (2 * j)) & 3;
+  } else {
+    for (int i = 0; i < D; ++i) u[i] = bytes[i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One INT4 / INT2 row: RHT (optional), per-row asymmetric scale and zero point,
+// codes, packing, pad = [fp16 s | fp16 m].
+void quant_row_token_head(int mode, const float* xin, int D, const int8_t* signs, uint8_t* row) {
+  std::vector<float> x(xin, xin + D);
+  if (signs) rht_forward_f32(x.data(), D, signs);  // NULL signs: RHT off
+  float mn = x[0], mx = x[0];
+  for (int i = 1; i < D; ++i) {
+    if (x[i] < mn) mn = x[i];
+    if (x[i] > mx) mx = x[i];
+  }
+  mn = mn + 0.0f;  // -0 -> +0, so the result does not depend on min order
+  mx = mx + 0.0f;
+  const int levels = (1 << code_bits(mode)) - 1;
+  float s = (mx - mn) / (float)levels;
+  uint16_t s_h = f16_saturate(s);
+  uint16_t m_h = f16_saturate(mn);
+  float S = f16_decode(s_h), M = f16_decode(m_h);
+  std::vector<uint8_t> u(D);
+  for (int i = 0; i < D; ++i) {
+    if (S == 0.0f) {
+      u[i] = 0;
+      continue;
+    }
+    float t = (x[i] - M) / S;
+    float r = std::nearbyint(t);  // round half to even
+    if (r < 0.0f) r = 0.0f;
+    if (r > (float)levels) r = (float)levels;
+    u[i] = (uint8_t)r;
+  }
+  const int data = D * code_bits(mode) / 8;
+  pack_codes(mode, u.data(), D, row);
+  row[data + 0] = (uint8_t)(s_h & 0xFF);
+  row[data + 1] = (uint8_t)(s_h >> 8);
+  row[data + 2] = (uint8_t)(m_h & 0xFF);
+  row[data + 3] = (uint8_t)(m_h >> 8);
+}
+
+void quant_row_int8(const float* x, int D, const float* amax, uint8_t* row) {
+  for (int c = 0; c < D; ++c) {
+    float s = amax[c] / 127.0f;
+    int q = 0;
+    if (s != 0.0f) {
+      float r = std::nearbyint(x[c] / s);
+      if (r < -127.0f) r = -127.0f;
+      if (r > 127.0f) r = 127.0f;
+      q = (int)r;
+    }
+    row[c] = (uint8_t)(int8_t)q;
+  }
+}
+
+// Dequantised row mapped back to the input domain, in double.
+void dequant_row(int mode, const uint8_t* row, int D, const int8_t* signs, const float* amax,
+                 double* out) {
+  std::vector<uint8_t> u(D);
+  unpack_codes(mode, row, D, u.data());
+  if (mode == MODE_INT8) {
+    for (int c = 0; c < D; ++c) {
+      float s = amax[c] / 127.0f;
+      out[c] = (double)(int8_t)u[c] * (double)s;
+    }
+    return;
+  }
+  const int data = D * code_bits(mode) / 8;
+  uint16_t s_h = (uint16_t)(row[data] | (row[data + 1] << 8));
+  uint16_t m_h = (uint16_t)(row[data + 2] | (row[data + 3] << 8));
+  double S = f16_decode(s_h), M = f16_decode(m_h);
+  for (int i = 0; i < D; ++i) out[i] = (double)u[i] * S + M;
+  if (signs) {  // inverse RHT: d * (H y) / D
+    wht_double(out, D);
+    for (int i = 0; i < D; ++i) out[i] = out[i] * (double)signs[i] / (double)D;
+  }
+}
+
+}  // namespace
+
+// ===========================================================================
+// exported C entry points (ctypes)
+
+extern "C" {
+
+struct OrcCache {
+  uint8_t* k_pages;
+  uint8_t* v_pages;
+  int32_t num_blocks, num_kv_heads, block_size, head_dim, mode;
+  const int8_t* signs;
+  float* ch_amax;   // [2][Hkv][D]
+  int32_t* ch_ready;
+};
+
+struct OrcPaging {
+  const int32_t* table;  // [rows][max_blocks]
+  int32_t headwise;
+  int32_t max_blocks;
+  int32_t batch;
+  const int32_t* seq_lens;
+  const int32_t* window;  // [Hkv] or NULL
+  int32_t sink;
+};
+
+int32_t orc_row_bytes(int32_t mode, int32_t D) { return row_bytes(mode, D); }
+uint16_t orc_f16_round(float x) { return f16_round_nearest_even(x); }
+uint16_t orc_f16_saturate(float x) { return f16_saturate(x); }
+float orc_f16_decode(uint16_t h) { return f16_decode(h); }
+void orc_rht_forward(float* x, int32_t D, const int8_t* signs) { rht_forward_f32(x, D, signs); }
+void orc_pack_codes(int32_t mode, const uint8_t* u, int32_t D, uint8_t* out) { pack_codes(mode, u, D, out); }
+void orc_unpack_codes(int32_t mode, const uint8_t* b, int32_t D, uint8_t* u) { unpack_codes(mode, b, D, u); }
+int32_t orc_signed_code(int32_t mode, int32_t u) {
+  // INT4 / INT2 offset encoding: stored u in [0, 2^b - 1] is q = u - 2^(b-1).
+  return u - (1 << (code_bits(mode) - 1));
+}
+void orc_quant_row(int32_t mode, const float* x, int32_t D, const int8_t* signs, uint8_t* row) {
+  quant_row_token_head(mode, x, D, signs, row);
+}
+void orc_dequant_row(int32_t mode, const uint8_t* row, int32_t D, const int8_t* signs,
+                     const float* amax, double* out) {
+  dequant_row(mode, row, D, signs, amax, out);
+}
+
+static int32_t table_row(const OrcPaging* pg, int b, int h, int Hkv) {
+  return pg->headwise ? b * Hkv + h : b;
+}
+
+// Quantise `num_tokens` new tokens of K and V and scatter them.  Returns the
+// OR of ERR_* bits for rows it had to skip.
+int32_t orc_write(const OrcCache* c, const OrcPaging* pg, const void* k, const void* v, int32_t dtype,
+                  const int32_t* cu_new, int32_t num_tokens) {
+  const int D = c->head_dim, Hkv = c->num_kv_heads, bs = c->block_size, mode = c->mode;
+  const int R = row_bytes(mode, D);
+  int32_t err = 0;
+  if (num_tokens <= 0) return 0;
+  if (mode == MODE_INT8 && *c->ch_ready == 0) {
+    // First K/V of the layer: channel amax over every token given.
+    for (int kv = 0; kv < 2; ++kv) {
+      const void* src = kv ? v : k;
+      for (int h = 0; h < Hkv; ++h)
+        for (int ch = 0; ch < D; ++ch) {
+          float a = 0.0f;
+          for (int t = 0; t < num_tokens; ++t) {
+            float x = std::fabs(widen(src, dtype, ((size_t)t * Hkv + h) * D + ch));
+            if (x > a) a = x;
+          }
+          c->ch_amax[((size_t)kv * Hkv + h) * D + ch] = a;
+        }
+    }
+    *c->ch_ready = 1;
+  }
+  std::vector<float> x(D);
+  for (int b = 0; b < pg->batch; ++b) {
+    const int n = cu_new[b + 1] - cu_new[b];
+    const int L = pg->seq_lens[b];
+    if (n == 0) continue;
+    if (L < 0 || n > L) {
+      err |= ERR_SEQ_LEN;
+      continue;
+    }
+    for (int i = 0; i < n; ++i) {
+      const int t = cu_new[b] + i;
+      const int p = L - n + i;
+      for (int h = 0; h < Hkv; ++h) {
+        const int row = table_row(pg, b, h, Hkv);
+        const int lb = p / bs;
+        if (lb >= pg->max_blocks) {
+          err |= ERR_TABLE_RANGE;
+          continue;
+        }
+        const int blk = pg->table[(size_t)row * pg->max_blocks + lb];
+        if (blk < 0) continue;  // evicted: nothing is written
+        if (blk >= c->num_blocks) {
+          err |= ERR_BLOCK_RANGE;
+          continue;
+        }
+        for (int kv = 0; kv < 2; ++kv) {
+          const void* src = kv ? v : k;
+          for (int d = 0; d < D; ++d) x[d] = widen(src, dtype, ((size_t)t * Hkv + h) * D + d);
+          uint8_t* pages = kv ? c->v_pages : c->k_pages;
+          uint8_t* dst = pages + (((size_t)blk * Hkv + h) * bs + (p % bs)) * R;
+          if (mode == MODE_INT8)
+            quant_row_int8(x.data(), D, c->ch_amax + ((size_t)kv * Hkv + h) * D, dst);
+          else
+            quant_row_token_head(mode, x.data(), D, c->signs, dst);
+        }
+      }
+    }
+  }
+  return err;
+}
+
+// Attention for selected query rows.  Decode (cu_q == NULL): row i is
+// sequence i's query at seq_lens[i] - 1.  Prefill: row i in [cu_q[b],
+// cu_q[b+1]) is at seq_lens[b] - n_b + (i - cu_q[b]).  `rows` lists the query
+// rows to compute (NULL = all total_q); out is double [n_rows][Hq][D].
+int32_t orc_attention(const OrcCache* c, const OrcPaging* pg, const void* q, int32_t dtype, int32_t Hq,
+                      const int32_t* cu_q, int32_t total_q, float scale, const int32_t* rows,
+                      int32_t n_rows, double* out, int32_t threads) {
+  const int D = c->head_dim, Hkv = c->num_kv_heads, bs = c->block_size, mode = c->mode;
+  const int R = row_bytes(mode, D);
+  if (Hq % Hkv) return -1;
+  const int g = Hq / Hkv;
+  std::vector<int32_t> sel;
+  if (rows) sel.assign(rows, rows + n_rows);
+  else {
+    for (int i = 0; i < total_q; ++i) sel.push_back(i);
+    n_rows = total_q;
+  }
+  // sequence and position of every selected row
+  std::vector<int32_t> seq(n_rows), pos(n_rows);
+  int32_t err = 0;
+  for (int r = 0; r < n_rows; ++r) {
+    const int i = sel[r];
+    int b = 0, p = 0;
+    if (!cu_q) {
+      b = i;
+      p = pg->seq_lens[b] - 1;
+    } else {
+      while (b + 1 <= pg->batch && cu_q[b + 1] <= i) ++b;
+      const int n = cu_q[b + 1] - cu_q[b];
+      p = pg->seq_lens[b] - n + (i - cu_q[b]);
+    }
+    seq[r] = b;
+    pos[r] = p;
+  }
+  // Phase 1: dequantise the keys each needed (sequence, kv head) can see.
+  struct Deq {
+    int b = -1, h = -1, n = 0;
+    std::vector<double> K, V;
+    std::vector<char> ok;
+  };
+  std::vector<Deq> deq((size_t)pg->batch * Hkv);
+  std::vector<int> need((size_t)pg->batch * Hkv, -1);  // max position needed
+  for (int r = 0; r < n_rows; ++r)
+    for (int h = 0; h < Hkv; ++h) {
+      int& m = need[(size_t)seq[r] * Hkv + h];
+      if (pos[r] > m) m = pos[r];
+    }
+  std::vector<int> items;
+  for (size_t it = 0; it < need.size(); ++it)
+    if (need[it] >= 0) items.push_back((int)it);
+  if (threads < 1) threads = 1;
+  std::atomic<int> next(0);
+  std::atomic<int32_t> aerr(0);
+  auto deq_worker = [&]() {
+    for (;;) {
+      int w = next.fetch_add(1);
+      if (w >= (int)items.size()) break;
+      const int it = items[w];
+      const int b = it / Hkv, h = it % Hkv;
+      Deq& dq = deq[it];
+      dq.b = b;
+      dq.h = h;
+      dq.n = std::min(need[it] + 1, pg->seq_lens[b]);
+      if (dq.n < 0) dq.n = 0;
+      dq.K.assign((size_t)dq.n * D, 0.0);
+      dq.V.assign((size_t)dq.n * D, 0.0);
+      dq.ok.assign(dq.n, 0);
+      const int row = table_row(pg, b, h, Hkv);
+      for (int j = 0; j < dq.n; ++j) {
+        const int lb = j / bs;
+        if (lb >= pg->max_blocks) {
+          aerr |= ERR_TABLE_RANGE;
+          continue;
+        }
+        const int blk = pg->table[(size_t)row * pg->max_blocks + lb];
+        if (blk < 0) continue;  // evicted: never addressed
+        if (blk >= c->num_blocks) {
+          aerr |= ERR_BLOCK_RANGE;
+          continue;
+        }
+        const size_t off = (((size_t)blk * Hkv + h) * bs + (j % bs)) * R;
+        dequant_row(mode, c->k_pages + off, D, c->signs,
+                    c->ch_amax ? c->ch_amax + ((size_t)0 * Hkv + h) * D : nullptr,
+                    &dq.K[(size_t)j * D]);
+        dequant_row(mode, c->v_pages + off, D, c->signs,
+                    c->ch_amax ? c->ch_amax + ((size_t)1 * Hkv + h) * D : nullptr,
+                    &dq.V[(size_t)j * D]);
+        dq.ok[j] = 1;
+      }
+    }
+  };
+  {
+    std::vector<std::thread> pool;
+    for (int t = 0; t < threads; ++t) pool.emplace_back(deq_worker);
+    for (auto& th : pool) th.join();
+  }
+  // Phase 2: softmax attention per (row, q head), in double.
+  next = 0;
+  const int n_items = n_rows * Hq;
+  auto attn_worker = [&]() {
+    std::vector<double> z, qd(D);
+    for (;;) {
+      int w = next.fetch_add(1);
+      if (w >= n_items) break;
+      const int r = w / Hq, hq = w % Hq, h = hq / g;
+      const int b = seq[r], p = pos[r];
+      const Deq& dq = deq[(size_t)b * Hkv + h];
+      double* o = out + ((size_t)r * Hq + hq) * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      for (int d = 0; d < D; ++d) qd[d] = (double)widen(q, dtype, ((size_t)sel[r] * Hq + hq) * D + d);
+      const int W = pg->window ? pg->window[h] : 0;
+      z.assign(dq.n, -INFINITY);
+      double zmax = -INFINITY;
+      for (int j = 0; j < dq.n && j <= p; ++j) {
+        if (!dq.ok[j]) continue;
+        if (W > 0 && !(j < pg->sink || j > p - W)) continue;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += qd[d] * dq.K[(size_t)j * D + d];
+        z[j] = (double)scale * dot;
+        if (z[j] > zmax) zmax = z[j];
+      }
+      if (zmax == -INFINITY) continue;  // no visible key: output 0
+      double l = 0.0;
+      for (int j = 0; j < dq.n && j <= p; ++j) {
+        if (z[j] == -INFINITY) continue;
+        const double e = std::exp(z[j] - zmax);
+        l += e;
+        for (int d = 0; d < D; ++d) o[d] += e * dq.V[(size_t)j * D + d];
+      }
+      for (int d = 0; d < D; ++d) o[d] /= l;
+    }
+  };
+  {
+    std::vector<std::thread> pool;
+    for (int t = 0; t < threads; ++t) pool.emplace_back(attn_worker);
+    for (auto& th : pool) th.join();
+  }
+  return err | aerr.load();
+}
+
+int32_t orc_rounding_mode_is_nearest(void) { return std::fegetround() == FE_TONEAREST; }
+
+}  // extern "C"

@@ -1,0 +1,447 @@
+"""Pins of the CPU oracle to facts fixed outside itself.
+
+Each test checks the oracle against something it does not share code with:
+values the pages print (tests/golden/page_constants.txt), closed forms
+(Sylvester's Hadamard matrix, worked grid rows), a library routine (numpy's
+IEEE binary16 conversion), or brute force (numpy softmax attention on inputs
+whose quantisation is exact).  A plausible slip in the oracle -- a dropped
+sign flip, a wrong butterfly stride, a swapped nibble, a scale off by one
+level, a window off by one, a sentinel that leaks -- fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import kvq_inputs as gen
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+INT4, INT2, INT8 = oracle.MODE_INT4, oracle.MODE_INT2, oracle.MODE_INT8
+
+
+def page_constants():
+    out = {}
+    with open(os.path.join(GOLDEN, "page_constants.txt")) as f:
+        for line in f:
+            line = line.split("|")[0].strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = [s.strip() for s in line.split("=")]
+            out[k] = float(v)
+    return out
+
+
+def sylvester(n):
+    i = np.arange(n)
+    pc = np.vectorize(lambda a: bin(a).count("1"))(i[:, None] & i[None, :])
+    return np.where(pc % 2 == 0, 1, -1).astype(np.int64)
+
+
+def f16_of_pad(row, data_bytes):
+    s = np.frombuffer(row[data_bytes:data_bytes + 2].tobytes(), dtype=np.float16)[0]
+    m = np.frombuffer(row[data_bytes + 2:data_bytes + 4].tobytes(), dtype=np.float16)[0]
+    return float(s), float(m)
+
+
+def test_rounding_mode_nearest():
+    assert oracle.lib().orc_rounding_mode_is_nearest() == 1
+
+
+# --------------------------------------------------------------------------
+# constants printed on the pages
+
+def test_page_constants_ranges_and_rows():
+    c = page_constants()
+    # offset encoding: stored nibble u -> signed q = u - 8 spans the page's range
+    assert oracle.signed_code(INT4, 0) == c["int4_quant_min"]
+    assert oracle.signed_code(INT4, 15) == c["int4_quant_max"]
+    assert [oracle.signed_code(INT2, u) for u in range(4)] == [-2, -1, 0, 1]
+    assert oracle.row_bytes(INT4, 128) == c["int4_row_bytes_head_dim_128"]
+    assert oracle.row_bytes(INT4, 64) == c["int4_row_bytes_head_dim_64"]
+    assert oracle.row_bytes(INT4, 128) == 128 * c["int4_data_bytes_per_head_dim"] + c["scale_pad_bytes"]
+    # INT2 packs twice as densely with the same pad; INT8 is one byte per element
+    assert oracle.row_bytes(INT2, 128) == 128 // 4 + c["scale_pad_bytes"]
+    assert oracle.row_bytes(INT8, 128) == 128 * c["storage_bytes_per_element_of_cache"]
+    assert oracle.row_bytes(INT4, 96) == 0  # unsupported head_dim
+
+
+# --------------------------------------------------------------------------
+# IEEE binary16 against numpy's conversion (a library routine)
+
+def test_f16_decode_all_patterns_match_numpy():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = pats.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f16_decode(int(p)) for p in pats[::7]], dtype=np.float32)
+    r = ref[::7]
+    fin = np.isfinite(r)
+    assert np.array_equal(got[fin], r[fin])
+    assert np.array_equal(np.isinf(got), np.isinf(r))
+
+
+def test_f16_round_matches_numpy_incl_ties_and_subnormals():
+    rng = np.random.default_rng(1)
+    vals = [0.0, -0.0, 1.0, 65504.0, 65519.99, 65520.0, 1e-8, 2.0 ** -24, 2.0 ** -25,
+            3 * 2.0 ** -26, 2.0 ** -14, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11,
+            1024.5, 1025.5, 2049.0, 2051.0, -7.00048828125]
+    vals += list(rng.standard_normal(3000) * 10.0 ** rng.uniform(-9, 5, 3000))
+    for x in vals:
+        xf = np.float32(x)
+        with np.errstate(over="ignore"):
+            want = np.array([xf]).astype(np.float16).view(np.uint16)[0]
+        assert oracle.f16_round(float(xf)) == int(want), x
+
+
+def test_f16_saturate():
+    assert oracle.f16_saturate(1e9) == 0x7BFF
+    assert oracle.f16_saturate(-1e9) == 0xFBFF
+    assert oracle.f16_saturate(65519.0) == 0x7BFF
+    assert oracle.f16_saturate(1.5) == 0x3E00
+
+
+# --------------------------------------------------------------------------
+# RHT: Sylvester closed form, orthogonality, exact inversion
+
+@pytest.mark.parametrize("D", [2, 8, 64, 128])
+def test_rht_equals_sylvester_closed_form(D):
+    rng = np.random.default_rng(D)
+    x = rng.integers(-50, 51, size=D).astype(np.float32)
+    signs = np.where(rng.integers(0, 2, size=D) == 1, 1, -1).astype(np.int8)
+    H = sylvester(D)
+    want = H @ (signs.astype(np.int64) * x.astype(np.int64))  # exact integers
+    got = oracle.rht_forward(x, signs)
+    assert np.array_equal(got.astype(np.int64), want)
+    assert np.array_equal(oracle.rht_forward(x, None).astype(np.int64), H @ x.astype(np.int64))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_rht_orthogonality_and_exact_inverse(D):
+    H = sylvester(D)
+    assert np.array_equal(H @ H.T, D * np.eye(D, dtype=np.int64))
+    rng = np.random.default_rng(7)
+    x = rng.integers(-100, 101, size=D).astype(np.float32)
+    twice = oracle.rht_forward(oracle.rht_forward(x, None), None)
+    assert np.array_equal(twice, D * x)
+
+
+# --------------------------------------------------------------------------
+# packing
+
+def test_pack_round_trip_all_bytes():
+    for mode, D in ((INT4, 64), (INT2, 128)):
+        n = D // 2 if mode == INT4 else D // 4
+        for b in range(256):
+            data = np.full(n, b, dtype=np.uint8)
+            codes = oracle.unpack_codes(mode, data, D)
+            assert np.array_equal(oracle.pack_codes(mode, codes), data)
+
+
+def test_pack_nibble_and_crumb_order():
+    c4 = np.zeros(64, np.uint8)
+    c4[0], c4[1] = 1, 2           # element 0 -> low nibble, element 1 -> high nibble
+    assert oracle.pack_codes(INT4, c4)[0] == 0x21
+    c2 = np.zeros(128, np.uint8)
+    c2[:4] = [1, 2, 3, 0]         # element 4i+j -> bits 2j
+    assert oracle.pack_codes(INT2, c2)[0] == 0b00111001
+
+
+# --------------------------------------------------------------------------
+# quantisation: worked grid rows, error bound, special cases
+
+@pytest.mark.parametrize("mode,D", [(INT4, 64), (INT4, 128), (INT2, 64), (INT2, 128)])
+def test_worked_grid_row_is_exact(mode, D):
+    levels = 15 if mode == INT4 else 3
+    s, m = 0.25, -1.5                       # powers of two / exact binary16 values
+    k = np.arange(D) % (levels + 1)
+    x = (m + s * k).astype(np.float32)
+    row = oracle.quant_row(mode, x, None)
+    data = D // 2 if mode == INT4 else D // 4
+    if mode == INT4:
+        want = (k[0::2] | (k[1::2] << 4)).astype(np.uint8)
+        assert want[0] == 0x10 and want[1] == 0x32 and want[7] == 0xFE
+    else:
+        want = (k[0::4] | (k[1::4] << 2) | (k[2::4] << 4) | (k[3::4] << 6)).astype(np.uint8)
+        assert want[0] == 0xE4
+    assert np.array_equal(row[:data], want)
+    S, M = f16_of_pad(row, data)
+    assert (S, M) == (s, m)
+    assert np.array_equal(oracle.dequant_row(mode, row, D), x.astype(np.float64))
+
+
+@pytest.mark.parametrize("mode", [INT4, INT2])
+@pytest.mark.parametrize("rht", [False, True])
+def test_half_step_error_bound(mode, rht):
+    D = 128
+    rng = np.random.default_rng(3 + mode + 2 * rht)
+    signs = np.where(rng.integers(0, 2, D) == 1, 1, -1).astype(np.int8) if rht else None
+    levels = 15 if mode == INT4 else 3
+    data = D // 2 if mode == INT4 else D // 4
+    H = sylvester(D).astype(np.float64)
+    for _ in range(200):
+        x = (rng.standard_normal(D) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+        x[rng.integers(0, D)] *= 20.0
+        row = oracle.quant_row(mode, x, signs)
+        S, M = f16_of_pad(row, data)
+        xd = x.astype(np.float64)
+        y = H @ (signs * xd) if rht else xd          # rotated row, closed form
+        mn, mx = y.min(), y.max()
+        s = (mx - mn) / levels
+        slack = abs(mn - M) + levels * abs(s - S) + 1e-6 * max(abs(mn), abs(mx))
+        xh = oracle.dequant_row(mode, row, D, signs)
+        yh = H @ (signs * xh) if rht else xh          # back in the rotated domain
+        assert np.max(np.abs(y - yh)) <= S / 2 + slack + 1e-9
+        # in the input domain the l2 error shrinks by the RHT's norm sqrt(D)
+        if rht:
+            assert np.linalg.norm(xd - xh) <= (S / 2 + slack) * 1.0000001 + 1e-9
+        codes = oracle.unpack_codes(mode, row[:data], D)
+        assert codes.max() <= levels
+        if S > 0 and slack < S / 2:
+            assert codes[np.argmin(y)] == 0 and codes[np.argmax(y)] == levels
+
+
+@pytest.mark.parametrize("mode", [INT4, INT2])
+def test_constant_row_has_zero_scale(mode):
+    D = 64
+    x = np.full(D, 3.25, np.float32)
+    row = oracle.quant_row(mode, x, None)
+    data = D // 2 if mode == INT4 else D // 4
+    assert np.all(row[:data] == 0)
+    S, M = f16_of_pad(row, data)
+    assert S == 0.0 and M == 3.25
+    assert np.all(oracle.dequant_row(mode, row, D) == 3.25)
+
+
+def test_signed_zero_is_canonical():
+    D = 64
+    x = np.zeros(D, np.float32)
+    x[::2] = -0.0
+    row = oracle.quant_row(INT4, x, None)
+    assert row[32:36].tolist() == [0, 0, 0, 0]
+
+
+def _single_seq_paging(num_blocks, bs, T, mode, D, Hkv=1, signs=None):
+    c = oracle.Cache(mode, num_blocks, Hkv, bs, D, signs)
+    nb = (T + bs - 1) // bs
+    table = np.arange(nb, dtype=np.int32)[None, :]
+    pg = oracle.Paging(table, False, np.array([T], np.int32))
+    return c, pg
+
+
+def test_int8_per_channel_amax_symmetry_saturation():
+    D, T = 64, 6
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((T, 1, D)).astype(np.float32)
+    x[3] = -x[2]                                  # symmetric pair of tokens
+    c, pg = _single_seq_paging(2, 16, T, INT8, D)
+    assert oracle.write(c, pg, x, x * 0.5, np.array([0, T], np.int32)) == 0
+    assert c.ready[0] == 1
+    amax = np.abs(x[:, 0, :]).max(axis=0)
+    assert np.array_equal(c.amax[0, 0], amax) and np.array_equal(c.amax[1, 0], amax * 0.5)
+    q = c.k[0, 0, :T].view(np.int8).astype(np.int32)
+    arg = np.abs(x[:, 0, :]).argmax(axis=0)
+    assert np.all(np.abs(q[arg, np.arange(D)]) == 127)
+    assert np.array_equal(q[3], -q[2])
+    assert np.abs(q).max() <= 127
+    # a later write reuses the frozen scales and saturates beyond them
+    pg2 = oracle.Paging(pg.table, False, np.array([T + 1], np.int32))
+    big = (x[:1] * 5.0).astype(np.float32)
+    oracle.write(c, pg2, big, big, np.array([0, 1], np.int32))
+    qb = c.k[0, 0, T].view(np.int8).astype(np.int32)
+    assert np.array_equal(c.amax[0, 0], amax)
+    assert np.all(qb[np.abs(big[0, 0]) >= amax * 1.01] ** 2 == 127 ** 2)
+
+
+# --------------------------------------------------------------------------
+# attention: brute force on exact (grid) data, special cases, paging
+
+def _grid_values(rng, n, D, mode):
+    """Rows that INT4/INT2 (RHT off) or INT8 represent exactly."""
+    if mode == INT8:
+        return None
+    levels = 15 if mode == INT4 else 3
+    k = rng.integers(0, levels + 1, size=(n, D))
+    k[:, 0], k[:, 1] = 0, levels                       # pin min and max of each row
+    s = 2.0 ** rng.integers(-3, 2, size=(n, 1))
+    m = -(2.0 ** rng.integers(-2, 3, size=(n, 1)))
+    return (m + s * k).astype(np.float32)
+
+
+def _softmax_ref(q, K, V, scale, mask):
+    z = scale * (K @ q)
+    z = np.where(mask, z, -np.inf)
+    if not mask.any():
+        return np.zeros(V.shape[1])
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    return p @ V
+
+
+@pytest.mark.parametrize("mode", [INT4, INT2])
+def test_attention_brute_force_on_exact_rows(mode):
+    rng = np.random.default_rng(11 + mode)
+    D, bs, Hkv, Hq = 64, 16, 2, 4
+    L = [23, 40]
+    c = oracle.Cache(mode, 8, Hkv, bs, D)
+    table = np.array([[5, 2, -1], [0, 7, 3]], np.int32)
+    pg = oracle.Paging(table, False, np.array(L, np.int32))
+    K = [_grid_values(rng, L[b] * Hkv, D, mode).reshape(L[b], Hkv, D) for b in range(2)]
+    V = [_grid_values(rng, L[b] * Hkv, D, mode).reshape(L[b], Hkv, D) for b in range(2)]
+    kk = np.concatenate(K)
+    vv = np.concatenate(V)
+    assert oracle.write(c, pg, kk, vv, np.array([0, L[0], L[0] + L[1]], np.int32)) == 0
+    q = rng.standard_normal((2, Hq, D)).astype(np.float32)
+    scale = 1.0 / math.sqrt(D)
+    out, err = oracle.attention(c, pg, q, scale, threads=2)
+    assert err == 0
+    for b in range(2):
+        for hq in range(Hq):
+            h = hq // (Hq // Hkv)
+            want = _softmax_ref(q[b, hq].astype(np.float64), K[b][:, h].astype(np.float64),
+                                V[b][:, h].astype(np.float64), scale, np.ones(L[b], bool))
+            np.testing.assert_allclose(out[b, hq], want, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(2)
+    D, bs = 64, 16
+    c = oracle.Cache(INT4, 4, 1, bs, D)
+    # single visible key -> its value row; equal keys -> mean of values
+    kk = _grid_values(rng, 3, D, INT4)
+    kk[1] = kk[0]
+    kk[2] = kk[0]
+    vv = _grid_values(rng, 3, D, INT4)
+    pg = oracle.Paging(np.array([[1, -1]], np.int32), False, np.array([3], np.int32))
+    oracle.write(c, pg, kk[:, None], vv[:, None], np.array([0, 3], np.int32))
+    q = rng.standard_normal((1, 1, D)).astype(np.float32)
+    out, _ = oracle.attention(c, pg, q, 0.125)
+    np.testing.assert_allclose(out[0, 0], vv.astype(np.float64).mean(axis=0), rtol=0, atol=1e-12)
+    pg1 = oracle.Paging(np.array([[1, -1]], np.int32), False, np.array([1], np.int32))
+    out1, _ = oracle.attention(c, pg1, q, 0.125)
+    assert np.array_equal(out1[0, 0], vv[0].astype(np.float64))
+    # all keys evicted -> zero output
+    pge = oracle.Paging(np.array([[-1, -1]], np.int32), False, np.array([3], np.int32))
+    oute, _ = oracle.attention(c, pge, q, 0.125)
+    assert np.all(oute == 0.0)
+
+
+def test_write_skips_sentinel_and_flags_bad_ids():
+    D, bs = 64, 16
+    c = oracle.Cache(INT4, 4, 1, bs, D, fill=0xA5)
+    x = np.ones((20, 1, D), np.float32)
+    pg = oracle.Paging(np.array([[-1, 2]], np.int32), False, np.array([20], np.int32))
+    assert oracle.write(c, pg, x, x, np.array([0, 20], np.int32)) == 0
+    assert np.all(c.k[[0, 1, 3]] == 0xA5)              # block of the -1 entry untouched
+    assert not np.all(c.k[2, 0, :4] == 0xA5)
+    pgb = oracle.Paging(np.array([[9, 2]], np.int32), False, np.array([20], np.int32))
+    assert oracle.write(c, pgb, x, x, np.array([0, 20], np.int32)) & 1
+    pgt = oracle.Paging(np.array([[0]], np.int32), False, np.array([20], np.int32))
+    assert oracle.write(c, pgt, x, x, np.array([0, 20], np.int32)) & 2
+    assert oracle.write(c, pg, x, x, np.array([0, 20], np.int32)) == 0
+    pgs = oracle.Paging(np.array([[0, 1]], np.int32), False, np.array([10], np.int32))
+    assert oracle.write(c, pgs, x, x, np.array([0, 20], np.int32)) & 4
+
+
+def test_evicted_blocks_do_not_contribute():
+    rng = np.random.default_rng(4)
+    D, bs, T = 64, 16, 64
+    c = oracle.Cache(INT4, 8, 1, bs, D)
+    kk = _grid_values(rng, T, D, INT4)[:, None]
+    vv = _grid_values(rng, T, D, INT4)[:, None]
+    full = oracle.Paging(np.array([[4, 5, 6, 7]], np.int32), False, np.array([T], np.int32))
+    oracle.write(c, full, kk, vv, np.array([0, T], np.int32))
+    q = rng.standard_normal((1, 1, D)).astype(np.float32)
+    evict = oracle.Paging(np.array([[4, -1, -1, 7]], np.int32), False, np.array([T], np.int32))
+    a, _ = oracle.attention(c, evict, q, 0.125)
+    c.k[5:7] = rng.integers(0, 256, size=c.k[5:7].shape, dtype=np.uint8)   # garbage in evicted pages
+    c.v[5:7] = rng.integers(0, 256, size=c.v[5:7].shape, dtype=np.uint8)
+    b_, _ = oracle.attention(c, evict, q, 0.125)
+    assert np.array_equal(a, b_)
+    mask = np.zeros(T, bool)
+    mask[:16] = True
+    mask[48:] = True
+    want = _softmax_ref(q[0, 0].astype(np.float64), kk[:, 0].astype(np.float64),
+                        vv[:, 0].astype(np.float64), 0.125, mask)
+    np.testing.assert_allclose(a[0, 0], want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("W,sink", [(5, 0), (5, 3), (17, 2), (1, 0)])
+def test_sliding_window_and_sink_visibility(W, sink):
+    rng = np.random.default_rng(W * 10 + sink)
+    D, bs, T, Hkv = 64, 16, 40, 2
+    c = oracle.Cache(INT4, 4, Hkv, bs, D)
+    kk = _grid_values(rng, T * Hkv, D, INT4).reshape(T, Hkv, D)
+    vv = _grid_values(rng, T * Hkv, D, INT4).reshape(T, Hkv, D)
+    pg = oracle.Paging(np.array([[0, 1, 2]], np.int32), False, np.array([T], np.int32),
+                       window=np.array([0, W], np.int32), sink=sink)
+    oracle.write(c, pg, kk, vv, np.array([0, T], np.int32))
+    # prefill of the last 6 positions: each query has its own window
+    n = 6
+    q = rng.standard_normal((n, 2, D)).astype(np.float32)
+    scale = float(np.float32(0.2))   # the oracle takes the scale as fp32
+    out, _ = oracle.attention(c, pg, q, scale, cu_q=np.array([0, n], np.int32))
+    for i in range(n):
+        p = T - n + i
+        j = np.arange(T)
+        for h in range(Hkv):
+            mask = j <= p
+            if h == 1:
+                mask &= (j < sink) | (j > p - W)
+            want = _softmax_ref(q[i, h].astype(np.float64), kk[:, h].astype(np.float64),
+                                vv[:, h].astype(np.float64), scale, mask)
+            np.testing.assert_allclose(out[i, h], want, rtol=1e-12, atol=1e-12)
+
+
+def test_headwise_table_rows_select_per_head_pages():
+    rng = np.random.default_rng(9)
+    D, bs, T, Hkv = 64, 16, 20, 2
+    c = oracle.Cache(INT4, 6, Hkv, bs, D)
+    kk = _grid_values(rng, T * Hkv, D, INT4).reshape(T, Hkv, D)
+    vv = _grid_values(rng, T * Hkv, D, INT4).reshape(T, Hkv, D)
+    hw = oracle.Paging(np.array([[0, 1], [2, 3]], np.int32), True, np.array([T], np.int32))
+    oracle.write(c, hw, kk, vv, np.array([0, T], np.int32))
+    # head 0 pages in blocks 0,1; head 1 pages in blocks 2,3
+    assert np.all(c.k[2:4, 0] == 0) and np.all(c.k[0:2, 1] == 0)
+    q = rng.standard_normal((1, 2, D)).astype(np.float32)
+    out, _ = oracle.attention(c, hw, q, 0.125)
+    for h in range(2):
+        want = _softmax_ref(q[0, h].astype(np.float64), kk[:, h].astype(np.float64),
+                            vv[:, h].astype(np.float64), 0.125, np.ones(T, bool))
+        np.testing.assert_allclose(out[0, h], want, rtol=1e-12, atol=1e-12)
+
+
+def test_rht_attention_matches_brute_force_dequant():
+    """With the RHT on, dequantised keys are d * (H y_hat) / D; check the
+    oracle's attention against numpy with Sylvester's matrix and numpy's
+    binary16 decoding of the stored scale and zero point."""
+    wl = gen.tiny_int4(0)
+    c = oracle.Cache(wl.mode, wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.signs)
+    pg = oracle.Paging(wl.table, False, wl.seq_lens)
+    B, Hkv, D = wl.batch, wl.num_kv_heads, wl.head_dim
+    kk = np.concatenate([gen.kv_values_host(wl, "k", b, 0, int(wl.seq_lens[b])) for b in range(B)])
+    vv = np.concatenate([gen.kv_values_host(wl, "v", b, 0, int(wl.seq_lens[b])) for b in range(B)])
+    assert oracle.write(c, pg, kk, vv, wl.cu(wl.seq_lens)) == 0
+    q = gen.q_values_host(wl)
+    out, err = oracle.attention(c, pg, q, 1.0 / math.sqrt(D))
+    assert err == 0
+    H = sylvester(D).astype(np.float64)
+    sg = wl.signs.astype(np.float64)
+    for b in range(B):
+        L = int(wl.seq_lens[b])
+        for hq in range(wl.num_q_heads):
+            h = hq // wl.group
+            Kh, Vh = np.zeros((L, D)), np.zeros((L, D))
+            for j in range(L):
+                blk = wl.table[b, j // 16]
+                for dst, pages in ((Kh, c.k), (Vh, c.v)):
+                    row = pages[blk, h, j % 16]
+                    S, M = f16_of_pad(row, D // 2)
+                    u = np.empty(D)
+                    u[0::2] = row[:D // 2] & 15
+                    u[1::2] = row[:D // 2] >> 4
+                    dst[j] = sg * (H @ (u * S + M)) / D
+            want = _softmax_ref(q[b, hq].astype(np.float64), Kh, Vh, 1.0 / math.sqrt(D), np.ones(L, bool))
+            np.testing.assert_allclose(out[b, hq], want, rtol=1e-10, atol=1e-12)
+    # and the quantisation error of the keys is within the half-step bound
+    err_k = np.abs(Kh - kk[-L:, h].astype(np.float64)).max()
+    assert err_k < 2.0
