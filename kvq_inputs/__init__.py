@@ -336,3 +336,50 @@ def describe(wl: Workload) -> dict:
         "num_blocks": wl.num_blocks, "cached_tokens": int(wl.seq_lens.sum()),
         "headwise": wl.headwise, "rht": wl.signs is not None, "step": wl.step,
     }
+
+
+def custom(mode: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int, dtype: str,
+           seq_lens, n_new, num_blocks: Optional[int] = None, headwise: bool = False, window=None,
+           sink: int = 0, rht: bool = True, seed: int = 0, step: str = "decode", q_std: float = 1.0,
+           outlier_frac: float = 0.01, outlier_factor: float = 10.0, evict_outside_window: bool = False,
+           max_blocks: Optional[int] = None) -> Workload:
+    """A small workload of arbitrary shape for parity tests: pages drawn at
+    distinct random blocks (per kv head for head-wise tables), optional
+    outlier channels, optional eviction (-1) of blocks that hold neither sink
+    nor window keys of the last query of each sequence."""
+    rng = _structure_rng(seed)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    n_new = np.asarray(n_new, dtype=np.int32)
+    B = len(seq_lens)
+    bs, Hkv, D = block_size, num_kv_heads, head_dim
+    signs = _draw_signs(rng, D) if (rht and mode != MODE_INT8) else None
+    n_out = int(round(outlier_frac * Hkv * D))
+    ok = _draw_outliers(rng, Hkv, D, n_out, outlier_factor) if n_out else _NO_OUTLIERS
+    ov = _draw_outliers(rng, Hkv, D, n_out, outlier_factor) if n_out else _NO_OUTLIERS
+    need = int(((seq_lens + bs - 1) // bs).sum())
+    if max_blocks is None:
+        max_blocks = int((seq_lens.max() + bs - 1) // bs)
+    if num_blocks is None:
+        num_blocks = need + 7
+    win = None if window is None else np.asarray(window, dtype=np.int32)
+    if headwise:
+        table = np.full((B * Hkv, max_blocks), -1, dtype=np.int32)
+        for h in range(Hkv):
+            t = _tables_from_pool(rng, seq_lens, bs, max_blocks, num_blocks)
+            for b in range(B):
+                table[b * Hkv + h] = t[b]
+        if evict_outside_window and win is not None:
+            for b in range(B):
+                p = int(seq_lens[b]) - 1
+                for h in range(Hkv):
+                    if win[h] <= 0:
+                        continue
+                    lo_blk = (p - int(win[h]) + 1) // bs
+                    hi_sink = (sink - 1) // bs if sink > 0 else -1
+                    for blk in range(max_blocks):
+                        if hi_sink < blk < lo_blk:
+                            table[b * Hkv + h, blk] = -1
+    else:
+        table = _tables_from_pool(rng, seq_lens, bs, max_blocks, num_blocks)
+    return Workload("custom", mode, num_q_heads, Hkv, D, bs, dtype, num_blocks, max_blocks, seq_lens, n_new,
+                    table, headwise, win, sink, signs, step, q_std, ok, ov, seed)

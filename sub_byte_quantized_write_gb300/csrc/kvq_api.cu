@@ -1,0 +1,270 @@
+// kvq_api.cu -- the C ABI of libkvq: argument validation, launch geometry,
+// status codes.  Every call validates everything it can on the host before
+// any launch (a bad call leaves device memory untouched) and then enqueues
+// its kernels on the caller's stream without synchronising.
+
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/kvq.h"
+#include "kvq_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvq_status fail(kvq_status st, const char* msg) {
+  g_last_error = msg;
+  return st;
+}
+
+kvq_status cuda_fail(cudaError_t e) {
+  g_last_error = std::string("CUDA: ") + cudaGetErrorString(e);
+  return KVQ_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+kvq_status check_cache(const kvq_cache* c) {
+  if (!c) return fail(KVQ_ERR_INVALID_ARG, "cache is NULL");
+  if (!c->k_pages || !c->v_pages) return fail(KVQ_ERR_INVALID_ARG, "k_pages / v_pages is NULL");
+  if (!aligned(c->k_pages, 16) || !aligned(c->v_pages, 16))
+    return fail(KVQ_ERR_INVALID_ARG, "k_pages / v_pages must be 16-byte aligned");
+  if (c->mode != KVQ_INT4_TOKEN_HEAD && c->mode != KVQ_INT2_TOKEN_HEAD && c->mode != KVQ_INT8_CHANNEL)
+    return fail(KVQ_ERR_UNSUPPORTED, "unknown mode");
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(KVQ_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c->block_size != 16 && c->block_size != 32 && c->block_size != 64)
+    return fail(KVQ_ERR_UNSUPPORTED, "block_size must be 16, 32 or 64");
+  if (c->num_blocks <= 0 || c->num_kv_heads <= 0) return fail(KVQ_ERR_INVALID_ARG, "num_blocks / num_kv_heads must be > 0");
+  if (c->mode == KVQ_INT8_CHANNEL) {
+    if (c->rht_signs) return fail(KVQ_ERR_INVALID_ARG, "INT8 per-channel mode takes no RHT signs");
+    if (!c->ch_amax || !c->ch_amax_ready) return fail(KVQ_ERR_INVALID_ARG, "INT8 mode needs ch_amax and ch_amax_ready");
+    if (!aligned(c->ch_amax, 16)) return fail(KVQ_ERR_INVALID_ARG, "ch_amax must be 16-byte aligned");
+  }
+  return KVQ_OK;
+}
+
+kvq_status check_paging(const kvq_paging* p, int num_kv_heads) {
+  (void)num_kv_heads;
+  if (!p) return fail(KVQ_ERR_INVALID_ARG, "paging is NULL");
+  if ((p->block_tables == nullptr) == (p->block_tables_headwise == nullptr))
+    return fail(KVQ_ERR_INVALID_ARG, "exactly one of block_tables / block_tables_headwise must be set");
+  if (p->batch < 0) return fail(KVQ_ERR_INVALID_ARG, "batch < 0");
+  if (p->batch > 0 && (!p->seq_lens || p->max_blocks <= 0))
+    return fail(KVQ_ERR_INVALID_ARG, "seq_lens is NULL or max_blocks <= 0");
+  if (p->sink_size < 0) return fail(KVQ_ERR_INVALID_ARG, "sink_size < 0");
+  if (p->batch > 65535) return fail(KVQ_ERR_UNSUPPORTED, "batch > 65535");
+  return KVQ_OK;
+}
+
+kvq::AttnParams attn_params(const kvq_cache* c, const kvq_paging* p, const void* q, int32_t dtype,
+                            int32_t hq, float scale, float* out, int32_t* dev_error) {
+  kvq::AttnParams a;
+  std::memset(&a, 0, sizeof(a));
+  a.k_pages = c->k_pages;
+  a.v_pages = c->v_pages;
+  a.num_blocks = c->num_blocks;
+  a.num_kv_heads = c->num_kv_heads;
+  a.block_size = c->block_size;
+  a.head_dim = c->head_dim;
+  a.mode = c->mode;
+  a.signs = c->mode == KVQ_INT8_CHANNEL ? nullptr : c->rht_signs;
+  a.ch_amax = c->ch_amax;
+  a.headwise = p->block_tables_headwise != nullptr;
+  a.table = a.headwise ? p->block_tables_headwise : p->block_tables;
+  a.max_blocks = p->max_blocks;
+  a.batch = p->batch;
+  a.seq_lens = p->seq_lens;
+  a.window = p->window_per_kv_head;
+  a.sink = p->sink_size;
+  a.q = q;
+  a.dtype = dtype;
+  a.num_q_heads = hq;
+  a.group = hq / c->num_kv_heads;
+  a.softmax_scale = scale;
+  a.out = out;
+  a.dev_error = dev_error;
+  return a;
+}
+
+kvq_status check_q(const kvq_cache* c, const void* q, int32_t dtype, int32_t hq, const float* out) {
+  if (!q || !out) return fail(KVQ_ERR_INVALID_ARG, "q / out is NULL");
+  if (dtype != KVQ_F32 && dtype != KVQ_BF16) return fail(KVQ_ERR_UNSUPPORTED, "dtype must be KVQ_F32 or KVQ_BF16");
+  if (!aligned(q, 16) || !aligned(out, 16)) return fail(KVQ_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
+  if (hq <= 0 || hq % c->num_kv_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (hq / c->num_kv_heads > 8) return fail(KVQ_ERR_UNSUPPORTED, "GQA group size above 8");
+  return KVQ_OK;
+}
+
+// Split-KV geometry: `tiles_per_split` 32-key tiles per CTA; the split count
+// covers the longest possible sequence (max_blocks * block_size keys).
+void decode_geometry(const kvq_cache* c, const kvq_paging* p, int32_t want_splits, int* splits, int* tps) {
+  const long long max_keys = (long long)p->max_blocks * c->block_size;
+  const int n_tiles = (int)((max_keys + kvq::DECODE_KEYS_PER_TILE - 1) / kvq::DECODE_KEYS_PER_TILE);
+  int t;
+  if (want_splits > 0) {
+    t = (n_tiles + want_splits - 1) / want_splits;
+  } else {
+    t = 16;  // 512 keys: 4 tiles per warp
+    const int cap = 64;
+    if ((n_tiles + t - 1) / t > cap) t = (n_tiles + cap - 1) / cap;
+  }
+  if (t < 1) t = 1;
+  *tps = t;
+  *splits = (n_tiles + t - 1) / t;
+  if (*splits < 1) *splits = 1;
+  (void)sm_count;
+}
+
+size_t decode_ws_bytes(int batch, int hq, int d, int splits) {
+  const size_t n = (size_t)batch * hq * splits;
+  size_t o = n * d * sizeof(float);
+  o = (o + 255) & ~(size_t)255;
+  return o + n * sizeof(float2);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kvq_row_bytes(int32_t mode, int32_t head_dim) {
+  if (head_dim != 64 && head_dim != 128) return 0;
+  if (mode == KVQ_INT4_TOKEN_HEAD) return head_dim / 2 + 4;
+  if (mode == KVQ_INT2_TOKEN_HEAD) return head_dim / 4 + 4;
+  if (mode == KVQ_INT8_CHANNEL) return head_dim;
+  return 0;
+}
+
+int32_t kvq_abi_version(void) { return KVQ_ABI_VERSION; }
+
+const char* kvq_status_string(int32_t s) {
+  switch (s) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_INVALID_ARG: return "KVQ_ERR_INVALID_ARG";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA";
+    case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE";
+    default: return "KVQ_UNKNOWN_STATUS";
+  }
+}
+
+const char* kvq_last_error(void) { return g_last_error.c_str(); }
+
+kvq_status kvq_write(const kvq_cache* cache, const kvq_paging* paging, const void* k, const void* v,
+                     int32_t dtype, const int32_t* cu_new_tokens, int32_t num_tokens, int32_t* dev_error,
+                     void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
+  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "num_tokens < 0");
+  if (num_tokens == 0 || paging->batch == 0) return KVQ_OK;
+  if (!k || !v || !cu_new_tokens) return fail(KVQ_ERR_INVALID_ARG, "k / v / cu_new_tokens is NULL");
+  if (dtype != KVQ_F32 && dtype != KVQ_BF16) return fail(KVQ_ERR_UNSUPPORTED, "dtype must be KVQ_F32 or KVQ_BF16");
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(KVQ_ERR_INVALID_ARG, "k / v must be 16-byte aligned");
+  if ((long long)num_tokens * cache->num_kv_heads * 2 / 8 + 1 > 0x7FFFFFFFLL)
+    return fail(KVQ_ERR_UNSUPPORTED, "too many tokens for one call");
+  kvq::WriteParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.k_pages = cache->k_pages;
+  P.v_pages = cache->v_pages;
+  P.num_blocks = cache->num_blocks;
+  P.num_kv_heads = cache->num_kv_heads;
+  P.block_size = cache->block_size;
+  P.head_dim = cache->head_dim;
+  P.mode = cache->mode;
+  P.signs = cache->mode == KVQ_INT8_CHANNEL ? nullptr : cache->rht_signs;
+  P.ch_amax = cache->ch_amax;
+  P.ch_ready = cache->ch_amax_ready;
+  P.headwise = paging->block_tables_headwise != nullptr;
+  P.table = P.headwise ? paging->block_tables_headwise : paging->block_tables;
+  P.max_blocks = paging->max_blocks;
+  P.batch = paging->batch;
+  P.seq_lens = paging->seq_lens;
+  P.cu_new = cu_new_tokens;
+  P.k = k;
+  P.v = v;
+  P.dtype = dtype;
+  P.num_tokens = num_tokens;
+  P.dev_error = dev_error;
+  cudaError_t e = kvq::launch_write(P, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_paging* paging, int32_t num_q_heads,
+                                     int32_t num_splits, size_t* bytes, int32_t* splits_used) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
+  if (!bytes) return fail(KVQ_ERR_INVALID_ARG, "bytes is NULL");
+  if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return fail(KVQ_ERR_INVALID_ARG, "bad num_q_heads");
+  int splits, tps;
+  decode_geometry(cache, paging, num_splits, &splits, &tps);
+  *bytes = decode_ws_bytes(paging->batch, num_q_heads, cache->head_dim, splits);
+  if (splits_used) *splits_used = splits;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, const void* q, int32_t dtype,
+                           int32_t num_q_heads, float softmax_scale, float* out, void* workspace,
+                           size_t workspace_bytes, int32_t num_splits, int32_t* dev_error, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
+  if (paging->batch == 0) return KVQ_OK;
+  if ((st = check_q(cache, q, dtype, num_q_heads, out)) != KVQ_OK) return st;
+  if (cache->num_kv_heads > 65535) return fail(KVQ_ERR_UNSUPPORTED, "num_kv_heads > 65535");
+  int splits, tps;
+  decode_geometry(cache, paging, num_splits, &splits, &tps);
+  const size_t need = decode_ws_bytes(paging->batch, num_q_heads, cache->head_dim, splits);
+  if (!workspace || workspace_bytes < need) return fail(KVQ_ERR_WORKSPACE, "workspace missing or too small");
+  if (!aligned(workspace, 256)) return fail(KVQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  kvq::AttnParams P = attn_params(cache, paging, q, dtype, num_q_heads, softmax_scale, out, dev_error);
+  P.num_splits = splits;
+  P.tiles_per_split = tps;
+  const size_t n = (size_t)paging->batch * num_q_heads * splits;
+  P.part_o = static_cast<float*>(workspace);
+  P.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + ((n * cache->head_dim * 4 + 255) & ~(size_t)255));
+  cudaError_t e = kvq::launch_decode(P, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KVQ_OK;
+}
+
+kvq_status kvq_prefill_attn(const kvq_cache* cache, const kvq_paging* paging, const void* q, int32_t dtype,
+                            int32_t num_q_heads, const int32_t* cu_q, int32_t total_q, int32_t max_q_per_seq,
+                            float softmax_scale, float* out, int32_t* dev_error, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
+  if (total_q < 0 || max_q_per_seq < 0) return fail(KVQ_ERR_INVALID_ARG, "total_q / max_q_per_seq < 0");
+  if (paging->batch == 0 || total_q == 0 || max_q_per_seq == 0) return KVQ_OK;
+  if ((st = check_q(cache, q, dtype, num_q_heads, out)) != KVQ_OK) return st;
+  if (!cu_q) return fail(KVQ_ERR_INVALID_ARG, "cu_q is NULL");
+  kvq::AttnParams P = attn_params(cache, paging, q, dtype, num_q_heads, softmax_scale, out, dev_error);
+  P.cu_q = cu_q;
+  P.total_q = total_q;
+  P.max_q_per_seq = max_q_per_seq;
+  const int qb = 64 / P.group;
+  if ((max_q_per_seq + qb - 1) / qb > 0x7FFFFFFF) return fail(KVQ_ERR_UNSUPPORTED, "too many queries");
+  cudaError_t e = kvq::launch_prefill(P, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KVQ_OK;
+}
+
+}  // extern "C"

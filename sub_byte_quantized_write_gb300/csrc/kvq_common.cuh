@@ -1,0 +1,156 @@
+// kvq_common.cuh -- device helpers shared by the libkvq kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace kvq {
+
+enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2 };
+enum { DT_F32 = 0, DT_BF16 = 1 };
+enum { DEVERR_BLOCK_RANGE = 1, DEVERR_TABLE_RANGE = 2, DEVERR_SEQ_LEN = 4 };
+
+__host__ __device__ constexpr int mode_bits(int mode) { return mode == MODE_INT4 ? 4 : (mode == MODE_INT2 ? 2 : 8); }
+__host__ __device__ constexpr int data_bytes(int mode, int D) { return D * mode_bits(mode) / 8; }
+__host__ __device__ constexpr int row_bytes_of(int mode, int D) { return mode == MODE_INT8 ? D : data_bytes(mode, D) + 4; }
+
+__device__ __forceinline__ void flag_error(int32_t* dev_error, int bit) {
+  if (dev_error) atomicOr(dev_error, bit);
+}
+
+// Load EPL consecutive input elements (fp32 or bf16) as fp32.
+template <int EPL>
+__device__ __forceinline__ void load_row_elems(const void* base, int dtype, size_t elem_off, float (&x)[EPL]) {
+  if (dtype == DT_F32) {
+    const float* p = reinterpret_cast<const float*>(base) + elem_off;
+    if constexpr (EPL == 4) {
+      float4 v = __ldg(reinterpret_cast<const float4*>(p));
+      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+      float2 v = __ldg(reinterpret_cast<const float2*>(p));
+      x[0] = v.x; x[1] = v.y;
+    }
+  } else {
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(base) + elem_off;
+    if constexpr (EPL == 4) {
+      uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+      x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+      x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    } else {
+      uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(p));
+      x[0] = __uint_as_float(v << 16); x[1] = __uint_as_float(v & 0xFFFF0000u);
+    }
+  }
+}
+
+// Warp-wide Walsh-Hadamard butterfly over D = 32 * EPL elements, lane l
+// holding elements l*EPL .. l*EPL+EPL-1.  Stage order h = 1, 2, ..., D/2, each
+// pair (j, j+h) -> (x_j + x_{j+h}, x_j - x_{j+h}) in fp32: every stage is a
+// single IEEE add or subtract per element, so the result is bit-identical to
+// a sequential evaluation in the same stage order.
+template <int EPL>
+__device__ __forceinline__ void wht_warp(float (&x)[EPL], int lane) {
+#pragma unroll
+  for (int h = 1; h < EPL; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      if (i & h) continue;
+      const float a = x[i], b = x[i + h];
+      x[i] = __fadd_rn(a, b);
+      x[i + h] = __fsub_rn(a, b);
+    }
+  }
+#pragma unroll
+  for (int lm = 1; lm < 32; lm <<= 1) {
+    const bool upper = (lane & lm) != 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[i], lm);
+      // lower lane holds x_j: x_j + x_{j+h}; upper lane holds x_{j+h}: x_j - x_{j+h}
+      x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// fp32 -> fp16 bits, round to nearest even, saturating at +-65504.
+__device__ __forceinline__ uint16_t f16_sat_bits(float x) {
+  x = fminf(fmaxf(x, -65504.0f), 65504.0f);
+  return __half_as_ushort(__float2half_rn(x));
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;  // (a & b) | c
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+__device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;  // (a & b) ^ c
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// cp.async 16 bytes global -> shared; src_bytes = 0 zero-fills without reading.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+
+}  // namespace kvq

@@ -1,0 +1,211 @@
+// kvq_write.cu -- write path: rotate, quantise, pack and scatter new K/V rows.
+//
+// INT4 / INT2 per (token, kv_head): vLLM PR #40835 review summary ("INT4
+// per-token-head KV cache for the Triton backend"), 实现拆解 item 2 (the write
+// kernel rotates each row with a random Hadamard transform, takes a per-token-
+// head scale and zero point, rounds and packs nibbles) and 关键源码片段
+// (row = head_size/2 data bytes + a 4-byte scale pad); FastDeploy PR #5173
+// "support dynamic int2 quantization cache kv", Modifications (cache-write
+// kernels of the dynamic 2-bit cache).
+// INT8 per channel: vllm-ascend-quantized-kv-cache METADATA ("Ascend INT8 KV
+// Cache Plugin"), 运行机制 (symmetric per-channel scales along tokens, from the
+// first K/V a layer receives, separately for K and V).
+// Scatter through a uniform or head-wise block table with -1 sentinels:
+// FastDeploy PR #7718 "Optimize AppendAttention for discrete head-wise
+// block_idx", Motivation and PR2-only delta table.
+//
+// One warp per (token, kv_head, K|V) row; each lane holds D/32 consecutive
+// elements.  The row's arithmetic is a fixed sequence of IEEE fp32 operations
+// (sign flip, butterfly in stage order, exact min/max, one division, fp16 RNE,
+// one subtract and one divide per element, round-half-even), so the packed
+// bytes are identical to any other evaluation in the same order.
+
+#include "kvq_internal.h"
+
+namespace kvq {
+
+// Sequence b that owns token t: the largest b with cu[b] <= t.
+__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int batch, int t) {
+  int lo = 0, hi = batch;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cu + mid) <= t) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Resolve the destination row of (token t, head h); returns nullptr when the
+// row is dropped (sentinel) or invalid (error bit set).
+__device__ __forceinline__ uint8_t* dest_row(const WriteParams& P, uint8_t* pages, int t, int h) {
+  if (t >= __ldg(P.cu_new + P.batch)) return nullptr;
+  const int b = find_seq(P.cu_new, P.batch, t);
+  const int n = __ldg(P.cu_new + b + 1) - __ldg(P.cu_new + b);
+  const int L = __ldg(P.seq_lens + b);
+  if (L < 0 || n > L) {
+    flag_error(P.dev_error, DEVERR_SEQ_LEN);
+    return nullptr;
+  }
+  const int p = L - n + (t - __ldg(P.cu_new + b));
+  const int row = P.headwise ? b * P.num_kv_heads + h : b;
+  const int lb = p / P.block_size;
+  if (lb >= P.max_blocks) {
+    flag_error(P.dev_error, DEVERR_TABLE_RANGE);
+    return nullptr;
+  }
+  const int blk = __ldg(P.table + (size_t)row * P.max_blocks + lb);
+  if (blk < 0) return nullptr;  // evicted slot: nothing is written
+  if (blk >= P.num_blocks) {
+    flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
+    return nullptr;
+  }
+  const int R = row_bytes_of(P.mode, P.head_dim);
+  return pages + (((size_t)blk * P.num_kv_heads + h) * P.block_size + (p % P.block_size)) * R;
+}
+
+// OR-combine `bits` (nbits per lane) of groups of 32/nbits lanes into one
+// 32-bit word held by the first lane of each group.
+template <int NBITS>
+__device__ __forceinline__ uint32_t gather_word(uint32_t bits, int lane) {
+  constexpr int LPW = 32 / NBITS;  // lanes per word
+  uint32_t v = bits << ((lane % LPW) * NBITS);
+#pragma unroll
+  for (int o = 1; o < LPW; o <<= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int MODE, int D>
+__global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
+  constexpr int EPL = D / 32;
+  constexpr int BITS = mode_bits(MODE);
+  constexpr int LEVELS = (1 << BITS) - 1;
+  constexpr int DATA = data_bytes(MODE, D);
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int kv = (int)(wid & 1);
+  const long long th = wid >> 1;
+  const int h = (int)(th % P.num_kv_heads);
+  const long long t = th / P.num_kv_heads;
+  if (t >= P.num_tokens) return;
+  uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h);
+  if (dst == nullptr) return;  // warp-uniform
+
+  float x[EPL];
+  load_row_elems<EPL>(kv ? P.v : P.k, P.dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, x);
+  if (P.signs) {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (__ldg(P.signs + lane * EPL + i) < 0) x[i] = -x[i];
+    wht_warp<EPL>(x, lane);
+  }
+  float mn = x[0], mx = x[0];
+#pragma unroll
+  for (int i = 1; i < EPL; ++i) {
+    mn = fminf(mn, x[i]);
+    mx = fmaxf(mx, x[i]);
+  }
+  mn = __fadd_rn(warp_min(mn), 0.0f);  // canonical +0
+  mx = __fadd_rn(warp_max(mx), 0.0f);
+  const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)LEVELS);
+  const uint16_t s_h = f16_sat_bits(s);
+  const uint16_t m_h = f16_sat_bits(mn);
+  const float S = __half2float(__ushort_as_half(s_h));
+  const float M = __half2float(__ushort_as_half(m_h));
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    uint32_t u = 0;
+    if (S != 0.0f) {
+      float r = rintf(__fdiv_rn(__fsub_rn(x[i], M), S));
+      r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
+      u = (uint32_t)r;
+    }
+    bits |= u << (i * BITS);
+  }
+  constexpr int NBITS = EPL * BITS;        // bits per lane: 16, 8 or 4
+  const uint32_t word = gather_word<NBITS>(bits, lane);
+  constexpr int LPW = 32 / NBITS;
+  if (lane % LPW == 0) *reinterpret_cast<uint32_t*>(dst + 4 * (lane / LPW)) = word;
+  if (lane == 0) *reinterpret_cast<uint32_t*>(dst + DATA) = (uint32_t)s_h | ((uint32_t)m_h << 16);
+}
+
+// INT8, pass 1 (only while *ready == 0): per-channel max |x| over all tokens.
+// Column c = (kv * Hkv + h) * D + d; amax must start at zero; non-negative
+// floats order like their bit patterns, so an integer atomicMax is exact.
+__global__ void __launch_bounds__(256) int8_amax_kernel(WriteParams P, int tokens_per_block) {
+  if (__ldg(P.ch_ready) != 0) return;
+  const int cols = 2 * P.num_kv_heads * P.head_dim;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  const int per_kv = P.num_kv_heads * P.head_dim;
+  const int kv = c / per_kv, hd = c % per_kv;
+  const void* src = kv ? P.v : P.k;
+  const int t0 = blockIdx.y * tokens_per_block;
+  const int t1 = min(P.num_tokens, t0 + tokens_per_block);
+  float a = 0.0f;
+  for (int t = t0; t < t1; ++t) {
+    float x[1];
+    const size_t off = (size_t)t * per_kv + hd;
+    x[0] = P.dtype == DT_F32 ? __ldg(reinterpret_cast<const float*>(src) + off)
+                             : __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(src) + off) << 16);
+    a = fmaxf(a, fabsf(x[0]));
+  }
+  atomicMax(reinterpret_cast<int*>(P.ch_amax) + c, __float_as_int(a));
+}
+
+// INT8, pass 2: q = clamp(rne(x / (amax / 127)), -127, 127).
+template <int D>
+__global__ void __launch_bounds__(256) int8_quant_kernel(WriteParams P) {
+  constexpr int EPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *P.ch_ready = 1;  // later calls reuse the scales
+  const int kv = (int)(wid & 1);
+  const long long th = wid >> 1;
+  const int h = (int)(th % P.num_kv_heads);
+  const long long t = th / P.num_kv_heads;
+  if (t >= P.num_tokens) return;
+  uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h);
+  if (dst == nullptr) return;
+  float x[EPL];
+  load_row_elems<EPL>(kv ? P.v : P.k, P.dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, x);
+  const float* am = P.ch_amax + ((size_t)kv * P.num_kv_heads + h) * D + lane * EPL;
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const float s = __fdiv_rn(am[i], 127.0f);
+    int q = 0;
+    if (s != 0.0f) {
+      float r = rintf(__fdiv_rn(x[i], s));
+      r = fminf(fmaxf(r, -127.0f), 127.0f);
+      q = (int)r;
+    }
+    bits |= ((uint32_t)q & 0xFFu) << (8 * i);
+  }
+  const uint32_t word = gather_word<EPL * 8>(bits, lane);
+  constexpr int LPW = 32 / (EPL * 8);
+  if (lane % LPW == 0) *reinterpret_cast<uint32_t*>(dst + 4 * (lane / LPW)) = word;
+}
+
+cudaError_t launch_write(const WriteParams& P, cudaStream_t stream) {
+  const long long warps = (long long)P.num_tokens * P.num_kv_heads * 2;
+  const int blocks = (int)((warps + 7) / 8);
+  if (P.mode == MODE_INT8) {
+    const int tpb = 1024;
+    dim3 g1((2 * P.num_kv_heads * P.head_dim + 255) / 256, (P.num_tokens + tpb - 1) / tpb);
+    int8_amax_kernel<<<g1, 256, 0, stream>>>(P, tpb);
+    if (P.head_dim == 128) int8_quant_kernel<128><<<blocks, 256, 0, stream>>>(P);
+    else int8_quant_kernel<64><<<blocks, 256, 0, stream>>>(P);
+    return cudaGetLastError();
+  }
+  if (P.mode == MODE_INT4) {
+    if (P.head_dim == 128) write_token_head_kernel<MODE_INT4, 128><<<blocks, 256, 0, stream>>>(P);
+    else write_token_head_kernel<MODE_INT4, 64><<<blocks, 256, 0, stream>>>(P);
+  } else {
+    if (P.head_dim == 128) write_token_head_kernel<MODE_INT2, 128><<<blocks, 256, 0, stream>>>(P);
+    else write_token_head_kernel<MODE_INT2, 64><<<blocks, 256, 0, stream>>>(P);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

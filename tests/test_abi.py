@@ -1,0 +1,89 @@
+"""Host-only checks of the C ABI: the library loads, exports every function
+include/kvq.h declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:kvq_status|int32_t|const char\*)\s+(kvq_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def K():
+    from sub_byte_quantized_write_gb300 import build_lib
+    build_lib.build()
+    import sub_byte_quantized_write_gb300 as m
+    return m
+
+
+def test_header_declares_the_three_calls():
+    names = _declared_functions()
+    for n in ("kvq_write", "kvq_decode_attn", "kvq_prefill_attn", "kvq_decode_workspace_size", "kvq_row_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(K):
+    lib = ctypes.CDLL(K.LIB_PATH)
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+    assert lib.kvq_abi_version() == 1
+
+
+def test_row_bytes(K):
+    assert K.kvq_row_bytes(K.KVQ_INT4_TOKEN_HEAD, 128) == 68
+    assert K.kvq_row_bytes(K.KVQ_INT4_TOKEN_HEAD, 64) == 36
+    assert K.kvq_row_bytes(K.KVQ_INT2_TOKEN_HEAD, 128) == 36
+    assert K.kvq_row_bytes(K.KVQ_INT8_CHANNEL, 128) == 128
+    assert K.kvq_row_bytes(K.KVQ_INT4_TOKEN_HEAD, 80) == 0
+
+
+def _cache(K, **kw):
+    base = dict(k_pages=4096, v_pages=8192, num_blocks=10, num_kv_heads=2, block_size=16, head_dim=128,
+                mode=K.KVQ_INT4_TOKEN_HEAD, rht_signs=None, ch_amax=None, ch_amax_ready=None)
+    base.update(kw)
+    return K.KvqCache(**base)
+
+
+def _paging(K, **kw):
+    base = dict(block_tables=4096, block_tables_headwise=None, max_blocks=4, batch=2, seq_lens=4096,
+                window_per_kv_head=None, sink_size=0)
+    base.update(kw)
+    return K.KvqPaging(**base)
+
+
+def test_host_validation_statuses(K):
+    L = K.lib()
+    bref = ctypes.byref
+    n, s = ctypes.c_size_t(0), ctypes.c_int32(0)
+    # workspace sizing is pure host arithmetic
+    assert L.kvq_decode_workspace_size(bref(_cache(K)), bref(_paging(K)), 8, 0, bref(n), bref(s)) == K.KVQ_OK
+    assert n.value > 0 and s.value >= 1
+    assert L.kvq_decode_workspace_size(bref(_cache(K)), bref(_paging(K)), 7, 0, bref(n), bref(s)) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_write(None, bref(_paging(K)), 16, 16, 1, 16, 1, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_write(bref(_cache(K, head_dim=96)), bref(_paging(K)), 16, 16, 1, 16, 1, None, None) == K.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_write(bref(_cache(K, block_size=8)), bref(_paging(K)), 16, 16, 1, 16, 1, None, None) == K.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_write(bref(_cache(K, k_pages=4097)), bref(_paging(K)), 16, 16, 1, 16, 1, None, None) == K.KVQ_ERR_INVALID_ARG
+    both = _paging(K, block_tables_headwise=4096)
+    assert L.kvq_write(bref(_cache(K)), bref(both), 16, 16, 1, 16, 1, None, None) == K.KVQ_ERR_INVALID_ARG
+    neither = _paging(K, block_tables=None)
+    assert L.kvq_write(bref(_cache(K)), bref(neither), 16, 16, 1, 16, 1, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_write(bref(_cache(K, mode=K.KVQ_INT8_CHANNEL)), bref(_paging(K)), 16, 16, 1, 16, 1, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_write(bref(_cache(K)), bref(_paging(K)), 16, 16, 7, 16, 1, None, None) == K.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_write(bref(_cache(K)), bref(_paging(K)), 16, 16, 1, 16, 0, None, None) == K.KVQ_OK  # no-op
+    # Hq not a multiple of Hkv (GQA divisibility), too small workspace, group > 8
+    assert L.kvq_decode_attn(bref(_cache(K)), bref(_paging(K)), 256, 1, 5, 0.1, 256, 256, 1 << 20, 0, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_decode_attn(bref(_cache(K)), bref(_paging(K)), 256, 1, 8, 0.1, 256, 256, 16, 0, None, None) == K.KVQ_ERR_WORKSPACE
+    assert L.kvq_decode_attn(bref(_cache(K)), bref(_paging(K)), 256, 1, 18, 0.1, 256, 256, 1 << 30, 0, None, None) == K.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_prefill_attn(bref(_cache(K)), bref(_paging(K)), 256, 1, 8, None, 4, 4, 0.1, 256, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert b"cu_q" in L.kvq_last_error()

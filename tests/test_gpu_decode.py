@@ -1,0 +1,137 @@
+"""kvq_decode_attn on the GPU against the CPU oracle (max abs error 2e-3 in
+fp32), plus metamorphic checks that need no oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kvq_inputs as gen
+from harness import (ATOL, assert_pools_equal, build_case, decode_gpu, decode_oracle, kvq, max_err, q_host,
+                     write_step)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(wl, splits=0, check_pool=True):
+    c = build_case(wl)
+    write_step(c)
+    if check_pool:
+        assert_pools_equal(c)
+    q = q_host(wl)
+    g = decode_gpu(c, q, num_splits=splits)
+    o = decode_oracle(c, q)
+    e = max_err(g, o)
+    assert e <= ATOL, "max abs err %.3g" % e
+    assert int(c.dev_err.item()) == 0
+    return c, q, g, e
+
+
+def test_decode_tiny_workload():
+    _run(gen.tiny_int4(0))
+
+
+def test_decode_llama_like_reduced():
+    _run(gen.llama_int4(0, batch=6, ctx_lo=100, ctx_hi=2100, num_blocks=4000))
+
+
+def test_decode_ernie_int2_reduced():
+    _run(gen.ernie_int2(0, batch=5, median=1500, lo=64, hi=4000, num_blocks=1000))
+
+
+def test_decode_qwen_int8_headwise_reduced():
+    _run(gen.qwen_int8_headwise(0, batch=2, context=3000, window=700, sink=4))
+
+
+@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 5, 8])
+def test_decode_modes_dims_groups(mode, D, group):
+    Hkv = 2
+    wl = gen.custom(mode, Hkv * group, Hkv, D, 32, "bf16", seq_lens=[1, 31, 33, 250, 700], n_new=[1] * 5,
+                    seed=7 * group + D + mode, outlier_frac=0.02)
+    _run(wl)
+
+
+@pytest.mark.parametrize("bs", [16, 64])
+def test_decode_sliding_window_sentinels(bs):
+    wl = gen.custom(gen.MODE_INT4, 8, 2, 128, bs, "bf16", seq_lens=[1500, 900, 40], n_new=[1, 1, 1],
+                    headwise=True, window=[0, 300], sink=4, evict_outside_window=True, seed=21)
+    _run(wl)
+
+
+def test_decode_window_without_eviction():
+    wl = gen.custom(gen.MODE_INT2, 10, 2, 128, 16, "f32", seq_lens=[700, 90], n_new=[1, 1],
+                    window=[100, 33], sink=7, seed=8)
+    _run(wl)
+
+
+def test_decode_split_count_invariance():
+    wl = gen.custom(gen.MODE_INT4, 16, 4, 128, 16, "bf16", seq_lens=[3000, 2000, 17], n_new=[1, 1, 1], seed=4)
+    c, q, g0, _ = _run(wl)
+    for s in (1, 3, 50):
+        g = decode_gpu(c, q, num_splits=s)
+        assert np.max(np.abs(g - g0)) <= 1e-5
+
+
+def test_decode_headwise_identical_rows_bit_identical_to_uniform():
+    """A head-wise table whose rows all equal the uniform row must give the
+    very same output bits as the uniform table (legacy path unchanged)."""
+    wl = gen.custom(gen.MODE_INT4, 16, 4, 128, 16, "bf16", seq_lens=[800, 333], n_new=[1, 1], seed=12)
+    c = build_case(wl)
+    write_step(c)
+    q = q_host(wl)
+    g_uni = decode_gpu(c, q)
+    K = kvq()
+    hw = np.repeat(wl.table, wl.num_kv_heads, axis=0)
+    pag = K.Paging(torch.from_numpy(wl.seq_lens).cuda(), block_tables_headwise=torch.from_numpy(hw).cuda())
+    g_hw = decode_gpu(c, q, paging=pag)
+    assert np.array_equal(g_uni, g_hw)
+
+
+def test_decode_evicted_pages_never_read():
+    """Garbage in -1 pages must not change the result."""
+    wl = gen.custom(gen.MODE_INT4, 8, 2, 128, 16, "bf16", seq_lens=[1200], n_new=[1], headwise=True,
+                    window=[0, 200], sink=4, evict_outside_window=True, seed=30)
+    c = build_case(wl)
+    write_step(c)
+    q = q_host(wl)
+    g0 = decode_gpu(c, q)
+    Hkv = wl.num_kv_heads
+    rows = wl.table.reshape(wl.batch, Hkv, -1)
+    for h in range(Hkv):
+        live = set(int(x) for x in rows[:, h].ravel() if x >= 0)
+        for b in range(wl.num_blocks):
+            if b not in live:  # this head's page of block b is referenced by no row of head h
+                c.gcache.k_pages[b, h] = 0x77
+                c.gcache.v_pages[b, h] = 0x77
+    g1 = decode_gpu(c, q)
+    assert np.array_equal(g0, g1)
+
+
+def test_decode_empty_and_zero_length():
+    wl = gen.custom(gen.MODE_INT4, 4, 2, 64, 16, "f32", seq_lens=[5, 9], n_new=[1, 1], seed=2)
+    c = build_case(wl)
+    write_step(c)
+    K = kvq()
+    pag = K.Paging(torch.tensor([0, 9], dtype=torch.int32, device="cuda"),
+                   block_tables=torch.from_numpy(wl.table).cuda())
+    q = q_host(wl)
+    g = decode_gpu(c, q, paging=pag)
+    assert np.all(g[0] == 0.0)
+
+
+def test_decode_full_size_llama_sampled():
+    """The benchmark's workload at full size (64 sequences, 200k-block pool),
+    in the launch configuration the bench times; sampled sequences checked
+    against the oracle, the whole pool compared byte for byte."""
+    wl = gen.llama_int4(0)
+    c = build_case(wl)
+    write_step(c)
+    assert_pools_equal(c)
+    q = q_host(wl)
+    g = decode_gpu(c, q)
+    rows = np.array([0, 17, 31, 63], dtype=np.int32)
+    o = decode_oracle(c, q, rows=rows)
+    assert max_err(g[rows], o) <= ATOL
+    assert np.all(np.isfinite(g))
