@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("libkvq.so is not built: run `python -m sub_byte_quantized_write_gb300.build_lib` "
+    raise ImportError("libkvq.so is not built: run `python sub_byte_quantized_write_gb300/build_lib.py` "
                       "(or __graft_entry__.build()) first")
 
 _lib = ctypes.CDLL(LIB_PATH)

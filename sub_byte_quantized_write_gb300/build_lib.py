@@ -2,7 +2,8 @@
 
 Each CUDA translation unit compiles in its own nvcc process (in parallel),
 then one link step makes the shared library next to this file.  Up-to-date
-objects are reused.  Run as ``python -m sub_byte_quantized_write_gb300.build_lib``.
+objects are reused.  Run as ``python sub_byte_quantized_write_gb300/build_lib.py`` (the
+package itself cannot be imported before the library exists).
 """
 from __future__ import annotations
 

@@ -21,7 +21,11 @@ def _declared_functions():
 
 @pytest.fixture(scope="module")
 def K():
-    from sub_byte_quantized_write_gb300 import build_lib
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "kvq_build_lib", os.path.join(ROOT, "sub_byte_quantized_write_gb300", "build_lib.py"))
+    build_lib = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(build_lib)
     build_lib.build()
     import sub_byte_quantized_write_gb300 as m
     return m

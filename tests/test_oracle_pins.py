@@ -252,6 +252,23 @@ def test_int8_per_channel_amax_symmetry_saturation():
     assert np.all(qb[np.abs(big[0, 0]) >= amax * 1.01] ** 2 == 127 ** 2)
 
 
+def test_int8_worked_grid_codes_and_dequant():
+    """Channel c holds x = j * s_c for j in [-127, 127] with s_c a power of
+    two: the amax is 127 s_c, the scale amax / 127 = s_c exactly, every code
+    equals j and dequantisation returns x exactly."""
+    D, T = 64, 255
+    s = 2.0 ** (np.arange(D) % 7 - 3)
+    j = np.arange(-127, 128)
+    x = (j[:, None] * s[None, :]).astype(np.float32)[:, None, :]
+    c, pg = _single_seq_paging(16, 16, T, INT8, D)
+    assert oracle.write(c, pg, x, x, np.array([0, T], np.int32)) == 0
+    assert np.array_equal(c.amax[0, 0], (127 * s).astype(np.float32))
+    codes = np.concatenate([c.k[blk, 0] for blk in range(16)])[:T].view(np.int8).astype(np.int64)
+    assert np.array_equal(codes, np.repeat(j[:, None], D, axis=1))
+    row = c.k[0, 0, 5]
+    assert np.array_equal(oracle.dequant_row(INT8, row, D, None, c.amax[0, 0]), x[5, 0].astype(np.float64))
+
+
 # --------------------------------------------------------------------------
 # attention: brute force on exact (grid) data, special cases, paging
 
@@ -393,21 +410,26 @@ def test_sliding_window_and_sink_visibility(W, sink):
 
 
 def test_headwise_table_rows_select_per_head_pages():
+    """Row b * Hkv + h of a head-wise table serves (sequence b, kv head h)."""
     rng = np.random.default_rng(9)
-    D, bs, T, Hkv = 64, 16, 20, 2
-    c = oracle.Cache(INT4, 6, Hkv, bs, D)
-    kk = _grid_values(rng, T * Hkv, D, INT4).reshape(T, Hkv, D)
-    vv = _grid_values(rng, T * Hkv, D, INT4).reshape(T, Hkv, D)
-    hw = oracle.Paging(np.array([[0, 1], [2, 3]], np.int32), True, np.array([T], np.int32))
-    oracle.write(c, hw, kk, vv, np.array([0, T], np.int32))
-    # head 0 pages in blocks 0,1; head 1 pages in blocks 2,3
-    assert np.all(c.k[2:4, 0] == 0) and np.all(c.k[0:2, 1] == 0)
-    q = rng.standard_normal((1, 2, D)).astype(np.float32)
+    D, bs, T, Hkv, B = 64, 16, 20, 2, 2
+    c = oracle.Cache(INT4, 10, Hkv, bs, D)
+    kk = _grid_values(rng, B * T * Hkv, D, INT4).reshape(B * T, Hkv, D)
+    vv = _grid_values(rng, B * T * Hkv, D, INT4).reshape(B * T, Hkv, D)
+    rows = np.array([[0, 1], [2, 3], [4, 5], [6, 7]], np.int32)   # (b0,h0) (b0,h1) (b1,h0) (b1,h1)
+    hw = oracle.Paging(rows, True, np.array([T, T], np.int32))
+    oracle.write(c, hw, kk, vv, np.array([0, T, 2 * T], np.int32))
+    # head 0 pages only in blocks 0,1,4,5; head 1 pages only in blocks 2,3,6,7
+    assert np.all(c.k[[2, 3, 6, 7], 0] == 0) and np.all(c.k[[0, 1, 4, 5], 1] == 0)
+    assert not np.all(c.k[4, 0] == 0) and not np.all(c.k[2, 1] == 0)
+    q = rng.standard_normal((B, 2, D)).astype(np.float32)
     out, _ = oracle.attention(c, hw, q, 0.125)
-    for h in range(2):
-        want = _softmax_ref(q[0, h].astype(np.float64), kk[:, h].astype(np.float64),
-                            vv[:, h].astype(np.float64), 0.125, np.ones(T, bool))
-        np.testing.assert_allclose(out[0, h], want, rtol=1e-12, atol=1e-12)
+    for b in range(B):
+        for h in range(2):
+            sl = slice(b * T, (b + 1) * T)
+            want = _softmax_ref(q[b, h].astype(np.float64), kk[sl, h].astype(np.float64),
+                                vv[sl, h].astype(np.float64), 0.125, np.ones(T, bool))
+            np.testing.assert_allclose(out[b, h], want, rtol=1e-12, atol=1e-12)
 
 
 def test_rht_attention_matches_brute_force_dequant():
