@@ -152,7 +152,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 
-def setup_gpu(wl, device):
+def setup_gpu(wl, device, want_splits=0):
     import torch
     import sub_byte_quantized_write_gb300 as K
     signs = torch.from_numpy(wl.signs).to(device)
@@ -180,7 +180,7 @@ def setup_gpu(wl, device):
         "seq_lens": torch.from_numpy(wl.seq_lens).to(device),
     }
     pag = K.Paging(step["seq_lens"], block_tables=table)
-    nbytes, splits = K.kvq_decode_workspace_size(cache, pag, wl.num_q_heads)
+    nbytes, splits = K.kvq_decode_workspace_size(cache, pag, wl.num_q_heads, want_splits)
     step["ws"] = torch.empty(nbytes, dtype=torch.uint8, device=device)
     step["out"] = torch.empty((B, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=device)
     step["splits"] = splits
@@ -192,19 +192,39 @@ def run_gpu(args, rank, world, local_rank):
     import sub_byte_quantized_write_gb300 as K
     device = "cuda:%d" % local_rank
     torch.cuda.set_device(local_rank)
-    wl = gen.llama_int4(seed=0)
-    cache, pag, st = setup_gpu(wl, device)
+    wl = gen.llama_int4(seed=0, num_blocks=args.pool_blocks)
+    cache, pag, st = setup_gpu(wl, device, args.splits)
     scale = 1.0 / math.sqrt(wl.head_dim)
-    stream = torch.cuda.current_stream()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device=device)
+
+    def write_call():
+        K.kvq_write(cache, pag, st["k"], st["v"], st["cu"], stream=stream)
+
+    def decode_call():
+        K.kvq_decode_attn(cache, pag, st["q"], scale, out=st["out"], workspace=st["ws"],
+                          num_splits=st["splits"], stream=stream)
 
     def step():
-        K.kvq_write(cache, pag, st["k"], st["v"], st["cu"], stream=stream)
-        K.kvq_decode_attn(cache, pag, st["q"], scale, out=st["out"], workspace=st["ws"], stream=stream)
+        write_call()
+        decode_call()
 
+    # the step's two library calls are captured once into CUDA graphs and
+    # replayed, so the timed region holds only device work
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()  # first calls set the kernels' shared-memory attributes outside capture
+        stream.synchronize()
+        g_write, g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_write, stream=stream):
+            write_call()
+        with torch.cuda.graph(g_decode, stream=stream):
+            decode_call()
     for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step()
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+        g_write.replay()
+        g_decode.replay()
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
@@ -213,14 +233,15 @@ def run_gpu(args, rank, world, local_rank):
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
         torch.cuda.synchronize()
-        for i in range(args.steps):
-            flush.fill_(float(i))  # inputs exceed L2 already; flush so no step reuses the last one's lines
-            e0, e1, e2 = ev[i]
-            e0.record(stream)
-            K.kvq_write(cache, pag, st["k"], st["v"], st["cu"], stream=stream)
-            e1.record(stream)
-            K.kvq_decode_attn(cache, pag, st["q"], scale, out=st["out"], workspace=st["ws"], stream=stream)
-            e2.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(float(i))  # packed KV already exceeds L2; flush so no step reuses the last one's lines
+                e0, e1, e2 = ev[i]
+                e0.record(stream)
+                g_write.replay()
+                e1.record(stream)
+                g_decode.replay()
+                e2.record(stream)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
     dec_ms = [b.elapsed_time(c) for a, b, c in ev]
@@ -245,6 +266,7 @@ def run_gpu(args, rank, world, local_rank):
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
+        # plain library calls (no graph), inputs from pinned host memory
         st["k"].copy_(hk, non_blocking=True)
         st["v"].copy_(hv, non_blocking=True)
         st["q"].copy_(hq, non_blocking=True)
@@ -253,19 +275,20 @@ def run_gpu(args, rank, world, local_rank):
         step()
         hout.copy_(st["out"], non_blocking=True)
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        e2e_step()
-    torch.cuda.synchronize()
     e2e_ms = []
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        c.record(stream)
-        c.synchronize()
-        e2e_ms.append(a.elapsed_time(c))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            e2e_step()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            c.record(stream)
+            c.synchronize()
+            e2e_ms.append(a.elapsed_time(c))
     e2e_value = world * wl.batch / (sum(e2e_ms) / len(e2e_ms) / 1e3)
 
     ab = algorithmic_bytes(wl)
@@ -282,6 +305,7 @@ def run_gpu(args, rank, world, local_rank):
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
                    "context": "uniform[1024,8192]", "cached_tokens": int(wl.seq_lens.sum()),
                    "pool_blocks": wl.num_blocks, "rht": True, "decode_splits": st["splits"],
+                   "timing": "CUDA graphs of the write call and the decode call, events around each replay",
                    "l2": "flushed between timed steps (256 MB write); packed KV 321 MB also exceeds L2",
                    "parallelism": "replicas only" if world > 1 else "single GPU"},
         "effective_kv_GBps": round(ab["decode"] / (dec / 1e3) / 1e9, 1),
@@ -379,6 +403,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-blocks", type=int, default=200000,
+                    help="block pool size (the workload's is 200000; smaller pools only for profiling)")
+    ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = the library's choice)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))

@@ -16,14 +16,18 @@
 // warp streams 32-key tiles (two 16-row page chunks each of K and V) through
 // its own cp.async ring in shared memory and keeps its own online softmax.
 // The RHT and the dequantisation are folded into the query and the weights:
-//   q . k_j = (s_j (q' . u_j) + m_j sum(q')) / D,   q' = H (d * q)
-//   sum_j P_j v_j = d * H( sum_j (P_j s_j) u_j + sum_j P_j m_j ) / D
-// so the hot loop multiplies raw codes u (exact small integers in fp16) on
+//   q . k_j = (s_j (q' . c_j) + z_j sum(q')) / D,   q' = H (d * q)
+//   sum_j P_j v_j = d * H( sum_j (P_j s_j) c_j + sum_j P_j z_j ) / D
+// with the signed code c = u - 2^(b-1) and z = m + 2^(b-1) s (the value of
+// code 2^(b-1)), so the hot loop multiplies codes (exact small integers in fp16) on
 // the tensor cores: QK^T as m16n8k16 with M = 16 keys and N = 8 slots (4 q
 // heads of the GQA group x {hi, lo} halves of q'), and P.V as m16n8k16 with
 // M = 16 head dims, K = 16 keys, N = the same 8 slots of (P s) hi / lo.
 // Splitting q' and (P s) into two fp16 terms keeps ~22 significant bits, so
-// the fp16 operands do not limit accuracy.  A second kernel merges the
+// the fp16 operands do not limit accuracy.  Signed (centred) codes keep the
+// fp32 accumulators small: with unsigned codes the P.V accumulator and the
+// zero-point sum grow large with opposite signs and their rounding errors no
+// longer cancel over tens of thousands of keys.  A second kernel merges the
 // splits (log-sum-exp) and applies the inverse RHT.
 
 #include <math_constants.h>
@@ -89,22 +93,33 @@ __device__ __forceinline__ uint2 load_range(const uint8_t* tile, int kappa, int 
   }
 }
 
-// Two codes of one key row as an exact fp16 pair.  Pair P of word w holds
-// head dims (d0, d1) = INT4 (8w+P, 8w+P+4), INT2 (16w+P, 16w+P+8),
-// INT8 (4w+2P, 4w+2P+1); kpair_dims gives the same map for the query side.
+// fp16 bit pattern of (magic + bias) in both halves, where `magic` places a
+// code's lowest bit at bit `pos` of a half with weight 1 (1024, 256, 64, 16
+// for pos 0, 2, 4, 6): OR-ing the code in gives magic + u exactly, and one
+// sub.f16x2 with this value leaves the SIGNED code u - bias exactly.
+__host__ __device__ constexpr uint32_t magic_minus(uint32_t magic_half, int pos, int bias) {
+  return (magic_half | ((uint32_t)bias << pos)) * 0x00010001u;
+}
+
+// Two codes of one key row as an exact fp16 pair of signed codes
+// q = u - 2^(b-1) (INT4 [-8, 7], INT2 [-2, 1], INT8 as stored).  Pair P of
+// word w holds head dims (d0, d1) = INT4 (8w+P, 8w+P+4), INT2 (16w+P,
+// 16w+P+8), INT8 (4w+2P, 4w+2P+1); kpair_dims gives the same map for the
+// query side.
 template <int MODE, int P>
 __device__ __forceinline__ uint32_t kpair(uint32_t w) {
   if constexpr (MODE == MODE_INT4) {
-    constexpr uint32_t mask = (P & 1) ? 0x00F000F0u : 0x000F000Fu;
+    constexpr int pos = (P & 1) ? 4 : 0;
+    constexpr uint32_t mask = 0x000F000Fu << pos;
     constexpr uint32_t magic = (P & 1) ? 0x54005400u : 0x64006400u;  // 64 + u, 1024 + u
     const uint32_t src = (P >= 2) ? (w >> 8) : w;
-    return hsub2_bits(lop3_and_or(src, mask, magic), magic);
+    return hsub2_bits(lop3_and_or(src, mask, magic), magic_minus(magic & 0xFFFF, pos, 8));
   } else if constexpr (MODE == MODE_INT2) {
     constexpr int q = P & 3;
     constexpr uint32_t mask = 0x00030003u << (2 * q);
     constexpr uint32_t magic = q == 0 ? 0x64006400u : q == 1 ? 0x5C005C00u : q == 2 ? 0x54005400u : 0x4C004C00u;
     const uint32_t src = (P >= 4) ? (w >> 8) : w;
-    return hsub2_bits(lop3_and_or(src, mask, magic), magic);
+    return hsub2_bits(lop3_and_or(src, mask, magic), magic_minus(magic & 0xFFFF, 2 * q, 2));
   } else {
     constexpr uint32_t sel = (2 * P) | (4 << 4) | ((2 * P + 1) << 8) | (4 << 12);
     const uint32_t x = prmt(w, 0u, sel);
@@ -120,23 +135,24 @@ __device__ __forceinline__ void kpair_dims(int w, int P, int& d0, int& d1) {
 }
 
 // Code C of the lane ranges of two keys (A: key e=0, B: key e=1) as an exact
-// fp16 pair (A's code in the low half).
+// fp16 pair of signed codes (A's code in the low half).
 template <int MODE, int C>
 __device__ __forceinline__ uint32_t vpair(uint2 A, uint2 B) {
   if constexpr (MODE == MODE_INT4) {
     constexpr int byte = C / 2;
     constexpr uint32_t sel = byte | (byte << 4) | ((4 + byte) << 8) | ((4 + byte) << 12);
     const uint32_t x = prmt(A.x, B.x, sel);
-    constexpr uint32_t mask = (C & 1) ? 0x00F000F0u : 0x000F000Fu;
+    constexpr int pos = (C & 1) ? 4 : 0;
+    constexpr uint32_t mask = 0x000F000Fu << pos;
     constexpr uint32_t magic = (C & 1) ? 0x54005400u : 0x64006400u;
-    return hsub2_bits(lop3_and_or(x, mask, magic), magic);
+    return hsub2_bits(lop3_and_or(x, mask, magic), magic_minus(magic & 0xFFFF, pos, 8));
   } else if constexpr (MODE == MODE_INT2) {
     constexpr int byte = C / 4, q = C % 4;
     constexpr uint32_t sel = byte | (byte << 4) | ((4 + byte) << 8) | ((4 + byte) << 12);
     const uint32_t x = prmt(A.x, B.x, sel);
     constexpr uint32_t mask = 0x00030003u << (2 * q);
     constexpr uint32_t magic = q == 0 ? 0x64006400u : q == 1 ? 0x5C005C00u : q == 2 ? 0x54005400u : 0x4C004C00u;
-    return hsub2_bits(lop3_and_or(x, mask, magic), magic);
+    return hsub2_bits(lop3_and_or(x, mask, magic), magic_minus(magic & 0xFFFF, 2 * q, 2));
   } else {
     constexpr int b = C & 3;
     constexpr uint32_t sel = b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12);
@@ -416,10 +432,11 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
         if constexpr (MODE != MODE_INT8) {
           const uint32_t pk = lds32(kt + kappa * C::R + C::DATA);
           const uint32_t pv = lds32(vt + kappa * C::R + C::DATA);
+          constexpr float half_range = (float)(1 << (C::BITS - 1));
           sk = __half2float(__ushort_as_half((unsigned short)(pk & 0xFFFF)));
-          mk = __half2float(__ushort_as_half((unsigned short)(pk >> 16)));
+          mk = fmaf(half_range, sk, __half2float(__ushort_as_half((unsigned short)(pk >> 16))));
           sv_[m][hh] = __half2float(__ushort_as_half((unsigned short)(pv & 0xFFFF)));
-          mv_[m][hh] = __half2float(__ushort_as_half((unsigned short)(pv >> 16)));
+          mv_[m][hh] = fmaf(half_range, sv_[m][hh], __half2float(__ushort_as_half((unsigned short)(pv >> 16))));
         } else {
           sv_[m][hh] = 1.0f;
           mv_[m][hh] = 0.0f;
@@ -453,6 +470,7 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
 #pragma unroll
           for (int r = 0; r < 4; ++r) oacc[nt][mt][r] *= f;
       }
+      float tl = 0.0f, tpm = 0.0f;  // tile-local sums, added once per tile
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         float wv[2];
@@ -460,8 +478,8 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
         for (int hh = 0; hh < 2; ++hh) {
           const float p = ex2(lg[m][hh][nt] - muse);
           const bool ok = vk[m][hh];
-          lrun[nt] += ok ? p : 0.0f;
-          if constexpr (MODE != MODE_INT8) pmrun[nt] += ok ? p * mv_[m][hh] : 0.0f;
+          tl += ok ? p : 0.0f;
+          if constexpr (MODE != MODE_INT8) tpm += ok ? p * mv_[m][hh] : 0.0f;
           wv[hh] = ok ? p * sv_[m][hh] : 0.0f;
         }
         const __half h0 = __float2half_rn(wv[0]), h1 = __float2half_rn(wv[1]);
@@ -470,6 +488,8 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
         xh[nt][m] = *reinterpret_cast<const uint32_t*>(&hp);
         xl[nt][m] = *reinterpret_cast<const uint32_t*>(&lp);
       }
+      lrun[nt] += tl;
+      pmrun[nt] += tpm;
     }
 
     // ---- P.V: O^T (D x slots) += U_V^T (D x 16 keys) . Wslots (16 keys x slots)
@@ -647,9 +667,17 @@ size_t decode_smem_bytes() {
 template <int MODE, int D, int NT>
 cudaError_t launch_decode_t(const AttnParams& P, cudaStream_t stream) {
   const size_t smem = decode_smem_bytes<MODE, D, NT>();
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<MODE, D, NT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the opt-in shared-memory size is set once per device (not inside later
+  // calls, which may be captured into a CUDA graph)
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(decode_split_kernel<MODE, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
   dim3 grid(P.num_splits, P.num_kv_heads, P.batch);
   decode_split_kernel<MODE, D, NT><<<grid, 128, smem, stream>>>(P);
   e = cudaGetLastError();

@@ -20,6 +20,9 @@
 // fp16 tiles in shared memory (exact small integers; per-key scale and zero
 // point kept aside), and each warp runs QK^T and P.V on the tensor cores
 // (m16n8k16) with the query and (P s) each split into fp16 hi + lo terms.
+// Codes enter the tensor cores signed (u - 2^(b-1)) with the zero point
+// moved to the value of code 2^(b-1), which keeps the fp32 accumulators
+// small over long prefixes.
 // The RHT is folded in: q' = H(d * q) once per row, and the epilogue applies
 // d * H(.) / D to the output rows.
 
@@ -72,7 +75,10 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
 }
 
 // Eight consecutive codes (head dims 8c .. 8c+7) of a raw row as four exact
-// fp16 pairs in dim order.
+// fp16 pairs in dim order, as signed codes u - 2^(b-1) (INT8: as stored).
+// The magic constants put a code's low bit at weight 1 (1024 + u for bits
+// 0-3, 64 + u for bits 4-7, 256 / 16 for the 2-bit positions 2 and 6); the
+// subtrahend is magic + 2^(b-1).
 template <int MODE>
 __device__ __forceinline__ uint4 codes8(const uint8_t* raw_row, int c) {
   uint32_t o[4];
@@ -82,15 +88,15 @@ __device__ __forceinline__ uint4 codes8(const uint8_t* raw_row, int c) {
     for (int j = 0; j < 4; ++j) {
       const uint32_t x = prmt(w, 0u, j | (4 << 4) | (j << 8) | (4 << 12));  // byte j in both halves
       // low half: low nibble -> 1024 + u; high half: high nibble -> 64 + u
-      o[j] = hsub2_bits(lop3_and_or(x, 0x00F0000Fu, 0x54006400u), 0x54006400u);
+      o[j] = hsub2_bits(lop3_and_or(x, 0x00F0000Fu, 0x54006400u), 0x54806408u);
     }
   } else if constexpr (MODE == MODE_INT2) {
     const uint32_t w = *reinterpret_cast<const uint16_t*>(raw_row + 2 * c);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const uint32_t x = prmt(w, 0u, j | (4 << 4) | (j << 8) | (4 << 12));
-      o[2 * j] = hsub2_bits(lop3_and_or(x, 0x000C0003u, 0x5C006400u), 0x5C006400u);
-      o[2 * j + 1] = hsub2_bits(lop3_and_or(x, 0x00C00030u, 0x4C005400u), 0x4C005400u);
+      o[2 * j] = hsub2_bits(lop3_and_or(x, 0x000C0003u, 0x5C006400u), 0x5C086402u);
+      o[2 * j + 1] = hsub2_bits(lop3_and_or(x, 0x00C00030u, 0x4C005400u), 0x4C805420u);
     }
   } else {
     const uint2 w = lds64(raw_row + 8 * c);
@@ -305,10 +311,11 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_kernel(AttnParams P) {
         const int key = threadIdx.x & (PF_KT - 1);
         const bool isv = threadIdx.x >= PF_KT;
         const uint32_t pad = lds32((isv ? rv : rk) + key * C::R + C::DATA);
+        constexpr float half_range = (float)(MODE == MODE_INT4 ? 8 : 2);
         const float s = __half2float(__ushort_as_half((unsigned short)(pad & 0xFFFF)));
         const float m = __half2float(__ushort_as_half((unsigned short)(pad >> 16)));
         (isv ? vs : ks)[key] = s;
-        (isv ? vm : km)[key] = m;
+        (isv ? vm : km)[key] = fmaf(half_range, s, m);  // value of the signed code 0
       }
     }
     __syncthreads();
@@ -370,6 +377,7 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_kernel(AttnParams P) {
       }
     }
     uint32_t whi[4][4], wlo[4][4];  // A fragments of (P s) per 16-key step
+    float tl[2] = {0.0f, 0.0f}, tpm[2] = {0.0f, 0.0f};  // tile-local sums
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       float w[4];
@@ -378,9 +386,9 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_kernel(AttnParams P) {
         const int x = r >> 1;
         const int kk = 8 * nt + 2 * tq + (r & 1);
         const float p = ex2(sacc[nt][r] - muse[x]);  // masked logits give 0
-        lrow[x] += p;
+        tl[x] += p;
         if constexpr (MODE != MODE_INT8) {
-          pmrow[x] += p * vm[kk];
+          tpm[x] += p * vm[kk];
           w[r] = p * vs[kk];
         } else {
           w[r] = p;
@@ -395,6 +403,11 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_kernel(AttnParams P) {
         whi[kk16][2 * half + x] = *reinterpret_cast<const uint32_t*>(&hp);
         wlo[kk16][2 * half + x] = *reinterpret_cast<const uint32_t*>(&lp);
       }
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      lrow[x] += tl[x];
+      pmrow[x] += tpm[x];
     }
     // ---- O += (P s) V
 #pragma unroll
@@ -499,8 +512,15 @@ __global__ void __launch_bounds__(PF_THREADS, 2) prefill_kernel(AttnParams P) {
 template <int MODE, int D>
 cudaError_t launch_prefill_t(const AttnParams& P, cudaStream_t stream) {
   using C = PfCfg<MODE, D>;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<MODE, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(prefill_kernel<MODE, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
   const int QB = PF_ROWS / P.group;
   dim3 grid((P.max_q_per_seq + QB - 1) / QB, P.num_kv_heads, P.batch);
   prefill_kernel<MODE, D><<<grid, PF_THREADS, C::SMEM, stream>>>(P);

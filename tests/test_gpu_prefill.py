@@ -19,7 +19,8 @@ def _run(wl, rows=None):
     o = prefill_oracle(c, q, rows=rows)
     gg = g if rows is None else g[rows]
     e = max_err(gg, o)
-    assert e <= ATOL, "max abs err %.3g" % e
+    worst = np.unravel_index(np.argmax(np.abs(gg.astype(np.float64) - o)), o.shape)
+    assert e <= ATOL, "max abs err %.3g at (row, head, dim) %s" % (e, worst)
     assert int(c.dev_err.item()) == 0
     return c, q, g
 
