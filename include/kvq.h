@@ -26,8 +26,9 @@
  *
  * Conventions shared by every call
  *   - Every pointer is a DEVICE pointer on the current CUDA device unless the
- *     comment says "host".  The library allocates nothing and keeps no state
- *     besides a per-device cache of the SM count.
+ *     comment says "host".  The library allocates nothing at call time; its
+ *     only state is a per-device record of kernel attributes it has set and,
+ *     for kvq_decode_attn_noalloc, one static scratch array per device.
  *   - Calls enqueue work on `stream` (a cudaStream_t passed as void*; NULL is
  *     the legacy default stream) and never synchronise.  Outputs are valid
  *     once the stream reaches the work.
@@ -218,6 +219,30 @@ kvq_status kvq_prefill_attn(const kvq_cache* cache, const kvq_paging* paging,
                             const int32_t* cu_q, int32_t total_q, int32_t max_q_per_seq,
                             float softmax_scale, float* out,
                             int32_t* dev_error, void* stream);
+
+/* kvq_decode_attn_noalloc -- kvq_decode_attn for callers that cannot
+ * allocate device memory (no counterpart on the pages; an addition of this
+ * library).  Some callers must not or cannot call cudaMalloc at call time:
+ * a plugin inside a host framework that owns all device memory and hands out
+ * no scratch, or a latency-critical path where an allocation's implicit
+ * synchronisation is unacceptable.  This entry point takes the same arguments
+ * as kvq_decode_attn minus the workspace and allocates nothing: the split-KV
+ * partials live in one static device array of KVQ_NOALLOC_SCRATCH_BYTES that
+ * the library reserves on every GPU it is loaded on, until the process exits.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents.  Nothing in it needs to start at zero (the kernels
+ *     write every partial before reading it), but calls whose work overlaps
+ *     on the GPU (different streams, or different host threads) race on it:
+ *     serialise them.
+ *   - Returns KVQ_ERR_WORKSPACE, with a message, when the call would need more
+ *     scratch than KVQ_NOALLOC_SCRATCH_BYTES (see kvq_decode_workspace_size). */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)
+kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_paging* paging,
+                                   const void* q, int32_t dtype, int32_t num_q_heads,
+                                   float softmax_scale, float* out, int32_t num_splits,
+                                   int32_t* dev_error, void* stream);
 
 /* Human-readable name of a status. */
 const char* kvq_status_string(int32_t status);

@@ -7,7 +7,8 @@ library's CUDA kernels; there is no fallback.  If ``libkvq.so`` has not been
 built, importing this package raises ImportError.
 
 Names mirror the C calls: ``kvq_write``, ``kvq_decode_attn``,
-``kvq_prefill_attn``, ``kvq_decode_workspace_size``, ``kvq_row_bytes``.
+``kvq_decode_attn_noalloc``, ``kvq_prefill_attn``, ``kvq_decode_workspace_size``,
+``kvq_row_bytes``.
 """
 from __future__ import annotations
 
@@ -60,6 +61,8 @@ _lib.kvq_decode_workspace_size.argtypes = [_CP, _PP, _I, _I, ctypes.POINTER(ctyp
 _lib.kvq_decode_workspace_size.restype = _I
 _lib.kvq_decode_attn.argtypes = [_CP, _PP, _P, _I, _I, ctypes.c_float, _P, _P, ctypes.c_size_t, _I, _P, _P]
 _lib.kvq_decode_attn.restype = _I
+_lib.kvq_decode_attn_noalloc.argtypes = [_CP, _PP, _P, _I, _I, ctypes.c_float, _P, _I, _P, _P]
+_lib.kvq_decode_attn_noalloc.restype = _I
 _lib.kvq_prefill_attn.argtypes = [_CP, _PP, _P, _I, _I, _P, _I, _I, ctypes.c_float, _P, _P, _P]
 _lib.kvq_prefill_attn.restype = _I
 
@@ -204,6 +207,24 @@ def kvq_decode_attn(cache: PagedCache, paging: Paging, q: torch.Tensor, softmax_
                                 float(softmax_scale), _dev_ptr(out, torch.float32, "out"),
                                 _dev_ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
                                 num_splits, _dev_ptr(dev_error, torch.int32, "dev_error"), _stream_ptr(stream)))
+    return out
+
+
+def kvq_decode_attn_noalloc(cache: PagedCache, paging: Paging, q: torch.Tensor, softmax_scale: float,
+                            out: Optional[torch.Tensor] = None, num_splits: int = 0,
+                            dev_error: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """kvq_decode_attn without a caller workspace: for callers that cannot
+    allocate device memory at call time.  Uses the library's one static
+    device scratch array (KVQ_NOALLOC_SCRATCH_BYTES per GPU); calls that
+    overlap on the GPU race on it, so serialise them.  The first call on a
+    device must come before any stream capture."""
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    cs, ps = cache.struct(), paging.struct()
+    _check(_lib.kvq_decode_attn_noalloc(ctypes.byref(cs), ctypes.byref(ps), _dev_ptr(q, name="q"), _qdtype(q), Hq,
+                                        float(softmax_scale), _dev_ptr(out, torch.float32, "out"), num_splits,
+                                        _dev_ptr(dev_error, torch.int32, "dev_error"), _stream_ptr(stream)))
     return out
 
 

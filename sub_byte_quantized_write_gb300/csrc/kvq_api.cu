@@ -7,6 +7,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "../../include/kvq.h"
@@ -139,6 +140,30 @@ size_t decode_ws_bytes(int batch, int hq, int d, int splits) {
   return o + n * sizeof(float2);
 }
 
+// Scratch of kvq_decode_attn_noalloc: one static device array per GPU that
+// loads the library.  Host code must not use the symbol's host-side name as a
+// pointer; the device address is looked up once per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+kvq_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return fail(KVQ_ERR_UNSUPPORTED, "device index >= 64");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return KVQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -244,6 +269,24 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, con
   cudaError_t e = kvq::launch_decode(P, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KVQ_OK;
+}
+
+kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_paging* paging, const void* q,
+                                   int32_t dtype, int32_t num_q_heads, float softmax_scale, float* out,
+                                   int32_t num_splits, int32_t* dev_error, void* stream) {
+  size_t need = 0;
+  kvq_status st = kvq_decode_workspace_size(cache, paging, num_q_heads, num_splits, &need, nullptr);
+  if (st != KVQ_OK) return st;
+  if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) {
+    char msg[160];
+    std::snprintf(msg, sizeof(msg), "decode needs %zu bytes of scratch; the static scratch holds %u",
+                  need, (unsigned)KVQ_NOALLOC_SCRATCH_BYTES);
+    return fail(KVQ_ERR_WORKSPACE, msg);
+  }
+  void* ws = nullptr;
+  if ((st = noalloc_scratch(&ws)) != KVQ_OK) return st;
+  return kvq_decode_attn(cache, paging, q, dtype, num_q_heads, softmax_scale, out, ws,
+                         (size_t)KVQ_NOALLOC_SCRATCH_BYTES, num_splits, dev_error, stream);
 }
 
 kvq_status kvq_prefill_attn(const kvq_cache* cache, const kvq_paging* paging, const void* q, int32_t dtype,
