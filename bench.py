@@ -304,7 +304,7 @@ def run_gpu(args, rank, world, local_rank):
         "config": {"workload": wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
                    "context": "uniform[1024,8192]", "cached_tokens": int(wl.seq_lens.sum()),
-                   "pool_blocks": wl.num_blocks, "rht": True, "decode_splits": st["splits"],
+                   "pool_blocks": wl.num_blocks, "rht": True, "decode_workers": st["splits"],
                    "timing": "CUDA graphs of the write call and the decode call, events around each replay",
                    "l2": "flushed between timed steps (256 MB write); packed KV 321 MB also exceeds L2",
                    "parallelism": "replicas only" if world > 1 else "single GPU"},

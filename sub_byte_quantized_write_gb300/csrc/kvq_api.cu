@@ -113,31 +113,10 @@ kvq_status check_q(const kvq_cache* c, const void* q, int32_t dtype, int32_t hq,
   return KVQ_OK;
 }
 
-// Split-KV geometry: `tiles_per_split` 32-key tiles per CTA; the split count
-// covers the longest possible sequence (max_blocks * block_size keys).
-void decode_geometry(const kvq_cache* c, const kvq_paging* p, int32_t want_splits, int* splits, int* tps) {
-  const long long max_keys = (long long)p->max_blocks * c->block_size;
-  const int n_tiles = (int)((max_keys + kvq::DECODE_KEYS_PER_TILE - 1) / kvq::DECODE_KEYS_PER_TILE);
-  int t;
-  if (want_splits > 0) {
-    t = (n_tiles + want_splits - 1) / want_splits;
-  } else {
-    t = 16;  // 512 keys: 4 tiles per warp
-    const int cap = 64;
-    if ((n_tiles + t - 1) / t > cap) t = (n_tiles + cap - 1) / cap;
-  }
-  if (t < 1) t = 1;
-  *tps = t;
-  *splits = (n_tiles + t - 1) / t;
-  if (*splits < 1) *splits = 1;
-  (void)sm_count;
-}
-
-size_t decode_ws_bytes(int batch, int hq, int d, int splits) {
-  const size_t n = (size_t)batch * hq * splits;
-  size_t o = n * d * sizeof(float);
-  o = (o + 255) & ~(size_t)255;
-  return o + n * sizeof(float2);
+kvq::DecodeLayout decode_layout(const kvq_cache* c, const kvq_paging* p, int32_t num_q_heads) {
+  const int group = num_q_heads / c->num_kv_heads;
+  return kvq::decode_ws_layout(p->batch, c->num_kv_heads, group, c->head_dim, sm_count(),
+                               kvq::decode_ctas_per_sm(c->mode, c->head_dim, group));
 }
 
 // Scratch of kvq_decode_attn_noalloc: one static device array per GPU that
@@ -239,10 +218,10 @@ kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_paging* p
   if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
   if (!bytes) return fail(KVQ_ERR_INVALID_ARG, "bytes is NULL");
   if (num_q_heads <= 0 || num_q_heads % cache->num_kv_heads) return fail(KVQ_ERR_INVALID_ARG, "bad num_q_heads");
-  int splits, tps;
-  decode_geometry(cache, paging, num_splits, &splits, &tps);
-  *bytes = decode_ws_bytes(paging->batch, num_q_heads, cache->head_dim, splits);
-  if (splits_used) *splits_used = splits;
+  if (num_q_heads / cache->num_kv_heads > 8) return fail(KVQ_ERR_UNSUPPORTED, "GQA group size above 8");
+  const kvq::DecodeLayout L = decode_layout(cache, paging, num_q_heads);
+  *bytes = L.total;
+  if (splits_used) *splits_used = num_splits > 0 ? (num_splits < L.nwall ? num_splits : L.nwall) : L.nwall;
   return KVQ_OK;
 }
 
@@ -254,19 +233,23 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, con
   if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
   if (paging->batch == 0) return KVQ_OK;
   if ((st = check_q(cache, q, dtype, num_q_heads, out)) != KVQ_OK) return st;
-  if (cache->num_kv_heads > 65535) return fail(KVQ_ERR_UNSUPPORTED, "num_kv_heads > 65535");
-  int splits, tps;
-  decode_geometry(cache, paging, num_splits, &splits, &tps);
-  const size_t need = decode_ws_bytes(paging->batch, num_q_heads, cache->head_dim, splits);
-  if (!workspace || workspace_bytes < need) return fail(KVQ_ERR_WORKSPACE, "workspace missing or too small");
+  if ((long long)paging->batch * cache->num_kv_heads + 1 > 0x7FFFFFFFLL)
+    return fail(KVQ_ERR_UNSUPPORTED, "batch * num_kv_heads too large");
+  const kvq::DecodeLayout L = decode_layout(cache, paging, num_q_heads);
+  if (!workspace || workspace_bytes < L.total) return fail(KVQ_ERR_WORKSPACE, "workspace missing or too small");
   if (!aligned(workspace, 256)) return fail(KVQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   kvq::AttnParams P = attn_params(cache, paging, q, dtype, num_q_heads, softmax_scale, out, dev_error);
-  P.num_splits = splits;
-  P.tiles_per_split = tps;
-  const size_t n = (size_t)paging->batch * num_q_heads * splits;
-  P.part_o = static_cast<float*>(workspace);
-  P.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + ((n * cache->head_dim * 4 + 255) & ~(size_t)255));
-  cudaError_t e = kvq::launch_decode(P, static_cast<cudaStream_t>(stream));
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  kvq::DecodeWs ws;
+  ws.tile_start = reinterpret_cast<int*>(w + L.off_tile_start);
+  ws.qfrag = reinterpret_cast<uint32_t*>(w + L.off_qfrag);
+  ws.qbg = reinterpret_cast<float4*>(w + L.off_qbg);
+  ws.part_ml = reinterpret_cast<float2*>(w + L.off_part_ml);
+  ws.part_o = reinterpret_cast<float*>(w + L.off_part_o);
+  ws.n_partials = L.n_partials;
+  ws.nwall = L.nwall;
+  ws.fixed_workers = num_splits > 0 ? num_splits : 0;
+  cudaError_t e = kvq::launch_decode(P, ws, L.grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KVQ_OK;
 }

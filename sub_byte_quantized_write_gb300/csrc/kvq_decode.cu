@@ -12,9 +12,22 @@
 // vllm-ascend-quantized-kv-cache METADATA ("Ascend INT8 KV Cache Plugin"),
 // 运行机制 (decode dequantises inside the attention kernel).
 //
-// Design (GB300): one CTA of 4 warps per (sequence, kv head, split).  Each
-// warp streams 32-key tiles (two 16-row page chunks each of K and V) through
-// its own cp.async ring in shared memory and keeps its own online softmax.
+// Design (GB300), three kernels per call:
+//  1. decode_prep_kernel: per (sequence, kv head) the count of 32-key tiles
+//     it must visit (sliding-window heads: sink tiles + window tiles) and its
+//     exclusive prefix sum over all (sequence, kv head) pairs; per pair the
+//     query fragments (q' split hi / lo, in the lane order of the MMA operand)
+//     and the per-head logit constants (for INT4 also the constant that the
+//     folded key unpack adds: 72 * sum of the query operand).
+//  2. decode_stream_kernel: persistent warps.  The concatenated tile lists of
+//     all pairs are cut into one contiguous, equal slice per warp
+//     ("stream-K"), so the work is balanced to within a tile whatever the
+//     context lengths.  Each warp streams its 32-key tiles (two 16-row page
+//     chunks each of K and V) through its own cp.async ring in shared memory,
+//     keeps its own online softmax, and writes one partial per pair its slice
+//     touches (no CTA-wide barrier in the loop).
+//  3. decode_reduce_kernel: per (sequence, q head) the log-sum-exp merge of
+//     the partials, the inverse RHT and 1 / l.
 // The RHT and the dequantisation are folded into the query and the weights:
 //   q . k_j = (s_j (q' . c_j) + z_j sum(q')) / D,   q' = H (d * q)
 //   sum_j P_j v_j = d * H( sum_j (P_j s_j) c_j + sum_j P_j z_j ) / D
@@ -27,8 +40,7 @@
 // the fp16 operands do not limit accuracy.  Signed (centred) codes keep the
 // fp32 accumulators small: with unsigned codes the P.V accumulator and the
 // zero-point sum grow large with opposite signs and their rounding errors no
-// longer cancel over tens of thousands of keys.  A second kernel merges the
-// splits (log-sum-exp) and applies the inverse RHT.
+// longer cancel over tens of thousands of keys.
 
 #include <math_constants.h>
 
@@ -127,6 +139,17 @@ __device__ __forceinline__ uint32_t kpair(uint32_t w) {
   }
 }
 
+// INT4 key pairs without the subtraction: every nibble is moved to bits 4-7
+// of its half and OR-ed into 64.0, giving 64 + u = 72 + (u - 8) exactly; the
+// constant 72 * sum(q'') per head is removed after the dot product (the
+// query side supplies it).  Same pair-to-dims map as kpair.
+template <int P>
+__device__ __forceinline__ uint32_t kpair_int4_fold(uint32_t w) {
+  const uint32_t src = P == 0 ? (w << 4) : P == 1 ? w : P == 2 ? (w >> 4) : (w >> 8);
+  return lop3_and_or(src, 0x00F000F0u, 0x54005400u);
+}
+constexpr float KFOLD_INT4 = 72.0f;
+
 template <int MODE>
 __device__ __forceinline__ void kpair_dims(int w, int P, int& d0, int& d1) {
   if (MODE == MODE_INT4) { d0 = 8 * w + P; d1 = d0 + 4; }
@@ -176,76 +199,116 @@ struct Unroll<0, MODE> {
 };
 
 // ---------------------------------------------------------------------------
+// Visible tile list of one (sequence, kv head): tiles [0, ns) and [tw, n_total)
+// when a sliding window leaves a gap after the sink tiles, else [0, n_total).
 
-template <int MODE, int D, int NT>
-__global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(AttnParams P) {
-  using C = DecCfg<MODE, D>;
-  constexpr int EPL = D / 32;
-  constexpr int NH = 4 * NT;  // head slots of the CTA (g <= NH)
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;  // mma groupID / thread-in-group
-  const int G = P.group, Hq = P.num_q_heads, S = P.num_splits, Hkv = P.num_kv_heads;
-  const int bs = P.block_size;
+struct TileList {
+  int L, Leff, W, ns, tw, n_total, n_virt;
+  bool gap;
+};
 
-  // smem carve-up: stage rings | q hi/lo (fp16) | per-head constants | chunk validity
-  uint8_t* rings = smem;
-  __half* qh = reinterpret_cast<__half*>(smem + DECODE_WARPS * C::NSTAGE * C::STAGE);  // [2][NH][D]
-  float* qbeta = reinterpret_cast<float*>(qh + 2 * NH * D);                            // [NH]
-  float* qgamma = qbeta + NH;                                                           // [NH]
-  int* vld = reinterpret_cast<int*>(qgamma + NH);                                       // [4][NSTAGE]
-
-  // ---- visible tile list of this (sequence, kv head)
+__device__ __forceinline__ TileList tile_list(const AttnParams& P, int b, int h, bool flag_errors) {
+  TileList t;
   int L = __ldg(P.seq_lens + b);
   if (L < 0) {
-    if (threadIdx.x == 0) flag_error(P.dev_error, DEVERR_SEQ_LEN);
+    if (flag_errors) flag_error(P.dev_error, DEVERR_SEQ_LEN);
     L = 0;
   }
-  const int p_q = L - 1;  // query position
-  int Leff = L;
-  if (Leff > P.max_blocks * bs) {
-    if (threadIdx.x == 0 && split == 0) flag_error(P.dev_error, DEVERR_TABLE_RANGE);
-    Leff = P.max_blocks * bs;
+  t.L = L;
+  t.Leff = L;
+  if (t.Leff > P.max_blocks * P.block_size) {
+    if (flag_errors) flag_error(P.dev_error, DEVERR_TABLE_RANGE);
+    t.Leff = P.max_blocks * P.block_size;
   }
-  const int W = P.window ? __ldg(P.window + h) : 0;
-  const int n_total = (Leff + 31) >> 5;
-  int ns = 0, tw = 0;
-  bool gap = false;
-  if (W > 0) {
-    const int kw = p_q - W + 1;  // first key of the window
+  t.W = P.window ? __ldg(P.window + h) : 0;
+  t.n_total = (t.Leff + DECODE_KEYS_PER_TILE - 1) / DECODE_KEYS_PER_TILE;
+  t.ns = 0;
+  t.tw = 0;
+  t.gap = false;
+  if (t.W > 0) {
+    const int kw = (L - 1) - t.W + 1;  // first key inside the window of the query at L - 1
     if (kw > 0) {
-      const int sk = min(P.sink, Leff);
-      ns = (sk + 31) >> 5;
-      tw = kw >> 5;
-      gap = tw > ns;
+      t.ns = (min(P.sink, t.Leff) + DECODE_KEYS_PER_TILE - 1) / DECODE_KEYS_PER_TILE;
+      t.tw = kw / DECODE_KEYS_PER_TILE;
+      t.gap = t.tw > t.ns;
     }
   }
-  const int n_virt = gap ? ns + (n_total - tw) : n_total;
-  const int v0 = split * P.tiles_per_split;
-  const int v1 = min(n_virt, v0 + P.tiles_per_split);
-  const size_t part_base = ((size_t)b * Hq + (size_t)h * G) * S + split;  // + i * S for head i
-  if (v0 >= v1) {
-    if (threadIdx.x < G) P.part_ml[part_base + (size_t)threadIdx.x * S] = make_float2(-CUDART_INF_F, 0.0f);
+  t.n_virt = t.gap ? t.ns + (t.n_total - t.tw) : t.n_total;
+  return t;
+}
+
+__device__ __forceinline__ int tile_of(const TileList& t, int v) {
+  return (t.gap && v >= t.ns) ? t.tw + (v - t.ns) : v;
+}
+
+// Number of stream warps actually used for T tiles: at least MIN tiles each.
+__device__ __forceinline__ int stream_workers(int T, int nwall, int fixed) {
+  if (fixed > 0) return max(1, min(fixed, nwall));
+  return max(1, min(nwall, T / DECODE_MIN_TILES_PER_WARP));
+}
+__device__ __forceinline__ int slice_lo(int w, int T, int nw) { return (int)((long long)w * T / nw); }
+// The worker whose slice holds global tile x.
+__device__ __forceinline__ int worker_of(int x, int T, int nw) {
+  return min(nw - 1, (int)(((long long)(x + 1) * nw - 1) / T));
+}
+
+// ---------------------------------------------------------------------------
+// 1. preparation
+
+template <int MODE, int D, int NT>
+__global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs ws) {
+  using C = DecCfg<MODE, D>;
+  constexpr int EPL = D / 32;
+  constexpr int NH = 4 * NT;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = P.num_kv_heads, G = P.group, Hq = P.num_q_heads;
+  const int BH = P.batch * Hkv;
+  __shared__ __half qh[2][NH][D];
+  __shared__ int wsum[4];
+
+  // partial records of this call start empty (l = 0)
+  const long long nml = (long long)ws.n_partials * G;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nml; i += (long long)gridDim.x * blockDim.x)
+    ws.part_ml[i] = make_float2(-CUDART_INF_F, 0.0f);
+
+  if (blockIdx.x == 0) {
+    // exclusive prefix sum of the tile counts over (sequence, kv head)
+    int running = 0;
+    for (int base = 0; base < BH; base += 128) {
+      const int bh = base + threadIdx.x;
+      int n = 0;
+      if (bh < BH) n = tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0).n_virt;
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      int before = running;
+      for (int w = 0; w < warp; ++w) before += wsum[w];
+      if (bh < BH) ws.tile_start[bh] = before + incl - n;
+      running += wsum[0] + wsum[1] + wsum[2] + wsum[3];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) ws.tile_start[BH] = running;
     return;
   }
-  const int trow = P.headwise ? b * Hkv + h : b;
-  const int32_t* tbl = P.table + (size_t)trow * P.max_blocks;
-  const uint8_t* kbase = P.k_pages + (size_t)h * bs * C::R;
-  const uint8_t* vbase = P.v_pages + (size_t)h * bs * C::R;
-  const size_t blk_stride = (size_t)Hkv * bs * C::R;
 
-  // ---- query preparation (once per CTA): q' = H(d * q) (or q * channel
-  // scale for INT8), scaled by a power of two, split into fp16 hi + lo.
+  // query fragments of one (sequence, kv head)
+  const int bh = blockIdx.x - 1;
+  if (bh >= BH) return;
+  const int b = bh / Hkv, h = bh % Hkv;
   const float log2e = 1.4426950408889634f;
   const float dnorm = (MODE != MODE_INT8 && P.signs) ? (float)D : 1.0f;
-  for (int i = warp; i < NH; i += DECODE_WARPS) {
+  for (int i = warp; i < NH; i += 4) {
     float x[EPL];
     if (i < G) {
       const int hq = h * G + i;
       load_row_elems<EPL>(P.q, P.dtype, ((size_t)b * Hq + hq) * D + lane * EPL, x);
       if constexpr (MODE == MODE_INT8) {
-        const float* am = P.ch_amax + (size_t)h * D + lane * EPL;  // K scales
+        const float* am = P.ch_amax + (size_t)h * D + lane * EPL;  // K channel scales
 #pragma unroll
         for (int e = 0; e < EPL; ++e) x[e] *= __fdiv_rn(am[e], 127.0f);
       } else {
@@ -274,118 +337,259 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
     for (int e = 0; e < EPL; ++e) {
       const float v = x[e] * sc;
       const __half hi = __float2half_rn(v);
-      const __half lo = __float2half_rn(v - __half2float(hi));
-      qh[(0 * NH + i) * D + lane * EPL + e] = hi;
-      qh[(1 * NH + i) * D + lane * EPL + e] = lo;
+      qh[0][i][lane * EPL + e] = hi;
+      qh[1][i][lane * EPL + e] = __float2half_rn(v - __half2float(hi));
     }
+    // sum of the exact operand values (hi + lo) for the folded key offset
+    float opsum = 0.0f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+      opsum += __half2float(qh[0][i][lane * EPL + e]) + __half2float(qh[1][i][lane * EPL + e]);
+    opsum = warp_sum(opsum);
     if (lane == 0) {
-      qbeta[i] = i < G ? P.softmax_scale * log2e / (dnorm * sc) : 0.0f;
-      qgamma[i] = i < G ? P.softmax_scale * log2e * sum / dnorm : 0.0f;
+      const float beta = i < G ? P.softmax_scale * log2e / (dnorm * sc) : 0.0f;
+      const float gamma = i < G ? P.softmax_scale * log2e * sum / dnorm : 0.0f;
+      const float corr = MODE == MODE_INT4 ? KFOLD_INT4 * opsum : 0.0f;
+      ws.qbg[(size_t)bh * NH + i] = make_float4(beta, gamma, corr, 0.0f);
     }
   }
   __syncthreads();
-
-  // B fragments of QK^T: slot gq of n-tile nt = head 4*nt + gq/2, half gq&1.
-  uint32_t bq[NT][C::KSTEPS][2];
-  float bet[NT], gam[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int head = 4 * nt + (gq >> 1);
-    const __half* src = qh + ((gq & 1) * NH + head) * D;
-#pragma unroll
-    for (int s = 0; s < C::KSTEPS; ++s) {
-      const int w = 4 * (s / C::KPW) + tq, sig = s % C::KPW;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        int d0, d1;
-        kpair_dims<MODE>(w, 2 * sig + r, d0, d1);
-        const __half2 pr = __halves2half2(src[d0], src[d1]);
-        bq[nt][s][r] = *reinterpret_cast<const uint32_t*>(&pr);
-      }
-    }
-    bet[nt] = qbeta[4 * nt + tq];
-    gam[nt] = qgamma[4 * nt + tq];
+  // B-operand image: [lane][nt][kstep][reg]; slot gq of n-tile nt = head
+  // 4 nt + gq/2, half gq & 1; the register pairs head dims in the order the
+  // key-side unpack produces them (kpair_dims).
+  constexpr int PER_LANE = NT * C::KSTEPS * 2;
+  uint32_t* dst = ws.qfrag + (size_t)bh * 32 * PER_LANE;
+  for (int idx = threadIdx.x; idx < 32 * PER_LANE; idx += blockDim.x) {
+    const int ln = idx / PER_LANE, rest = idx % PER_LANE;
+    const int nt = rest / (C::KSTEPS * 2), s = (rest / 2) % C::KSTEPS, r = rest & 1;
+    const int g_ = ln >> 2, t_ = ln & 3;
+    const int head = 4 * nt + (g_ >> 1), hl = g_ & 1;
+    const int w = 4 * (s / C::KPW) + t_, sig = s % C::KPW;
+    int d0, d1;
+    kpair_dims<MODE>(w, 2 * sig + r, d0, d1);
+    const __half2 pr = __halves2half2(qh[hl][head][d0], qh[hl][head][d1]);
+    dst[idx] = *reinterpret_cast<const uint32_t*>(&pr);
   }
+}
 
-  // ---- this warp's tiles: virtual indices v0 + warp, v0 + warp + 4, ...
-  const int first = v0 + warp;
-  const int n_my = first < v1 ? (v1 - first + DECODE_WARPS - 1) / DECODE_WARPS : 0;
-  uint8_t* ring = rings + warp * C::NSTAGE * C::STAGE;
-  int* wvld = vld + warp * C::NSTAGE;
+// ---------------------------------------------------------------------------
+// 2. stream kernel
 
-  auto tile_of = [&](int k) {
-    const int v = first + DECODE_WARPS * k;
-    return (gap && v >= ns) ? tw + (v - ns) : v;
+// Ring depth and residency: NT == 1 kernels run 4 CTAs per SM (3 for INT8's
+// larger rows), NT == 2 kernels 2 CTAs per SM; the ring is sized to fit.
+template <int MODE, int D, int NT>
+struct StreamCfg {
+  static constexpr int NSTAGE = NT == 1 ? (MODE == MODE_INT4 ? 3 : (MODE == MODE_INT2 ? 5 : 2))
+                                        : (MODE == MODE_INT4 ? 4 : (MODE == MODE_INT2 ? 6 : 3));
+  static constexpr int CTAS = NT == 1 ? (MODE == MODE_INT8 ? 3 : 4) : 2;
+};
+
+// One (sequence, kv head) as seen by a cursor walking the global tile order.
+struct Seg {
+  int bh, start, end;
+  TileList t;
+  const int32_t* tbl;
+};
+
+__device__ __forceinline__ void load_seg(const AttnParams& P, const int* tile_start, int bh, Seg& s) {
+  const int Hkv = P.num_kv_heads;
+  s.bh = bh;
+  s.start = __ldg(tile_start + bh);
+  s.end = __ldg(tile_start + bh + 1);
+  const int b = bh / Hkv, h = bh % Hkv;
+  s.t = tile_list(P, b, h, false);
+  s.tbl = P.table + (size_t)(P.headwise ? bh : b) * P.max_blocks;
+}
+
+template <int MODE, int D, int NT>
+__global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_stream_kernel(AttnParams P, DecodeWs ws) {
+  using C = DecCfg<MODE, D>;
+  constexpr int NSTAGE = StreamCfg<MODE, D, NT>::NSTAGE;
+  constexpr int NH = 4 * NT;
+  constexpr int PER_LANE = NT * C::KSTEPS * 2;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int G = P.group, Hkv = P.num_kv_heads, bs = P.block_size;
+  const int BH = P.batch * Hkv;
+
+  const int T = __ldg(ws.tile_start + BH);
+  const int nw = stream_workers(T, gridDim.x * DECODE_WARPS, ws.fixed_workers);
+  const int gw = blockIdx.x * DECODE_WARPS + warp;
+  if (gw >= nw) return;  // whole warp; the kernel has no CTA-wide barrier
+  const int lo = slice_lo(gw, T, nw), hi = slice_lo(gw + 1, T, nw);
+  if (lo >= hi) return;
+
+  uint8_t* ring = smem + warp * NSTAGE * C::STAGE;
+  int* wvld = reinterpret_cast<int*>(smem + DECODE_WARPS * NSTAGE * C::STAGE) + warp * NSTAGE;
+
+  // first (sequence, kv head) of the slice: the last bh with tile_start[bh] <= lo
+  int a = 0, z = BH;
+  while (z - a > 1) {
+    const int mid = (a + z) >> 1;
+    if (__ldg(ws.tile_start + mid) <= lo) a = mid;
+    else z = mid;
+  }
+  Seg is;  // lookup / issue cursor
+  load_seg(P, ws.tile_start, a, is);
+  Seg cs = is;  // compute cursor
+
+  const size_t blk_stride = (size_t)Hkv * bs * C::R;
+  const int bs_log2 = __ffs(bs) - 1;
+
+  // Table lookups run one tile ahead of the copies that use them, so the
+  // latency of the block-id load overlaps a whole tile of compute.
+  int x_lookup = lo;                 // next tile to look up
+  int nx_h = 0, nx_key = 0, nx_leff = 0;
+  int nx_blk[2] = {0, 0};
+  bool nx_have = false;
+  auto lookup = [&]() {
+    nx_have = x_lookup < hi;
+    if (nx_have) {
+      while (x_lookup >= is.end) load_seg(P, ws.tile_start, is.bh + 1, is);
+      nx_h = is.bh % Hkv;
+      nx_key = DECODE_KEYS_PER_TILE * tile_of(is.t, x_lookup - is.start);
+      nx_leff = is.t.Leff;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int key = nx_key + 16 * c;
+        nx_blk[c] = key < nx_leff ? __ldg(is.tbl + (key >> bs_log2)) : -1;
+      }
+      ++x_lookup;
+    }
   };
 
-  auto issue = [&](int k) {
-    if (k < n_my) {
-      const int T = tile_of(k);
-      uint8_t* kt = ring + (k % C::NSTAGE) * C::STAGE;
+  int st_issue = 0;
+  auto issue = [&]() {
+    if (nx_have) {
+      uint8_t* kt = ring + st_issue * C::STAGE;
       uint8_t* vt = kt + C::TILE;
+      const uint8_t* kbase = P.k_pages + (size_t)nx_h * bs * C::R;
+      const uint8_t* vbase = P.v_pages + (size_t)nx_h * bs * C::R;
       int valid = 0;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int key = 32 * T + 16 * c;
-        bool ok = key < Leff;
-        int blk = 0;
-        if (ok) {
-          blk = __ldg(tbl + key / bs);
-          if (blk < 0) ok = false;  // evicted: never addressed
-          else if (blk >= P.num_blocks) {
-            ok = false;
-            flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
-          }
+        const int key = nx_key + 16 * c;
+        const int blk = nx_blk[c];
+        bool ok = blk >= 0;  // -1: evicted (never addressed) or beyond the sequence
+        if (blk >= P.num_blocks) {
+          ok = false;
+          flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
         }
-        const size_t off = ok ? (size_t)blk * blk_stride + (size_t)(key % bs) * C::R : 0;
+        const size_t off = ok ? (size_t)blk * blk_stride + (size_t)(key & (bs - 1)) * C::R : 0;
         const uint8_t* ks = kbase + off;
         const uint8_t* vs = vbase + off;
         const int nbytes = ok ? 16 : 0;
-        for (int q = lane; q < C::R; q += 32) {
-          int dst;
-          if constexpr (MODE == MODE_INT8) {
-            const int kappa = 16 * c + q / C::PPR;
-            dst = kappa * D + 16 * ((q % C::PPR) ^ ((kappa >> 2) & (C::PPR - 1)));
-          } else {
-            dst = c * C::CHUNK + 16 * q;
+#pragma unroll
+        for (int i = 0; i < (C::R + 31) / 32; ++i) {
+          const int q = lane + 32 * i;  // 16-byte piece of the 16-row chunk
+          if (q < C::R) {
+            int dst;
+            if constexpr (MODE == MODE_INT8) {
+              const int kappa = 16 * c + q / C::PPR;
+              dst = kappa * D + 16 * ((q % C::PPR) ^ ((kappa >> 2) & (C::PPR - 1)));
+            } else {
+              dst = c * C::CHUNK + 16 * q;
+            }
+            cp_async16(kt + dst, ks + 16 * q, nbytes);
+            cp_async16(vt + dst, vs + 16 * q, nbytes);
           }
-          cp_async16(kt + dst, ks + 16 * q, nbytes);
-          cp_async16(vt + dst, vs + 16 * q, nbytes);
         }
         valid |= (ok ? 1 : 0) << c;
       }
-      if (lane == 0) wvld[k % C::NSTAGE] = valid;
+      if (lane == 0) wvld[st_issue] = valid;
+      st_issue = st_issue + 1 == NSTAGE ? 0 : st_issue + 1;
     }
     cp_async_commit();
+    lookup();
   };
 
+  // per-segment state
+  uint32_t bq[NT][C::KSTEPS][2];
+  float bet[NT], gam[NT], kcorr[NT];
   float oacc[NT][C::MT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) oacc[nt][mt][r] = 0.0f;
   float mrun[NT], lrun[NT], pmrun[NT];
+  int part_id = 0;
+
+  auto begin_seg = [&](int x) {
+    // partial record id: slice index + pair index (unique, see reduce)
+    part_id = gw + cs.bh;
+    const uint4* src = reinterpret_cast<const uint4*>(ws.qfrag + ((size_t)cs.bh * 32 + lane) * PER_LANE);
+    uint32_t tmp[PER_LANE];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    mrun[nt] = -CUDART_INF_F;
-    lrun[nt] = 0.0f;
-    pmrun[nt] = 0.0f;
-  }
+    for (int i = 0; i < PER_LANE / 4; ++i) {
+      const uint4 v = __ldg(src + i);
+      tmp[4 * i] = v.x; tmp[4 * i + 1] = v.y; tmp[4 * i + 2] = v.z; tmp[4 * i + 3] = v.w;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int s = 0; s < C::KSTEPS; ++s) {
+        bq[nt][s][0] = tmp[(nt * C::KSTEPS + s) * 2];
+        bq[nt][s][1] = tmp[(nt * C::KSTEPS + s) * 2 + 1];
+      }
+      const float4 bg = __ldg(ws.qbg + (size_t)cs.bh * NH + 4 * nt + tq);
+      bet[nt] = bg.x;
+      gam[nt] = bg.y;
+      kcorr[nt] = bg.z;
+      mrun[nt] = -CUDART_INF_F;
+      lrun[nt] = 0.0f;
+      pmrun[nt] = 0.0f;
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) oacc[nt][mt][r] = 0.0f;
+    }
+  };
 
-#pragma unroll 1
-  for (int k = 0; k < C::NSTAGE - 1; ++k) issue(k);
+  auto flush_seg = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float l = lrun[nt], pm = pmrun[nt];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l += __shfl_xor_sync(0xffffffffu, l, o);
+        pm += __shfl_xor_sync(0xffffffffu, pm, o);
+      }
+      const int head = 4 * nt + tq;
+      if (head < G) {
+        float* po = ws.part_o + ((size_t)part_id * G + head) * D;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+          po[gq * (D / 16) + mt] = oacc[nt][mt][0] + oacc[nt][mt][1] + pm;
+          po[(8 + gq) * (D / 16) + mt] = oacc[nt][mt][2] + oacc[nt][mt][3] + pm;
+        }
+        if (gq == 0) ws.part_ml[(size_t)part_id * G + head] = make_float2(mrun[nt], l);
+      }
+    }
+  };
 
+  lookup();
 #pragma unroll 1
-  for (int k = 0; k < n_my; ++k) {
-    cp_async_wait<C::NSTAGE - 2>();
+  for (int k = 0; k < NSTAGE - 1; ++k) issue();
+
+  begin_seg(lo);
+  int st = 0;
+#pragma unroll 1
+  for (int x = lo; x < hi; ++x) {
+    cp_async_wait<NSTAGE - 2>();
     __syncwarp();
-    issue(k + C::NSTAGE - 1);
-    const uint8_t* kt = ring + (k % C::NSTAGE) * C::STAGE;
+    issue();
+    if (x >= cs.end) {
+      flush_seg();
+      do load_seg(P, ws.tile_start, cs.bh + 1, cs);
+      while (x >= cs.end);
+      begin_seg(x);
+    }
+    const uint8_t* kt = ring + st * C::STAGE;
     const uint8_t* vt = kt + C::TILE;
-    const int valid = wvld[k % C::NSTAGE];
-    const int key0 = 32 * tile_of(k);
+    const int valid = wvld[st];
+    st = st + 1 == NSTAGE ? 0 : st + 1;
+    const int key0 = DECODE_KEYS_PER_TILE * tile_of(cs.t, x - cs.start);
+    const int Leff = cs.t.Leff, W = cs.t.W, p_q = cs.t.L - 1;
+    // every key of the tile visible (the common case): no per-key masks
+    const bool full = valid == 3 && key0 + DECODE_KEYS_PER_TILE <= Leff &&
+                      (W <= 0 || key0 > p_q - W || key0 + DECODE_KEYS_PER_TILE <= P.sink);
 
     // ---- S^T = U_K (keys x D) . Q (D x slots); lane rows: keys 4gq + 2m + hh
     float sacc[2][NT][4];
@@ -407,8 +611,18 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
         const int s = C::KPW * wi + sig;
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          const uint32_t a[4] = {kpair<MODE, 2 * sig>(kw[m][0]), kpair<MODE, 2 * sig>(kw[m][1]),
-                                 kpair<MODE, 2 * sig + 1>(kw[m][0]), kpair<MODE, 2 * sig + 1>(kw[m][1])};
+          uint32_t a[4];
+          if constexpr (MODE == MODE_INT4) {
+            a[0] = kpair_int4_fold<2 * sig>(kw[m][0]);
+            a[1] = kpair_int4_fold<2 * sig>(kw[m][1]);
+            a[2] = kpair_int4_fold<2 * sig + 1>(kw[m][0]);
+            a[3] = kpair_int4_fold<2 * sig + 1>(kw[m][1]);
+          } else {
+            a[0] = kpair<MODE, 2 * sig>(kw[m][0]);
+            a[1] = kpair<MODE, 2 * sig>(kw[m][1]);
+            a[2] = kpair<MODE, 2 * sig + 1>(kw[m][0]);
+            a[3] = kpair<MODE, 2 * sig + 1>(kw[m][1]);
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[m][nt], a, bq[nt][s][0], bq[nt][s][1]);
         }
@@ -424,9 +638,12 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int kappa = 4 * gq + 2 * m + hh;
-        const int j = key0 + kappa;
-        bool ok = ((valid >> (kappa >> 4)) & 1) && j < Leff;
-        if (W > 0) ok = ok && (j < P.sink || j > p_q - W);
+        bool ok = true;
+        if (!full) {
+          const int j = key0 + kappa;
+          ok = ((valid >> (kappa >> 4)) & 1) && j < Leff;
+          if (W > 0) ok = ok && (j < P.sink || j > p_q - W);
+        }
         vk[m][hh] = ok;
         float sk = 0.0f, mk = 0.0f;
         if constexpr (MODE != MODE_INT8) {
@@ -443,11 +660,12 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float cdot = sacc[m][nt][2 * hh] + sacc[m][nt][2 * hh + 1];  // hi + lo slots
-          float z;
-          if constexpr (MODE == MODE_INT8) z = bet[nt] * cdot;
-          else z = fmaf(bet[nt] * sk, cdot, gam[nt] * mk);
-          lg[m][hh][nt] = ok ? z : -CUDART_INF_F;
+          float cdot = sacc[m][nt][2 * hh] + sacc[m][nt][2 * hh + 1];  // hi + lo slots
+          if constexpr (MODE == MODE_INT4) cdot -= kcorr[nt];
+          float zz;
+          if constexpr (MODE == MODE_INT8) zz = bet[nt] * cdot;
+          else zz = fmaf(bet[nt] * sk, cdot, gam[nt] * mk);
+          lg[m][hh][nt] = ok ? zz : -CUDART_INF_F;
         }
       }
 
@@ -482,9 +700,9 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
           if constexpr (MODE != MODE_INT8) tpm += ok ? p * mv_[m][hh] : 0.0f;
           wv[hh] = ok ? p * sv_[m][hh] : 0.0f;
         }
-        const __half h0 = __float2half_rn(wv[0]), h1 = __float2half_rn(wv[1]);
-        const __half2 hp = __halves2half2(h0, h1);
-        const __half2 lp = __floats2half2_rn(wv[0] - __half2float(h0), wv[1] - __half2float(h1));
+        const __half2 hp = __floats2half2_rn(wv[0], wv[1]);
+        const float2 hf = __half22float2(hp);
+        const __half2 lp = __floats2half2_rn(wv[0] - hf.x, wv[1] - hf.y);
         xh[nt][m] = *reinterpret_cast<const uint32_t*>(&hp);
         xl[nt][m] = *reinterpret_cast<const uint32_t*>(&lp);
       }
@@ -524,94 +742,58 @@ __global__ void __launch_bounds__(128, (NT == 1 ? 3 : 2)) decode_split_kernel(At
       });
     }
   }
-
-  // ---- per-warp totals, then merge the 4 warps of the CTA
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      lrun[nt] += __shfl_xor_sync(0xffffffffu, lrun[nt], o);
-      pmrun[nt] += __shfl_xor_sync(0xffffffffu, pmrun[nt], o);
-    }
-  }
+  flush_seg();
   cp_async_wait<0>();
-  __syncthreads();
-  float* osm = reinterpret_cast<float*>(rings);               // [4][NH][2][D]
-  float* stat = osm + DECODE_WARPS * NH * 2 * D;               // [4][NH][3]
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int head = 4 * nt + tq;
-#pragma unroll
-    for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int rg = (r < 2) ? gq : 8 + gq;
-        const int d = rg * (D / 16) + mt;
-        osm[((warp * NH + head) * 2 + (r & 1)) * D + d] = oacc[nt][mt][r];
-      }
-    if (gq == 0) {
-      float* st = stat + (warp * NH + head) * 3;
-      st[0] = mrun[nt];
-      st[1] = lrun[nt];
-      st[2] = pmrun[nt];
-    }
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int i = idx / D, d = idx % D;
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < DECODE_WARPS; ++w) M = fmaxf(M, stat[(w * NH + i) * 3]);
-    const size_t pidx = part_base + (size_t)i * S;
-    if (M == -CUDART_INF_F) {
-      if (d == 0) P.part_ml[pidx] = make_float2(-CUDART_INF_F, 0.0f);
-      continue;
-    }
-    float o = 0.0f, l = 0.0f, pm = 0.0f;
-#pragma unroll
-    for (int w = 0; w < DECODE_WARPS; ++w) {
-      const float* st = stat + (w * NH + i) * 3;
-      const float f = ex2(st[0] - M);
-      o += f * (osm[((w * NH + i) * 2 + 0) * D + d] + osm[((w * NH + i) * 2 + 1) * D + d]);
-      l += f * st[1];
-      pm += f * st[2];
-    }
-    P.part_o[pidx * D + d] = o + pm;
-    if (d == 0) P.part_ml[pidx] = make_float2(M, l);
-  }
 }
 
-// Merge the splits of one (sequence, q head): log-sum-exp weights, then the
-// inverse RHT (d * H o / D) or the INT8 value-channel scales, then 1 / l.
+// ---------------------------------------------------------------------------
+// 3. merge of the partials of one (sequence, q head) + inverse RHT
+
 template <int D>
-__global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P) {
+__global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, DecodeWs ws) {
   constexpr int EPL = D / 32;
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int Hq = P.num_q_heads, S = P.num_splits;
+  const int Hq = P.num_q_heads, G = P.group, Hkv = P.num_kv_heads;
   if (wid >= (long long)P.batch * Hq) return;
-  const int hq = (int)(wid % Hq);
-  const int h = hq / P.group;
-  const size_t base = (size_t)wid * S;
+  const int b = (int)(wid / Hq), hq = (int)(wid % Hq);
+  const int h = hq / G, i = hq % G;
+  const int bh = b * Hkv + h;
+  const int BH = P.batch * Hkv;
   float* out = P.out + (size_t)wid * D;
-  float M = -CUDART_INF_F;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, P.part_ml[base + s].x);
-  M = warp_max(M);
+  const int T = __ldg(ws.tile_start + BH);
+  const int start = __ldg(ws.tile_start + bh), end = __ldg(ws.tile_start + bh + 1);
   float o[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
+  if (start >= end) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = 0.0f;
+    return;
+  }
+  // the slices holding this pair's tiles are workers w_first .. w_last; the
+  // record of (worker w, pair bh) is w + bh
+  const int nw = stream_workers(T, ws.nwall, ws.fixed_workers);
+  const int w0 = worker_of(start, T, nw), w1 = worker_of(end - 1, T, nw);
+  float M = -CUDART_INF_F;
+  for (int w = w0 + lane; w <= w1; w += 32) {
+    const float2 ml = ws.part_ml[(size_t)(w + bh) * G + i];
+    if (ml.y > 0.0f) M = fmaxf(M, ml.x);
+  }
+  M = warp_max(M);
   if (M == -CUDART_INF_F) {
 #pragma unroll
     for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = 0.0f;
     return;
   }
   float l = 0.0f;
-  for (int s = 0; s < S; ++s) {
-    const float2 ml = P.part_ml[base + s];
-    if (ml.y == 0.0f) continue;
+  for (int w = w0; w <= w1; ++w) {
+    const size_t rec = (size_t)(w + bh) * G + i;
+    const float2 ml = ws.part_ml[rec];
+    if (!(ml.y > 0.0f)) continue;
     const float f = ex2(ml.x - M);
     l += f * ml.y;
-    const float* po = P.part_o + (base + s) * D;
+    const float* po = ws.part_o + rec * D;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] += f * po[lane + 32 * e];
   }
@@ -642,7 +824,7 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P) {
       out[d] = (__ldg(P.signs + d) < 0 ? -o[e] : o[e]) * inv;
     }
   } else if (P.mode == MODE_INT8) {
-    const float* am = P.ch_amax + ((size_t)1 * P.num_kv_heads + h) * D;  // V scales
+    const float* am = P.ch_amax + ((size_t)Hkv + h) * D;  // V channel scales
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
       const int d = lane + 32 * e;
@@ -654,19 +836,25 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// launch
+
 template <int MODE, int D, int NT>
-size_t decode_smem_bytes() {
+size_t stream_smem_bytes() {
   using C = DecCfg<MODE, D>;
-  constexpr int NH = 4 * NT;
-  const size_t rings = (size_t)DECODE_WARPS * C::NSTAGE * C::STAGE;
-  const size_t merge = (size_t)DECODE_WARPS * NH * 2 * D * 4 + DECODE_WARPS * NH * 3 * 4;
-  const size_t first = rings > merge ? rings : merge;
-  return first + 2 * NH * D * 2 + 2 * NH * 4 + DECODE_WARPS * C::NSTAGE * 4;
+  constexpr int NSTAGE = StreamCfg<MODE, D, NT>::NSTAGE;
+  return (size_t)DECODE_WARPS * NSTAGE * C::STAGE + DECODE_WARPS * NSTAGE * 4;
+}
+
+int decode_ctas_per_sm(int mode, int head_dim, int group) {
+  (void)head_dim;
+  if (group > 4) return StreamCfg<MODE_INT4, 128, 2>::CTAS;
+  return mode == MODE_INT8 ? StreamCfg<MODE_INT8, 128, 1>::CTAS : StreamCfg<MODE_INT4, 128, 1>::CTAS;
 }
 
 template <int MODE, int D, int NT>
-cudaError_t launch_decode_t(const AttnParams& P, cudaStream_t stream) {
-  const size_t smem = decode_smem_bytes<MODE, D, NT>();
+cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream) {
+  const size_t smem = stream_smem_bytes<MODE, D, NT>();
   // the opt-in shared-memory size is set once per device (not inside later
   // calls, which may be captured into a CUDA graph)
   static bool attr_set[64] = {false};
@@ -674,33 +862,36 @@ cudaError_t launch_decode_t(const AttnParams& P, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_split_kernel<MODE, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(decode_stream_kernel<MODE, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  dim3 grid(P.num_splits, P.num_kv_heads, P.batch);
-  decode_split_kernel<MODE, D, NT><<<grid, 128, smem, stream>>>(P);
+  const int BH = P.batch * P.num_kv_heads;
+  decode_prep_kernel<MODE, D, NT><<<BH + 1, 128, 0, stream>>>(P, ws);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_stream_kernel<MODE, D, NT><<<grid, 128, smem, stream>>>(P, ws);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long warps = (long long)P.batch * P.num_q_heads;
-  decode_reduce_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(P);
+  decode_reduce_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(P, ws);
   return cudaGetLastError();
 }
 
 template <int MODE, int D>
-cudaError_t launch_decode_md(const AttnParams& P, cudaStream_t stream) {
-  if (P.group <= 4) return launch_decode_t<MODE, D, 1>(P, stream);
-  return launch_decode_t<MODE, D, 2>(P, stream);
+cudaError_t launch_decode_md(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream) {
+  if (P.group <= 4) return launch_decode_t<MODE, D, 1>(P, ws, grid, stream);
+  return launch_decode_t<MODE, D, 2>(P, ws, grid, stream);
 }
 
-cudaError_t launch_decode(const AttnParams& P, cudaStream_t stream) {
+cudaError_t launch_decode(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream) {
   switch (P.mode * 1000 + P.head_dim) {
-    case MODE_INT4 * 1000 + 128: return launch_decode_md<MODE_INT4, 128>(P, stream);
-    case MODE_INT4 * 1000 + 64: return launch_decode_md<MODE_INT4, 64>(P, stream);
-    case MODE_INT2 * 1000 + 128: return launch_decode_md<MODE_INT2, 128>(P, stream);
-    case MODE_INT2 * 1000 + 64: return launch_decode_md<MODE_INT2, 64>(P, stream);
-    case MODE_INT8 * 1000 + 128: return launch_decode_md<MODE_INT8, 128>(P, stream);
-    case MODE_INT8 * 1000 + 64: return launch_decode_md<MODE_INT8, 64>(P, stream);
+    case MODE_INT4 * 1000 + 128: return launch_decode_md<MODE_INT4, 128>(P, ws, grid, stream);
+    case MODE_INT4 * 1000 + 64: return launch_decode_md<MODE_INT4, 64>(P, ws, grid, stream);
+    case MODE_INT2 * 1000 + 128: return launch_decode_md<MODE_INT2, 128>(P, ws, grid, stream);
+    case MODE_INT2 * 1000 + 64: return launch_decode_md<MODE_INT2, 64>(P, ws, grid, stream);
+    case MODE_INT8 * 1000 + 128: return launch_decode_md<MODE_INT8, 128>(P, ws, grid, stream);
+    case MODE_INT8 * 1000 + 64: return launch_decode_md<MODE_INT8, 64>(P, ws, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

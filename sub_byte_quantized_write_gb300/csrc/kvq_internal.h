@@ -42,21 +42,58 @@ struct AttnParams {
   float softmax_scale;
   float* out;
   int32_t* dev_error;
-  // decode
-  int num_splits, tiles_per_split;  // tiles of 32 keys
-  float* part_o;                    // [B][Hq][S][D]
-  float2* part_ml;                  // [B][Hq][S]  (max in log2 units, sum)
   // prefill
   const int32_t* cu_q;
   int total_q, max_q_per_seq;
 };
 
-cudaError_t launch_write(const WriteParams& P, cudaStream_t stream);
-cudaError_t launch_decode(const AttnParams& P, cudaStream_t stream);
-cudaError_t launch_prefill(const AttnParams& P, cudaStream_t stream);
+// Decode workspace (caller-owned scratch), carved by decode_ws_layout.
+struct DecodeWs {
+  int* tile_start;     // [B*Hkv + 1] exclusive prefix sum of visible 32-key tiles
+  uint32_t* qfrag;     // [B*Hkv][32 lanes][NT * D/16 * 2] query B-operand images
+  float4* qbg;         // [B*Hkv][4*NT] per-head logit constants (beta, gamma, key fold, 0)
+  float2* part_ml;     // [n_partials][G] (running max in log2 units, sum of weights)
+  float* part_o;       // [n_partials][G][D] unnormalised partial outputs
+  int n_partials;      // stream workers + B*Hkv
+  int nwall;           // stream warps launched
+  int fixed_workers;   // > 0: use exactly this many workers
+};
 
 // Split-KV geometry shared by the host API and the kernels.
 constexpr int DECODE_KEYS_PER_TILE = 32;
 constexpr int DECODE_WARPS = 4;
+constexpr int DECODE_MIN_TILES_PER_WARP = 8;
+
+struct DecodeLayout {
+  size_t off_tile_start, off_qfrag, off_qbg, off_part_ml, off_part_o, total;
+  int grid, nwall, n_partials;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace layout for one decode call; sm_count * ctas_per_sm CTAs of 4 warps.
+inline DecodeLayout decode_ws_layout(int batch, int num_kv_heads, int group, int head_dim, int sm_count,
+                                     int ctas_per_sm) {
+  DecodeLayout L;
+  const int BH = batch * num_kv_heads;
+  const int NT = group <= 4 ? 1 : 2;
+  L.grid = sm_count * ctas_per_sm;
+  L.nwall = L.grid * DECODE_WARPS;
+  L.n_partials = L.nwall + BH;
+  size_t o = 0;
+  L.off_tile_start = o; o = align256(o + (size_t)(BH + 1) * 4);
+  L.off_qfrag = o;      o = align256(o + (size_t)BH * 32 * NT * (head_dim / 16) * 2 * 4);
+  L.off_qbg = o;        o = align256(o + (size_t)BH * 4 * NT * 16);
+  L.off_part_ml = o;    o = align256(o + (size_t)L.n_partials * group * 8);
+  L.off_part_o = o;     o = align256(o + (size_t)L.n_partials * group * head_dim * 4);
+  L.total = o;
+  return L;
+}
+
+int decode_ctas_per_sm(int mode, int head_dim, int group);
+
+cudaError_t launch_write(const WriteParams& P, cudaStream_t stream);
+cudaError_t launch_decode(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream);
+cudaError_t launch_prefill(const AttnParams& P, cudaStream_t stream);
 
 }  // namespace kvq

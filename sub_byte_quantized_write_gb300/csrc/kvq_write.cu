@@ -24,39 +24,53 @@
 
 namespace kvq {
 
-// Sequence b that owns token t: the largest b with cu[b] <= t.
-__device__ __forceinline__ int find_seq(const int32_t* __restrict__ cu, int batch, int t) {
-  int lo = 0, hi = batch;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(cu + mid) <= t) lo = mid;
-    else hi = mid;
+// Destination row of (token t, kv head h) for every lane of the warp;
+// nullptr when the row is dropped (-1 sentinel) or invalid (error bit set).
+// The owning sequence is found with one round of parallel loads: lane j
+// holds cu[j + 32 i] and ballots whether it is <= t (cu is non-decreasing,
+// so the ballot's population count locates the sequence).
+__device__ __forceinline__ uint8_t* dest_row(const WriteParams& P, uint8_t* pages, int t, int h, int lane) {
+  int b = -1, cu_b = 0, cu_b1 = 0, L = 0;
+  int prev_c = 0, prev_l = 0;  // cu and seq_lens at the previous chunk's last lane
+  for (int base = 0; base <= P.batch; base += 32) {
+    const int j = base + lane;
+    const int cj = j <= P.batch ? __ldg(P.cu_new + j) : 0x7FFFFFFF;
+    const int lj = j < P.batch ? __ldg(P.seq_lens + j) : 0;
+    const int cnt = __popc(__ballot_sync(0xffffffffu, cj <= t));
+    if (cnt < 32) {  // the last entry <= t is in this chunk, or ended the previous one
+      if (cnt == 0) {
+        b = base - 1;
+        cu_b = prev_c;
+        L = prev_l;
+        cu_b1 = __shfl_sync(0xffffffffu, cj, 0);
+      } else {
+        b = base + cnt - 1;
+        cu_b = __shfl_sync(0xffffffffu, cj, cnt - 1);
+        L = __shfl_sync(0xffffffffu, lj, cnt - 1);
+        cu_b1 = __shfl_sync(0xffffffffu, cj, cnt);
+      }
+      break;
+    }
+    prev_c = __shfl_sync(0xffffffffu, cj, 31);
+    prev_l = __shfl_sync(0xffffffffu, lj, 31);
   }
-  return lo;
-}
-
-// Resolve the destination row of (token t, head h); returns nullptr when the
-// row is dropped (sentinel) or invalid (error bit set).
-__device__ __forceinline__ uint8_t* dest_row(const WriteParams& P, uint8_t* pages, int t, int h) {
-  if (t >= __ldg(P.cu_new + P.batch)) return nullptr;
-  const int b = find_seq(P.cu_new, P.batch, t);
-  const int n = __ldg(P.cu_new + b + 1) - __ldg(P.cu_new + b);
-  const int L = __ldg(P.seq_lens + b);
+  if (b < 0 || b >= P.batch || t >= cu_b1) return nullptr;  // token outside every sequence
+  const int n = cu_b1 - cu_b;
   if (L < 0 || n > L) {
-    flag_error(P.dev_error, DEVERR_SEQ_LEN);
+    if (lane == 0) flag_error(P.dev_error, DEVERR_SEQ_LEN);
     return nullptr;
   }
-  const int p = L - n + (t - __ldg(P.cu_new + b));
+  const int p = L - n + (t - cu_b);
   const int row = P.headwise ? b * P.num_kv_heads + h : b;
   const int lb = p / P.block_size;
   if (lb >= P.max_blocks) {
-    flag_error(P.dev_error, DEVERR_TABLE_RANGE);
+    if (lane == 0) flag_error(P.dev_error, DEVERR_TABLE_RANGE);
     return nullptr;
   }
   const int blk = __ldg(P.table + (size_t)row * P.max_blocks + lb);
   if (blk < 0) return nullptr;  // evicted slot: nothing is written
   if (blk >= P.num_blocks) {
-    flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
+    if (lane == 0) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
     return nullptr;
   }
   const int R = row_bytes_of(P.mode, P.head_dim);
@@ -87,11 +101,10 @@ __global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
   const int h = (int)(th % P.num_kv_heads);
   const long long t = th / P.num_kv_heads;
   if (t >= P.num_tokens) return;
-  uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h);
-  if (dst == nullptr) return;  // warp-uniform
-
-  float x[EPL];
+  float x[EPL];  // issued before the (dependent) table lookups
   load_row_elems<EPL>(kv ? P.v : P.k, P.dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, x);
+  uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h, lane);
+  if (dst == nullptr) return;  // warp-uniform
   if (P.signs) {
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
@@ -165,10 +178,10 @@ __global__ void __launch_bounds__(256) int8_quant_kernel(WriteParams P) {
   const int h = (int)(th % P.num_kv_heads);
   const long long t = th / P.num_kv_heads;
   if (t >= P.num_tokens) return;
-  uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h);
-  if (dst == nullptr) return;
   float x[EPL];
   load_row_elems<EPL>(kv ? P.v : P.k, P.dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, x);
+  uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h, lane);
+  if (dst == nullptr) return;
   const float* am = P.ch_amax + ((size_t)kv * P.num_kv_heads + h) * D + lane * EPL;
   uint32_t bits = 0;
 #pragma unroll

@@ -54,15 +54,17 @@ def test_noalloc_decode_matches_workspace_decode_twice():
 
 
 def test_noalloc_rejects_oversized_calls():
+    """A batch large enough that its partials and query images exceed the
+    static scratch is refused before any launch."""
     K = kvq()
-    wl = gen.custom(gen.MODE_INT4, 64, 8, 128, 16, "bf16", seq_lens=[16] * 4, n_new=[1] * 4, seed=1,
-                    max_blocks=131072 // 16)
+    B, Hkv, Hq = 4096, 8, 64
+    wl = gen.custom(gen.MODE_INT4, Hq, Hkv, 128, 16, "bf16", seq_lens=[16] * 4, n_new=[1] * 4, seed=1)
     c = build_case(wl)
-    big = K.Paging(torch.from_numpy(np.repeat(wl.seq_lens, 64)).cuda(),
-                   block_tables=torch.from_numpy(np.repeat(wl.table, 64, axis=0)).cuda())
-    q = torch.zeros((256, 64, 128), dtype=torch.bfloat16, device="cuda")
-    out = torch.empty((256, 64, 128), dtype=torch.float32, device="cuda")
-    need, _ = K.kvq_decode_workspace_size(c.gcache, big, 64)
+    big = K.Paging(torch.full((B,), 16, dtype=torch.int32, device="cuda"),
+                   block_tables=torch.zeros((B, 1), dtype=torch.int32, device="cuda"))
+    q = torch.zeros((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    need, _ = K.kvq_decode_workspace_size(c.gcache, big, Hq)
     assert need > (32 << 20)
     assert _noalloc_via_c_abi(K, c.gcache, big, q, 0.1, out) == K.KVQ_ERR_WORKSPACE
     assert b"static scratch" in K.lib().kvq_last_error()
