@@ -69,7 +69,7 @@ def algorithmic_bytes(wl: gen.Workload) -> dict:
 def recorded_traffic(src_hash: str):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "decode_split_llama_int4.md")
+    p = os.path.join(ROOT, "profiles", "decode_stream_llama_int4.md")
     if not os.path.exists(p):
         return None
     vals = {}
@@ -310,14 +310,14 @@ def run_gpu(args, rank, world, local_rank):
                    "parallelism": "replicas only" if world > 1 else "single GPU"},
         "effective_kv_GBps": round(ab["decode"] / (dec / 1e3) / 1e9, 1),
         "decode_ms": round(dec, 5), "write_ms": round(sum(wr_ms) / len(wr_ms), 5),
-        "roofline": {"bound": "hbm", "kernel": "decode attention (split-KV + merge, one kvq_decode_attn call)",
+        "roofline": {"bound": "hbm", "kernel": "decode attention (query prep + stream-K split-KV + merge, one kvq_decode_attn call)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind + " (copy bandwidth)",
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "frac_of_nominal_8000": round(achieved / 8000.0, 4),
                      "algorithmic_bytes_per_launch": ab["decode"], "traffic": traffic},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(sum(e2e_ms) / len(e2e_ms), 5)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,  # write + (prep, stream, merge) per step
         "clocks": clk.summary(),
     }
     return result, wl

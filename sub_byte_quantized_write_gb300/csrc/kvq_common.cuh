@@ -9,7 +9,7 @@ namespace kvq {
 
 enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2 };
 enum { DT_F32 = 0, DT_BF16 = 1 };
-enum { DEVERR_BLOCK_RANGE = 1, DEVERR_TABLE_RANGE = 2, DEVERR_SEQ_LEN = 4 };
+enum { DEVERR_BLOCK_RANGE = 1, DEVERR_TABLE_RANGE = 2, DEVERR_SEQ_LEN = 4, DEVERR_TIMEOUT = 8 };
 
 __host__ __device__ constexpr int mode_bits(int mode) { return mode == MODE_INT4 ? 4 : (mode == MODE_INT2 ? 2 : 8); }
 __host__ __device__ constexpr int data_bytes(int mode, int D) { return D * mode_bits(mode) / 8; }
@@ -149,6 +149,57 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+
+// ---------------------------------------------------------------------------
+// mbarrier + 1-D bulk (TMA) copies.  Every wait is bounded: after
+// WAIT_LIMIT_CYCLES of polling the caller gets `false` and must report an
+// error instead of spinning on.
+
+constexpr long long WAIT_LIMIT_CYCLES = 1000000000LL;  // about 0.5 s at 2 GHz
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) return false;
+  return true;
+}
+// global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte
+// aligned), completion counted on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while its predecessor runs; it must call
+// grid_dependency_wait() before touching anything the predecessor writes.
+// The predecessor lets it launch early with allow_dependent_launch().
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }

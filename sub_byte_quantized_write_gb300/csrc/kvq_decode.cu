@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
   const int BH = P.batch * Hkv;
   __shared__ __half qh[2][NH][D];
   __shared__ int wsum[4];
+  allow_dependent_launch();  // the stream kernel may launch; it waits for this grid to finish
 
   // partial records of this call start empty (l = 0)
   const long long nml = (long long)ws.n_partials * G;
@@ -386,7 +387,7 @@ struct StreamCfg {
 
 // One (sequence, kv head) as seen by a cursor walking the global tile order.
 struct Seg {
-  int bh, start, end;
+  int bh, h, start, end;
   TileList t;
   const int32_t* tbl;
 };
@@ -397,6 +398,7 @@ __device__ __forceinline__ void load_seg(const AttnParams& P, const int* tile_st
   s.start = __ldg(tile_start + bh);
   s.end = __ldg(tile_start + bh + 1);
   const int b = bh / Hkv, h = bh % Hkv;
+  s.h = h;
   s.t = tile_list(P, b, h, false);
   s.tbl = P.table + (size_t)(P.headwise ? bh : b) * P.max_blocks;
 }
@@ -413,15 +415,31 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   const int G = P.group, Hkv = P.num_kv_heads, bs = P.block_size;
   const int BH = P.batch * Hkv;
 
-  const int T = __ldg(ws.tile_start + BH);
+  grid_dependency_wait();    // tile prefix sums, query images and cleared partials are ready
+  allow_dependent_launch();  // the merge kernel may launch; it waits for this grid to finish
+  const int T = ws.tile_start[BH];
   const int nw = stream_workers(T, gridDim.x * DECODE_WARPS, ws.fixed_workers);
   const int gw = blockIdx.x * DECODE_WARPS + warp;
   if (gw >= nw) return;  // whole warp; the kernel has no CTA-wide barrier
   const int lo = slice_lo(gw, T, nw), hi = slice_lo(gw + 1, T, nw);
   if (lo >= hi) return;
 
+  // INT4 / INT2 pages move by 1-D bulk copies (one per 16-row chunk, tracked
+  // by a per-stage mbarrier); INT8 rows are XOR-swizzled by 16-byte piece on
+  // the way in, so they use per-lane cp.async.
+  constexpr bool BULK = MODE != MODE_INT8;
   uint8_t* ring = smem + warp * NSTAGE * C::STAGE;
   int* wvld = reinterpret_cast<int*>(smem + DECODE_WARPS * NSTAGE * C::STAGE) + warp * NSTAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * NSTAGE * C::STAGE + DECODE_WARPS * NSTAGE * 4) +
+                   warp * NSTAGE;
+  if constexpr (BULK) {
+    if (lane == 0) {
+      for (int i = 0; i < NSTAGE; ++i) mbar_init(bars + i, 1);
+      mbar_init_fence();
+    }
+    __syncwarp();
+  }
+  uint32_t phase_bits = 0;  // parity of the next completion to wait for, per stage
 
   // first (sequence, kv head) of the slice: the last bh with tile_start[bh] <= lo
   int a = 0, z = BH;
@@ -447,7 +465,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
     nx_have = x_lookup < hi;
     if (nx_have) {
       while (x_lookup >= is.end) load_seg(P, ws.tile_start, is.bh + 1, is);
-      nx_h = is.bh % Hkv;
+      nx_h = is.h;
       nx_key = DECODE_KEYS_PER_TILE * tile_of(is.t, x_lookup - is.start);
       nx_leff = is.t.Leff;
 #pragma unroll
@@ -467,6 +485,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
       const uint8_t* kbase = P.k_pages + (size_t)nx_h * bs * C::R;
       const uint8_t* vbase = P.v_pages + (size_t)nx_h * bs * C::R;
       int valid = 0;
+      size_t off[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int key = nx_key + 16 * c;
@@ -474,33 +493,46 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
         bool ok = blk >= 0;  // -1: evicted (never addressed) or beyond the sequence
         if (blk >= P.num_blocks) {
           ok = false;
-          flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
+          if (lane == 0) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
         }
-        const size_t off = ok ? (size_t)blk * blk_stride + (size_t)(key & (bs - 1)) * C::R : 0;
-        const uint8_t* ks = kbase + off;
-        const uint8_t* vs = vbase + off;
-        const int nbytes = ok ? 16 : 0;
-#pragma unroll
-        for (int i = 0; i < (C::R + 31) / 32; ++i) {
-          const int q = lane + 32 * i;  // 16-byte piece of the 16-row chunk
-          if (q < C::R) {
-            int dst;
-            if constexpr (MODE == MODE_INT8) {
-              const int kappa = 16 * c + q / C::PPR;
-              dst = kappa * D + 16 * ((q % C::PPR) ^ ((kappa >> 2) & (C::PPR - 1)));
-            } else {
-              dst = c * C::CHUNK + 16 * q;
-            }
-            cp_async16(kt + dst, ks + 16 * q, nbytes);
-            cp_async16(vt + dst, vs + 16 * q, nbytes);
-          }
-        }
+        off[c] = ok ? (size_t)blk * blk_stride + (size_t)(key & (bs - 1)) * C::R : 0;
         valid |= (ok ? 1 : 0) << c;
       }
-      if (lane == 0) wvld[st_issue] = valid;
+      if constexpr (BULK) {
+        if (lane == 0) {
+          wvld[st_issue] = valid;
+          const uint32_t bytes = (uint32_t)(__popc(valid) * 2 * C::CHUNK);
+          mbar_arrive_expect_tx(bars + st_issue, bytes);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            if ((valid >> c) & 1) {
+              bulk_g2s(kt + c * C::CHUNK, kbase + off[c], C::CHUNK, bars + st_issue);
+              bulk_g2s(vt + c * C::CHUNK, vbase + off[c], C::CHUNK, bars + st_issue);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint8_t* ks = kbase + off[c];
+          const uint8_t* vs = vbase + off[c];
+          const int nbytes = ((valid >> c) & 1) ? 16 : 0;
+#pragma unroll
+          for (int i = 0; i < (C::R + 31) / 32; ++i) {
+            const int q = lane + 32 * i;  // 16-byte piece of the 16-row chunk
+            if (q < C::R) {
+              const int kappa = 16 * c + q / C::PPR;
+              const int dst = kappa * D + 16 * ((q % C::PPR) ^ ((kappa >> 2) & (C::PPR - 1)));
+              cp_async16(kt + dst, ks + 16 * q, nbytes);
+              cp_async16(vt + dst, vs + 16 * q, nbytes);
+            }
+          }
+        }
+        if (lane == 0) wvld[st_issue] = valid;
+      }
       st_issue = st_issue + 1 == NSTAGE ? 0 : st_issue + 1;
     }
-    cp_async_commit();
+    if constexpr (!BULK) cp_async_commit();
     lookup();
   };
 
@@ -570,9 +602,23 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
 
   begin_seg(lo);
   int st = 0;
+  // per-lane shared-memory offsets (loop invariant): key rows 4gq + 2m + hh,
+  // value rows 8tq + 4m' + 2h' + e
+  const int koff = 4 * gq * C::R + 4 * tq;
+  const int poff = 4 * gq * C::R + C::DATA;
+  const int vrow = 8 * tq * C::R;
+  bool timed_out = false;
 #pragma unroll 1
   for (int x = lo; x < hi; ++x) {
-    cp_async_wait<NSTAGE - 2>();
+    if constexpr (BULK) {
+      if (!mbar_wait_bounded(bars + st, (phase_bits >> st) & 1)) {
+        timed_out = true;
+        break;
+      }
+      phase_bits ^= 1u << st;
+    } else {
+      cp_async_wait<NSTAGE - 2>();
+    }
     __syncwarp();
     issue();
     if (x >= cs.end) {
@@ -605,7 +651,10 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) kw[m][hh] = load_kword<MODE, D>(kt, 4 * gq + 2 * m + hh, 4 * wi + tq);
+        for (int hh = 0; hh < 2; ++hh) {
+          if constexpr (MODE == MODE_INT8) kw[m][hh] = load_kword<MODE, D>(kt, 4 * gq + 2 * m + hh, 4 * wi + tq);
+          else kw[m][hh] = lds32(kt + koff + (2 * m + hh) * C::R + 16 * wi);
+        }
       Unroll<C::KPW, MODE>::run([&](auto sig_c) {
         constexpr int sig = decltype(sig_c)::value;
         const int s = C::KPW * wi + sig;
@@ -647,8 +696,8 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
         vk[m][hh] = ok;
         float sk = 0.0f, mk = 0.0f;
         if constexpr (MODE != MODE_INT8) {
-          const uint32_t pk = lds32(kt + kappa * C::R + C::DATA);
-          const uint32_t pv = lds32(vt + kappa * C::R + C::DATA);
+          const uint32_t pk = lds32(kt + poff + (2 * m + hh) * C::R);
+          const uint32_t pv = lds32(vt + poff + (2 * m + hh) * C::R);
           constexpr float half_range = (float)(1 << (C::BITS - 1));
           sk = __half2float(__ushort_as_half((unsigned short)(pk & 0xFFFF)));
           mk = fmaf(half_range, sk, __half2float(__ushort_as_half((unsigned short)(pk >> 16))));
@@ -729,9 +778,14 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
       for (int hp = 0; hp < 2; ++hp)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int kappa = 8 * tq + 4 * mp + 2 * hp + e;
-          vl[hp][e] = load_range<MODE, D>(vt, kappa, gq);
-          vh[hp][e] = load_range<MODE, D>(vt, kappa, 8 + gq);
+          if constexpr (MODE == MODE_INT8) {
+            const int kappa = 8 * tq + 4 * mp + 2 * hp + e;
+            vl[hp][e] = load_range<MODE, D>(vt, kappa, gq);
+            vh[hp][e] = load_range<MODE, D>(vt, kappa, 8 + gq);
+          } else {
+            vl[hp][e] = load_range<MODE, D>(vt + vrow + (4 * mp + 2 * hp + e) * C::R, 0, gq);
+            vh[hp][e] = load_range<MODE, D>(vt + vrow + (4 * mp + 2 * hp + e) * C::R, 0, 8 + gq);
+          }
         }
       Unroll<C::MT, MODE>::run([&](auto mt_c) {
         constexpr int mt = decltype(mt_c)::value;
@@ -742,8 +796,16 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
       });
     }
   }
+  if (timed_out) {
+    // a copy never arrived: report it, give the copies in flight one more
+    // bounded chance to land, and leave without writing this slice's partial
+    if (lane == 0) flag_error(P.dev_error, DEVERR_TIMEOUT);
+    if constexpr (BULK)
+      for (int i = 0; i < NSTAGE; ++i) (void)mbar_wait_bounded(bars + i, (phase_bits >> i) & 1);
+    return;
+  }
   flush_seg();
-  cp_async_wait<0>();
+  if constexpr (!BULK) cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -761,7 +823,8 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
   const int bh = b * Hkv + h;
   const int BH = P.batch * Hkv;
   float* out = P.out + (size_t)wid * D;
-  const int T = __ldg(ws.tile_start + BH);
+  grid_dependency_wait();  // every partial of the stream kernel is written
+  const int T = ws.tile_start[BH];
   const int start = __ldg(ws.tile_start + bh), end = __ldg(ws.tile_start + bh + 1);
   float o[EPL];
 #pragma unroll
@@ -843,13 +906,28 @@ template <int MODE, int D, int NT>
 size_t stream_smem_bytes() {
   using C = DecCfg<MODE, D>;
   constexpr int NSTAGE = StreamCfg<MODE, D, NT>::NSTAGE;
-  return (size_t)DECODE_WARPS * NSTAGE * C::STAGE + DECODE_WARPS * NSTAGE * 4;
+  return (size_t)DECODE_WARPS * NSTAGE * C::STAGE + DECODE_WARPS * NSTAGE * 4 + DECODE_WARPS * NSTAGE * 8;
 }
 
 int decode_ctas_per_sm(int mode, int head_dim, int group) {
   (void)head_dim;
   if (group > 4) return StreamCfg<MODE_INT4, 128, 2>::CTAS;
   return mode == MODE_INT8 ? StreamCfg<MODE_INT8, 128, 1>::CTAS : StreamCfg<MODE_INT4, 128, 1>::CTAS;
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_dependent(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int MODE, int D, int NT>
@@ -870,12 +948,12 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
   decode_prep_kernel<MODE, D, NT><<<BH + 1, 128, 0, stream>>>(P, ws);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_stream_kernel<MODE, D, NT><<<grid, 128, smem, stream>>>(P, ws);
-  e = cudaGetLastError();
+  // the stream and merge kernels launch programmatically: their CTAs become
+  // resident while the previous kernel drains and wait on its completion
+  e = launch_dependent(decode_stream_kernel<MODE, D, NT>, dim3(grid), dim3(128), smem, stream, P, ws);
   if (e != cudaSuccess) return e;
   const long long warps = (long long)P.batch * P.num_q_heads;
-  decode_reduce_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(P, ws);
-  return cudaGetLastError();
+  return launch_dependent(decode_reduce_kernel<D>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, P, ws);
 }
 
 template <int MODE, int D>

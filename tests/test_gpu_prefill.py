@@ -52,7 +52,11 @@ def test_prefill_single_query_equals_decode():
     q = q_host(wl)
     gd = decode_gpu(c, q)
     gp = prefill_gpu(c, q)
-    assert np.max(np.abs(gd - gp)) <= 1e-5
+    # Same fold and the same fp16 hi/lo operands on both paths; they differ
+    # only in fp32 summation order (32-key mma.sync tiles vs 64-key tcgen05
+    # tiles with a tensor-core accumulation order), i.e. a few ulps of
+    # outputs of size ~1 summed over ~1e3 keys.
+    assert np.max(np.abs(gd - gp)) <= 5e-5
 
 
 def test_prefill_full_size_sampled_rows():
