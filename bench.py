@@ -39,37 +39,28 @@ METRIC = "INT4 paged decode tokens/s and effective KV GB/s (% of GB300 HBM peak)
 UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, kind) from the measured-peaks file, else the fallback."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def algorithmic_bytes(wl: gen.Workload) -> dict:
-    """Bytes the decode step must move at minimum: every visible packed K and
-    V row once (row_bytes each), the block-table entries of the visible pages
-    (per kv head), q in and out, plus the write of one token per sequence."""
-    R = wl.head_dim // 2 + 4
-    Hkv, bs = wl.num_kv_heads, wl.block_size
-    ctx = wl.seq_lens.astype(np.int64)
-    kv_rows = int(ctx.sum()) * Hkv
-    pages = int(((ctx + bs - 1) // bs).sum()) * Hkv
-    q_bytes = wl.batch * wl.num_q_heads * wl.head_dim * 2
-    out_bytes = wl.batch * wl.num_q_heads * wl.head_dim * 4
-    decode = kv_rows * R * 2 + pages * 4 + q_bytes + out_bytes
-    write = wl.batch * Hkv * 2 * (wl.head_dim * 2 + R)
-    return {"decode": decode, "write": write, "kv_only": kv_rows * R * 2}
+def row_bytes(mode: int, D: int) -> int:
+    """Bytes of one cache row: packed codes plus the fp16 scale / zero-point pad (INT8: codes only)."""
+    return {gen.MODE_INT4: D // 2 + 4, gen.MODE_INT2: D // 4 + 4, gen.MODE_INT8: D}[mode]
 
 
-def recorded_traffic(src_hash: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "decode_stream_llama_int4.md")
+def recorded_units(profile: str, key: str, src_hash: str):
+    """A per-launch figure (DRAM bytes) from a committed ncu summary, if that
+    summary was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", profile)
     if not os.path.exists(p):
         return None
     vals = {}
@@ -81,14 +72,14 @@ def recorded_traffic(src_hash: str):
     if vals.get("kernel_source_sha256") != src_hash:
         return None
     try:
-        return float(vals["dram_bytes_per_decode_call"])
+        return float(vals[key])
     except (KeyError, ValueError):
         return None
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files) -> str:
     h = hashlib.sha256()
-    for fn in ("kvq_decode.cu", "kvq_common.cuh", "kvq_internal.h"):
+    for fn in files:
         with open(os.path.join(ROOT, "sub_byte_quantized_write_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -150,40 +141,107 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# GPU arm
+# workloads
+
+WORKLOADS = {
+    # name: (factory, metric, kind)
+    "llama_int4": (lambda a: gen.llama_int4(seed=0, num_blocks=a.pool_blocks or 200000), METRIC, "decode"),
+    "ernie_int2": (lambda a: gen.ernie_int2(seed=0, num_blocks=a.pool_blocks or 100000),
+                   "INT2 paged decode tokens/s and effective KV GB/s (% of GB300 HBM peak)", "decode"),
+    "qwen_int8_headwise": (lambda a: gen.qwen_int8_headwise(seed=0),
+                           "INT8 head-wise paged decode tokens/s and effective KV GB/s (% of GB300 HBM peak)",
+                           "decode"),
+    "prefill_int4": (lambda a: gen.prefill_int4(seed=0, prefixes=tuple(a.prefill_prefixes), chunk=a.prefill_chunk,
+                                                num_blocks=a.pool_blocks or 200000),
+                     "INT4 chunked-prefill tokens/s (causal attention over the paged cache, % of tensor peak)",
+                     "prefill"),
+}
+
+
+def visible_keys(wl, b, h, p):
+    """Keys a query at position p of sequence b sees in kv head h."""
+    W = 0 if wl.window is None else int(wl.window[h])
+    if W > 0 and p - W + 1 > wl.sink:
+        return min(wl.sink, p + 1) + W
+    return p + 1
+
+
+def algorithmic_units(wl: gen.Workload) -> dict:
+    """Decode: bytes the call must move at minimum (every visible packed K and
+    V row once, the table entries of the visible pages per kv head, q in, out
+    out).  Prefill: tensor FLOPs of causal attention, 4 D per visible (query,
+    key) pair per q head.  Write: bf16 K/V in, packed rows out."""
+    R = row_bytes(wl.mode, wl.head_dim)
+    Hkv, bs, D, G = wl.num_kv_heads, wl.block_size, wl.head_dim, wl.group
+    n_new = int(wl.n_new.sum())
+    write = n_new * Hkv * 2 * (D * 2 + R)
+    if wl.step == "decode":
+        rows = pages = 0
+        for b in range(wl.batch):
+            p = int(wl.seq_lens[b]) - 1
+            for h in range(Hkv):
+                vis = visible_keys(wl, b, h, p)
+                rows += vis
+                pages += (vis + bs - 1) // bs
+        q_bytes = wl.batch * wl.num_q_heads * D * 2
+        out_bytes = wl.batch * wl.num_q_heads * D * 4
+        return {"decode": rows * R * 2 + pages * 4 + q_bytes + out_bytes, "write": write, "kv_only": rows * R * 2}
+    pairs = 0
+    for b in range(wl.batch):
+        L, n = int(wl.seq_lens[b]), int(wl.n_new[b])
+        for h in range(Hkv):
+            if wl.window is None or int(wl.window[h]) <= 0:
+                pairs += n * (L - n) + n * (n + 1) // 2
+            else:
+                pairs += sum(visible_keys(wl, b, h, p) for p in range(L - n, L))
+    return {"prefill_flops": 4 * D * pairs * G, "write": write}
+
 
 def setup_gpu(wl, device, want_splits=0):
+    """Cache with every sequence's prefix written (untimed, values drawn on
+    the device), plus the step's inputs: the new tokens, the queries and the
+    outputs / decode workspace."""
     import torch
     import sub_byte_quantized_write_gb300 as K
-    signs = torch.from_numpy(wl.signs).to(device)
+    signs = None if wl.signs is None else torch.from_numpy(wl.signs).to(device)
     cache = K.PagedCache(wl.mode, wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, signs, device)
     table = torch.from_numpy(wl.table).to(device)
+    win = None if wl.window is None else torch.from_numpy(wl.window).to(device)
+
+    def paging(lens_t):
+        if wl.headwise:
+            return K.Paging(lens_t, block_tables_headwise=table, window_per_kv_head=win, sink_size=wl.sink)
+        return K.Paging(lens_t, block_tables=table, window_per_kv_head=win, sink_size=wl.sink)
+
     pre = wl.prefix_lens
-    pag_pre = K.Paging(torch.from_numpy(pre).to(device), block_tables=table)
-    # prefix (untimed): write each sequence's cached tokens, drawn on the device
     B = wl.batch
-    chunk = 16
-    for b0 in range(0, B, chunk):
-        bsel = list(range(b0, min(B, b0 + chunk)))
-        ks = [gen.kv_values_device(wl, "k", b, 0, int(pre[b]), device) for b in bsel]
-        vs = [gen.kv_values_device(wl, "v", b, 0, int(pre[b]), device) for b in bsel]
+    # INT8: the first write defines the channel scales, so the whole prefix goes in one call
+    groups = [list(range(B))] if wl.mode == gen.MODE_INT8 else [list(range(b0, min(B, b0 + 16))) for b0 in range(0, B, 16)]
+    pag_pre = paging(torch.from_numpy(np.ascontiguousarray(pre, np.int32)).to(device))
+    for bsel in groups:
         counts = np.zeros(B, np.int32)
         counts[bsel] = pre[bsel]
-        cu = torch.from_numpy(wl.cu(counts)).to(device)
-        K.kvq_write(cache, pag_pre, torch.cat(ks), torch.cat(vs), cu)
+        if counts.sum() == 0:
+            continue
+        ks = torch.cat([gen.kv_values_device(wl, "k", b, 0, int(pre[b]), device) for b in bsel if pre[b] > 0])
+        vs = torch.cat([gen.kv_values_device(wl, "v", b, 0, int(pre[b]), device) for b in bsel if pre[b] > 0])
+        K.kvq_write(cache, pag_pre, ks, vs, torch.from_numpy(wl.cu(counts)).to(device))
+        del ks, vs
     torch.cuda.synchronize()
     step = {
-        "k": torch.cat([gen.kv_values_device(wl, "k", b, int(pre[b]), 1, device) for b in range(B)]).contiguous(),
-        "v": torch.cat([gen.kv_values_device(wl, "v", b, int(pre[b]), 1, device) for b in range(B)]).contiguous(),
+        "k": torch.cat([gen.kv_values_device(wl, "k", b, int(pre[b]), int(wl.n_new[b]), device) for b in range(B)]).contiguous(),
+        "v": torch.cat([gen.kv_values_device(wl, "v", b, int(pre[b]), int(wl.n_new[b]), device) for b in range(B)]).contiguous(),
         "q": gen.q_values_device(wl, device).contiguous(),
         "cu": torch.from_numpy(wl.cu(wl.n_new)).to(device),
         "seq_lens": torch.from_numpy(wl.seq_lens).to(device),
     }
-    pag = K.Paging(step["seq_lens"], block_tables=table)
-    nbytes, splits = K.kvq_decode_workspace_size(cache, pag, wl.num_q_heads, want_splits)
-    step["ws"] = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    step["out"] = torch.empty((B, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=device)
-    step["splits"] = splits
+    pag = paging(step["seq_lens"])
+    step["out"] = torch.empty(tuple(step["q"].shape), dtype=torch.float32, device=device)
+    step["splits"] = 0
+    if wl.step == "decode":
+        nbytes, splits = K.kvq_decode_workspace_size(cache, pag, wl.num_q_heads, want_splits)
+        step["ws"] = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        step["splits"] = splits
     return cache, pag, step
 
 
@@ -192,39 +250,45 @@ def run_gpu(args, rank, world, local_rank):
     import sub_byte_quantized_write_gb300 as K
     device = "cuda:%d" % local_rank
     torch.cuda.set_device(local_rank)
-    wl = gen.llama_int4(seed=0, num_blocks=args.pool_blocks)
+    factory, metric, kind = WORKLOADS[args.workload]
+    wl = factory(args)
     cache, pag, st = setup_gpu(wl, device, args.splits)
     scale = 1.0 / math.sqrt(wl.head_dim)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device=device)
+    max_q = int(wl.n_new.max())
 
     def write_call():
         K.kvq_write(cache, pag, st["k"], st["v"], st["cu"], stream=stream)
 
-    def decode_call():
-        K.kvq_decode_attn(cache, pag, st["q"], scale, out=st["out"], workspace=st["ws"],
-                          num_splits=st["splits"], stream=stream)
+    def attn_call():
+        if kind == "decode":
+            K.kvq_decode_attn(cache, pag, st["q"], scale, out=st["out"], workspace=st["ws"],
+                              num_splits=st["splits"], stream=stream)
+        else:
+            K.kvq_prefill_attn(cache, pag, st["q"], st["cu"], max_q, scale, out=st["out"], stream=stream)
 
     def step():
         write_call()
-        decode_call()
+        attn_call()
 
     # the step's two library calls are captured once into CUDA graphs and
-    # replayed, so the timed region holds only device work
+    # replayed, so the timed region holds only device work (re-writing the
+    # same new tokens at the same positions is idempotent)
     with torch.cuda.stream(stream):
         for _ in range(2):
             step()  # first calls set the kernels' shared-memory attributes outside capture
         stream.synchronize()
-        g_write, g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        g_write, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_write, stream=stream):
             write_call()
-        with torch.cuda.graph(g_decode, stream=stream):
-            decode_call()
+        with torch.cuda.graph(g_attn, stream=stream):
+            attn_call()
     for _ in range(args.warmup):
         with torch.cuda.stream(stream):
             flush.fill_(1.0)
         g_write.replay()
-        g_decode.replay()
+        g_attn.replay()
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
@@ -235,16 +299,16 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             for i in range(args.steps):
-                flush.fill_(float(i))  # packed KV already exceeds L2; flush so no step reuses the last one's lines
+                flush.fill_(float(i))  # no step reuses the previous step's L2 lines
                 e0, e1, e2 = ev[i]
                 e0.record(stream)
                 g_write.replay()
                 e1.record(stream)
-                g_decode.replay()
+                g_attn.replay()
                 e2.record(stream)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
-    dec_ms = [b.elapsed_time(c) for a, b, c in ev]
+    att_ms = [b.elapsed_time(c) for a, b, c in ev]
     wr_ms = [a.elapsed_time(b) for a, b, c in ev]
     ms = sum(step_ms) / len(step_ms)
     if world > 1:
@@ -252,10 +316,11 @@ def run_gpu(args, rank, world, local_rank):
         t = torch.tensor([ms], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    value = world * wl.batch / (ms / 1e3)
+    tokens = wl.batch if kind == "decode" else int(wl.n_new.sum())
+    value = world * tokens / (ms / 1e3)
 
     # end to end through the C ABI with host buffers: H2D of the step's
-    # inputs from pinned memory, write + decode, D2H of the output
+    # inputs from pinned memory, write + attention, D2H of the output
     hk = st["k"].cpu().pin_memory()
     hv = st["v"].cpu().pin_memory()
     hq = st["q"].cpu().pin_memory()
@@ -289,105 +354,181 @@ def run_gpu(args, rank, world, local_rank):
             c.record(stream)
             c.synchronize()
             e2e_ms.append(a.elapsed_time(c))
-    e2e_value = world * wl.batch / (sum(e2e_ms) / len(e2e_ms) / 1e3)
+    e2e_value = world * tokens / (sum(e2e_ms) / len(e2e_ms) / 1e3)
 
-    ab = algorithmic_bytes(wl)
-    dec = sum(dec_ms) / len(dec_ms)
-    peak, peak_kind = peaks()
-    achieved = ab["decode"] / (dec / 1e3) / 1e9
-    traffic = recorded_traffic(kernel_source_hash())
+    units = algorithmic_units(wl)
+    att = sum(att_ms) / len(att_ms)
+    hbm, tensor, peak_kind = peaks()
+    cfg = {"workload": wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
+           "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+           "mode": {0: "int4", 1: "int2", 2: "int8"}[wl.mode], "headwise_table": bool(wl.headwise),
+           "cached_tokens": int(wl.seq_lens.sum()), "new_tokens_per_step": int(wl.n_new.sum()),
+           "pool_blocks": wl.num_blocks, "rht": wl.signs is not None,
+           "timing": "CUDA graphs of the write call and the attention call, events around each replay",
+           "l2": "flushed between timed steps (256 MB write)",
+           "parallelism": "replicas only" if world > 1 else "single GPU"}
+    if args.workload == "llama_int4":
+        cfg["context"] = "uniform[1024,8192]"
+    if kind == "decode":
+        cfg["decode_workers"] = st["splits"]
+        achieved = units["decode"] / (att / 1e3) / 1e9
+        traffic = recorded_units("decode_stream_%s.md" % args.workload, "dram_bytes_per_decode_call",
+                                 kernel_source_hash(("kvq_decode.cu", "kvq_common.cuh", "kvq_internal.h")))
+        roof = {"bound": "hbm", "kernel": "decode attention (query prep + stream-K split-KV + merge, "
+                                          "one kvq_decode_attn call)",
+                "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind + " (copy bandwidth)",
+                "unit": "GB/s", "frac": round(achieved / hbm, 4), "frac_of_nominal_8000": round(achieved / 8000.0, 4),
+                "algorithmic_bytes_per_launch": units["decode"], "traffic": traffic}
+        extra = {"effective_kv_GBps": round(achieved, 1), "decode_ms": round(att, 5)}
+        launches = 4  # write + (prep, stream, merge)
+        dtype = {0: "u4", 1: "u2", 2: "s8"}[wl.mode] + " codes x fp16 tensor-core math, fp32 accumulate/softmax"
+    else:
+        achieved = units["prefill_flops"] / (att / 1e3) / 1e12
+        traffic = recorded_units("prefill_tc_%s.md" % args.workload, "dram_bytes_per_prefill_call",
+                                 kernel_source_hash(("kvq_prefill_tc.cu", "kvq_tc.cuh", "kvq_common.cuh",
+                                                     "kvq_internal.h")))
+        roof = {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05, one kvq_prefill_attn call)",
+                "achieved": round(achieved, 2), "peak": tensor,
+                "peak_kind": peak_kind + " (cuBLAS bf16 burst; kind::f16 fp16 runs at the bf16 rate)",
+                "unit": "TFLOP/s", "frac": round(achieved / tensor, 4),
+                "executed_tflops": round(2 * achieved, 2),
+                "algorithmic_flops_per_launch": units["prefill_flops"], "traffic": traffic}
+        extra = {"prefill_ms": round(att, 5)}
+        launches = 2  # write + prefill
+        dtype = "u4 codes x fp16 (hi+lo) tcgen05 math, fp32 TMEM accumulate/softmax"
+    if wl.mode == gen.MODE_INT8:
+        launches += 1  # INT8 write: channel-amax kernel (returns at once once the scales exist) + quantise kernel
     result = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u4 codes x fp16 tensor-core math, fp32 accumulate/softmax",
-        "data": "synthetic (seeded; K/V ~ N(0,1) with 1% outlier channels x10)",
-        "config": {"workload": wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
-                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
-                   "context": "uniform[1024,8192]", "cached_tokens": int(wl.seq_lens.sum()),
-                   "pool_blocks": wl.num_blocks, "rht": True, "decode_workers": st["splits"],
-                   "timing": "CUDA graphs of the write call and the decode call, events around each replay",
-                   "l2": "flushed between timed steps (256 MB write); packed KV 321 MB also exceeds L2",
-                   "parallelism": "replicas only" if world > 1 else "single GPU"},
-        "effective_kv_GBps": round(ab["decode"] / (dec / 1e3) / 1e9, 1),
-        "decode_ms": round(dec, 5), "write_ms": round(sum(wr_ms) / len(wr_ms), 5),
-        "roofline": {"bound": "hbm", "kernel": "decode attention (query prep + stream-K split-KV + merge, one kvq_decode_attn call)",
-                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind + " (copy bandwidth)",
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "frac_of_nominal_8000": round(achieved / 8000.0, 4),
-                     "algorithmic_bytes_per_launch": ab["decode"], "traffic": traffic},
+        "vs_baseline": None, "dtype": dtype,
+        "data": "synthetic (seeded; K/V ~ N(0,1)%s)" % (", 1% outlier channels x10" if args.workload in ("llama_int4", "prefill_int4") else ""),
+        "config": cfg, **extra, "write_ms": round(sum(wr_ms) / len(wr_ms), 5),
+        "roofline": roof,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(sum(e2e_ms) / len(e2e_ms), 5)},
-        "gpu_launches": 4 * args.steps,  # write + (prep, stream, merge) per step
+        "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
     }
     return result, wl
 
 
+def _oracle_paging(wl, lens):
+    import oracle
+    return oracle.Paging(wl.table, wl.headwise, np.ascontiguousarray(lens, np.int32), wl.window, wl.sink)
+
+
 def _oracle_step_setup(wl, sample_seqs):
-    """Oracle cache holding the prefixes of the sampled sequences (host values)."""
+    """Oracle cache holding the prefixes of the sampled sequences (host values),
+    and the step's host inputs (bf16 bits) for those sequences."""
     import oracle
     oc = oracle.Cache(wl.mode, wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.signs)
     pre = wl.prefix_lens.copy()
     counts = np.zeros(wl.batch, np.int32)
     counts[sample_seqs] = pre[sample_seqs]
-    lens = pre.copy()
-    ks = [gen.kv_values_host(wl, "k", int(b), 0, int(pre[b])) for b in sample_seqs]
-    vs = [gen.kv_values_host(wl, "v", int(b), 0, int(pre[b])) for b in sample_seqs]
-    oracle.write(oc, oracle.Paging(wl.table, False, lens), gen.f32_to_bf16_bits(np.concatenate(ks)),
-                 gen.f32_to_bf16_bits(np.concatenate(vs)), wl.cu(counts))
-    new_k = gen.f32_to_bf16_bits(np.concatenate([gen.kv_values_host(wl, "k", int(b), int(pre[b]), 1) for b in sample_seqs]))
-    new_v = gen.f32_to_bf16_bits(np.concatenate([gen.kv_values_host(wl, "v", int(b), int(pre[b]), 1) for b in sample_seqs]))
+    ks = [gen.kv_values_host(wl, "k", int(b), 0, int(pre[b])) for b in sample_seqs if pre[b] > 0]
+    vs = [gen.kv_values_host(wl, "v", int(b), 0, int(pre[b])) for b in sample_seqs if pre[b] > 0]
+    if ks:
+        oracle.write(oc, _oracle_paging(wl, pre), gen.f32_to_bf16_bits(np.concatenate(ks)),
+                     gen.f32_to_bf16_bits(np.concatenate(vs)), wl.cu(counts))
+    nk = gen.f32_to_bf16_bits(np.concatenate([gen.kv_values_host(wl, "k", int(b), int(pre[b]), int(wl.n_new[b]))
+                                              for b in sample_seqs]))
+    nv = gen.f32_to_bf16_bits(np.concatenate([gen.kv_values_host(wl, "v", int(b), int(pre[b]), int(wl.n_new[b]))
+                                              for b in sample_seqs]))
     q = gen.f32_to_bf16_bits(gen.q_values_host(wl))
-    return oc, new_k, new_v, q
+    return oc, nk, nv, q
 
 
-def oracle_step(wl, oc, new_k, new_v, q, sample_seqs, threads):
+def oracle_step(wl, oc, new_k, new_v, q, sample_seqs, threads, rows=None):
+    """One step of the oracle on the sampled sequences: write their new
+    tokens, then attention (decode: their one query each; prefill: the
+    sampled query rows `rows` of the chunk)."""
     import oracle
     counts = np.zeros(wl.batch, np.int32)
-    counts[sample_seqs] = 1
-    pag = oracle.Paging(wl.table, False, wl.seq_lens)
+    counts[sample_seqs] = wl.n_new[sample_seqs]
+    pag = _oracle_paging(wl, wl.seq_lens)
     oracle.write(oc, pag, new_k, new_v, wl.cu(counts))
-    oracle.attention(oc, pag, q, 1.0 / math.sqrt(wl.head_dim), rows=np.asarray(sample_seqs, np.int32),
-                     threads=threads)
+    scale = 1.0 / math.sqrt(wl.head_dim)
+    if wl.step == "decode":
+        oracle.attention(oc, pag, q, scale, rows=np.asarray(sample_seqs, np.int32), threads=threads)
+    else:
+        oracle.attention(oc, pag, q, scale, cu_q=wl.cu(wl.n_new), rows=rows, threads=threads)
+
+
+def _prefill_rows(wl, per_seq):
+    """per_seq query rows of each sequence's chunk, evenly spaced (the last
+    row of each chunk, the one that sees the most keys, included)."""
+    cu = wl.cu(wl.n_new)
+    rows = []
+    for b in range(wl.batch):
+        n = int(wl.n_new[b])
+        for i in range(per_seq):
+            rows.append(int(cu[b]) + (n - 1) - (i * n) // per_seq)
+    return np.asarray(sorted(rows), np.int32)
 
 
 def cpu_baseline(wl, budget_s=15.0):
-    """The CPU oracle, as it stands, on a bounded sample of the workload:
-    whole decode steps (write one token + attend with all 32 q heads) of a
-    subset of the sequences, repeated until ~budget_s of work."""
+    """The CPU oracle, as it stands, on a bounded sample of the workload,
+    repeated until ~budget_s of work.  Decode: whole steps (write one token +
+    attend with every q head) of a subset of the sequences.  Prefill: the
+    write of the whole chunk + attention of a few query rows per sequence."""
     threads = os.cpu_count() or 1
-    sample = list(range(0, wl.batch, 4))  # 16 of the 64 sequences
+    if wl.step == "decode":
+        sample = list(range(0, wl.batch, 4))
+        rows = None
+        per_step = len(sample)
+    else:
+        sample = list(range(wl.batch))
+        rows = _prefill_rows(wl, 4)
+        per_step = len(rows)
     oc, nk, nv, q = _oracle_step_setup(wl, sample)
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle_step(wl, oc, nk, nv, q, sample, threads)
+        oracle_step(wl, oc, nk, nv, q, sample, threads, rows)
         n += 1
         if time.perf_counter() - t0 >= budget_s or n >= 50:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(n * len(sample) / dt, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": "%d decode steps of %d of the 64 sequences (every 4th; write 1 token + attention over the "
-                      "cached context, all 32 q heads), %.1f s" % (n, len(sample), dt)}
+    if wl.step == "decode":
+        desc = ("%d decode steps of %d of the %d sequences (every 4th; write 1 token + attention over the cached "
+                "context, all %d q heads), %.1f s" % (n, len(sample), wl.batch, wl.num_q_heads, dt))
+    else:
+        desc = ("%d steps of: write of the %d-token chunk + attention of %d query rows (4 per sequence, all %d q "
+                "heads), %.1f s; tokens/s counts the attended rows" % (n, int(wl.n_new.sum()), per_step,
+                                                                       wl.num_q_heads, dt))
+    return {"value": round(n * per_step / dt, 2), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
 
 
 def run_reference(args):
-    """Reference arm: the CPU oracle timed alone on the same workload."""
-    wl = gen.llama_int4(seed=0)
+    """Reference arm: the CPU oracle timed alone on the same workload (a
+    bounded sample of it per step)."""
+    factory, metric, kind = WORKLOADS[args.workload]
+    wl = factory(args)
     threads = os.cpu_count() or 1
-    sample = list(range(0, wl.batch, 16))  # 4 sequences per step
+    if kind == "decode":
+        sample = list(range(0, wl.batch, 16))
+        rows = None
+        per_step = len(sample)
+        desc = "%d of the %d sequences per step (every 16th): write 1 token + attention, all %d q heads" % (
+            per_step, wl.batch, wl.num_q_heads)
+    else:
+        sample = list(range(wl.batch))
+        rows = _prefill_rows(wl, 1)
+        per_step = len(rows)
+        desc = ("write of the %d-token chunk + attention of the last query row of each sequence, all %d q heads"
+                % (int(wl.n_new.sum()), wl.num_q_heads))
     oc, nk, nv, q = _oracle_step_setup(wl, sample)
     for _ in range(args.warmup):
-        oracle_step(wl, oc, nk, nv, q, sample, threads)
+        oracle_step(wl, oc, nk, nv, q, sample, threads, rows)
     ts = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_step(wl, oc, nk, nv, q, sample, threads)
+        oracle_step(wl, oc, nk, nv, q, sample, threads, rows)
         ts.append(time.perf_counter() - t0)
     ms = 1e3 * sum(ts) / len(ts)
-    value = len(sample) / (ms / 1e3)
-    desc = "%d of the 64 sequences per step (every 16th): write 1 token + attention, all 32 q heads" % len(sample)
-    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 0,
+    value = per_step / (ms / 1e3)
+    return {"impl": "reference", "metric": metric, "value": round(value, 3), "unit": UNIT, "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, f32 write (CPU oracle)",
             "data": "synthetic (seeded)", "config": {"workload": wl.name, "batch": wl.batch},
@@ -403,8 +544,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pool-blocks", type=int, default=200000,
-                    help="block pool size (the workload's is 200000; smaller pools only for profiling)")
+    ap.add_argument("--workload", default="llama_int4", choices=sorted(WORKLOADS),
+                    help="llama_int4 (the headline decode workload), ernie_int2, qwen_int8_headwise, prefill_int4")
+    ap.add_argument("--pool-blocks", type=int, default=0,
+                    help="block pool size (0 = the workload's own; smaller pools only for profiling)")
+    ap.add_argument("--prefill-prefixes", type=int, nargs="+", default=[0, 4096, 16384, 61440],
+                    help="cached prefix per sequence of the prefill workload")
+    ap.add_argument("--prefill-chunk", type=int, default=2048, help="new tokens per sequence of the prefill workload")
     ap.add_argument("--splits", type=int, default=0, help="decode split count (0 = the library's choice)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

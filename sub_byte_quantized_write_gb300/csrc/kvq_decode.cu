@@ -273,13 +273,22 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
     ws.part_ml[i] = make_float2(-CUDART_INF_F, 0.0f);
 
   if (blockIdx.x == 0) {
-    // exclusive prefix sum of the tile counts over (sequence, kv head)
+    // exclusive prefix sum of the tile counts over (sequence, kv head): each
+    // pass covers 128 x ITEMS pairs, thread t owning ITEMS consecutive ones,
+    // so the pass's seq_lens loads are all in flight together
+    constexpr int ITEMS = 8;
     int running = 0;
-    for (int base = 0; base < BH; base += 128) {
-      const int bh = base + threadIdx.x;
-      int n = 0;
-      if (bh < BH) n = tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0).n_virt;
-      int incl = n;
+    for (int base = 0; base < BH; base += 128 * ITEMS) {
+      const int first = base + threadIdx.x * ITEMS;
+      int n[ITEMS];
+      int tsum = 0;
+#pragma unroll
+      for (int k = 0; k < ITEMS; ++k) {
+        const int bh = first + k;
+        n[k] = bh < BH ? tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0).n_virt : 0;
+        tsum += n[k];
+      }
+      int incl = tsum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -289,7 +298,12 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
       __syncthreads();
       int before = running;
       for (int w = 0; w < warp; ++w) before += wsum[w];
-      if (bh < BH) ws.tile_start[bh] = before + incl - n;
+      int x = before + incl - tsum;
+#pragma unroll
+      for (int k = 0; k < ITEMS; ++k) {
+        if (first + k < BH) ws.tile_start[first + k] = x;
+        x += n[k];
+      }
       running += wsum[0] + wsum[1] + wsum[2] + wsum[3];
       __syncthreads();
     }
@@ -838,9 +852,13 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
   // record of (worker w, pair bh) is w + bh
   const int nw = stream_workers(T, ws.nwall, ws.fixed_workers);
   const int w0 = worker_of(start, T, nw), w1 = worker_of(end - 1, T, nw);
+  const int nrec = w1 - w0 + 1;
+  // lane j holds record w0 + j (+ 32 k): its running max and weight sum
   float M = -CUDART_INF_F;
-  for (int w = w0 + lane; w <= w1; w += 32) {
-    const float2 ml = ws.part_ml[(size_t)(w + bh) * G + i];
+  float2 ml0 = make_float2(-CUDART_INF_F, 0.0f);
+  for (int j = lane; j < nrec; j += 32) {
+    const float2 ml = ws.part_ml[(size_t)(w0 + j + bh) * G + i];
+    if (j < 32) ml0 = ml;
     if (ml.y > 0.0f) M = fmaxf(M, ml.x);
   }
   M = warp_max(M);
@@ -850,16 +868,35 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
     return;
   }
   float l = 0.0f;
-  for (int w = w0; w <= w1; ++w) {
-    const size_t rec = (size_t)(w + bh) * G + i;
-    const float2 ml = ws.part_ml[rec];
-    if (!(ml.y > 0.0f)) continue;
-    const float f = ex2(ml.x - M);
+  for (int c0 = 0; c0 < nrec; c0 += 32) {
+    float2 ml = ml0;
+    if (c0 > 0) {
+      ml = make_float2(-CUDART_INF_F, 0.0f);
+      if (c0 + lane < nrec) ml = ws.part_ml[(size_t)(w0 + c0 + lane + bh) * G + i];
+    }
+    const float f = (c0 + lane < nrec && ml.y > 0.0f) ? ex2(ml.x - M) : 0.0f;
     l += f * ml.y;
-    const float* po = ws.part_o + rec * D;
+    const int n = min(32, nrec - c0);
+    // four records per round, their loads issued together
+    for (int k0 = 0; k0 < n; k0 += 4) {
+      float fk[4];
+      float v[4][EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] += f * po[lane + 32 * e];
+      for (int u = 0; u < 4; ++u) {
+        fk[u] = __shfl_sync(0xffffffffu, f, (k0 + u) & 31);
+        const bool use = k0 + u < n && fk[u] != 0.0f;
+        const float* po = ws.part_o + ((size_t)(w0 + c0 + k0 + u + bh) * G + i) * D;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) v[u][e] = use ? po[lane + 32 * e] : 0.0f;
+        if (!use) fk[u] = 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = fmaf(fk[u], v[u][e], o[e]);
+    }
   }
+  l = warp_sum(l);
   // element d = lane + 32 e: lane bits are d bits 0-4, e bits are d bits 5-6
   if (P.mode != MODE_INT8 && P.signs) {
 #pragma unroll

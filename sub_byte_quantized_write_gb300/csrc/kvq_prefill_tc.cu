@@ -44,40 +44,64 @@ namespace {
 
 constexpr int TP_ROWS = 128;
 constexpr int TP_KT = 64;
-constexpr int TP_THREADS = 256;
-constexpr int TP_PRODUCERS = 96;  // warps 5-7
-constexpr int TP_MMA_WARP = 4;
+constexpr int TP_THREADS = 448;
+constexpr int TP_SOFTMAX = 256;    // warps 0-7: warp w owns rows 32 (w % 4) .. + 31, keys 32 (w / 4) .. + 31 of a tile
+constexpr int TP_MMA_WARP = 8;
+constexpr int TP_PROD_WARP0 = 9;   // warps 9-12 expand codes
+constexpr int TP_PRODUCERS = 128;
+constexpr int TP_ISSUE_WARP = 13;
+// O is rescaled only when a row's maximum grows by more than 2^TP_SLACK, so
+// weights p reach at most 2^TP_SLACK and p * s stays inside fp16 for any
+// scale s below 65504 / 2^TP_SLACK (4094).
+constexpr float TP_SLACK = 4.0f;
 
 template <int MODE, int D>
 struct TpCfg {
   static constexpr int BITS = mode_bits(MODE);
   static constexpr int DATA = data_bytes(MODE, D);
   static constexpr int R = row_bytes_of(MODE, D);
-  static constexpr int CHUNK = 16 * R;
+  static constexpr int CHUNK = 16 * R;          // one 16-row chunk of a page (contiguous)
   static constexpr int RAW = TP_KT * R;         // raw bytes of one tensor per tile
   static constexpr int KSTEPS = D / 16;
   static constexpr int QATOM = TP_ROWS * 128;   // one 64-wide K atom of Q (16 KB)
   static constexpr int KATOM = TP_KT * 128;     // one 64-wide atom of the K tile (8 KB)
+  static constexpr int KTILE = (D / 64) * KATOM;
+  static constexpr int VTILE = D * 128;         // V^T: D rows x 64 keys
+  // expanded K / V^T stages (three where shared memory allows) and raw stages
+  static constexpr int NKV = (MODE == MODE_INT8 && D == 128) ? 2 : 3;
+  static constexpr int NRAW = 3;
   // shared-memory layout (swizzled tiles at 1024-byte boundaries)
   static constexpr int OFF_QHI = 0;
   static constexpr int OFF_QLO = OFF_QHI + (D / 64) * QATOM;
-  static constexpr int OFF_K = OFF_QLO + (D / 64) * QATOM;            // [2] K tiles
-  static constexpr int OFF_VT = OFF_K + 2 * (D / 64) * KATOM;          // [2] V^T tiles (D rows x 128 B)
-  static constexpr int OFF_PHI = OFF_VT + 2 * D * 128;
+  static constexpr int OFF_K = OFF_QLO + (D / 64) * QATOM;             // [NKV] K tiles
+  static constexpr int OFF_VT = OFF_K + NKV * KTILE;                   // [NKV] V^T tiles
+  static constexpr int OFF_PHI = OFF_VT + NKV * VTILE;
   static constexpr int OFF_PLO = OFF_PHI + TP_ROWS * 128;
-  static constexpr int OFF_RAW = OFF_PLO + TP_ROWS * 128;              // [2][K,V][RAW]
-  static constexpr int OFF_SC = OFF_RAW + ((4 * RAW + 15) / 16) * 16;  // [2][ks, kz, vs, vz][64] f32
-  static constexpr int OFF_KVAL = OFF_SC + 2 * 4 * TP_KT * 4;          // [2][4] chunk validity of the expanded tiles
-  static constexpr int OFF_RAWVAL = OFF_KVAL + 32;                     // [2][4] chunk validity of the raw tiles
-  static constexpr int OFF_ROW = OFF_RAWVAL + 32;                      // beta, gamma [128] f32, pos [128] int
+  static constexpr int OFF_RAW = OFF_PLO + TP_ROWS * 128;              // [NRAW][K,V][RAW]
+  static constexpr int OFF_SC = OFF_RAW + NRAW * 2 * RAW;              // [NKV][ks, kz, vs, vz][64] f32
+  static constexpr int OFF_KVAL = OFF_SC + NKV * 4 * TP_KT * 4;        // [NKV][4] chunk validity of the expanded tiles
+  static constexpr int OFF_RAWVAL = OFF_KVAL + 64;                     // [NRAW][4] chunk validity of the raw tiles
+  static constexpr int OFF_XMAX = OFF_RAWVAL + 64;                     // [2 tile parity][2 key halves][128] f32
+  static constexpr int OFF_ROW = OFF_XMAX + 2 * 2 * TP_ROWS * 4;       // beta, gamma [128] f32, pos [128] int
   static constexpr int OFF_BAR = OFF_ROW + 3 * TP_ROWS * 4;            // mbarriers
-  static constexpr int NBAR = 12;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;                  // tmem slot, abort flag
+  static constexpr int NBAR = 32;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;                  // tmem slot, abort flag, sequence
   static constexpr int SMEM = OFF_MISC + 16 + 1024;                    // + alignment slack
   static constexpr int TMEM_COLS = 256;                                // S[2] (64 each) + O (D)
+  // the epilogue stages O rows (fp32, 16-byte pieces XOR-swizzled by row)
+  // in the K / V^T stages, free once the last P.V is done
+  static_assert(TP_ROWS * D * 4 <= NKV * (KTILE + VTILE), "epilogue staging does not fit");
+  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(CHUNK % 16 == 0 && R % 4 == 0, "bulk copies need 16-byte multiples");
 };
 
-enum { B_KVFULL = 0, B_KVEMPTY = 2, B_SFULL = 4, B_SEMPTY = 6, B_PFULL = 8, B_ODONE = 9, B_DRAIN = 10 };
+// barriers: raw stage full [3] / empty [3], K/V stage full [3] / empty [3],
+// S full [2] / empty [2], P full, O done, drain, and per row quad the
+// exchange between its two softmax warps [4][tile parity] and at the end [4]
+enum {
+  B_RAWFULL = 0, B_RAWEMPTY = 3, B_KVFULL = 6, B_KVEMPTY = 9, B_SFULL = 12, B_SEMPTY = 14, B_PFULL = 16, B_ODONE = 17,
+  B_DRAIN = 18, B_XCH = 20, B_EPI = 28
+};
 
 // Eight consecutive codes (head dims 8c .. 8c+7) of a raw row as four exact
 // fp16 pairs of signed codes u - 2^(b-1) (INT8: as stored), in dim order.
@@ -133,13 +157,50 @@ __device__ __forceinline__ uint32_t codes2(const uint8_t* raw_row, int d) {
 
 }  // namespace
 
+// Heaviest sequences first: CTA row z of the grid takes the sequence of
+// rank z by 2 L - n (a proxy for its keys per query), so the long prefixes
+// start in the first wave and the short ones fill the tail.  Batches above
+// 64 sequences keep their order.
+__device__ __forceinline__ int heavy_first_sequence(const AttnParams& P, int z) {
+  if (P.batch > 64) return z;
+  const int lane = threadIdx.x & 31;
+  int key[2], me = -1;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int b = lane + 32 * k;
+    key[k] = b < P.batch ? 2 * __ldg(P.seq_lens + b) - (__ldg(P.cu_q + b + 1) - __ldg(P.cu_q + b)) : INT_MIN;
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int b = lane + 32 * k;
+    int rank = 0;
+    for (int j = 0; j < P.batch; ++j) {
+      const int kj = __shfl_sync(0xffffffffu, key[j >> 5], j & 31);
+      rank += (kj > key[k] || (kj == key[k] && j < b)) ? 1 : 0;
+    }
+    if (b < P.batch && rank == z) me = b;
+  }
+  const unsigned m = __ballot_sync(0xffffffffu, me >= 0);
+  const int src = m ? __ffs(m) - 1 : 0;
+  const int b = __shfl_sync(0xffffffffu, me, src);
+  return m ? b : z;
+}
+
 template <int MODE, int D>
 __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P) {
   using C = TpCfg<MODE, D>;
+  constexpr int NKV = C::NKV;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-  const int qtile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* seq_slot = reinterpret_cast<int*>(sm + C::OFF_MISC + 8);
+  if (warp == 0) {
+    const int b0 = heavy_first_sequence(P, blockIdx.z);
+    if (lane == 0) *seq_slot = b0;
+  }
+  __syncthreads();
+  const int b = *seq_slot, h = blockIdx.y;
+  const int qtile = gridDim.x - 1 - blockIdx.x;  // later queries (more keys) first
   const int G = P.group, Hq = P.num_q_heads, Hkv = P.num_kv_heads, bs = P.block_size;
   const int QB = TP_ROWS / G;
 
@@ -189,17 +250,23 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
 
   // ---- set-up: barriers, TMEM, query rows
   if (tid == 0) {
-    mbar_init(bar + B_KVFULL + 0, TP_PRODUCERS);
-    mbar_init(bar + B_KVFULL + 1, TP_PRODUCERS);
-    mbar_init(bar + B_KVEMPTY + 0, 1);
-    mbar_init(bar + B_KVEMPTY + 1, 1);
+    for (int i = 0; i < C::NRAW; ++i) {
+      mbar_init(bar + B_RAWFULL + i, 1);
+      mbar_init(bar + B_RAWEMPTY + i, TP_PRODUCERS);
+    }
+    for (int i = 0; i < NKV; ++i) {
+      mbar_init(bar + B_KVFULL + i, TP_PRODUCERS);
+      mbar_init(bar + B_KVEMPTY + i, 1);
+    }
     mbar_init(bar + B_SFULL + 0, 1);
     mbar_init(bar + B_SFULL + 1, 1);
-    mbar_init(bar + B_SEMPTY + 0, TP_ROWS);
-    mbar_init(bar + B_SEMPTY + 1, TP_ROWS);
-    mbar_init(bar + B_PFULL, TP_ROWS);
+    mbar_init(bar + B_SEMPTY + 0, TP_SOFTMAX);
+    mbar_init(bar + B_SEMPTY + 1, TP_SOFTMAX);
+    mbar_init(bar + B_PFULL, TP_SOFTMAX);
     mbar_init(bar + B_ODONE, 1);
     mbar_init(bar + B_DRAIN, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(bar + B_XCH + i, 64);
+    for (int i = 0; i < 4; ++i) mbar_init(bar + B_EPI + i, 64);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -231,6 +298,10 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
 #pragma unroll
         for (int e = 0; e < EPL; ++e) x[e] = 0.0f;
       }
+      if (P.softmax_scale < 0.0f) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) x[e] = -x[e];
+      }
       float sum = 0.0f, amx = 0.0f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
@@ -252,8 +323,11 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         *reinterpret_cast<__half*>(qlo + off) = lo;
       }
       if (lane == 0) {
-        rbeta[r] = P.softmax_scale * log2e / (dnorm * scl);
-        rgamma[r] = P.softmax_scale * log2e * sum / dnorm;
+        // logit = beta * (s c.q'') + gamma * z, beta > 0: a negative scale is
+        // carried by q'' (negated above), a zero scale by a tiny beta
+        const float sabs = fabsf(P.softmax_scale);
+        rbeta[r] = fmaxf(sabs * log2e / (dnorm * scl), 1e-30f);
+        rgamma[r] = sabs * log2e * sum / dnorm;
         rpos[r] = rv ? (L - n + q0 + ql) : -1;
       }
     }
@@ -265,73 +339,110 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_o = tmem + 128;  // O after the two 64-column S buffers
 
-  if (warp >= 5) {
-    // ======================= producers =======================
-    const int pt = tid - 5 * 32;  // 0..95
-    const int pwarp = warp - 5;
-    const int trow = P.headwise ? b * Hkv + h : b;
-    const int32_t* tbl = P.table + (size_t)trow * P.max_blocks;
-    const size_t blk_stride = (size_t)Hkv * bs * C::R;
-    const uint8_t* kbase = P.k_pages + (size_t)h * bs * C::R;
-    const uint8_t* vbase = P.v_pages + (size_t)h * bs * C::R;
-    auto issue_raw = [&](int v) {
-      if (v < n_virt) {
-        const int T = tile_of(v);
-        uint8_t* rk = sm + C::OFF_RAW + (v & 1) * 2 * C::RAW;
-        uint8_t* rvp = rk + C::RAW;
-        for (int idx = pt; idx < 4 * C::R; idx += TP_PRODUCERS) {
-          const int c = idx / C::R, q = idx % C::R;
-          const int key = TP_KT * T + 16 * c;
-          bool ok = key < Leff;
-          int blk = 0;
-          if (ok) {
-            blk = __ldg(tbl + key / bs);
-            if (blk < 0) ok = false;
-            else if (blk >= P.num_blocks) {
-              ok = false;
-              if (q == 0) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
-            }
+  if (warp == TP_ISSUE_WARP) {
+    // ======================= raw page copies (one lane) =======================
+    // Bulk copies of each tile's valid 16-row chunks into a ring of NRAW raw
+    // stages, up to NRAW tiles ahead of the expansion; the page-table
+    // entries are read two tiles ahead of the copies that use them.
+    if (lane == 0) {
+      const int trow = P.headwise ? b * Hkv + h : b;
+      const int32_t* tbl = P.table + (size_t)trow * P.max_blocks;
+      const size_t blk_stride = (size_t)Hkv * bs * C::R;
+      const int bs_log2 = __ffs(bs) - 1;
+      const uint8_t* kbase = P.k_pages + (size_t)h * bs * C::R;
+      const uint8_t* vbase = P.v_pages + (size_t)h * bs * C::R;
+      auto lookup = [&](int v, int (&out)[4]) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) out[c] = -1;
+        if (v < n_virt) {
+          const int key0 = TP_KT * tile_of(v);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int key = key0 + 16 * c;
+            if (key < Leff) out[c] = __ldg(tbl + (key >> bs_log2));
           }
-          const size_t off = ok ? (size_t)blk * blk_stride + (size_t)(key % bs) * C::R : 0;
-          cp_async16(rk + c * C::CHUNK + 16 * q, kbase + off + 16 * q, ok ? 16 : 0);
-          cp_async16(rvp + c * C::CHUNK + 16 * q, vbase + off + 16 * q, ok ? 16 : 0);
-          if (q == 0) rawval[(v & 1) * 4 + c] = ok ? 1 : 0;
         }
+      };
+      int rs = 0, rphase = 0;
+      bool ok = true;
+      // one tile: look up tile v + 2 into `far`, then copy tile v (ids in `cur`)
+      auto step = [&](int v, int (&cur)[4], int (&far)[4]) {
+        if (!ok || v >= n_virt) return;
+        lookup(v + 2, far);
+        // the producers are done with this raw stage (tile v - NRAW)
+        if (!mbar_wait_bounded(bar + B_RAWEMPTY + rs, rphase ^ 1) || *abort_flag) {
+          *abort_flag = 1;
+          flag_error(P.dev_error, DEVERR_TIMEOUT);
+          ok = false;
+          return;
+        }
+        const int key0 = TP_KT * tile_of(v);
+        uint8_t* rk = sm + C::OFF_RAW + rs * 2 * C::RAW;
+        uint8_t* rvp = rk + C::RAW;
+        int valid = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (cur[c] >= P.num_blocks) {
+            flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
+            cur[c] = -1;
+          }
+          if (cur[c] >= 0) valid |= 1 << c;
+          rawval[rs * 4 + c] = cur[c] >= 0 ? 1 : 0;
+        }
+        mbar_arrive_expect_tx(bar + B_RAWFULL + rs, (uint32_t)(__popc(valid) * 2 * C::CHUNK));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if ((valid >> c) & 1) {
+            const int key = key0 + 16 * c;
+            const size_t off = (size_t)cur[c] * blk_stride + (size_t)(key & (bs - 1)) * C::R;
+            bulk_g2s(rk + c * C::CHUNK, kbase + off, C::CHUNK, bar + B_RAWFULL + rs);
+            bulk_g2s(rvp + c * C::CHUNK, vbase + off, C::CHUNK, bar + B_RAWFULL + rs);
+          }
+        }
+        if (++rs == C::NRAW) {
+          rs = 0;
+          rphase ^= 1;
+        }
+      };
+      // three id sets rotate by position (no register moves that would wait
+      // on a table load still in flight)
+      int ids0[4], ids1[4], ids2[4];
+      lookup(0, ids0);
+      lookup(1, ids1);
+#pragma unroll 1
+      for (int v = 0; v < n_virt && ok; v += 3) {
+        step(v, ids0, ids2);
+        step(v + 1, ids1, ids0);
+        step(v + 2, ids2, ids1);
       }
-      cp_async_commit();
-    };
-    // producer-only named barrier with an OR reduction: every producer leaves
-    // the loop at the same iteration
-    auto producers_any = [&](bool pred) -> bool {
-      uint32_t out;
-      asm volatile(
-          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
-          : "=r"(out)
-          : "r"((uint32_t)pred), "n"(TP_PRODUCERS)
-          : "memory");
-      return out != 0;
-    };
-    issue_raw(0);
+    }
+    __syncwarp();
+  } else if (warp >= TP_PROD_WARP0) {
+    // ======================= producers: code expansion =======================
+    const int pt = tid - TP_PROD_WARP0 * 32;  // 0..127
+    const int pwarp = warp - TP_PROD_WARP0;
+    int kvs = 0, kv_phase = 0;  // K/V stage of tile v and its wrap count parity
+    int rs = 0, rphase = 0;     // raw stage of tile v
 #pragma unroll 1
     for (int v = 0; v < n_virt; ++v) {
-      // all producers are done expanding tile v - 1 (its raw stage is refilled next)
-      if (producers_any(*abort_flag != 0)) break;
-      const int st = v & 1;
-      issue_raw(v + 1);
-      cp_async_wait<1>();
-      // the tensor cores are done with this stage's K / V^T tiles (tile v - 2)
-      const bool late = !mbar_wait_bounded(bar + B_KVEMPTY + st, ((v >> 1) & 1) ^ 1);
-      if (producers_any(late)) {  // also: raw tile v visible to every producer
+      // raw tile v has landed; the tensor cores are done with this K/V stage
+      const bool late = !mbar_wait_bounded(bar + B_RAWFULL + rs, rphase) ||
+                        !mbar_wait_bounded(bar + B_KVEMPTY + kvs, kv_phase ^ 1);
+      if (late || *abort_flag) {
         *abort_flag = 1;
         flag_error(P.dev_error, DEVERR_TIMEOUT);
         break;
       }
-      if (pt < 4) kval[st * 4 + pt] = rawval[st * 4 + pt];
-      const uint8_t* rk = sm + C::OFF_RAW + st * 2 * C::RAW;
+      const int key0 = TP_KT * tile_of(v);
+      const int vmask = rawval[rs * 4 + 0] | (rawval[rs * 4 + 1] << 1) | (rawval[rs * 4 + 2] << 2) |
+                        (rawval[rs * 4 + 3] << 3);
+      if (pt < 4) kval[kvs * 4 + pt] = (vmask >> pt) & 1;
+      const uint8_t* rk = sm + C::OFF_RAW + rs * 2 * C::RAW;
       const uint8_t* rvp = rk + C::RAW;
-      uint8_t* kt = sm + C::OFF_K + st * (D / 64) * C::KATOM;
-      uint8_t* vt = sm + C::OFF_VT + st * D * 128;
-      // K: key rows, 8 dims per 16-byte chunk
+      uint8_t* kt = sm + C::OFF_K + kvs * C::KTILE;
+      uint8_t* vt = sm + C::OFF_VT + kvs * C::VTILE;
+      // K: key rows, 8 dims per 16-byte chunk (rows of skipped chunks hold
+      // stale bytes: finite codes, masked in the softmax)
       for (int it = pt; it < TP_KT * (D / 8); it += TP_PRODUCERS) {
         const int key = it / (D / 8), c8 = it % (D / 8);
         const uint4 hv = codes8<MODE>(rk + key * C::R, c8);
@@ -353,22 +464,36 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         }
       }
       if constexpr (MODE != MODE_INT8) {
+        // per-key scale and zero point; 0 for keys without data (skipped
+        // chunks, rows past the sequence) so that masked keys add exact zeros
         for (int idx = pt; idx < 2 * TP_KT; idx += TP_PRODUCERS) {
           const int key = idx & (TP_KT - 1);
           const bool isv = idx >= TP_KT;
-          const uint32_t pad = lds32((isv ? rvp : rk) + key * C::R + C::DATA);
-          constexpr float half_range = (float)(1 << (C::BITS - 1));
-          const float s = __half2float(__ushort_as_half((unsigned short)(pad & 0xFFFF)));
-          const float m = __half2float(__ushort_as_half((unsigned short)(pad >> 16)));
-          float* scs = sc + st * 4 * TP_KT;
+          const bool has = ((vmask >> (key >> 4)) & 1) && key0 + key < Leff;
+          float s = 0.0f, z = 0.0f;
+          if (has) {
+            const uint32_t pad = lds32((isv ? rvp : rk) + key * C::R + C::DATA);
+            constexpr float half_range = (float)(1 << (C::BITS - 1));
+            s = __half2float(__ushort_as_half((unsigned short)(pad & 0xFFFF)));
+            z = fmaf(half_range, s, __half2float(__ushort_as_half((unsigned short)(pad >> 16))));  // code 0
+          }
+          float* scs = sc + kvs * 4 * TP_KT;
           scs[(isv ? 2 : 0) * TP_KT + key] = s;
-          scs[(isv ? 3 : 1) * TP_KT + key] = fmaf(half_range, s, m);  // value of the signed code 0
+          scs[(isv ? 3 : 1) * TP_KT + key] = z;
         }
       }
+      tc::mbar_arrive(bar + B_RAWEMPTY + rs);  // this thread is done reading the raw stage
       tc::fence_proxy_async();
-      tc::mbar_arrive(bar + B_KVFULL + st);
+      tc::mbar_arrive(bar + B_KVFULL + kvs);
+      if (++kvs == NKV) {
+        kvs = 0;
+        kv_phase ^= 1;
+      }
+      if (++rs == C::NRAW) {
+        rs = 0;
+        rphase ^= 1;
+      }
     }
-    cp_async_wait<0>();
   } else if (warp == TP_MMA_WARP) {
     // ======================= MMA issue =======================
     if (lane == 0) {
@@ -376,11 +501,10 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
       const uint32_t idesc_pv = tc::idesc_f16(TP_ROWS, D);
       const uint32_t a_qhi = smem_addr(sm + C::OFF_QHI), a_qlo = smem_addr(sm + C::OFF_QLO);
       const uint32_t a_phi = smem_addr(sm + C::OFF_PHI), a_plo = smem_addr(sm + C::OFF_PLO);
-      auto pv = [&](int i) -> bool {
-        const int st = i & 1;
+      auto pv = [&](int i, int kvs_i) -> bool {
         if (!mbar_wait_bounded(bar + B_PFULL, i & 1)) return false;
         tc::fence_after();
-        const uint32_t a_vt = smem_addr(sm + C::OFF_VT + st * D * 128);
+        const uint32_t a_vt = smem_addr(sm + C::OFF_VT + kvs_i * C::VTILE);
 #pragma unroll
         for (int kk = 0; kk < TP_KT / 16; ++kk)
           tc::mma_f16(tmem_o, tc::sw128_desc(a_phi + 32 * kk), tc::sw128_desc(a_vt + 32 * kk), idesc_pv,
@@ -389,20 +513,21 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         for (int kk = 0; kk < TP_KT / 16; ++kk)
           tc::mma_f16(tmem_o, tc::sw128_desc(a_plo + 32 * kk), tc::sw128_desc(a_vt + 32 * kk), idesc_pv, 1u);
         tc::commit(bar + B_ODONE);
-        tc::commit(bar + B_KVEMPTY + st);
+        tc::commit(bar + B_KVEMPTY + kvs_i);
         return true;
       };
       bool ok = true;
+      int kvs = 0, kv_phase = 0, kvs_prev = 0;
 #pragma unroll 1
       for (int v = 0; v < n_virt && ok; ++v) {
         const int st = v & 1;
-        if (!mbar_wait_bounded(bar + B_KVFULL + st, (v >> 1) & 1) ||
+        if (!mbar_wait_bounded(bar + B_KVFULL + kvs, kv_phase) ||
             !mbar_wait_bounded(bar + B_SEMPTY + st, ((v >> 1) & 1) ^ 1)) {
           ok = false;
           break;
         }
         tc::fence_after();
-        const uint32_t a_k = smem_addr(sm + C::OFF_K + st * (D / 64) * C::KATOM);
+        const uint32_t a_k = smem_addr(sm + C::OFF_K + kvs * C::KTILE);
         const uint32_t s_tm = tmem + st * TP_KT;
 #pragma unroll
         for (int s = 0; s < C::KSTEPS; ++s) {
@@ -415,10 +540,15 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
           tc::mma_f16(s_tm, tc::sw128_desc(a_qlo + ao), tc::sw128_desc(a_k + bo), idesc_qk, 1u);
         }
         tc::commit(bar + B_SFULL + st);
-        if (v >= 1) ok = pv(v - 1);
+        if (v >= 1) ok = pv(v - 1, kvs_prev);
         if (*abort_flag) ok = false;
+        kvs_prev = kvs;
+        if (++kvs == NKV) {
+          kvs = 0;
+          kv_phase ^= 1;
+        }
       }
-      if (ok && n_virt >= 1) ok = pv(n_virt - 1);
+      if (ok && n_virt >= 1) ok = pv(n_virt - 1, kvs_prev);
       if (!ok) {
         *abort_flag = 1;
         flag_error(P.dev_error, DEVERR_TIMEOUT);
@@ -429,15 +559,26 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
     }
     __syncwarp();
   } else {
-    // ======================= softmax (thread r = row r) =======================
-    const int r = tid;
-    const float rb = rbeta[r], rg = rgamma[r];
+    // ======================= softmax =======================
+    // Row r is shared by warps r / 32 (keys 0-31 of each tile) and r / 32 + 4
+    // (keys 32-63), which may both read TMEM lanes 32 (w % 4) ...  Per tile
+    // each half makes two passes over its 32 logits in 16-key chunks: pass 1
+    // forms y = s c.q'' + rho z (rho = gamma / beta), masks it, writes it back
+    // over S in TMEM and takes the half's maximum; the pair combines the two
+    // maxima through shared memory; pass 2 re-reads y, forms
+    // p = 2^(beta y - m) and writes (p s) hi / lo of its 32 keys to P.
+    const int quad = warp & 3, hf = warp >> 2;
+    const int r = quad * 32 + lane;
+    const float rb = rbeta[r];
+    const float rho = rgamma[r] / rb;
     const int rp = rpos[r];
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float mrow = -CUDART_INF_F, lrow = 0.0f, pzrow = 0.0f;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    float* xmax = reinterpret_cast<float*>(sm + C::OFF_XMAX);
+    float mrow = -CUDART_INF_F, lrow = 0.0f, pzrow = 0.0f;  // lrow, pzrow: this half's keys
     uint8_t* phi = sm + C::OFF_PHI;
     uint8_t* plo = sm + C::OFF_PLO;
     bool ok = true;
+    int kvs = 0;
 #pragma unroll 1
     for (int v = 0; v < n_virt; ++v) {
       const int st = v & 1;
@@ -448,159 +589,215 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         break;
       }
       tc::fence_after();
-      float z[TP_KT];
-      {
-        uint32_t rr[TP_KT / 16][16];
-#pragma unroll
-        for (int c = 0; c < TP_KT / 16; ++c) tc::ld16(tmem + lane_base + st * TP_KT + 16 * c, rr[c]);
-        tc::wait_ld();
-#pragma unroll
-        for (int c = 0; c < TP_KT / 16; ++c)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) z[16 * c + j] = __uint_as_float(rr[c][j]);
-      }
-      tc::fence_before();
-      tc::mbar_arrive(bar + B_SEMPTY + st);
-      // logits (log2 units) and masks
-      const float* scs = sc + st * 4 * TP_KT;
-      const int kv4 = kval[st * 4 + 0] | (kval[st * 4 + 1] << 1) | (kval[st * 4 + 2] << 2) | (kval[st * 4 + 3] << 3);
+      const float4* s4 = reinterpret_cast<const float4*>(sc + kvs * 4 * TP_KT);  // ks, kz, vs, vz: 16 float4 each
+      const int kv4 = kval[kvs * 4 + 0] | (kval[kvs * 4 + 1] << 1) | (kval[kvs * 4 + 2] << 2) | (kval[kvs * 4 + 3] << 3);
       const int key0 = TP_KT * T;
       const bool full = kv4 == 15 && key0 + TP_KT - 1 <= rp && key0 + TP_KT <= Leff &&
                         (W <= 0 || key0 > rp - W || key0 + TP_KT <= P.sink);
-      float tmax = -CUDART_INF_F;
+      const uint32_t s_col = tmem + lane_base + st * TP_KT;
+      float ymax = -CUDART_INF_F;
+#pragma unroll 1
+      for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
+        uint32_t rr[16];
+        tc::ld16(s_col + 16 * c, rr);
+        tc::wait_ld();
 #pragma unroll
-      for (int k = 0; k < TP_KT; ++k) {
-        float zz;
-        if constexpr (MODE == MODE_INT8) zz = rb * z[k];
-        else zz = fmaf(rb * scs[k], z[k], rg * scs[TP_KT + k]);
-        if (!full) {
-          const int j = key0 + k;
-          bool vis = ((kv4 >> (k >> 4)) & 1) && j <= rp && j < Leff;
-          if (W > 0) vis = vis && (j < P.sink || j > rp - W);
-          zz = vis ? zz : -CUDART_INF_F;
+        for (int j4 = 0; j4 < 4; ++j4) {
+          float4 ks = make_float4(0.f, 0.f, 0.f, 0.f), kz = ks;
+          if constexpr (MODE != MODE_INT8) {
+            ks = s4[4 * c + j4];
+            kz = s4[16 + 4 * c + j4];
+          }
+          const float ksv[4] = {ks.x, ks.y, ks.z, ks.w}, kzv[4] = {kz.x, kz.y, kz.z, kz.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int jj = 4 * j4 + e;
+            const float dot = __uint_as_float(rr[jj]);
+            float y = MODE == MODE_INT8 ? dot : fmaf(ksv[e], dot, rho * kzv[e]);
+            if (!full) {
+              const int j = key0 + 16 * c + jj;
+              bool vis = ((kv4 >> c) & 1) && j <= rp && j < Leff;
+              if (W > 0) vis = vis && (j < P.sink || j > rp - W);
+              y = vis ? y : -CUDART_INF_F;
+            }
+            rr[jj] = __float_as_uint(y);
+            ymax = fmaxf(ymax, y);
+          }
         }
-        z[k] = zz;
-        tmax = fmaxf(tmax, zz);
+        tc::st16(s_col + 16 * c, rr);
       }
-      const float mnew = fmaxf(mrow, tmax);
-      const float muse = mnew == -CUDART_INF_F ? 0.0f : mnew;
+      // the pair's maxima meet in shared memory (bounded wait: a partner
+      // that left the loop turns into an error, not a hang)
+      xmax[(st * 2 + hf) * TP_ROWS + r] = ymax;
+      tc::mbar_arrive(bar + B_XCH + quad * 2 + st);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_XCH + quad * 2 + st, (v >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      ymax = fmaxf(ymax, xmax[(st * 2 + (hf ^ 1)) * TP_ROWS + r]);
+      tc::wait_st();
+      // lazy rescale: keep the reference maximum until a row's maximum
+      // passes it by more than 2^TP_SLACK (both halves decide alike)
+      const float tmax = rb * ymax;
+      const bool grow = tmax > mrow + TP_SLACK;
+      const float mref = grow ? tmax : mrow;
+      const float muse = mref == -CUDART_INF_F ? 0.0f : mref;
       // the previous P.V must be done before P is overwritten or O rescaled
       if (v >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_ODONE, (v - 1) & 1))) {
         ok = false;
         break;
       }
-      const bool grow = v >= 1 && mnew > mrow && mrow != -CUDART_INF_F;
-      if (__any_sync(0xffffffffu, grow)) {  // whole warp: rows that did not grow scale by 1
+      const bool resc = v >= 1 && grow && mrow != -CUDART_INF_F;
+      if (__any_sync(0xffffffffu, resc)) {  // this half's O columns; rows keeping their reference scale by 1
         tc::fence_after();
-        const float f = grow ? ex2(mrow - muse) : 1.0f;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t rr[16];
-          tc::ld16(tmem_o + lane_base + c0, rr);
+        const float f = resc ? ex2(mrow - muse) : 1.0f;
+#pragma unroll 1
+        for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+          uint32_t ra[16], rb2[16];
+          tc::ld16(tmem_o + lane_base + c0, ra);
+          tc::ld16(tmem_o + lane_base + c0 + 16, rb2);
           tc::wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * f);
-          tc::st16(tmem_o + lane_base + c0, rr);
+          for (int j = 0; j < 16; ++j) {
+            ra[j] = __float_as_uint(__uint_as_float(ra[j]) * f);
+            rb2[j] = __float_as_uint(__uint_as_float(rb2[j]) * f);
+          }
+          tc::st16(tmem_o + lane_base + c0, ra);
+          tc::st16(tmem_o + lane_base + c0 + 16, rb2);
         }
         tc::wait_st();
         lrow *= f;
         pzrow *= f;
       }
-      mrow = mnew;
+      mrow = mref;
       float tl = 0.0f, tpz = 0.0f;
+#pragma unroll 1
+      for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
+        uint32_t rr[16];
+        tc::ld16(s_col + 16 * c, rr);
+        tc::wait_ld();
+        uint32_t hv[8], lv[8];
 #pragma unroll
-      for (int c = 0; c < TP_KT / 8; ++c) {
-        uint32_t hv[4], lv[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float w2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int k = 8 * c + 2 * j + e;
-            const float p = ex2(z[k] - muse);
-            tl += p;
-            if constexpr (MODE != MODE_INT8) {
-              tpz += p * scs[3 * TP_KT + k];
-              w2[e] = p * scs[2 * TP_KT + k];
-            } else {
-              w2[e] = p;
-            }
+        for (int j4 = 0; j4 < 4; ++j4) {
+          float4 vs = make_float4(1.f, 1.f, 1.f, 1.f), vz = make_float4(0.f, 0.f, 0.f, 0.f);
+          if constexpr (MODE != MODE_INT8) {
+            vs = s4[32 + 4 * c + j4];
+            vz = s4[48 + 4 * c + j4];
           }
-          const __half2 hp = __floats2half2_rn(w2[0], w2[1]);
-          const float2 hf = __half22float2(hp);
-          const __half2 lp = __floats2half2_rn(w2[0] - hf.x, w2[1] - hf.y);
-          hv[j] = *reinterpret_cast<const uint32_t*>(&hp);
-          lv[j] = *reinterpret_cast<const uint32_t*>(&lp);
+          const float vsv[4] = {vs.x, vs.y, vs.z, vs.w}, vzv[4] = {vz.x, vz.y, vz.z, vz.w};
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            float w2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int jj = 4 * j4 + 2 * e2 + e;
+              const float p = ex2(fmaf(rb, __uint_as_float(rr[jj]), -muse));
+              tl += p;
+              if constexpr (MODE != MODE_INT8) tpz = fmaf(p, vzv[2 * e2 + e], tpz);
+              w2[e] = MODE != MODE_INT8 ? p * vsv[2 * e2 + e] : p;
+            }
+            const __half2 hp = __floats2half2_rn(w2[0], w2[1]);
+            const float2 hf2 = __half22float2(hp);
+            const __half2 lp = __floats2half2_rn(w2[0] - hf2.x, w2[1] - hf2.y);
+            hv[2 * j4 + e2] = *reinterpret_cast<const uint32_t*>(&hp);
+            lv[2 * j4 + e2] = *reinterpret_cast<const uint32_t*>(&lp);
+          }
         }
-        *reinterpret_cast<uint4*>(phi + tc::sw128_off(r, c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<uint4*>(plo + tc::sw128_off(r, c)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        *reinterpret_cast<uint4*>(phi + tc::sw128_off(r, 2 * c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4*>(phi + tc::sw128_off(r, 2 * c + 1)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+        *reinterpret_cast<uint4*>(plo + tc::sw128_off(r, 2 * c)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        *reinterpret_cast<uint4*>(plo + tc::sw128_off(r, 2 * c + 1)) = make_uint4(lv[4], lv[5], lv[6], lv[7]);
       }
+      tc::fence_before();
+      tc::mbar_arrive(bar + B_SEMPTY + st);  // y consumed: the S buffer may be overwritten
       lrow += tl;
       pzrow += tpz;
       tc::fence_proxy_async();
       tc::fence_before();
       tc::mbar_arrive(bar + B_PFULL);
+      if (++kvs == NKV) kvs = 0;
       if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         ok = false;
         break;
       }
     }
-    // ---- epilogue: O row, zero-point term, inverse RHT, 1 / l
+    // ---- epilogue: each half stages its O columns in shared memory, the
+    // pair adds up its l and zero-point sums, then per row a warp applies
+    // the zero-point term, the inverse RHT (or the INT8 V channel scales) and
+    // 1 / l and stores the row with coalesced writes
     if (ok && n_virt >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_ODONE, (n_virt - 1) & 1)))
       ok = false;
-    if (!ok) {
+    float4* stage = reinterpret_cast<float4*>(sm + C::OFF_K);  // [128 rows][D / 4], piece j at j ^ (row & 7)
+    float* xsum = reinterpret_cast<float*>(sm + C::OFF_RAW);    // [2 halves][l, pz, ok][128]
+    constexpr int P4 = D / 4;
+    if (ok) {  // every P.V is done: the K / V^T stages are free for staging
+      xsum[(hf * 3 + 0) * TP_ROWS + r] = lrow;
+      xsum[(hf * 3 + 1) * TP_ROWS + r] = MODE != MODE_INT8 ? pzrow : 0.0f;
+      if (n_virt >= 1) {  // whole warp reads its 32 TMEM rows, valid or not
+        tc::fence_after();
+#pragma unroll 1
+        for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+          uint32_t ra[16], rb2[16];
+          tc::ld16(tmem_o + lane_base + c0, ra);
+          tc::ld16(tmem_o + lane_base + c0 + 16, rb2);
+          tc::wait_ld();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            stage[r * P4 + ((c0 / 4 + j) ^ (r & 7))] =
+                make_float4(__uint_as_float(ra[4 * j]), __uint_as_float(ra[4 * j + 1]), __uint_as_float(ra[4 * j + 2]),
+                            __uint_as_float(ra[4 * j + 3]));
+            stage[r * P4 + ((c0 / 4 + 4 + j) ^ (r & 7))] =
+                make_float4(__uint_as_float(rb2[4 * j]), __uint_as_float(rb2[4 * j + 1]),
+                            __uint_as_float(rb2[4 * j + 2]), __uint_as_float(rb2[4 * j + 3]));
+          }
+        }
+      } else {
+        for (int j = hf * (P4 / 2); j < (hf + 1) * (P4 / 2); ++j) stage[r * P4 + j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    xsum[(hf * 3 + 2) * TP_ROWS + r] = ok ? 1.0f : 0.0f;
+    tc::mbar_arrive(bar + B_EPI + quad);  // both halves of these 32 rows are staged (or failed)
+    const bool met = mbar_wait_bounded(bar + B_EPI + quad, 0);
+    const bool pair_ok = __all_sync(0xffffffffu, ok && met && xsum[((hf ^ 1) * 3 + 2) * TP_ROWS + r] != 0.0f);
+    if (!pair_ok) {
       *abort_flag = 1;
       if (lane == 0) flag_error(P.dev_error, DEVERR_TIMEOUT);
     } else {
-      const int ql = r / G, i = r % G;
-      float o[D];
-      if (n_virt >= 1) {  // whole warp reads its 32 TMEM rows, valid or not
-        tc::fence_after();
+      constexpr int EPL = D / 32;  // lane holds dims lane * EPL .. + EPL - 1
+      for (int k = 16 * hf; k < 16 * hf + 16; ++k) {
+        const int row = quad * 32 + k;
+        const int ql = row / G, i = row % G;
+        if (ql >= nq) continue;  // warp-uniform
+        const float lr = xsum[0 * TP_ROWS + row] + xsum[3 * TP_ROWS + row];
+        const float pz = xsum[1 * TP_ROWS + row] + xsum[4 * TP_ROWS + row];
+        float o[EPL];
+        const float* src = reinterpret_cast<const float*>(stage + row * P4 + ((lane * EPL / 4) ^ (row & 7))) +
+                           (lane * EPL) % 4;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t rr[16];
-          tc::ld16(tmem_o + lane_base + c0, rr);
-          tc::wait_ld();
+        for (int e = 0; e < EPL; ++e) o[e] = src[e] + pz;
+        if (lr == 0.0f) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) o[c0 + j] = __uint_as_float(rr[j]);
-        }
-      } else {
+          for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
+        } else if constexpr (MODE != MODE_INT8) {
+          if (P.signs) {
+            wht_warp<EPL>(o, lane);
+            const float inv = 1.0f / ((float)D * lr);
 #pragma unroll
-        for (int d = 0; d < D; ++d) o[d] = 0.0f;
-      }
-      if (ql < nq) {
-        float* orow = P.out + ((size_t)(cq0 + q0 + ql) * Hq + h * G + i) * D;
-        if (lrow == 0.0f) {
-#pragma unroll
-          for (int d = 0; d < D; d += 4) *reinterpret_cast<float4*>(orow + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-          if constexpr (MODE != MODE_INT8) {
-#pragma unroll
-            for (int d = 0; d < D; ++d) o[d] += pzrow;
-            if (P.signs) {
-#pragma unroll
-              for (int hs = 1; hs < D; hs <<= 1)
-#pragma unroll
-                for (int d = 0; d < D; ++d) {
-                  if (d & hs) continue;
-                  const float a = o[d], c = o[d + hs];
-                  o[d] = a + c;
-                  o[d + hs] = a - c;
-                }
-              const float inv = 1.0f / ((float)D * lrow);
-#pragma unroll
-              for (int d = 0; d < D; ++d) o[d] = (__ldg(P.signs + d) < 0 ? -o[d] : o[d]) * inv;
-            } else {
-#pragma unroll
-              for (int d = 0; d < D; ++d) o[d] /= lrow;
-            }
+            for (int e = 0; e < EPL; ++e) o[e] = (__ldg(P.signs + lane * EPL + e) < 0 ? -o[e] : o[e]) * inv;
           } else {
-            const float* am = P.ch_amax + ((size_t)Hkv + h) * D;
 #pragma unroll
-            for (int d = 0; d < D; ++d) o[d] = o[d] * __fdiv_rn(am[d], 127.0f) / lrow;
+            for (int e = 0; e < EPL; ++e) o[e] /= lr;
           }
+        } else {
+          const float* am = P.ch_amax + ((size_t)Hkv + h) * D + lane * EPL;
 #pragma unroll
-          for (int d = 0; d < D; d += 4) *reinterpret_cast<float4*>(orow + d) = make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]);
+          for (int e = 0; e < EPL; ++e) o[e] = o[e] * __fdiv_rn(am[e], 127.0f) / lr;
+        }
+        float* orow = P.out + ((size_t)(cq0 + q0 + ql) * Hq + h * G + i) * D + lane * EPL;
+        if constexpr (EPL == 4) {
+          *reinterpret_cast<float4*>(orow) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+          *reinterpret_cast<float2*>(orow) = make_float2(o[0], o[1]);
         }
       }
     }
@@ -627,7 +824,7 @@ cudaError_t launch_prefill_tc_t(const AttnParams& P, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int QB = TP_ROWS / P.group;
-  dim3 grid((P.max_q_per_seq + QB - 1) / QB, P.num_kv_heads, P.batch);
+  dim3 grid((P.max_q_per_seq + QB - 1) / QB, P.num_kv_heads, P.batch);  // TP_THREADS threads each
   prefill_tc_kernel<MODE, D><<<grid, TP_THREADS, C::SMEM, stream>>>(P);
   return cudaGetLastError();
 }
