@@ -63,21 +63,16 @@ struct TpCfg {
   static constexpr int CHUNK = 16 * R;          // one 16-row chunk of a page (contiguous)
   static constexpr int RAW = TP_KT * R;         // raw bytes of one tensor per tile
   static constexpr int KSTEPS = D / 16;
-  static constexpr int QATOM = TP_ROWS * 128;   // one 64-wide K atom of Q (16 KB)
   static constexpr int KATOM = TP_KT * 128;     // one 64-wide atom of the K tile (8 KB)
   static constexpr int KTILE = (D / 64) * KATOM;
   static constexpr int VTILE = D * 128;         // V^T: D rows x 64 keys
-  // expanded K / V^T stages (three where shared memory allows) and raw stages
-  static constexpr int NKV = (MODE == MODE_INT8 && D == 128) ? 2 : 3;
+  // expanded K / V^T stages and raw stages
+  static constexpr int NKV = 3;
   static constexpr int NRAW = 3;
   // shared-memory layout (swizzled tiles at 1024-byte boundaries)
-  static constexpr int OFF_QHI = 0;
-  static constexpr int OFF_QLO = OFF_QHI + (D / 64) * QATOM;
-  static constexpr int OFF_K = OFF_QLO + (D / 64) * QATOM;             // [NKV] K tiles
+  static constexpr int OFF_K = 0;                                       // [NKV] K tiles
   static constexpr int OFF_VT = OFF_K + NKV * KTILE;                   // [NKV] V^T tiles
-  static constexpr int OFF_PHI = OFF_VT + NKV * VTILE;
-  static constexpr int OFF_PLO = OFF_PHI + TP_ROWS * 128;
-  static constexpr int OFF_RAW = OFF_PLO + TP_ROWS * 128;              // [NRAW][K,V][RAW]
+  static constexpr int OFF_RAW = OFF_VT + NKV * VTILE;                 // [NRAW][K,V][RAW]
   static constexpr int OFF_SC = OFF_RAW + NRAW * 2 * RAW;              // [NKV][ks, kz, vs, vz][64] f32
   static constexpr int OFF_KVAL = OFF_SC + NKV * 4 * TP_KT * 4;        // [NKV][4] chunk validity of the expanded tiles
   static constexpr int OFF_RAWVAL = OFF_KVAL + 64;                     // [NRAW][4] chunk validity of the raw tiles
@@ -87,10 +82,19 @@ struct TpCfg {
   static constexpr int NBAR = 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;                  // tmem slot, abort flag, sequence
   static constexpr int SMEM = OFF_MISC + 16 + 1024;                    // + alignment slack
-  static constexpr int TMEM_COLS = 256;                                // S[2] (64 each) + O (D)
+  // TMEM columns: S[2] (64 fp32 each; P hi / lo overwrite them), O (D fp32),
+  // Q hi and Q lo (D / 2 columns each: two fp16 per column)
+  static constexpr int TM_O = 2 * TP_KT;
+  static constexpr int TM_QHI = TM_O + D;
+  static constexpr int TM_QLO = TM_QHI + D / 2;
+  static constexpr int TMEM_COLS = TM_QLO + D / 2 <= 256 ? 256 : 512;
+  // the query rows are staged (fp16 hi / lo, rows padded by 16 bytes) in the
+  // K / V^T stages before they are moved to TMEM
+  static constexpr int QROW = 2 * D + 16;
   // the epilogue stages O rows (fp32, 16-byte pieces XOR-swizzled by row)
   // in the K / V^T stages, free once the last P.V is done
   static_assert(TP_ROWS * D * 4 <= NKV * (KTILE + VTILE), "epilogue staging does not fit");
+  static_assert(2 * TP_ROWS * QROW <= NKV * (KTILE + VTILE), "query staging does not fit");
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(CHUNK % 16 == 0 && R % 4 == 0, "bulk copies need 16-byte multiples");
 };
@@ -260,8 +264,6 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
     }
     mbar_init(bar + B_SFULL + 0, 1);
     mbar_init(bar + B_SFULL + 1, 1);
-    mbar_init(bar + B_SEMPTY + 0, TP_SOFTMAX);
-    mbar_init(bar + B_SEMPTY + 1, TP_SOFTMAX);
     mbar_init(bar + B_PFULL, TP_SOFTMAX);
     mbar_init(bar + B_ODONE, 1);
     mbar_init(bar + B_DRAIN, 1);
@@ -276,8 +278,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
   const float dnorm = (MODE != MODE_INT8 && P.signs) ? (float)D : 1.0f;
   {
     constexpr int EPL = D / 32;
-    uint8_t* qhi = sm + C::OFF_QHI;
-    uint8_t* qlo = sm + C::OFF_QLO;
+    uint8_t* qhi = sm + C::OFF_K;                      // [128 rows][QROW] fp16 hi
+    uint8_t* qlo = sm + C::OFF_K + TP_ROWS * C::QROW;  // [128 rows][QROW] fp16 lo
     for (int r = warp; r < TP_ROWS; r += TP_THREADS / 32) {
       const int ql = r / G, i = r % G;
       const bool rv = ql < nq;
@@ -318,9 +320,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         const float v = x[e] * scl;
         const __half hi = __float2half_rn(v);
         const __half lo = __float2half_rn(v - __half2float(hi));
-        const int off = (d >> 6) * C::QATOM + tc::sw128_off(r, (d & 63) >> 3) + 2 * (d & 7);
-        *reinterpret_cast<__half*>(qhi + off) = hi;
-        *reinterpret_cast<__half*>(qlo + off) = lo;
+        *reinterpret_cast<__half*>(qhi + r * C::QROW + 2 * d) = hi;
+        *reinterpret_cast<__half*>(qlo + r * C::QROW + 2 * d) = lo;
       }
       if (lane == 0) {
         // logit = beta * (s c.q'') + gamma * z, beta > 0: a negative scale is
@@ -332,12 +333,43 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
       }
     }
   }
-  tc::fence_proxy_async();  // query tiles are read by the tensor cores
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
+  {
+    const uint32_t tmem0 = *tmem_slot;
+    // the softmax warps move the query rows into TMEM: warp w writes lanes
+    // 32 (w % 4) .. + 31, half w / 4 of the columns of Q hi and of Q lo
+    if (warp < TP_SOFTMAX / 32) {
+      const int quad = warp & 3, hf = warp >> 2;
+      const int r = quad * 32 + lane;
+      const uint32_t lb = (uint32_t)(quad * 32) << 16;
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+        const uint8_t* src = sm + C::OFF_K + part * TP_ROWS * C::QROW + r * C::QROW;
+        const uint32_t col0 = (part == 0 ? C::TM_QHI : C::TM_QLO) + hf * (D / 4);
+#pragma unroll 1
+        for (int c = 0; c < D / 4; c += 16) {  // 16 columns = 32 dims
+          uint32_t rr[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src + 4 * (hf * (D / 4) + c) + 16 * j);
+            rr[4 * j] = w.x;
+            rr[4 * j + 1] = w.y;
+            rr[4 * j + 2] = w.z;
+            rr[4 * j + 3] = w.w;
+          }
+          tc::st16(tmem0 + lb + col0 + c, rr);
+        }
+      }
+      tc::wait_st();
+    }
+  }
+  tc::fence_before();
+  __syncthreads();  // the query rows are in TMEM; the staging area is free again
+  tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + 128;  // O after the two 64-column S buffers
+  const uint32_t tmem_o = tmem + C::TM_O;
 
   if (warp == TP_ISSUE_WARP) {
     // ======================= raw page copies (one lane) =======================
@@ -499,19 +531,19 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
     if (lane == 0) {
       const uint32_t idesc_qk = tc::idesc_f16(TP_ROWS, TP_KT);
       const uint32_t idesc_pv = tc::idesc_f16(TP_ROWS, D);
-      const uint32_t a_qhi = smem_addr(sm + C::OFF_QHI), a_qlo = smem_addr(sm + C::OFF_QLO);
-      const uint32_t a_phi = smem_addr(sm + C::OFF_PHI), a_plo = smem_addr(sm + C::OFF_PLO);
+      // O += P V with P (hi / lo interleaved per 16 keys, where the tile's S
+      // was) from TMEM and V^T from shared memory
       auto pv = [&](int i, int kvs_i) -> bool {
         if (!mbar_wait_bounded(bar + B_PFULL, i & 1)) return false;
         tc::fence_after();
         const uint32_t a_vt = smem_addr(sm + C::OFF_VT + kvs_i * C::VTILE);
+        const uint32_t p_tm = tmem + (i & 1) * TP_KT;
 #pragma unroll
-        for (int kk = 0; kk < TP_KT / 16; ++kk)
-          tc::mma_f16(tmem_o, tc::sw128_desc(a_phi + 32 * kk), tc::sw128_desc(a_vt + 32 * kk), idesc_pv,
-                      (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < TP_KT / 16; ++kk)
-          tc::mma_f16(tmem_o, tc::sw128_desc(a_plo + 32 * kk), tc::sw128_desc(a_vt + 32 * kk), idesc_pv, 1u);
+        for (int kk = 0; kk < TP_KT / 16; ++kk) {
+          const uint64_t bdesc = tc::sw128_desc(a_vt + 32 * kk);
+          tc::mma_f16_ts(tmem_o, p_tm + 16 * kk, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_f16_ts(tmem_o, p_tm + 16 * kk + 8, bdesc, idesc_pv, 1u);
+        }
         tc::commit(bar + B_ODONE);
         tc::commit(bar + B_KVEMPTY + kvs_i);
         return true;
@@ -521,8 +553,9 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
 #pragma unroll 1
       for (int v = 0; v < n_virt && ok; ++v) {
         const int st = v & 1;
-        if (!mbar_wait_bounded(bar + B_KVFULL + kvs, kv_phase) ||
-            !mbar_wait_bounded(bar + B_SEMPTY + st, ((v >> 1) & 1) ^ 1)) {
+        // S(v) goes where P(v - 2) was: P.V(v - 2) was issued before it and
+        // the tensor cores run this thread's MMAs in order
+        if (!mbar_wait_bounded(bar + B_KVFULL + kvs, kv_phase)) {
           ok = false;
           break;
         }
@@ -531,13 +564,9 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         const uint32_t s_tm = tmem + st * TP_KT;
 #pragma unroll
         for (int s = 0; s < C::KSTEPS; ++s) {
-          const uint32_t ao = (s >> 2) * C::QATOM + (s & 3) * 32, bo = (s >> 2) * C::KATOM + (s & 3) * 32;
-          tc::mma_f16(s_tm, tc::sw128_desc(a_qhi + ao), tc::sw128_desc(a_k + bo), idesc_qk, s > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int s = 0; s < C::KSTEPS; ++s) {
-          const uint32_t ao = (s >> 2) * C::QATOM + (s & 3) * 32, bo = (s >> 2) * C::KATOM + (s & 3) * 32;
-          tc::mma_f16(s_tm, tc::sw128_desc(a_qlo + ao), tc::sw128_desc(a_k + bo), idesc_qk, 1u);
+          const uint64_t bdesc = tc::sw128_desc(a_k + (s >> 2) * C::KATOM + (s & 3) * 32);
+          tc::mma_f16_ts(s_tm, tmem + C::TM_QHI + 8 * s, bdesc, idesc_qk, s > 0 ? 1u : 0u);
+          tc::mma_f16_ts(s_tm, tmem + C::TM_QLO + 8 * s, bdesc, idesc_qk, 1u);
         }
         tc::commit(bar + B_SFULL + st);
         if (v >= 1) ok = pv(v - 1, kvs_prev);
@@ -575,8 +604,6 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     float* xmax = reinterpret_cast<float*>(sm + C::OFF_XMAX);
     float mrow = -CUDART_INF_F, lrow = 0.0f, pzrow = 0.0f;  // lrow, pzrow: this half's keys
-    uint8_t* phi = sm + C::OFF_PHI;
-    uint8_t* plo = sm + C::OFF_PLO;
     bool ok = true;
     int kvs = 0;
 #pragma unroll 1
@@ -676,7 +703,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         uint32_t rr[16];
         tc::ld16(s_col + 16 * c, rr);
         tc::wait_ld();
-        uint32_t hv[8], lv[8];
+        uint32_t pw[16];  // P hi (8 columns) then P lo (8 columns) of these 16 keys
 #pragma unroll
         for (int j4 = 0; j4 < 4; ++j4) {
           float4 vs = make_float4(1.f, 1.f, 1.f, 1.f), vz = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -699,20 +726,15 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
             const __half2 hp = __floats2half2_rn(w2[0], w2[1]);
             const float2 hf2 = __half22float2(hp);
             const __half2 lp = __floats2half2_rn(w2[0] - hf2.x, w2[1] - hf2.y);
-            hv[2 * j4 + e2] = *reinterpret_cast<const uint32_t*>(&hp);
-            lv[2 * j4 + e2] = *reinterpret_cast<const uint32_t*>(&lp);
+            pw[2 * j4 + e2] = *reinterpret_cast<const uint32_t*>(&hp);
+            pw[8 + 2 * j4 + e2] = *reinterpret_cast<const uint32_t*>(&lp);
           }
         }
-        *reinterpret_cast<uint4*>(phi + tc::sw128_off(r, 2 * c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-        *reinterpret_cast<uint4*>(phi + tc::sw128_off(r, 2 * c + 1)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-        *reinterpret_cast<uint4*>(plo + tc::sw128_off(r, 2 * c)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-        *reinterpret_cast<uint4*>(plo + tc::sw128_off(r, 2 * c + 1)) = make_uint4(lv[4], lv[5], lv[6], lv[7]);
+        tc::st16(s_col + 16 * c, pw);  // over the 16 y values just read
       }
-      tc::fence_before();
-      tc::mbar_arrive(bar + B_SEMPTY + st);  // y consumed: the S buffer may be overwritten
+      tc::wait_st();
       lrow += tl;
       pzrow += tpz;
-      tc::fence_proxy_async();
       tc::fence_before();
       tc::mbar_arrive(bar + B_PFULL);
       if (++kvs == NKV) kvs = 0;
