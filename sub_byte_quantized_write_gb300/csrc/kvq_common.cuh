@@ -191,12 +191,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The polling loop is one out-of-line function shared by every call site,
+// so the kernels' hot loops stay small in the instruction cache.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try_wait_sleep(bar, parity, 1000000u))
     if (clock64() - t0 > WAIT_LIMIT_CYCLES) return false;
   return true;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity);
 }
 // global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte
 // aligned), completion counted on `bar` as transaction bytes.

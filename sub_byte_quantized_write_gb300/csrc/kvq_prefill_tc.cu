@@ -396,17 +396,20 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         }
       };
       int rs = 0, rphase = 0;
-      bool ok = true;
-      // one tile: look up tile v + 2 into `far`, then copy tile v (ids in `cur`)
-      auto step = [&](int v, int (&cur)[4], int (&far)[4]) {
-        if (!ok || v >= n_virt) return;
-        lookup(v + 2, far);
+      // block ids of tiles v, v + 1, v + 2: each table load is issued three
+      // tiles before its copies and moved between registers a tile after it
+      // was issued, so no step waits on a load in flight
+      int ids0[4], ids1[4], ids2[4];
+      lookup(0, ids0);
+      lookup(1, ids1);
+      lookup(2, ids2);
+#pragma unroll 1
+      for (int v = 0; v < n_virt; ++v) {
         // the producers are done with this raw stage (tile v - NRAW)
         if (!mbar_wait_bounded(bar + B_RAWEMPTY + rs, rphase ^ 1) || *abort_flag) {
           *abort_flag = 1;
           flag_error(P.dev_error, DEVERR_TIMEOUT);
-          ok = false;
-          return;
+          break;
         }
         const int key0 = TP_KT * tile_of(v);
         uint8_t* rk = sm + C::OFF_RAW + rs * 2 * C::RAW;
@@ -414,38 +417,33 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         int valid = 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          if (cur[c] >= P.num_blocks) {
+          if (ids0[c] >= P.num_blocks) {
             flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
-            cur[c] = -1;
+            ids0[c] = -1;
           }
-          if (cur[c] >= 0) valid |= 1 << c;
-          rawval[rs * 4 + c] = cur[c] >= 0 ? 1 : 0;
+          if (ids0[c] >= 0) valid |= 1 << c;
+          rawval[rs * 4 + c] = ids0[c] >= 0 ? 1 : 0;
         }
         mbar_arrive_expect_tx(bar + B_RAWFULL + rs, (uint32_t)(__popc(valid) * 2 * C::CHUNK));
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if ((valid >> c) & 1) {
             const int key = key0 + 16 * c;
-            const size_t off = (size_t)cur[c] * blk_stride + (size_t)(key & (bs - 1)) * C::R;
+            const size_t off = (size_t)ids0[c] * blk_stride + (size_t)(key & (bs - 1)) * C::R;
             bulk_g2s(rk + c * C::CHUNK, kbase + off, C::CHUNK, bar + B_RAWFULL + rs);
             bulk_g2s(rvp + c * C::CHUNK, vbase + off, C::CHUNK, bar + B_RAWFULL + rs);
           }
         }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          ids0[c] = ids1[c];
+          ids1[c] = ids2[c];
+        }
+        lookup(v + 3, ids2);
         if (++rs == C::NRAW) {
           rs = 0;
           rphase ^= 1;
         }
-      };
-      // three id sets rotate by position (no register moves that would wait
-      // on a table load still in flight)
-      int ids0[4], ids1[4], ids2[4];
-      lookup(0, ids0);
-      lookup(1, ids1);
-#pragma unroll 1
-      for (int v = 0; v < n_virt && ok; v += 3) {
-        step(v, ids0, ids2);
-        step(v + 1, ids1, ids0);
-        step(v + 2, ids2, ids1);
       }
     }
     __syncwarp();
