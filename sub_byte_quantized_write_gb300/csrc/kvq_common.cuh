@@ -192,16 +192,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 // The polling loop is one out-of-line function shared by every call site,
-// so the kernels' hot loops stay small in the instruction cache.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
+// so the kernels' hot loops stay small in the instruction cache.  Between
+// polls the thread sleeps `sleep_ns`, so that warps waiting off the critical
+// path leave the issue slots to the warps that work.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t sleep_ns) {
   const long long t0 = clock64();
-  while (!mbar_try_wait_sleep(bar, parity, 1000000u))
+  while (!mbar_try_wait_sleep(bar, parity, 1000000u)) {
     if (clock64() - t0 > WAIT_LIMIT_CYCLES) return false;
+    if (sleep_ns) __nanosleep(sleep_ns);
+  }
   return true;
 }
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity);
+  return mbar_wait_slow(bar, parity, sleep_ns);
 }
 // global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte
 // aligned), completion counted on `bar` as transaction bytes.

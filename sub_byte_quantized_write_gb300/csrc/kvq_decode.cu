@@ -390,13 +390,14 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
 // ---------------------------------------------------------------------------
 // 2. stream kernel
 
-// Ring depth and residency: NT == 1 kernels run 4 CTAs per SM (3 for INT8's
-// larger rows), NT == 2 kernels 2 CTAs per SM; the ring is sized to fit.
+// Ring depth and residency (from sweeps on the decode workloads): NT == 1
+// kernels run 4 CTAs per SM (3 for INT8's larger rows), NT == 2 kernels 3
+// (2 for INT8); the ring is sized to fit.
 template <int MODE, int D, int NT>
 struct StreamCfg {
-  static constexpr int NSTAGE = NT == 1 ? (MODE == MODE_INT4 ? 3 : (MODE == MODE_INT2 ? 5 : 2))
-                                        : (MODE == MODE_INT4 ? 4 : (MODE == MODE_INT2 ? 6 : 3));
-  static constexpr int CTAS = NT == 1 ? (MODE == MODE_INT8 ? 3 : 4) : 2;
+  static constexpr int NSTAGE = NT == 1 ? (MODE == MODE_INT4 ? 2 : (MODE == MODE_INT2 ? 5 : 2))
+                                        : (MODE == MODE_INT4 ? 4 : (MODE == MODE_INT2 ? 3 : 3));
+  static constexpr int CTAS = NT == 1 ? (MODE == MODE_INT8 ? 3 : 4) : (MODE == MODE_INT8 ? 2 : 3);
 };
 
 // One (sequence, kv head) as seen by a cursor walking the global tile order.
@@ -406,14 +407,15 @@ struct Seg {
   const int32_t* tbl;
 };
 
-__device__ __forceinline__ void load_seg(const AttnParams& P, const int* tile_start, int bh, Seg& s) {
+// Pair bh whose tiles start at global tile `start`.
+__device__ __forceinline__ void load_seg(const AttnParams& P, int bh, int start, Seg& s) {
   const int Hkv = P.num_kv_heads;
   s.bh = bh;
-  s.start = __ldg(tile_start + bh);
-  s.end = __ldg(tile_start + bh + 1);
   const int b = bh / Hkv, h = bh % Hkv;
   s.h = h;
   s.t = tile_list(P, b, h, false);
+  s.start = start;
+  s.end = start + s.t.n_virt;
   s.tbl = P.table + (size_t)(P.headwise ? bh : b) * P.max_blocks;
 }
 
@@ -429,12 +431,39 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   const int G = P.group, Hkv = P.num_kv_heads, bs = P.block_size;
   const int BH = P.batch * Hkv;
 
-  grid_dependency_wait();    // tile prefix sums, query images and cleared partials are ready
   allow_dependent_launch();  // the merge kernel may launch; it waits for this grid to finish
-  const int T = ws.tile_start[BH];
+  // Slices come from the tile counts themselves (a prefix scan per CTA over
+  // all (sequence, kv head) pairs, thread t owning a contiguous run of
+  // pairs), so the first page copies go out while the preparation kernel
+  // still builds the query images.
+  __shared__ int run_start[129];
+  const int items = (BH + 127) / 128;
+  {
+    const int first = threadIdx.x * items;
+    int tsum = 0;
+    for (int k = 0; k < items && first + k < BH; ++k) {
+      const int bh = first + k;
+      tsum += tile_list(P, bh / Hkv, bh % Hkv, false).n_virt;
+    }
+    int incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    __shared__ int wtot[DECODE_WARPS];
+    if (lane == 31) wtot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += wtot[w];
+    run_start[threadIdx.x + 1] = before + incl;
+    if (threadIdx.x == 0) run_start[0] = 0;
+    __syncthreads();
+  }
+  const int T = run_start[128];
   const int nw = stream_workers(T, gridDim.x * DECODE_WARPS, ws.fixed_workers);
   const int gw = blockIdx.x * DECODE_WARPS + warp;
-  if (gw >= nw) return;  // whole warp; the kernel has no CTA-wide barrier
+  if (gw >= nw) return;  // whole warp; no CTA-wide barrier follows
   const int lo = slice_lo(gw, T, nw), hi = slice_lo(gw + 1, T, nw);
   if (lo >= hi) return;
 
@@ -455,15 +484,23 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   }
   uint32_t phase_bits = 0;  // parity of the next completion to wait for, per stage
 
-  // first (sequence, kv head) of the slice: the last bh with tile_start[bh] <= lo
-  int a = 0, z = BH;
+  // first (sequence, kv head) of the slice: the run holding tile lo, then
+  // the pair inside it
+  int a = 0, z = 128;
   while (z - a > 1) {
     const int mid = (a + z) >> 1;
-    if (__ldg(ws.tile_start + mid) <= lo) a = mid;
+    if (run_start[mid] <= lo) a = mid;
     else z = mid;
   }
+  int bh0 = a * items, st0 = run_start[a];
+  for (;;) {
+    const int n0 = tile_list(P, bh0 / Hkv, bh0 % Hkv, false).n_virt;
+    if (st0 + n0 > lo) break;
+    st0 += n0;
+    ++bh0;
+  }
   Seg is;  // lookup / issue cursor
-  load_seg(P, ws.tile_start, a, is);
+  load_seg(P, bh0, st0, is);
   Seg cs = is;  // compute cursor
 
   const size_t blk_stride = (size_t)Hkv * bs * C::R;
@@ -478,7 +515,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   auto lookup = [&]() {
     nx_have = x_lookup < hi;
     if (nx_have) {
-      while (x_lookup >= is.end) load_seg(P, ws.tile_start, is.bh + 1, is);
+      while (x_lookup >= is.end) load_seg(P, is.bh + 1, is.end, is);
       nx_h = is.h;
       nx_key = DECODE_KEYS_PER_TILE * tile_of(is.t, x_lookup - is.start);
       nx_leff = is.t.Leff;
@@ -614,6 +651,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
 #pragma unroll 1
   for (int k = 0; k < NSTAGE - 1; ++k) issue();
 
+  grid_dependency_wait();  // query images and per-head constants are ready
   begin_seg(lo);
   int st = 0;
   // per-lane shared-memory offsets (loop invariant): key rows 4gq + 2m + hh,
@@ -637,7 +675,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
     issue();
     if (x >= cs.end) {
       flush_seg();
-      do load_seg(P, ws.tile_start, cs.bh + 1, cs);
+      do load_seg(P, cs.bh + 1, cs.end, cs);
       while (x >= cs.end);
       begin_seg(x);
     }
@@ -837,9 +875,17 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
   const int bh = b * Hkv + h;
   const int BH = P.batch * Hkv;
   float* out = P.out + (size_t)wid * D;
+  // the output transform's constants do not depend on the kernels before
+  float tsign[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const int d = lane + 32 * e;
+    if (P.mode == MODE_INT8) tsign[e] = __fdiv_rn(__ldg(P.ch_amax + ((size_t)Hkv + h) * D + d), 127.0f);  // V scales
+    else tsign[e] = (P.signs && __ldg(P.signs + d) < 0) ? -1.0f : 1.0f;
+  }
   grid_dependency_wait();  // every partial of the stream kernel is written
   const int T = ws.tile_start[BH];
-  const int start = __ldg(ws.tile_start + bh), end = __ldg(ws.tile_start + bh + 1);
+  const int start = ws.tile_start[bh], end = ws.tile_start[bh + 1];
   float o[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
@@ -853,12 +899,20 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
   const int nw = stream_workers(T, ws.nwall, ws.fixed_workers);
   const int w0 = worker_of(start, T, nw), w1 = worker_of(end - 1, T, nw);
   const int nrec = w1 - w0 + 1;
-  // lane j holds record w0 + j (+ 32 k): its running max and weight sum
-  float M = -CUDART_INF_F;
+  // one round trip for the first 32 records' sums and the first four
+  // records' outputs; lane j holds record w0 + j
   float2 ml0 = make_float2(-CUDART_INF_F, 0.0f);
-  for (int j = lane; j < nrec; j += 32) {
+  if (lane < nrec) ml0 = ws.part_ml[(size_t)(w0 + lane + bh) * G + i];
+  float v0[4][EPL];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float* po = ws.part_o + ((size_t)(w0 + u + bh) * G + i) * D;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v0[u][e] = u < nrec ? po[lane + 32 * e] : 0.0f;
+  }
+  float M = ml0.y > 0.0f ? ml0.x : -CUDART_INF_F;
+  for (int j = 32 + lane; j < nrec; j += 32) {
     const float2 ml = ws.part_ml[(size_t)(w0 + j + bh) * G + i];
-    if (j < 32) ml0 = ml;
     if (ml.y > 0.0f) M = fmaxf(M, ml.x);
   }
   M = warp_max(M);
@@ -877,7 +931,8 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
     const float f = (c0 + lane < nrec && ml.y > 0.0f) ? ex2(ml.x - M) : 0.0f;
     l += f * ml.y;
     const int n = min(32, nrec - c0);
-    // four records per round, their loads issued together
+    // four records per round, their loads issued together (the first round's
+    // were issued with the sums above)
     for (int k0 = 0; k0 < n; k0 += 4) {
       float fk[4];
       float v[4][EPL];
@@ -885,9 +940,14 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
       for (int u = 0; u < 4; ++u) {
         fk[u] = __shfl_sync(0xffffffffu, f, (k0 + u) & 31);
         const bool use = k0 + u < n && fk[u] != 0.0f;
-        const float* po = ws.part_o + ((size_t)(w0 + c0 + k0 + u + bh) * G + i) * D;
+        if (c0 == 0 && k0 == 0) {
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) v[u][e] = use ? po[lane + 32 * e] : 0.0f;
+          for (int e = 0; e < EPL; ++e) v[u][e] = use ? v0[u][e] : 0.0f;
+        } else {
+          const float* po = ws.part_o + ((size_t)(w0 + c0 + k0 + u + bh) * G + i) * D;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) v[u][e] = use ? po[lane + 32 * e] : 0.0f;
+        }
         if (!use) fk[u] = 0.0f;
       }
 #pragma unroll
@@ -919,17 +979,10 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
       }
     const float inv = 1.0f / ((float)D * l);
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const int d = lane + 32 * e;
-      out[d] = (__ldg(P.signs + d) < 0 ? -o[e] : o[e]) * inv;
-    }
+    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = tsign[e] * o[e] * inv;
   } else if (P.mode == MODE_INT8) {
-    const float* am = P.ch_amax + ((size_t)Hkv + h) * D;  // V channel scales
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const int d = lane + 32 * e;
-      out[d] = o[e] * __fdiv_rn(am[d], 127.0f) / l;
-    }
+    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = o[e] * tsign[e] / l;
   } else {
 #pragma unroll
     for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = o[e] / l;
@@ -948,7 +1001,7 @@ size_t stream_smem_bytes() {
 
 int decode_ctas_per_sm(int mode, int head_dim, int group) {
   (void)head_dim;
-  if (group > 4) return StreamCfg<MODE_INT4, 128, 2>::CTAS;
+  if (group > 4) return mode == MODE_INT8 ? StreamCfg<MODE_INT8, 128, 2>::CTAS : StreamCfg<MODE_INT4, 128, 2>::CTAS;
   return mode == MODE_INT8 ? StreamCfg<MODE_INT8, 128, 1>::CTAS : StreamCfg<MODE_INT4, 128, 1>::CTAS;
 }
 

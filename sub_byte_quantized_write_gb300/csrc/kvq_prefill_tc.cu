@@ -54,6 +54,9 @@ constexpr int TP_ISSUE_WARP = 13;
 // weights p reach at most 2^TP_SLACK and p * s stays inside fp16 for any
 // scale s below 65504 / 2^TP_SLACK (4094).
 constexpr float TP_SLACK = 4.0f;
+// sleep between polls of a barrier wait, by role (ns): the softmax and the
+// MMA issuer are the critical path, the copy issuer and the producers run ahead
+constexpr uint32_t TP_NAP_SOFTMAX = 20, TP_NAP_MMA = 20, TP_NAP_PRODUCER = 100, TP_NAP_ISSUER = 200;
 
 template <int MODE, int D>
 struct TpCfg {
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
 #pragma unroll 1
       for (int v = 0; v < n_virt; ++v) {
         // the producers are done with this raw stage (tile v - NRAW)
-        if (!mbar_wait_bounded(bar + B_RAWEMPTY + rs, rphase ^ 1) || *abort_flag) {
+        if (!mbar_wait_bounded(bar + B_RAWEMPTY + rs, rphase ^ 1, TP_NAP_ISSUER) || *abort_flag) {
           *abort_flag = 1;
           flag_error(P.dev_error, DEVERR_TIMEOUT);
           break;
@@ -456,8 +459,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
 #pragma unroll 1
     for (int v = 0; v < n_virt; ++v) {
       // raw tile v has landed; the tensor cores are done with this K/V stage
-      const bool late = !mbar_wait_bounded(bar + B_RAWFULL + rs, rphase) ||
-                        !mbar_wait_bounded(bar + B_KVEMPTY + kvs, kv_phase ^ 1);
+      const bool late = !mbar_wait_bounded(bar + B_RAWFULL + rs, rphase, TP_NAP_PRODUCER) ||
+                        !mbar_wait_bounded(bar + B_KVEMPTY + kvs, kv_phase ^ 1, TP_NAP_PRODUCER);
       if (late || *abort_flag) {
         *abort_flag = 1;
         flag_error(P.dev_error, DEVERR_TIMEOUT);
@@ -532,7 +535,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
       // O += P V with P (hi / lo interleaved per 16 keys, where the tile's S
       // was) from TMEM and V^T from shared memory
       auto pv = [&](int i, int kvs_i) -> bool {
-        if (!mbar_wait_bounded(bar + B_PFULL, i & 1)) return false;
+        if (!mbar_wait_bounded(bar + B_PFULL, i & 1, TP_NAP_MMA)) return false;
         tc::fence_after();
         const uint32_t a_vt = smem_addr(sm + C::OFF_VT + kvs_i * C::VTILE);
         const uint32_t p_tm = tmem + (i & 1) * TP_KT;
@@ -553,7 +556,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
         const int st = v & 1;
         // S(v) goes where P(v - 2) was: P.V(v - 2) was issued before it and
         // the tensor cores run this thread's MMAs in order
-        if (!mbar_wait_bounded(bar + B_KVFULL + kvs, kv_phase)) {
+        if (!mbar_wait_bounded(bar + B_KVFULL + kvs, kv_phase, TP_NAP_MMA)) {
           ok = false;
           break;
         }
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
       const int st = v & 1;
       const int T = tile_of(v);
       // every decision around a .sync.aligned TMEM access is warp-uniform
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_SFULL + st, (v >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_SFULL + st, (v >> 1) & 1, TP_NAP_SOFTMAX))) {
         ok = false;
         break;
       }
@@ -655,7 +658,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
       // that left the loop turns into an error, not a hang)
       xmax[(st * 2 + hf) * TP_ROWS + r] = ymax;
       tc::mbar_arrive(bar + B_XCH + quad * 2 + st);
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_XCH + quad * 2 + st, (v >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_XCH + quad * 2 + st, (v >> 1) & 1, TP_NAP_SOFTMAX))) {
         ok = false;
         break;
       }
@@ -668,7 +671,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
       const float mref = grow ? tmax : mrow;
       const float muse = mref == -CUDART_INF_F ? 0.0f : mref;
       // the previous P.V must be done before P is overwritten or O rescaled
-      if (v >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_ODONE, (v - 1) & 1))) {
+      if (v >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_ODONE, (v - 1) & 1, TP_NAP_SOFTMAX))) {
         ok = false;
         break;
       }
