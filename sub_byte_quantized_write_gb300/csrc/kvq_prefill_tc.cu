@@ -476,16 +476,30 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
       uint8_t* vt = sm + C::OFF_VT + kvs * C::VTILE;
       // K: key rows, 8 dims per 16-byte chunk (rows of skipped chunks hold
       // stale bytes: finite codes, masked in the softmax)
-      for (int it = pt; it < TP_KT * (D / 8); it += TP_PRODUCERS) {
-        const int key = it / (D / 8), c8 = it % (D / 8);
-        const uint4 hv = codes8<MODE>(rk + key * C::R, c8);
-        *reinterpret_cast<uint4*>(kt + (c8 >> 3) * C::KATOM + tc::sw128_off(key, c8 & 7)) = hv;
+      {
+        // thread pt always expands the same 8 dims (c8) of keys pt / (D/8) + step * j
+        constexpr int ITEMS = TP_KT * (D / 8) / TP_PRODUCERS;
+        constexpr int KSTEP = TP_PRODUCERS / (D / 8);
+        static_assert(TP_KT * (D / 8) % TP_PRODUCERS == 0 && TP_PRODUCERS % (D / 8) == 0, "K expansion split");
+        const int c8 = pt % (D / 8), key_0 = pt / (D / 8);
+        const uint8_t* src = rk + key_0 * C::R;
+        uint8_t* dst = kt + (c8 >> 3) * C::KATOM;
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j) {
+          const int key = key_0 + KSTEP * j;
+          const uint4 hv = codes8<MODE>(src + KSTEP * j * C::R, c8);
+          *reinterpret_cast<uint4*>(dst + tc::sw128_off(key, c8 & 7)) = hv;
+        }
       }
       // V^T: 8 keys x 32 dims per stmatrix (four 8x8 blocks, stored transposed)
       {
         const int g8 = lane >> 2, t4 = lane & 3;
         constexpr int JOBS = (TP_KT / 8) * (D / 32);
-        for (int job = pwarp; job < JOBS; job += TP_PRODUCERS / 32) {
+        constexpr int PW = TP_PRODUCERS / 32;
+        static_assert(JOBS % PW == 0, "V expansion split");
+#pragma unroll
+        for (int jj = 0; jj < JOBS / PW; ++jj) {
+          const int job = pwarp + PW * jj;
           const int kb = job % (TP_KT / 8), db = job / (TP_KT / 8);  // key block, 32-dim block
           const uint8_t* row = rvp + (8 * kb + g8) * C::R;
           uint32_t r4[4];
@@ -622,6 +636,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
       const int key0 = TP_KT * T;
       const bool full = kv4 == 15 && key0 + TP_KT - 1 <= rp && key0 + TP_KT <= Leff &&
                         (W <= 0 || key0 > rp - W || key0 + TP_KT <= P.sink);
+      const bool all_full = __all_sync(0xffffffffu, full);
       const uint32_t s_col = tmem + lane_base + st * TP_KT;
       float ymax = -CUDART_INF_F;
 #pragma unroll 1
@@ -641,17 +656,20 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
           for (int e = 0; e < 4; ++e) {
             const int jj = 4 * j4 + e;
             const float dot = __uint_as_float(rr[jj]);
-            float y = MODE == MODE_INT8 ? dot : fmaf(ksv[e], dot, rho * kzv[e]);
-            if (!full) {
-              const int j = key0 + 16 * c + jj;
-              bool vis = ((kv4 >> c) & 1) && j <= rp && j < Leff;
-              if (W > 0) vis = vis && (j < P.sink || j > rp - W);
-              y = vis ? y : -CUDART_INF_F;
-            }
-            rr[jj] = __float_as_uint(y);
-            ymax = fmaxf(ymax, y);
+            rr[jj] = __float_as_uint(MODE == MODE_INT8 ? dot : fmaf(ksv[e], dot, rho * kzv[e]));
           }
         }
+        if (!all_full) {  // warp-uniform: masks only where some row of the warp needs them
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = key0 + 16 * c + jj;
+            bool vis = ((kv4 >> c) & 1) && j <= rp && j < Leff;
+            if (W > 0) vis = vis && (j < P.sink || j > rp - W);
+            if (!vis) rr[jj] = __float_as_uint(-CUDART_INF_F);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) ymax = fmaxf(ymax, __uint_as_float(rr[jj]));
         tc::st16(s_col + 16 * c, rr);
       }
       // the pair's maxima meet in shared memory (bounded wait: a partner
