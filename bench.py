@@ -398,13 +398,20 @@ def run_gpu(args, rank, world, local_rank):
         dtype = "u4 codes x fp16 (hi+lo) tcgen05 math, fp32 TMEM accumulate/softmax"
     if wl.mode == gen.MODE_INT8:
         launches += 1  # INT8 write: channel-amax kernel (returns at once once the scales exist) + quantise kernel
+    wr = sum(wr_ms) / len(wr_ms)
+    write_gbs = units["write"] / (wr / 1e3) / 1e9
+    write_roof = {"bound": "hbm", "kernel": "kvq_write (RHT, scale / zero point, codes, pack, scatter)",
+                  "achieved": round(write_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(write_gbs / hbm, 4),
+                  "algorithmic_bytes_per_launch": units["write"],
+                  "note": "bf16 K/V in + packed rows out; a 1-token decode write is launch-latency bound"}
     result = {
         "metric": metric, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded; K/V ~ N(0,1)%s)" % (", 1% outlier channels x10" if args.workload in ("llama_int4", "prefill_int4") else ""),
-        "config": cfg, **extra, "write_ms": round(sum(wr_ms) / len(wr_ms), 5),
+        "config": cfg, **extra, "write_ms": round(wr, 5),
         "roofline": roof,
+        "write_roofline": write_roof,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(sum(e2e_ms) / len(e2e_ms), 5)},
         "gpu_launches": launches * args.steps,

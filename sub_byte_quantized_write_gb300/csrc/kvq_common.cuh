@@ -207,6 +207,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, sleep_ns);
 }
+// Predicated forms for code run by a whole warp where one lane acts: no
+// divergent branch around them.
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(bool pred, uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}\n" ::"r"(
+          smem_addr(bar)),
+      "r"(bytes), "r"((int)pred)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_if(bool pred, void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}\n" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "r"((int)pred)
+      : "memory");
+}
 // global -> shared bulk copy of `bytes` (multiple of 16, both ends 16-byte
 // aligned), completion counted on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -550,17 +550,15 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
         valid |= (ok ? 1 : 0) << c;
       }
       if constexpr (BULK) {
-        if (lane == 0) {
-          wvld[st_issue] = valid;
-          const uint32_t bytes = (uint32_t)(__popc(valid) * 2 * C::CHUNK);
-          mbar_arrive_expect_tx(bars + st_issue, bytes);
+        // lane 0 acts through predicates, so the warp forms no divergent region
+        const bool l0 = lane == 0;
+        if (l0) wvld[st_issue] = valid;
+        mbar_arrive_expect_tx_if(l0, bars + st_issue, (uint32_t)(__popc(valid) * 2 * C::CHUNK));
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            if ((valid >> c) & 1) {
-              bulk_g2s(kt + c * C::CHUNK, kbase + off[c], C::CHUNK, bars + st_issue);
-              bulk_g2s(vt + c * C::CHUNK, vbase + off[c], C::CHUNK, bars + st_issue);
-            }
-          }
+        for (int c = 0; c < 2; ++c) {
+          const bool go = l0 && ((valid >> c) & 1);
+          bulk_g2s_if(go, kt + c * C::CHUNK, kbase + off[c], C::CHUNK, bars + st_issue);
+          bulk_g2s_if(go, vt + c * C::CHUNK, vbase + off[c], C::CHUNK, bars + st_issue);
         }
       } else {
 #pragma unroll
