@@ -272,14 +272,19 @@ def run_gpu(args, rank, world, local_rank):
         write_call()
         attn_call()
 
-    # the step's two library calls are captured once into CUDA graphs and
+    # The step's two library calls are captured once into a CUDA graph and
     # replayed, so the timed region holds only device work (re-writing the
-    # same new tokens at the same positions is idempotent)
+    # same new tokens at the same positions is idempotent).  One graph holds
+    # the whole step (its kernels chain with programmatic dependent launch);
+    # two more hold one call each, for the per-call breakdown and rooflines.
     with torch.cuda.stream(stream):
         for _ in range(2):
             step()  # first calls set the kernels' shared-memory attributes outside capture
         stream.synchronize()
-        g_write, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        g_step, g_write, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step, stream=stream):
+            write_call()
+            attn_call()
         with torch.cuda.graph(g_write, stream=stream):
             write_call()
         with torch.cuda.graph(g_attn, stream=stream):
@@ -287,19 +292,27 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(args.warmup):
         with torch.cuda.stream(stream):
             flush.fill_(1.0)
+        g_step.replay()
         g_write.replay()
         g_attn.replay()
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
-            for i in range(args.steps):
+            for i in range(args.steps):  # the K timed steps
                 flush.fill_(float(i))  # no step reuses the previous step's L2 lines
+                a, c = evs[i]
+                a.record(stream)
+                g_step.replay()
+                c.record(stream)
+            for i in range(args.steps):  # per-call breakdown, same steps replayed call by call
+                flush.fill_(float(i))
                 e0, e1, e2 = ev[i]
                 e0.record(stream)
                 g_write.replay()
@@ -307,7 +320,7 @@ def run_gpu(args, rank, world, local_rank):
                 g_attn.replay()
                 e2.record(stream)
         torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    step_ms = [a.elapsed_time(c) for a, c in evs]
     att_ms = [b.elapsed_time(c) for a, b, c in ev]
     wr_ms = [a.elapsed_time(b) for a, b, c in ev]
     ms = sum(step_ms) / len(step_ms)
@@ -364,7 +377,8 @@ def run_gpu(args, rank, world, local_rank):
            "mode": {0: "int4", 1: "int2", 2: "int8"}[wl.mode], "headwise_table": bool(wl.headwise),
            "cached_tokens": int(wl.seq_lens.sum()), "new_tokens_per_step": int(wl.n_new.sum()),
            "pool_blocks": wl.num_blocks, "rht": wl.signs is not None,
-           "timing": "CUDA graphs of the write call and the attention call, events around each replay",
+           "timing": "one CUDA graph per step (write + attention call), events around each replay; "
+                     "per-call graphs for the breakdown",
            "l2": "flushed between timed steps (256 MB write)",
            "parallelism": "replicas only" if world > 1 else "single GPU"}
     if args.workload == "llama_int4":

@@ -308,12 +308,22 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
       __syncthreads();
     }
     if (threadIdx.x == 0) ws.tile_start[BH] = running;
+    grid_dependency_wait();  // see below
     return;
   }
 
+  // This kernel may start while the write kernel before it still runs
+  // (programmatic launch): nothing here reads what the write produces except
+  // the INT8 channel scales, so INT8 waits for the write first and the other
+  // modes only before exiting -- the stream kernel, which waits for this
+  // grid, then also sees the new tokens.
+  if (MODE == MODE_INT8) grid_dependency_wait();
   // query fragments of one (sequence, kv head)
   const int bh = blockIdx.x - 1;
-  if (bh >= BH) return;
+  if (bh >= BH) {
+    grid_dependency_wait();
+    return;
+  }
   const int b = bh / Hkv, h = bh % Hkv;
   const float log2e = 1.4426950408889634f;
   const float dnorm = (MODE != MODE_INT8 && P.signs) ? (float)D : 1.0f;
@@ -385,6 +395,7 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
     const __half2 pr = __halves2half2(qh[hl][head][d0], qh[hl][head][d1]);
     dst[idx] = *reinterpret_cast<const uint32_t*>(&pr);
   }
+  if (MODE != MODE_INT8) grid_dependency_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -434,8 +445,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   allow_dependent_launch();  // the merge kernel may launch; it waits for this grid to finish
   // Slices come from the tile counts themselves (a prefix scan per CTA over
   // all (sequence, kv head) pairs, thread t owning a contiguous run of
-  // pairs), so the first page copies go out while the preparation kernel
-  // still builds the query images.
+  // pairs), worked out while the kernels before still run.
   __shared__ int run_start[129];
   const int items = (BH + 127) / 128;
   {
@@ -646,10 +656,13 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   };
 
   lookup();
+  // Copies wait for the kernels before: the write of this step's tokens may
+  // still run (the preparation kernel starts alongside it), and the query
+  // images and per-head constants must be ready.
+  grid_dependency_wait();
 #pragma unroll 1
   for (int k = 0; k < NSTAGE - 1; ++k) issue();
 
-  grid_dependency_wait();  // query images and per-head constants are ready
   begin_seg(lo);
   int st = 0;
   // per-lane shared-memory offsets (loop invariant): key rows 4gq + 2m + hh,
@@ -1033,7 +1046,8 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int BH = P.batch * P.num_kv_heads;
-  decode_prep_kernel<MODE, D, NT><<<BH + 1, 128, 0, stream>>>(P, ws);
+  e = launch_dependent(decode_prep_kernel<MODE, D, NT>, dim3(BH + 1), dim3(128), 0, stream, P, ws);
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the stream and merge kernels launch programmatically: their CTAs become

@@ -95,6 +95,9 @@ __global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
   constexpr int LEVELS = (1 << BITS) - 1;
   constexpr int DATA = data_bytes(MODE, D);
   const int lane = threadIdx.x & 31;
+  // a decode call after this write may start its query preparation now; it
+  // waits for this grid before anything reads the pages written here
+  allow_dependent_launch();
   const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int kv = (int)(wid & 1);
   const long long th = wid >> 1;
@@ -171,6 +174,7 @@ template <int D>
 __global__ void __launch_bounds__(256) int8_quant_kernel(WriteParams P) {
   constexpr int EPL = D / 32;
   const int lane = threadIdx.x & 31;
+  allow_dependent_launch();  // as in write_token_head_kernel
   const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (blockIdx.x == 0 && threadIdx.x == 0) *P.ch_ready = 1;  // later calls reuse the scales
   const int kv = (int)(wid & 1);
