@@ -207,7 +207,7 @@ struct TileList {
   bool gap;
 };
 
-__device__ __forceinline__ TileList tile_list(const AttnParams& P, int b, int h, bool flag_errors) {
+__device__ __forceinline__ TileList tile_list(const AttnParams& P, int b, int h, bool flag_errors, int KT) {
   TileList t;
   int L = __ldg(P.seq_lens + b);
   if (L < 0) {
@@ -221,15 +221,15 @@ __device__ __forceinline__ TileList tile_list(const AttnParams& P, int b, int h,
     t.Leff = P.max_blocks * P.block_size;
   }
   t.W = P.window ? __ldg(P.window + h) : 0;
-  t.n_total = (t.Leff + DECODE_KEYS_PER_TILE - 1) / DECODE_KEYS_PER_TILE;
+  t.n_total = (t.Leff + KT - 1) / KT;
   t.ns = 0;
   t.tw = 0;
   t.gap = false;
   if (t.W > 0) {
     const int kw = (L - 1) - t.W + 1;  // first key inside the window of the query at L - 1
     if (kw > 0) {
-      t.ns = (min(P.sink, t.Leff) + DECODE_KEYS_PER_TILE - 1) / DECODE_KEYS_PER_TILE;
-      t.tw = kw / DECODE_KEYS_PER_TILE;
+      t.ns = (min(P.sink, t.Leff) + KT - 1) / KT;
+      t.tw = kw / KT;
       t.gap = t.tw > t.ns;
     }
   }
@@ -251,6 +251,24 @@ __device__ __forceinline__ int slice_lo(int w, int T, int nw) { return (int)((lo
 __device__ __forceinline__ int worker_of(int x, int T, int nw) {
   return min(nw - 1, (int)(((long long)(x + 1) * nw - 1) / T));
 }
+
+// ---------------------------------------------------------------------------
+// Stream-kernel shape per configuration (from sweeps on the decode
+// workloads): keys per tile, ring depth and CTAs per SM.  INT4 with GQA
+// groups up to 4 takes 64-key tiles (two independent 32-key halves per step
+// of a warp) at 3 CTAs per SM; the others 32-key tiles, NT == 1 kernels at 4
+// CTAs per SM (3 for INT8's larger rows), NT == 2 kernels at 3 (2 for INT8).
+template <int MODE, int D, int NT>
+struct StreamCfg {
+  static constexpr int KT = (MODE == MODE_INT4 && NT == 1) ? 64 : 32;
+  static constexpr int NCH = KT / 16;  // 16-row page chunks per tile
+  static constexpr int NH2 = KT / 32;  // 32-key halves per tile
+  static constexpr int NSTAGE = NT == 1 ? (MODE == MODE_INT4 ? 2 : (MODE == MODE_INT2 ? 5 : 2))
+                                        : (MODE == MODE_INT4 ? 4 : (MODE == MODE_INT2 ? 3 : 3));
+  static constexpr int CTAS = NT == 1 ? (MODE == MODE_INT4 ? 3 : (MODE == MODE_INT8 ? 3 : 4)) : (MODE == MODE_INT8 ? 2 : 3);
+  static constexpr int TILE = KT * row_bytes_of(MODE, D);  // key rows of K (or V)
+  static constexpr int STAGE = 2 * TILE;                   // K tile then V tile
+};
 
 // ---------------------------------------------------------------------------
 // 1. preparation
@@ -285,7 +303,7 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
 #pragma unroll
       for (int k = 0; k < ITEMS; ++k) {
         const int bh = first + k;
-        n[k] = bh < BH ? tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0).n_virt : 0;
+        n[k] = bh < BH ? tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0, StreamCfg<MODE, D, NT>::KT).n_virt : 0;
         tsum += n[k];
       }
       int incl = tsum;
@@ -401,16 +419,6 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
 // ---------------------------------------------------------------------------
 // 2. stream kernel
 
-// Ring depth and residency (from sweeps on the decode workloads): NT == 1
-// kernels run 4 CTAs per SM (3 for INT8's larger rows), NT == 2 kernels 3
-// (2 for INT8); the ring is sized to fit.
-template <int MODE, int D, int NT>
-struct StreamCfg {
-  static constexpr int NSTAGE = NT == 1 ? (MODE == MODE_INT4 ? 2 : (MODE == MODE_INT2 ? 5 : 2))
-                                        : (MODE == MODE_INT4 ? 4 : (MODE == MODE_INT2 ? 3 : 3));
-  static constexpr int CTAS = NT == 1 ? (MODE == MODE_INT8 ? 3 : 4) : (MODE == MODE_INT8 ? 2 : 3);
-};
-
 // One (sequence, kv head) as seen by a cursor walking the global tile order.
 struct Seg {
   int bh, h, start, end;
@@ -419,12 +427,12 @@ struct Seg {
 };
 
 // Pair bh whose tiles start at global tile `start`.
-__device__ __forceinline__ void load_seg(const AttnParams& P, int bh, int start, Seg& s) {
+__device__ __forceinline__ void load_seg(const AttnParams& P, int bh, int start, Seg& s, int KT) {
   const int Hkv = P.num_kv_heads;
   s.bh = bh;
   const int b = bh / Hkv, h = bh % Hkv;
   s.h = h;
-  s.t = tile_list(P, b, h, false);
+  s.t = tile_list(P, b, h, false, KT);
   s.start = start;
   s.end = start + s.t.n_virt;
   s.tbl = P.table + (size_t)(P.headwise ? bh : b) * P.max_blocks;
@@ -433,7 +441,9 @@ __device__ __forceinline__ void load_seg(const AttnParams& P, int bh, int start,
 template <int MODE, int D, int NT>
 __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_stream_kernel(AttnParams P, DecodeWs ws) {
   using C = DecCfg<MODE, D>;
-  constexpr int NSTAGE = StreamCfg<MODE, D, NT>::NSTAGE;
+  using SC = StreamCfg<MODE, D, NT>;
+  constexpr int NSTAGE = SC::NSTAGE;
+  constexpr int KT = SC::KT, NCH = SC::NCH, NH2 = SC::NH2;
   constexpr int NH = 4 * NT;
   constexpr int PER_LANE = NT * C::KSTEPS * 2;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -453,7 +463,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
     int tsum = 0;
     for (int k = 0; k < items && first + k < BH; ++k) {
       const int bh = first + k;
-      tsum += tile_list(P, bh / Hkv, bh % Hkv, false).n_virt;
+      tsum += tile_list(P, bh / Hkv, bh % Hkv, false, KT).n_virt;
     }
     int incl = tsum;
 #pragma unroll
@@ -481,9 +491,9 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   // by a per-stage mbarrier); INT8 rows are XOR-swizzled by 16-byte piece on
   // the way in, so they use per-lane cp.async.
   constexpr bool BULK = MODE != MODE_INT8;
-  uint8_t* ring = smem + warp * NSTAGE * C::STAGE;
-  int* wvld = reinterpret_cast<int*>(smem + DECODE_WARPS * NSTAGE * C::STAGE) + warp * NSTAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * NSTAGE * C::STAGE + DECODE_WARPS * NSTAGE * 4) +
+  uint8_t* ring = smem + warp * NSTAGE * SC::STAGE;
+  int* wvld = reinterpret_cast<int*>(smem + DECODE_WARPS * NSTAGE * SC::STAGE) + warp * NSTAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * NSTAGE * SC::STAGE + DECODE_WARPS * NSTAGE * 4) +
                    warp * NSTAGE;
   if constexpr (BULK) {
     if (lane == 0) {
@@ -504,13 +514,13 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   }
   int bh0 = a * items, st0 = run_start[a];
   for (;;) {
-    const int n0 = tile_list(P, bh0 / Hkv, bh0 % Hkv, false).n_virt;
+    const int n0 = tile_list(P, bh0 / Hkv, bh0 % Hkv, false, KT).n_virt;
     if (st0 + n0 > lo) break;
     st0 += n0;
     ++bh0;
   }
   Seg is;  // lookup / issue cursor
-  load_seg(P, bh0, st0, is);
+  load_seg(P, bh0, st0, is, KT);
   Seg cs = is;  // compute cursor
 
   const size_t blk_stride = (size_t)Hkv * bs * C::R;
@@ -520,17 +530,19 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   // latency of the block-id load overlaps a whole tile of compute.
   int x_lookup = lo;                 // next tile to look up
   int nx_h = 0, nx_key = 0, nx_leff = 0;
-  int nx_blk[2] = {0, 0};
+  int nx_blk[NCH];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) nx_blk[c] = 0;
   bool nx_have = false;
   auto lookup = [&]() {
     nx_have = x_lookup < hi;
     if (nx_have) {
-      while (x_lookup >= is.end) load_seg(P, is.bh + 1, is.end, is);
+      while (x_lookup >= is.end) load_seg(P, is.bh + 1, is.end, is, KT);
       nx_h = is.h;
-      nx_key = DECODE_KEYS_PER_TILE * tile_of(is.t, x_lookup - is.start);
+      nx_key = KT * tile_of(is.t, x_lookup - is.start);
       nx_leff = is.t.Leff;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         const int key = nx_key + 16 * c;
         nx_blk[c] = key < nx_leff ? __ldg(is.tbl + (key >> bs_log2)) : -1;
       }
@@ -541,14 +553,14 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   int st_issue = 0;
   auto issue = [&]() {
     if (nx_have) {
-      uint8_t* kt = ring + st_issue * C::STAGE;
-      uint8_t* vt = kt + C::TILE;
+      uint8_t* kt = ring + st_issue * SC::STAGE;
+      uint8_t* vt = kt + SC::TILE;
       const uint8_t* kbase = P.k_pages + (size_t)nx_h * bs * C::R;
       const uint8_t* vbase = P.v_pages + (size_t)nx_h * bs * C::R;
       int valid = 0;
-      size_t off[2];
+      size_t off[NCH];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         const int key = nx_key + 16 * c;
         const int blk = nx_blk[c];
         bool ok = blk >= 0;  // -1: evicted (never addressed) or beyond the sequence
@@ -565,14 +577,14 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
         if (l0) wvld[st_issue] = valid;
         mbar_arrive_expect_tx_if(l0, bars + st_issue, (uint32_t)(__popc(valid) * 2 * C::CHUNK));
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < NCH; ++c) {
           const bool go = l0 && ((valid >> c) & 1);
           bulk_g2s_if(go, kt + c * C::CHUNK, kbase + off[c], C::CHUNK, bars + st_issue);
           bulk_g2s_if(go, vt + c * C::CHUNK, vbase + off[c], C::CHUNK, bars + st_issue);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < NCH; ++c) {
           const uint8_t* ks = kbase + off[c];
           const uint8_t* vs = vbase + off[c];
           const int nbytes = ((valid >> c) & 1) ? 16 : 0;
@@ -686,105 +698,119 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
     issue();
     if (x >= cs.end) {
       flush_seg();
-      do load_seg(P, cs.bh + 1, cs.end, cs);
+      do load_seg(P, cs.bh + 1, cs.end, cs, KT);
       while (x >= cs.end);
       begin_seg(x);
     }
-    const uint8_t* kt = ring + st * C::STAGE;
-    const uint8_t* vt = kt + C::TILE;
+    const uint8_t* kt = ring + st * SC::STAGE;
+    const uint8_t* vt = kt + SC::TILE;
     const int valid = wvld[st];
     st = st + 1 == NSTAGE ? 0 : st + 1;
-    const int key0 = DECODE_KEYS_PER_TILE * tile_of(cs.t, x - cs.start);
+    const int key0 = KT * tile_of(cs.t, x - cs.start);
     const int Leff = cs.t.Leff, W = cs.t.W, p_q = cs.t.L - 1;
     // every key of the tile visible (the common case): no per-key masks
-    const bool full = valid == 3 && key0 + DECODE_KEYS_PER_TILE <= Leff &&
-                      (W <= 0 || key0 > p_q - W || key0 + DECODE_KEYS_PER_TILE <= P.sink);
+    const bool full = valid == (1 << NCH) - 1 && key0 + KT <= Leff &&
+                      (W <= 0 || key0 > p_q - W || key0 + KT <= P.sink);
 
-    // ---- S^T = U_K (keys x D) . Q (D x slots); lane rows: keys 4gq + 2m + hh
-    float sacc[2][NT][4];
+    // ---- S^T = U_K (keys x D) . Q (D x slots), per 32-key half h2; lane
+    // rows: keys 32 h2 + 4gq + 2m + hh
+    float sacc[NH2][2][NT][4];
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) sacc[m][nt][r] = 0.0f;
-#pragma unroll
-    for (int wi = 0; wi < C::WPL; ++wi) {
-      uint32_t kw[2][2];
+    for (int h2 = 0; h2 < NH2; ++h2)
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          if constexpr (MODE == MODE_INT8) kw[m][hh] = load_kword<MODE, D>(kt, 4 * gq + 2 * m + hh, 4 * wi + tq);
-          else kw[m][hh] = lds32(kt + koff + (2 * m + hh) * C::R + 16 * wi);
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) sacc[h2][m][nt][r] = 0.0f;
+#pragma unroll
+    for (int wi = 0; wi < C::WPL; ++wi) {
+      uint32_t kw[NH2][2][2];
+#pragma unroll
+      for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            if constexpr (MODE == MODE_INT8)
+              kw[h2][m][hh] = load_kword<MODE, D>(kt, 32 * h2 + 4 * gq + 2 * m + hh, 4 * wi + tq);
+            else kw[h2][m][hh] = lds32(kt + koff + (32 * h2 + 2 * m + hh) * C::R + 16 * wi);
+          }
       Unroll<C::KPW, MODE>::run([&](auto sig_c) {
         constexpr int sig = decltype(sig_c)::value;
         const int s = C::KPW * wi + sig;
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          uint32_t a[4];
-          if constexpr (MODE == MODE_INT4) {
-            a[0] = kpair_int4_fold<2 * sig>(kw[m][0]);
-            a[1] = kpair_int4_fold<2 * sig>(kw[m][1]);
-            a[2] = kpair_int4_fold<2 * sig + 1>(kw[m][0]);
-            a[3] = kpair_int4_fold<2 * sig + 1>(kw[m][1]);
-          } else {
-            a[0] = kpair<MODE, 2 * sig>(kw[m][0]);
-            a[1] = kpair<MODE, 2 * sig>(kw[m][1]);
-            a[2] = kpair<MODE, 2 * sig + 1>(kw[m][0]);
-            a[3] = kpair<MODE, 2 * sig + 1>(kw[m][1]);
-          }
+        for (int h2 = 0; h2 < NH2; ++h2)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[m][nt], a, bq[nt][s][0], bq[nt][s][1]);
-        }
+          for (int m = 0; m < 2; ++m) {
+            uint32_t a[4];
+            if constexpr (MODE == MODE_INT4) {
+              a[0] = kpair_int4_fold<2 * sig>(kw[h2][m][0]);
+              a[1] = kpair_int4_fold<2 * sig>(kw[h2][m][1]);
+              a[2] = kpair_int4_fold<2 * sig + 1>(kw[h2][m][0]);
+              a[3] = kpair_int4_fold<2 * sig + 1>(kw[h2][m][1]);
+            } else {
+              a[0] = kpair<MODE, 2 * sig>(kw[h2][m][0]);
+              a[1] = kpair<MODE, 2 * sig>(kw[h2][m][1]);
+              a[2] = kpair<MODE, 2 * sig + 1>(kw[h2][m][0]);
+              a[3] = kpair<MODE, 2 * sig + 1>(kw[h2][m][1]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[h2][m][nt], a, bq[nt][s][0], bq[nt][s][1]);
+          }
       });
     }
 
     // ---- logits (log2 units), masks, online softmax
-    float lg[2][2][NT];
-    float sv_[2][2], mv_[2][2];
-    bool vk[2][2];
+    float lg[NH2][2][2][NT];
+    float sv_[NH2][2][2], mv_[NH2][2][2];
+    bool vk[NH2][2][2];
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
+    for (int h2 = 0; h2 < NH2; ++h2)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int kappa = 4 * gq + 2 * m + hh;
-        bool ok = true;
-        if (!full) {
-          const int j = key0 + kappa;
-          ok = ((valid >> (kappa >> 4)) & 1) && j < Leff;
-          if (W > 0) ok = ok && (j < P.sink || j > p_q - W);
-        }
-        vk[m][hh] = ok;
-        float sk = 0.0f, mk = 0.0f;
-        if constexpr (MODE != MODE_INT8) {
-          const uint32_t pk = lds32(kt + poff + (2 * m + hh) * C::R);
-          const uint32_t pv = lds32(vt + poff + (2 * m + hh) * C::R);
-          constexpr float half_range = (float)(1 << (C::BITS - 1));
-          sk = __half2float(__ushort_as_half((unsigned short)(pk & 0xFFFF)));
-          mk = fmaf(half_range, sk, __half2float(__ushort_as_half((unsigned short)(pk >> 16))));
-          sv_[m][hh] = __half2float(__ushort_as_half((unsigned short)(pv & 0xFFFF)));
-          mv_[m][hh] = fmaf(half_range, sv_[m][hh], __half2float(__ushort_as_half((unsigned short)(pv >> 16))));
-        } else {
-          sv_[m][hh] = 1.0f;
-          mv_[m][hh] = 0.0f;
-        }
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float cdot = sacc[m][nt][2 * hh] + sacc[m][nt][2 * hh + 1];  // hi + lo slots
-          if constexpr (MODE == MODE_INT4) cdot -= kcorr[nt];
-          float zz;
-          if constexpr (MODE == MODE_INT8) zz = bet[nt] * cdot;
-          else zz = fmaf(bet[nt] * sk, cdot, gam[nt] * mk);
-          lg[m][hh][nt] = ok ? zz : -CUDART_INF_F;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int kappa = 32 * h2 + 4 * gq + 2 * m + hh;
+          bool ok = true;
+          if (!full) {
+            const int j = key0 + kappa;
+            ok = ((valid >> (kappa >> 4)) & 1) && j < Leff;
+            if (W > 0) ok = ok && (j < P.sink || j > p_q - W);
+          }
+          vk[h2][m][hh] = ok;
+          float sk = 0.0f, mk = 0.0f;
+          if constexpr (MODE != MODE_INT8) {
+            const uint32_t pk = lds32(kt + poff + (32 * h2 + 2 * m + hh) * C::R);
+            const uint32_t pv = lds32(vt + poff + (32 * h2 + 2 * m + hh) * C::R);
+            constexpr float half_range = (float)(1 << (C::BITS - 1));
+            sk = __half2float(__ushort_as_half((unsigned short)(pk & 0xFFFF)));
+            mk = fmaf(half_range, sk, __half2float(__ushort_as_half((unsigned short)(pk >> 16))));
+            sv_[h2][m][hh] = __half2float(__ushort_as_half((unsigned short)(pv & 0xFFFF)));
+            mv_[h2][m][hh] =
+                fmaf(half_range, sv_[h2][m][hh], __half2float(__ushort_as_half((unsigned short)(pv >> 16))));
+          } else {
+            sv_[h2][m][hh] = 1.0f;
+            mv_[h2][m][hh] = 0.0f;
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float cdot = sacc[h2][m][nt][2 * hh] + sacc[h2][m][nt][2 * hh + 1];  // hi + lo slots
+            if constexpr (MODE == MODE_INT4) cdot -= kcorr[nt];
+            float zz;
+            if constexpr (MODE == MODE_INT8) zz = bet[nt] * cdot;
+            else zz = fmaf(bet[nt] * sk, cdot, gam[nt] * mk);
+            lg[h2][m][hh][nt] = ok ? zz : -CUDART_INF_F;
+          }
         }
-      }
 
-    uint32_t xh[NT][2], xl[NT][2];  // packed (P s) hi / lo per m: (key hh=0, key hh=1)
+    uint32_t xh[NH2][NT][2], xl[NH2][NT][2];  // packed (P s) hi / lo per (h2, m): (key hh=0, key hh=1)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float tmax = fmaxf(fmaxf(lg[0][0][nt], lg[0][1][nt]), fmaxf(lg[1][0][nt], lg[1][1][nt]));
+      float tmax = -CUDART_INF_F;
+#pragma unroll
+      for (int h2 = 0; h2 < NH2; ++h2)
+        tmax = fmaxf(tmax, fmaxf(fmaxf(lg[h2][0][0][nt], lg[h2][0][1][nt]), fmaxf(lg[h2][1][0][nt], lg[h2][1][1][nt])));
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
@@ -802,62 +828,67 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
       }
       float tl = 0.0f, tpm = 0.0f;  // tile-local sums, added once per tile
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        float wv[2];
+      for (int h2 = 0; h2 < NH2; ++h2)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float p = ex2(lg[m][hh][nt] - muse);
-          const bool ok = vk[m][hh];
-          tl += ok ? p : 0.0f;
-          if constexpr (MODE != MODE_INT8) tpm += ok ? p * mv_[m][hh] : 0.0f;
-          wv[hh] = ok ? p * sv_[m][hh] : 0.0f;
+        for (int m = 0; m < 2; ++m) {
+          float wv[2];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float p = ex2(lg[h2][m][hh][nt] - muse);
+            const bool ok = vk[h2][m][hh];
+            tl += ok ? p : 0.0f;
+            if constexpr (MODE != MODE_INT8) tpm += ok ? p * mv_[h2][m][hh] : 0.0f;
+            wv[hh] = ok ? p * sv_[h2][m][hh] : 0.0f;
+          }
+          const __half2 hp = __floats2half2_rn(wv[0], wv[1]);
+          const float2 hf = __half22float2(hp);
+          const __half2 lp = __floats2half2_rn(wv[0] - hf.x, wv[1] - hf.y);
+          xh[h2][nt][m] = *reinterpret_cast<const uint32_t*>(&hp);
+          xl[h2][nt][m] = *reinterpret_cast<const uint32_t*>(&lp);
         }
-        const __half2 hp = __floats2half2_rn(wv[0], wv[1]);
-        const float2 hf = __half22float2(hp);
-        const __half2 lp = __floats2half2_rn(wv[0] - hf.x, wv[1] - hf.y);
-        xh[nt][m] = *reinterpret_cast<const uint32_t*>(&hp);
-        xl[nt][m] = *reinterpret_cast<const uint32_t*>(&lp);
-      }
       lrun[nt] += tl;
       pmrun[nt] += tpm;
     }
 
     // ---- P.V: O^T (D x slots) += U_V^T (D x 16 keys) . Wslots (16 keys x slots)
 #pragma unroll
-    for (int mp = 0; mp < 2; ++mp) {
-      uint32_t bw[NT][2];
-      const int src = ((2 * tq + mp) << 2) | (gq >> 1);
+    for (int h2 = 0; h2 < NH2; ++h2)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t a0 = __shfl_sync(0xffffffffu, xh[nt][0], src);
-        const uint32_t b0 = __shfl_sync(0xffffffffu, xl[nt][0], src);
-        const uint32_t a1 = __shfl_sync(0xffffffffu, xh[nt][1], src);
-        const uint32_t b1 = __shfl_sync(0xffffffffu, xl[nt][1], src);
-        bw[nt][0] = (gq & 1) ? b0 : a0;
-        bw[nt][1] = (gq & 1) ? b1 : a1;
-      }
-      uint2 vl[2][2], vh[2][2];
+      for (int mp = 0; mp < 2; ++mp) {
+        uint32_t bw[NT][2];
+        const int src = ((2 * tq + mp) << 2) | (gq >> 1);
 #pragma unroll
-      for (int hp = 0; hp < 2; ++hp)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          if constexpr (MODE == MODE_INT8) {
-            const int kappa = 8 * tq + 4 * mp + 2 * hp + e;
-            vl[hp][e] = load_range<MODE, D>(vt, kappa, gq);
-            vh[hp][e] = load_range<MODE, D>(vt, kappa, 8 + gq);
-          } else {
-            vl[hp][e] = load_range<MODE, D>(vt + vrow + (4 * mp + 2 * hp + e) * C::R, 0, gq);
-            vh[hp][e] = load_range<MODE, D>(vt + vrow + (4 * mp + 2 * hp + e) * C::R, 0, 8 + gq);
-          }
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t a0 = __shfl_sync(0xffffffffu, xh[h2][nt][0], src);
+          const uint32_t b0 = __shfl_sync(0xffffffffu, xl[h2][nt][0], src);
+          const uint32_t a1 = __shfl_sync(0xffffffffu, xh[h2][nt][1], src);
+          const uint32_t b1 = __shfl_sync(0xffffffffu, xl[h2][nt][1], src);
+          bw[nt][0] = (gq & 1) ? b0 : a0;
+          bw[nt][1] = (gq & 1) ? b1 : a1;
         }
-      Unroll<C::MT, MODE>::run([&](auto mt_c) {
-        constexpr int mt = decltype(mt_c)::value;
-        const uint32_t a[4] = {vpair<MODE, mt>(vl[0][0], vl[0][1]), vpair<MODE, mt>(vh[0][0], vh[0][1]),
-                               vpair<MODE, mt>(vl[1][0], vl[1][1]), vpair<MODE, mt>(vh[1][0], vh[1][1])};
+        uint2 vl[2][2], vh[2][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[nt][mt], a, bw[nt][0], bw[nt][1]);
-      });
-    }
+        for (int hp = 0; hp < 2; ++hp)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            if constexpr (MODE == MODE_INT8) {
+              const int kappa = 32 * h2 + 8 * tq + 4 * mp + 2 * hp + e;
+              vl[hp][e] = load_range<MODE, D>(vt, kappa, gq);
+              vh[hp][e] = load_range<MODE, D>(vt, kappa, 8 + gq);
+            } else {
+              const uint8_t* vr = vt + vrow + (32 * h2 + 4 * mp + 2 * hp + e) * C::R;
+              vl[hp][e] = load_range<MODE, D>(vr, 0, gq);
+              vh[hp][e] = load_range<MODE, D>(vr, 0, 8 + gq);
+            }
+          }
+        Unroll<C::MT, MODE>::run([&](auto mt_c) {
+          constexpr int mt = decltype(mt_c)::value;
+          const uint32_t a[4] = {vpair<MODE, mt>(vl[0][0], vl[0][1]), vpair<MODE, mt>(vh[0][0], vh[0][1]),
+                                 vpair<MODE, mt>(vl[1][0], vl[1][1]), vpair<MODE, mt>(vh[1][0], vh[1][1])};
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[nt][mt], a, bw[nt][0], bw[nt][1]);
+        });
+      }
   }
   if (timed_out) {
     // a copy never arrived: report it, give the copies in flight one more
@@ -1005,9 +1036,9 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
 
 template <int MODE, int D, int NT>
 size_t stream_smem_bytes() {
-  using C = DecCfg<MODE, D>;
-  constexpr int NSTAGE = StreamCfg<MODE, D, NT>::NSTAGE;
-  return (size_t)DECODE_WARPS * NSTAGE * C::STAGE + DECODE_WARPS * NSTAGE * 4 + DECODE_WARPS * NSTAGE * 8;
+  using SC = StreamCfg<MODE, D, NT>;
+  constexpr int NSTAGE = SC::NSTAGE;
+  return (size_t)DECODE_WARPS * NSTAGE * SC::STAGE + DECODE_WARPS * NSTAGE * 4 + DECODE_WARPS * NSTAGE * 8;
 }
 
 int decode_ctas_per_sm(int mode, int head_dim, int group) {
