@@ -146,6 +146,10 @@ class ClockSampler:
 WORKLOADS = {
     # name: (factory, metric, kind)
     "llama_int4": (lambda a: gen.llama_int4(seed=0, num_blocks=a.pool_blocks or 200000), METRIC, "decode"),
+    "llama_int4_d64_bs64": (lambda a: gen.llama_int4(seed=0, num_blocks=a.pool_blocks or 50000, head_dim=64,
+                                                     block_size=64),
+                            "INT4 paged decode (head_dim 64, block_size 64) tokens/s and effective KV GB/s "
+                            "(% of GB300 HBM peak)", "decode"),
     "ernie_int2": (lambda a: gen.ernie_int2(seed=0, num_blocks=a.pool_blocks or 100000),
                    "INT2 paged decode tokens/s and effective KV GB/s (% of GB300 HBM peak)", "decode"),
     "qwen_int8_headwise": (lambda a: gen.qwen_int8_headwise(seed=0),
@@ -381,7 +385,7 @@ def run_gpu(args, rank, world, local_rank):
                      "per-call graphs for the breakdown",
            "l2": "flushed between timed steps (256 MB write)",
            "parallelism": "replicas only" if world > 1 else "single GPU"}
-    if args.workload == "llama_int4":
+    if args.workload.startswith("llama_int4"):
         cfg["context"] = "uniform[1024,8192]"
     if kind == "decode":
         cfg["decode_workers"] = st["splits"]
@@ -422,7 +426,7 @@ def run_gpu(args, rank, world, local_rank):
         "metric": metric, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype,
-        "data": "synthetic (seeded; K/V ~ N(0,1)%s)" % (", 1% outlier channels x10" if args.workload in ("llama_int4", "prefill_int4") else ""),
+        "data": "synthetic (seeded; K/V ~ N(0,1)%s)" % (", 1% outlier channels x10" if args.workload in ("llama_int4", "llama_int4_d64_bs64", "prefill_int4") else ""),
         "config": cfg, **extra, "write_ms": round(wr, 5),
         "roofline": roof,
         "write_roofline": write_roof,
@@ -566,7 +570,8 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_int4", choices=sorted(WORKLOADS),
-                    help="llama_int4 (the headline decode workload), ernie_int2, qwen_int8_headwise, prefill_int4")
+                    help="llama_int4 (the headline decode workload), llama_int4_d64_bs64, ernie_int2, "
+                         "qwen_int8_headwise, prefill_int4")
     ap.add_argument("--pool-blocks", type=int, default=0,
                     help="block pool size (0 = the workload's own; smaller pools only for profiling)")
     ap.add_argument("--prefill-prefixes", type=int, nargs="+", default=[0, 4096, 16384, 61440],

@@ -7,7 +7,9 @@ import pytest
 import torch
 
 import kvq_inputs as gen
+import oracle
 from harness import (ATOL, assert_pools_equal, build_case, decode_gpu, decode_oracle, kvq, max_err, q_host,
+                     to_dev_input, to_orc_input,
                      write_step)
 
 pytestmark = pytest.mark.gpu
@@ -135,3 +137,110 @@ def test_decode_full_size_llama_sampled():
     o = decode_oracle(c, q, rows=rows)
     assert max_err(g[rows], o) <= ATOL
     assert np.all(np.isfinite(g))
+
+
+def _full_size_sampled(wl, sample):
+    """Full-size workload in the bench's launch configuration with only the
+    sampled sequences known to the oracle: the GPU cache holds every sequence
+    (host values for the sampled ones, device values for the rest); the
+    sampled prefixes go first, in a call of their own, so that an INT8 first
+    write defines the channel scales from the same tokens on both sides; the
+    oracle writes only the sampled sequences.  Checks the sampled sequences'
+    outputs against the oracle and their pages byte for byte."""
+    K = kvq()
+    dev = "cuda"
+    B, pre = wl.batch, wl.prefix_lens
+    sample = np.asarray(sample, dtype=np.int32)
+    rest = np.setdiff1d(np.arange(B, dtype=np.int32), sample)
+    signs_t = None if wl.signs is None else torch.from_numpy(wl.signs).to(dev)
+    gc = K.PagedCache(wl.mode, wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, signs_t, dev)
+    oc = oracle.Cache(wl.mode, wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.signs, 0)
+    gc.k_pages.zero_()
+    gc.v_pages.zero_()
+    t_dev = torch.from_numpy(wl.table).to(dev)
+    win = None if wl.window is None else torch.from_numpy(wl.window).to(dev)
+
+    def gpag(lens):
+        lt = torch.from_numpy(np.ascontiguousarray(lens, dtype=np.int32)).to(dev)
+        if wl.headwise:
+            return K.Paging(lt, block_tables_headwise=t_dev, window_per_kv_head=win, sink_size=wl.sink)
+        return K.Paging(lt, block_tables=t_dev, window_per_kv_head=win, sink_size=wl.sink)
+
+    opag = lambda lens: oracle.Paging(wl.table, wl.headwise, np.ascontiguousarray(lens, np.int32), wl.window, wl.sink)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    # 1) the sampled prefixes (host values), first on both sides
+    counts = np.zeros(B, np.int32)
+    counts[sample] = pre[sample]
+    ks = np.concatenate([gen.kv_values_host(wl, "k", int(b), 0, int(pre[b])) for b in sample])
+    vs = np.concatenate([gen.kv_values_host(wl, "v", int(b), 0, int(pre[b])) for b in sample])
+    K.kvq_write(gc, gpag(pre), to_dev_input(ks, wl.dtype), to_dev_input(vs, wl.dtype),
+                torch.from_numpy(wl.cu(counts)).to(dev), dev_error=err)
+    assert oracle.write(oc, opag(pre), to_orc_input(ks, wl.dtype), to_orc_input(vs, wl.dtype), wl.cu(counts)) == 0
+    del ks, vs
+    # 2) the other prefixes, GPU only (device values), in groups of 16 sequences
+    for g0 in range(0, len(rest), 16):
+        grp = rest[g0:g0 + 16]
+        counts = np.zeros(B, np.int32)
+        counts[grp] = pre[grp]
+        if counts.sum() == 0:
+            continue
+        kd = torch.cat([gen.kv_values_device(wl, "k", int(b), 0, int(pre[b]), dev) for b in grp if pre[b] > 0])
+        vd = torch.cat([gen.kv_values_device(wl, "v", int(b), 0, int(pre[b]), dev) for b in grp if pre[b] > 0])
+        K.kvq_write(gc, gpag(pre), kd, vd, torch.from_numpy(wl.cu(counts)).to(dev), dev_error=err)
+        del kd, vd
+    # 3) the step: one new token per sequence (host values for the sampled ones)
+    parts_k, parts_v = [], []
+    for b in range(B):
+        if b in set(sample.tolist()):
+            parts_k.append(to_dev_input(gen.kv_values_host(wl, "k", b, int(pre[b]), 1), wl.dtype))
+            parts_v.append(to_dev_input(gen.kv_values_host(wl, "v", b, int(pre[b]), 1), wl.dtype))
+        else:
+            parts_k.append(gen.kv_values_device(wl, "k", b, int(pre[b]), 1, dev))
+            parts_v.append(gen.kv_values_device(wl, "v", b, int(pre[b]), 1, dev))
+    K.kvq_write(gc, gpag(wl.seq_lens), torch.cat(parts_k), torch.cat(parts_v),
+                torch.from_numpy(wl.cu(wl.n_new)).to(dev), dev_error=err)
+    counts = np.zeros(B, np.int32)
+    counts[sample] = 1
+    nk = np.concatenate([gen.kv_values_host(wl, "k", int(b), int(pre[b]), 1) for b in sample])
+    nv = np.concatenate([gen.kv_values_host(wl, "v", int(b), int(pre[b]), 1) for b in sample])
+    assert oracle.write(oc, opag(wl.seq_lens), to_orc_input(nk, wl.dtype), to_orc_input(nv, wl.dtype),
+                        wl.cu(counts)) == 0
+    # decode every sequence; compare the sampled ones
+    q = q_host(wl)
+    out = K.kvq_decode_attn(gc, gpag(wl.seq_lens), to_dev_input(q, wl.dtype), 1.0 / math.sqrt(wl.head_dim),
+                            dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    g = out.cpu().numpy()
+    assert np.all(np.isfinite(g))
+    o, oerr = oracle.attention(oc, opag(wl.seq_lens), to_orc_input(q, wl.dtype), 1.0 / math.sqrt(wl.head_dim),
+                               rows=sample)
+    assert oerr == 0
+    assert max_err(g[sample], o) <= ATOL
+    # the sampled sequences' pages, byte for byte
+    gk, gv = gc.k_pages.cpu().numpy(), gc.v_pages.cpu().numpy()
+    Hkv = wl.num_kv_heads
+    for b in sample.tolist():
+        nblk = (int(wl.seq_lens[b]) + wl.block_size - 1) // wl.block_size
+        for h in range(Hkv):
+            row = wl.table[b * Hkv + h] if wl.headwise else wl.table[b]
+            for blk in row[:nblk]:
+                if blk < 0:
+                    continue
+                assert np.array_equal(gk[blk, h], oc.k[blk, h]), "K page %d head %d differs" % (blk, h)
+                assert np.array_equal(gv[blk, h], oc.v[blk, h]), "V page %d head %d differs" % (blk, h)
+    if wl.mode == gen.MODE_INT8:
+        assert np.array_equal(gc.ch_amax.cpu().numpy(), oc.amax)
+
+
+def test_decode_full_size_ernie_int2_sampled():
+    """Config 3 at full size: 96 sequences, log-normal contexts up to 128k,
+    100k-block pool, INT2 with RHT."""
+    _full_size_sampled(gen.ernie_int2(0), [0, 41, 95])
+
+
+def test_decode_full_size_qwen_int8_headwise_sampled():
+    """Config 5 at full size: 32 sequences at context 32768, INT8 channel
+    scales from the first write, head-wise tables with -1 outside the sink
+    and window of heads 4-7."""
+    _full_size_sampled(gen.qwen_int8_headwise(0), [0, 19])
