@@ -30,6 +30,7 @@ import numpy as np
 MODE_INT4 = 0
 MODE_INT2 = 1
 MODE_INT8 = 2
+MODE_INT4_STEGO = 3  # INT4 with the zero point in the low 4 bits of an fp32 scale
 
 _TAG_K, _TAG_V, _TAG_Q = 11, 13, 17
 

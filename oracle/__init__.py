@@ -29,7 +29,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-MODE_INT4, MODE_INT2, MODE_INT8 = 0, 1, 2
+MODE_INT4, MODE_INT2, MODE_INT8, MODE_INT4_STEGO = 0, 1, 2, 3
 DT_F32, DT_BF16 = 0, 1
 
 

@@ -18,6 +18,9 @@
 //     ("Ascend INT8 KV Cache Plugin"), 运行机制: symmetric per-channel scales
 //     taken along the token axis on the first K/V a layer receives, separately
 //     for K and V.
+//   * Write, INT4 with the zero point hidden in the scale -- same vLLM page,
+//     评论区精华 (zero-point steganography): the 4-bit zero point is stored in
+//     the low 4 bits of the fp32 scale, so the row needs no extra bytes.
 //   * Paging -- FastDeploy PR #7718 "Optimize AppendAttention for discrete
 //     head-wise block_idx", Motivation: uniform [batch, block] table or
 //     head-wise [batch * kv_heads, block] table; PR2-only delta table and
@@ -33,7 +36,11 @@
 //   codes by round-half-to-even; element 2i in the low nibble; element 4i+j in
 //   bits 2j; pad = fp16 s then fp16 m; INT8 range [-127, 127] with scale
 //   amax / 127; a query at p sees key j iff j <= p and (no window, or j < sink,
-//   or j > p - W) and its block entry is a valid id.
+//   or j > p - W) and its block entry is a valid id.  Zero-point-in-scale
+//   INT4: the grid (u - zp) * s always holds 0, so it spans [min(min, 0),
+//   max(max, 0)]: s = (max(max, 0) - min(min, 0)) / 15 with its low 4
+//   mantissa bits cleared; zero point zp = clamp(rne(-min(min, 0) / s), 0, 15);
+//   codes clamp(rne(x / s) + zp, 0, 15); pad = bits(s) | zp; value (u - zp) * s.
 //
 // Built with -O2 -ffp-contract=off -fno-fast-math so that the fp32 write path
 // is evaluated exactly in the order written.
@@ -49,7 +56,7 @@
 
 namespace {
 
-enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2 };
+enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2, MODE_INT4_STEGO = 3 };
 enum { DT_F32 = 0, DT_BF16 = 1 };
 enum { ERR_BLOCK_RANGE = 1, ERR_TABLE_RANGE = 2, ERR_SEQ_LEN = 4 };
 
@@ -124,11 +131,12 @@ float widen(const void* base, int dtype, size_t idx) {
   return f;
 }
 
-int code_bits(int mode) { return mode == MODE_INT4 ? 4 : (mode == MODE_INT2 ? 2 : 8); }
+int code_bits(int mode) { return (mode == MODE_INT4 || mode == MODE_INT4_STEGO) ? 4 : (mode == MODE_INT2 ? 2 : 8); }
 
 int row_bytes(int mode, int D) {
   if (D != 64 && D != 128) return 0;
   if (mode == MODE_INT4) return D / 2 + 4;  // nibbles + fp16 s + fp16 m
+  if (mode == MODE_INT4_STEGO) return D / 2 + 4;  // nibbles + fp32 s carrying the zero point
   if (mode == MODE_INT2) return D / 4 + 4;  // crumbs + fp16 s + fp16 m
   if (mode == MODE_INT8) return D;
   return 0;
@@ -168,7 +176,7 @@ void wht_double(double* x, int D) {
 // Code packing.  INT4: byte i = u[2i] | u[2i+1] << 4.  INT2: byte i =
 // sum_j u[4i+j] << 2j.  INT8: byte i = two's complement of the signed code.
 void pack_codes(int mode, const uint8_t* u, int D, uint8_t* out) {
-  if (mode == MODE_INT4) {
+  if (mode == MODE_INT4 || mode == MODE_INT4_STEGO) {
     for (int i = 0; i < D / 2; ++i) out[i] = (uint8_t)((u[2 * i] & 15) | ((u[2 * i + 1] & 15) << 4));
   } else if (mode == MODE_INT2) {
     for (int i = 0; i < D / 4; ++i) {
@@ -182,7 +190,7 @@ void pack_codes(int mode, const uint8_t* u, int D, uint8_t* out) {
 }
 
 void unpack_codes(int mode, const uint8_t* bytes, int D, uint8_t* u) {
-  if (mode == MODE_INT4) {
+  if (mode == MODE_INT4 || mode == MODE_INT4_STEGO) {
     for (int i = 0; i < D / 2; ++i) {
       u[2 * i] = bytes[i] & 15;
       u[2 * i + 1] = bytes[i] >> 4;
@@ -233,6 +241,56 @@ void quant_row_token_head(int mode, const float* xin, int D, const int8_t* signs
   row[data + 3] = (uint8_t)(m_h >> 8);
 }
 
+// One INT4 row whose 4-byte pad is an fp32 scale with the integer zero point
+// in its low 4 mantissa bits.
+float bits_to_float(uint32_t b) {
+  float f;
+  std::memcpy(&f, &b, 4);
+  return f;
+}
+uint32_t float_to_bits(float f) {
+  uint32_t b;
+  std::memcpy(&b, &f, 4);
+  return b;
+}
+void quant_row_stego(const float* xin, int D, const int8_t* signs, uint8_t* row) {
+  std::vector<float> x(xin, xin + D);
+  if (signs) rht_forward_f32(x.data(), D, signs);
+  float mn = x[0], mx = x[0];
+  for (int i = 1; i < D; ++i) {
+    if (x[i] < mn) mn = x[i];
+    if (x[i] > mx) mx = x[i];
+  }
+  mn = mn + 0.0f;
+  mx = mx + 0.0f;
+  const float lo = mn < 0.0f ? mn : 0.0f;  // the grid holds 0 (code zp)
+  const float hi = mx > 0.0f ? mx : 0.0f;
+  float s = (hi - lo) / 15.0f;
+  const uint32_t sb = float_to_bits(s) & ~15u;  // the low 4 bits carry the zero point
+  const float st = bits_to_float(sb);
+  int zp = 0;
+  if (st != 0.0f) {
+    float r = std::nearbyint(-lo / st);
+    if (r < 0.0f) r = 0.0f;
+    if (r > 15.0f) r = 15.0f;
+    zp = (int)r;
+  }
+  std::vector<uint8_t> u(D);
+  for (int i = 0; i < D; ++i) {
+    if (st == 0.0f) {
+      u[i] = 0;
+      continue;
+    }
+    float r = std::nearbyint(x[i] / st) + (float)zp;
+    if (r < 0.0f) r = 0.0f;
+    if (r > 15.0f) r = 15.0f;
+    u[i] = (uint8_t)r;
+  }
+  pack_codes(MODE_INT4_STEGO, u.data(), D, row);
+  const uint32_t pad = sb | (uint32_t)zp;
+  for (int b = 0; b < 4; ++b) row[D / 2 + b] = (uint8_t)(pad >> (8 * b));
+}
+
 void quant_row_int8(const float* x, int D, const float* amax, uint8_t* row) {
   for (int c = 0; c < D; ++c) {
     float s = amax[c] / 127.0f;
@@ -260,10 +318,18 @@ void dequant_row(int mode, const uint8_t* row, int D, const int8_t* signs, const
     return;
   }
   const int data = D * code_bits(mode) / 8;
-  uint16_t s_h = (uint16_t)(row[data] | (row[data + 1] << 8));
-  uint16_t m_h = (uint16_t)(row[data + 2] | (row[data + 3] << 8));
-  double S = f16_decode(s_h), M = f16_decode(m_h);
-  for (int i = 0; i < D; ++i) out[i] = (double)u[i] * S + M;
+  if (mode == MODE_INT4_STEGO) {
+    const uint32_t pad = (uint32_t)row[data] | ((uint32_t)row[data + 1] << 8) | ((uint32_t)row[data + 2] << 16) |
+                         ((uint32_t)row[data + 3] << 24);
+    const int zp = (int)(pad & 15u);
+    const double S = bits_to_float(pad & ~15u);
+    for (int i = 0; i < D; ++i) out[i] = (double)((int)u[i] - zp) * S;
+  } else {
+    uint16_t s_h = (uint16_t)(row[data] | (row[data + 1] << 8));
+    uint16_t m_h = (uint16_t)(row[data + 2] | (row[data + 3] << 8));
+    double S = f16_decode(s_h), M = f16_decode(m_h);
+    for (int i = 0; i < D; ++i) out[i] = (double)u[i] * S + M;
+  }
   if (signs) {  // inverse RHT: d * (H y) / D
     wht_double(out, D);
     for (int i = 0; i < D; ++i) out[i] = out[i] * (double)signs[i] / (double)D;
@@ -308,7 +374,8 @@ int32_t orc_signed_code(int32_t mode, int32_t u) {
   return u - (1 << (code_bits(mode) - 1));
 }
 void orc_quant_row(int32_t mode, const float* x, int32_t D, const int8_t* signs, uint8_t* row) {
-  quant_row_token_head(mode, x, D, signs, row);
+  if (mode == MODE_INT4_STEGO) quant_row_stego(x, D, signs, row);
+  else quant_row_token_head(mode, x, D, signs, row);
 }
 void orc_dequant_row(int32_t mode, const uint8_t* row, int32_t D, const int8_t* signs,
                      const float* amax, double* out) {
@@ -375,6 +442,8 @@ int32_t orc_write(const OrcCache* c, const OrcPaging* pg, const void* k, const v
           uint8_t* dst = pages + (((size_t)blk * Hkv + h) * bs + (p % bs)) * R;
           if (mode == MODE_INT8)
             quant_row_int8(x.data(), D, c->ch_amax + ((size_t)kv * Hkv + h) * D, dst);
+          else if (mode == MODE_INT4_STEGO)
+            quant_row_stego(x.data(), D, c->signs, dst);
           else
             quant_row_token_head(mode, x.data(), D, c->signs, dst);
         }

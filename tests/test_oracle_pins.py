@@ -19,6 +19,7 @@ import kvq_inputs as gen
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 INT4, INT2, INT8 = oracle.MODE_INT4, oracle.MODE_INT2, oracle.MODE_INT8
+STEGO = oracle.MODE_INT4_STEGO
 
 
 def page_constants():
@@ -212,6 +213,74 @@ def test_constant_row_has_zero_scale(mode):
     assert np.all(oracle.dequant_row(mode, row, D) == 3.25)
 
 
+# ---------------------------------------------------------------------------
+# INT4 with the zero point in the low 4 bits of an fp32 scale (vLLM PR #40835
+# review summary, 评论区精华: zero-point steganography)
+
+def stego_pad(row, D):
+    w = int.from_bytes(bytes(row[D // 2:D // 2 + 4].tolist()), "little")
+    return float(np.array([w & ~15], dtype=np.uint32).view(np.float32)[0]), w & 15
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_stego_worked_grid_row_is_exact(D):
+    k = np.arange(D) % 16
+    x = ((k - 5) * 0.125).astype(np.float32)     # scale 2^-3, zero point 5
+    row = oracle.quant_row(STEGO, x, None)
+    want = (k[0::2] | (k[1::2] << 4)).astype(np.uint8)
+    assert np.array_equal(row[:D // 2], want)
+    # 0.125 is 0x3E000000; the zero point sits in the low 4 bits
+    assert row[D // 2:D // 2 + 4].tolist() == [0x05, 0x00, 0x00, 0x3E]
+    assert np.array_equal(oracle.dequant_row(STEGO, row, D), x.astype(np.float64))
+
+
+@pytest.mark.parametrize("rht", [False, True])
+def test_stego_error_bound(rht):
+    """The grid (u - zp) s_t holds 0 and spans lo = min(min, 0) .. hi =
+    max(max, 0): zp = rne(-lo / s_t) puts lo within half a step of the grid's
+    bottom and hi within half a step plus the truncated scale bits of its top,
+    so every value is within s_t / 2 + 15 (s - s_t) of its reconstruction
+    (s = (hi - lo) / 15, s_t the stored scale)."""
+    D = 128
+    rng = np.random.default_rng(29 + rht)
+    signs = np.where(rng.integers(0, 2, D) == 1, 1, -1).astype(np.int8) if rht else None
+    H = sylvester(D).astype(np.float64)
+    for _ in range(200):
+        x = (rng.standard_normal(D) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+        x[rng.integers(0, D)] *= 20.0
+        row = oracle.quant_row(STEGO, x, signs)
+        st, zp = stego_pad(row, D)
+        xd = x.astype(np.float64)
+        y = H @ (signs * xd) if rht else xd
+        mn, mx = y.min(), y.max()
+        lo, hi = min(mn, 0.0), max(mx, 0.0)
+        s = (hi - lo) / 15
+        assert 0 <= zp <= 15
+        assert s * (1 - 4e-6) <= st <= s * (1 + 1e-6)    # 4 mantissa bits cleared
+        xh = oracle.dequant_row(STEGO, row, D, signs)
+        yh = H @ (signs * xh) if rht else xh
+        bound = st / 2 + 15 * abs(s - st) + 2e-6 * max(abs(mn), abs(mx))
+        assert np.max(np.abs(y - yh)) <= bound
+        assert abs(lo - (-zp * st)) <= st / 2 + 2e-6 * max(abs(mn), abs(mx))
+
+
+def test_stego_zero_constant_and_one_signed_rows():
+    D = 64
+    row = oracle.quant_row(STEGO, np.zeros(D, np.float32), None)
+    assert np.all(row == 0)
+    for c in (3.25, -3.25):                      # 15 steps between 0 and the value
+        row = oracle.quant_row(STEGO, np.full(D, c, np.float32), None)
+        st, zp = stego_pad(row, D)
+        assert zp == (0 if c > 0 else 15)
+        assert abs(15 * st - abs(c)) <= abs(c) * 2e-6
+        xh = oracle.dequant_row(STEGO, row, D)
+        assert np.max(np.abs(xh - c)) <= abs(c) * 2e-6
+    x = np.linspace(2.0, 23.0, D).astype(np.float32)   # all positive: the grid still reaches the top
+    row = oracle.quant_row(STEGO, x, None)
+    st, zp = stego_pad(row, D)
+    assert zp == 0 and np.max(np.abs(oracle.dequant_row(STEGO, row, D) - x)) <= st / 2 * 1.0001
+
+
 def test_signed_zero_is_canonical():
     D = 64
     x = np.zeros(D, np.float32)
@@ -276,6 +345,12 @@ def _grid_values(rng, n, D, mode):
     """Rows that INT4/INT2 (RHT off) or INT8 represent exactly."""
     if mode == INT8:
         return None
+    if mode == STEGO:  # (k - zp) * s with s a power of two, min and max pinned
+        k = rng.integers(0, 16, size=(n, D))
+        k[:, 0], k[:, 1] = 0, 15
+        s = 2.0 ** rng.integers(-3, 2, size=(n, 1))
+        zp = rng.integers(0, 16, size=(n, 1))
+        return ((k - zp) * s).astype(np.float32)
     levels = 15 if mode == INT4 else 3
     k = rng.integers(0, levels + 1, size=(n, D))
     k[:, 0], k[:, 1] = 0, levels                       # pin min and max of each row
@@ -294,7 +369,7 @@ def _softmax_ref(q, K, V, scale, mask):
     return p @ V
 
 
-@pytest.mark.parametrize("mode", [INT4, INT2])
+@pytest.mark.parametrize("mode", [INT4, INT2, STEGO])
 def test_attention_brute_force_on_exact_rows(mode):
     rng = np.random.default_rng(11 + mode)
     D, bs, Hkv, Hq = 64, 16, 2, 4
