@@ -69,11 +69,19 @@ typedef enum {
  *   code 0); the signed view q = u - 2^(b-1) covers [-8, 7] for INT4
  *   ([vLLM-INT4] 关键源码片段, INT4_CONFIG) and [-2, 1] for INT2 ([FD-INT2]).
  * INT8: dynamic symmetric per-channel codes in [-127, 127] with one fp32
- *   scale per (K|V, kv_head, channel) ([ASCEND-INT8] 运行机制); no RHT. */
+ *   scale per (K|V, kv_head, channel) ([ASCEND-INT8] 运行机制); no RHT.
+ * INT4_STEGO: the INT4 row layout, with the 4-byte pad an fp32 scale whose
+ *   low 4 mantissa bits carry an integer zero point ([vLLM-INT4] 评论区精华,
+ *   zero-point steganography).  Per row (after the optional RHT): the grid
+ *   (u - zp) * s holds 0, so it spans lo = min(min, 0) .. hi = max(max, 0);
+ *   s = (hi - lo) / 15 with its low 4 mantissa bits cleared, zp =
+ *   clamp(rne(-lo / s), 0, 15), u = clamp(rne(x / s) + zp, 0, 15), pad =
+ *   bits(s) | zp, value (u - zp) * s. */
 typedef enum {
   KVQ_INT4_TOKEN_HEAD = 0,
   KVQ_INT2_TOKEN_HEAD = 1,
-  KVQ_INT8_CHANNEL = 2
+  KVQ_INT8_CHANNEL = 2,
+  KVQ_INT4_STEGO = 3
 } kvq_mode;
 
 /* Element type of q / k / v inputs. */

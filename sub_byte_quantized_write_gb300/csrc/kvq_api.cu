@@ -41,12 +41,17 @@ int sm_count() {
   return cached[dev];
 }
 
+// Kernel code family of an API mode: the zero-point-in-scale INT4 rows are
+// INT4 rows with another pad (the `stego` flag of the kernel parameters).
+int kernel_mode(int32_t mode) { return mode == KVQ_INT4_STEGO ? kvq::MODE_INT4 : mode; }
+
 kvq_status check_cache(const kvq_cache* c) {
   if (!c) return fail(KVQ_ERR_INVALID_ARG, "cache is NULL");
   if (!c->k_pages || !c->v_pages) return fail(KVQ_ERR_INVALID_ARG, "k_pages / v_pages is NULL");
   if (!aligned(c->k_pages, 16) || !aligned(c->v_pages, 16))
     return fail(KVQ_ERR_INVALID_ARG, "k_pages / v_pages must be 16-byte aligned");
-  if (c->mode != KVQ_INT4_TOKEN_HEAD && c->mode != KVQ_INT2_TOKEN_HEAD && c->mode != KVQ_INT8_CHANNEL)
+  if (c->mode != KVQ_INT4_TOKEN_HEAD && c->mode != KVQ_INT2_TOKEN_HEAD && c->mode != KVQ_INT8_CHANNEL &&
+      c->mode != KVQ_INT4_STEGO)
     return fail(KVQ_ERR_UNSUPPORTED, "unknown mode");
   if (c->head_dim != 64 && c->head_dim != 128) return fail(KVQ_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (c->block_size != 16 && c->block_size != 32 && c->block_size != 64)
@@ -83,7 +88,8 @@ kvq::AttnParams attn_params(const kvq_cache* c, const kvq_paging* p, const void*
   a.num_kv_heads = c->num_kv_heads;
   a.block_size = c->block_size;
   a.head_dim = c->head_dim;
-  a.mode = c->mode;
+  a.mode = kernel_mode(c->mode);
+  a.stego = c->mode == KVQ_INT4_STEGO;
   a.signs = c->mode == KVQ_INT8_CHANNEL ? nullptr : c->rht_signs;
   a.ch_amax = c->ch_amax;
   a.headwise = p->block_tables_headwise != nullptr;
@@ -116,7 +122,7 @@ kvq_status check_q(const kvq_cache* c, const void* q, int32_t dtype, int32_t hq,
 kvq::DecodeLayout decode_layout(const kvq_cache* c, const kvq_paging* p, int32_t num_q_heads) {
   const int group = num_q_heads / c->num_kv_heads;
   return kvq::decode_ws_layout(p->batch, c->num_kv_heads, group, c->head_dim, sm_count(),
-                               kvq::decode_ctas_per_sm(c->mode, c->head_dim, group));
+                               kvq::decode_ctas_per_sm(kernel_mode(c->mode), c->head_dim, group));
 }
 
 // Scratch of kvq_decode_attn_noalloc: one static device array per GPU that
@@ -149,7 +155,7 @@ extern "C" {
 
 int32_t kvq_row_bytes(int32_t mode, int32_t head_dim) {
   if (head_dim != 64 && head_dim != 128) return 0;
-  if (mode == KVQ_INT4_TOKEN_HEAD) return head_dim / 2 + 4;
+  if (mode == KVQ_INT4_TOKEN_HEAD || mode == KVQ_INT4_STEGO) return head_dim / 2 + 4;
   if (mode == KVQ_INT2_TOKEN_HEAD) return head_dim / 4 + 4;
   if (mode == KVQ_INT8_CHANNEL) return head_dim;
   return 0;
@@ -191,7 +197,8 @@ kvq_status kvq_write(const kvq_cache* cache, const kvq_paging* paging, const voi
   P.num_kv_heads = cache->num_kv_heads;
   P.block_size = cache->block_size;
   P.head_dim = cache->head_dim;
-  P.mode = cache->mode;
+  P.mode = kernel_mode(cache->mode);
+  P.stego = cache->mode == KVQ_INT4_STEGO;
   P.signs = cache->mode == KVQ_INT8_CHANNEL ? nullptr : cache->rht_signs;
   P.ch_amax = cache->ch_amax;
   P.ch_ready = cache->ch_amax_ready;

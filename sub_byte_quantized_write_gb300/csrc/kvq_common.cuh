@@ -240,6 +240,22 @@ __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepco
 __device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// Scale s and the value z of the signed code 0 (stored code 2^(b-1)) from an
+// INT4 / INT2 row's 4-byte pad: fp16 s then fp16 m (z = m + 2^(b-1) s), or,
+// for zero-point-in-scale INT4 rows, an fp32 s whose low 4 bits hold the zero
+// point zp (z = (8 - zp) s, exact).
+template <int MODE>
+__device__ __forceinline__ void pad_scale_zero(uint32_t pad, bool stego, float& s, float& z) {
+  constexpr float half_range = (float)(1 << (mode_bits(MODE) - 1));
+  if (MODE == MODE_INT4 && stego) {
+    s = __uint_as_float(pad & ~15u);
+    z = s * (float)(8 - (int)(pad & 15u));
+  } else {
+    s = __half2float(__ushort_as_half((unsigned short)(pad & 0xFFFF)));
+    z = fmaf(half_range, s, __half2float(__ushort_as_half((unsigned short)(pad >> 16))));
+  }
+}
 __device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
 
 }  // namespace kvq

@@ -680,6 +680,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   // per-lane shared-memory offsets (loop invariant): key rows 4gq + 2m + hh,
   // value rows 8tq + 4m' + 2h' + e
   const int koff = 4 * gq * C::R + 4 * tq;
+  const bool stego = P.stego != 0;
   const int poff = 4 * gq * C::R + C::DATA;
   const int vrow = 8 * tq * C::R;
   bool timed_out = false;
@@ -783,12 +784,8 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
           if constexpr (MODE != MODE_INT8) {
             const uint32_t pk = lds32(kt + poff + (32 * h2 + 2 * m + hh) * C::R);
             const uint32_t pv = lds32(vt + poff + (32 * h2 + 2 * m + hh) * C::R);
-            constexpr float half_range = (float)(1 << (C::BITS - 1));
-            sk = __half2float(__ushort_as_half((unsigned short)(pk & 0xFFFF)));
-            mk = fmaf(half_range, sk, __half2float(__ushort_as_half((unsigned short)(pk >> 16))));
-            sv_[h2][m][hh] = __half2float(__ushort_as_half((unsigned short)(pv & 0xFFFF)));
-            mv_[h2][m][hh] =
-                fmaf(half_range, sv_[h2][m][hh], __half2float(__ushort_as_half((unsigned short)(pv >> 16))));
+            pad_scale_zero<MODE>(pk, stego, sk, mk);
+            pad_scale_zero<MODE>(pv, stego, sv_[h2][m][hh], mv_[h2][m][hh]);
           } else {
             sv_[h2][m][hh] = 1.0f;
             mv_[h2][m][hh] = 0.0f;

@@ -12,6 +12,7 @@ struct WriteParams {
   uint8_t* k_pages;
   uint8_t* v_pages;
   int num_blocks, num_kv_heads, block_size, head_dim, mode;
+  int stego;                  // INT4 rows whose pad is an fp32 scale carrying the zero point
   const int8_t* signs;
   float* ch_amax;
   int32_t* ch_ready;
@@ -30,6 +31,7 @@ struct AttnParams {
   const uint8_t* k_pages;
   const uint8_t* v_pages;
   int num_blocks, num_kv_heads, block_size, head_dim, mode;
+  int stego;                  // INT4 rows whose pad is an fp32 scale carrying the zero point
   const int8_t* signs;        // NULL = RHT off
   const float* ch_amax;       // INT8: [2][Hkv][D]
   const int32_t* table;

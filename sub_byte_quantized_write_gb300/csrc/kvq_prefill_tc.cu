@@ -520,9 +520,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
           float s = 0.0f, z = 0.0f;
           if (has) {
             const uint32_t pad = lds32((isv ? rvp : rk) + key * C::R + C::DATA);
-            constexpr float half_range = (float)(1 << (C::BITS - 1));
-            s = __half2float(__ushort_as_half((unsigned short)(pad & 0xFFFF)));
-            z = fmaf(half_range, s, __half2float(__ushort_as_half((unsigned short)(pad >> 16))));  // code 0
+            pad_scale_zero<MODE>(pad, P.stego != 0, s, z);  // z: the value of the signed code 0
           }
           float* scs = sc + kvs * 4 * TP_KT;
           scs[(isv ? 2 : 0) * TP_KT + key] = s;

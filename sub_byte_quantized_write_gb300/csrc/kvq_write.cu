@@ -88,7 +88,7 @@ __device__ __forceinline__ uint32_t gather_word(uint32_t bits, int lane) {
   return v;
 }
 
-template <int MODE, int D>
+template <int MODE, int D, bool STEGO>
 __global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
   constexpr int EPL = D / 32;
   constexpr int BITS = mode_bits(MODE);
@@ -122,27 +122,49 @@ __global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
   }
   mn = __fadd_rn(warp_min(mn), 0.0f);  // canonical +0
   mx = __fadd_rn(warp_max(mx), 0.0f);
-  const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)LEVELS);
-  const uint16_t s_h = f16_sat_bits(s);
-  const uint16_t m_h = f16_sat_bits(mn);
-  const float S = __half2float(__ushort_as_half(s_h));
-  const float M = __half2float(__ushort_as_half(m_h));
-  uint32_t bits = 0;
+  uint32_t bits = 0, pad;
+  if constexpr (STEGO) {
+    // the grid (u - zp) * s holds 0: it spans min(mn, 0) .. max(mx, 0); the
+    // scale's low 4 mantissa bits are cleared and carry the zero point
+    const float lo = mn < 0.0f ? mn : 0.0f, hi = mx > 0.0f ? mx : 0.0f;
+    const uint32_t sb = __float_as_uint(__fdiv_rn(__fsub_rn(hi, lo), (float)LEVELS)) & ~15u;
+    const float st = __uint_as_float(sb);
+    float zp = 0.0f;
+    if (st != 0.0f) zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, st)), 0.0f), (float)LEVELS);
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    uint32_t u = 0;
-    if (S != 0.0f) {
-      float r = rintf(__fdiv_rn(__fsub_rn(x[i], M), S));
-      r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
-      u = (uint32_t)r;
+    for (int i = 0; i < EPL; ++i) {
+      uint32_t u = 0;
+      if (st != 0.0f) {
+        float r = __fadd_rn(rintf(__fdiv_rn(x[i], st)), zp);
+        r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
+        u = (uint32_t)r;
+      }
+      bits |= u << (i * BITS);
     }
-    bits |= u << (i * BITS);
+    pad = sb | (uint32_t)zp;
+  } else {
+    const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)LEVELS);
+    const uint16_t s_h = f16_sat_bits(s);
+    const uint16_t m_h = f16_sat_bits(mn);
+    const float S = __half2float(__ushort_as_half(s_h));
+    const float M = __half2float(__ushort_as_half(m_h));
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      uint32_t u = 0;
+      if (S != 0.0f) {
+        float r = rintf(__fdiv_rn(__fsub_rn(x[i], M), S));
+        r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
+        u = (uint32_t)r;
+      }
+      bits |= u << (i * BITS);
+    }
+    pad = (uint32_t)s_h | ((uint32_t)m_h << 16);
   }
   constexpr int NBITS = EPL * BITS;        // bits per lane: 16, 8 or 4
   const uint32_t word = gather_word<NBITS>(bits, lane);
   constexpr int LPW = 32 / NBITS;
   if (lane % LPW == 0) *reinterpret_cast<uint32_t*>(dst + 4 * (lane / LPW)) = word;
-  if (lane == 0) *reinterpret_cast<uint32_t*>(dst + DATA) = (uint32_t)s_h | ((uint32_t)m_h << 16);
+  if (lane == 0) *reinterpret_cast<uint32_t*>(dst + DATA) = pad;
 }
 
 // INT8, pass 1 (only while *ready == 0): per-channel max |x| over all tokens.
@@ -215,12 +237,15 @@ cudaError_t launch_write(const WriteParams& P, cudaStream_t stream) {
     else int8_quant_kernel<64><<<blocks, 256, 0, stream>>>(P);
     return cudaGetLastError();
   }
-  if (P.mode == MODE_INT4) {
-    if (P.head_dim == 128) write_token_head_kernel<MODE_INT4, 128><<<blocks, 256, 0, stream>>>(P);
-    else write_token_head_kernel<MODE_INT4, 64><<<blocks, 256, 0, stream>>>(P);
+  if (P.mode == MODE_INT4 && P.stego) {
+    if (P.head_dim == 128) write_token_head_kernel<MODE_INT4, 128, true><<<blocks, 256, 0, stream>>>(P);
+    else write_token_head_kernel<MODE_INT4, 64, true><<<blocks, 256, 0, stream>>>(P);
+  } else if (P.mode == MODE_INT4) {
+    if (P.head_dim == 128) write_token_head_kernel<MODE_INT4, 128, false><<<blocks, 256, 0, stream>>>(P);
+    else write_token_head_kernel<MODE_INT4, 64, false><<<blocks, 256, 0, stream>>>(P);
   } else {
-    if (P.head_dim == 128) write_token_head_kernel<MODE_INT2, 128><<<blocks, 256, 0, stream>>>(P);
-    else write_token_head_kernel<MODE_INT2, 64><<<blocks, 256, 0, stream>>>(P);
+    if (P.head_dim == 128) write_token_head_kernel<MODE_INT2, 128, false><<<blocks, 256, 0, stream>>>(P);
+    else write_token_head_kernel<MODE_INT2, 64, false><<<blocks, 256, 0, stream>>>(P);
   }
   return cudaGetLastError();
 }
