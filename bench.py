@@ -141,6 +141,25 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# ranks (one process per GPU; replicas: every rank runs the whole workload)
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest per-rank value (step time) of the job; the value itself on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, ms_max: float, world: int) -> float:
+    """Units of all ranks per second, timed by the slowest rank."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # workloads
 
 WORKLOADS = {
@@ -327,14 +346,9 @@ def run_gpu(args, rank, world, local_rank):
     step_ms = [a.elapsed_time(c) for a, c in evs]
     att_ms = [b.elapsed_time(c) for a, b, c in ev]
     wr_ms = [a.elapsed_time(b) for a, b, c in ev]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), device)
     tokens = wl.batch if kind == "decode" else int(wl.n_new.sum())
-    value = world * tokens / (ms / 1e3)
+    value = whole_job_rate(tokens, ms, world)
 
     # end to end through the C ABI with host buffers: H2D of the step's
     # inputs from pinned memory, write + attention, D2H of the output
@@ -371,7 +385,7 @@ def run_gpu(args, rank, world, local_rank):
             c.record(stream)
             c.synchronize()
             e2e_ms.append(a.elapsed_time(c))
-    e2e_value = world * tokens / (sum(e2e_ms) / len(e2e_ms) / 1e3)
+    e2e_value = whole_job_rate(tokens, max_over_ranks(sum(e2e_ms) / len(e2e_ms), device), world)
 
     units = algorithmic_units(wl)
     att = sum(att_ms) / len(att_ms)
