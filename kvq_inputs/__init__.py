@@ -147,12 +147,14 @@ def tiny_int4(seed: int = 0) -> Workload:
 
 
 def llama_int4(seed: int = 0, batch: int = 64, ctx_lo: int = 1024, ctx_hi: int = 8192,
-               num_blocks: int = 200000, head_dim: int = 128, block_size: int = 16) -> Workload:
+               num_blocks: int = 200000, head_dim: int = 128, block_size: int = 16,
+               mode: int = MODE_INT4) -> Workload:
     """INT4 per-token-head decode, Llama-3-8B-like layer: Hq=32, Hkv=8, D=128,
     bf16, bs=16, contexts uniform in [ctx_lo, ctx_hi], pages at distinct random
     blocks of the pool, K/V ~ N(0,1) with 1% of (head, channel) pairs x10, RHT
     on, one new token per sequence per step.  `head_dim` / `block_size` give
-    the same layer at D = 64 and bs = 32 or 64."""
+    the same layer at D = 64 and bs = 32 or 64; `mode` MODE_INT4_STEGO the
+    same cache with the zero point carried in the fp32 scale."""
     rng = _structure_rng(seed)
     D, Hkv, bs = head_dim, 8, block_size
     signs = _draw_signs(rng, D)
@@ -163,7 +165,9 @@ def llama_int4(seed: int = 0, batch: int = 64, ctx_lo: int = 1024, ctx_hi: int =
     max_blocks = (ctx_hi + bs - 1) // bs
     table = _tables_from_pool(rng, seq_lens, bs, max_blocks, num_blocks)
     name = "llama_int4_decode" if (D, bs) == (128, 16) else "llama_int4_d%d_bs%d_decode" % (D, bs)
-    return Workload(name, MODE_INT4, 32, Hkv, D, bs, "bf16", num_blocks,
+    if mode == MODE_INT4_STEGO:
+        name = name.replace("int4", "int4_stego")
+    return Workload(name, mode, 32, Hkv, D, bs, "bf16", num_blocks,
                     max_blocks, seq_lens, np.ones(batch, np.int32), table, False, None, 0,
                     signs, "decode", 1.0, ok, ov, seed)
 
