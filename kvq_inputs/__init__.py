@@ -31,6 +31,8 @@ MODE_INT4 = 0
 MODE_INT2 = 1
 MODE_INT8 = 2
 MODE_INT4_STEGO = 3  # INT4 with the zero point in the low 4 bits of an fp32 scale
+MODE_INT8_TOKEN_HEAD = 4  # symmetric INT8, one fp32 scale per (token, kv head)
+MODE_FP8_TOKEN_HEAD = 5  # FP8 E4M3 codes, one fp32 scale per (token, kv head)
 
 _TAG_K, _TAG_V, _TAG_Q = 11, 13, 17
 

@@ -30,6 +30,7 @@ _lock = threading.Lock()
 _lib = None
 
 MODE_INT4, MODE_INT2, MODE_INT8, MODE_INT4_STEGO = 0, 1, 2, 3
+MODE_INT8_TOKEN_HEAD, MODE_FP8_TOKEN_HEAD = 4, 5
 DT_F32, DT_BF16 = 0, 1
 
 
@@ -76,6 +77,8 @@ def lib():
             L.orc_pack_codes.argtypes, L.orc_pack_codes.restype = [I, P, I, P], None
             L.orc_unpack_codes.argtypes, L.orc_unpack_codes.restype = [I, P, I, P], None
             L.orc_signed_code.argtypes, L.orc_signed_code.restype = [I, I], I
+            L.orc_e4m3_decode.argtypes, L.orc_e4m3_decode.restype = [ctypes.c_uint8], ctypes.c_double
+            L.orc_e4m3_round.argtypes, L.orc_e4m3_round.restype = [F], ctypes.c_uint8
             L.orc_quant_row.argtypes, L.orc_quant_row.restype = [I, P, I, P, P], None
             L.orc_dequant_row.argtypes, L.orc_dequant_row.restype = [I, P, I, P, P, P], None
             L.orc_write.argtypes = [ctypes.POINTER(OrcCache), ctypes.POINTER(OrcPaging), P, P, I, P, I]
@@ -128,6 +131,14 @@ def unpack_codes(mode: int, data: np.ndarray, D: int) -> np.ndarray:
     u = np.zeros(D, dtype=np.uint8)
     lib().orc_unpack_codes(mode, _ptr(b), D, _ptr(u))
     return u
+
+
+def e4m3_decode(code: int) -> float:
+    return lib().orc_e4m3_decode(int(code))
+
+
+def e4m3_round(x: float) -> int:
+    return lib().orc_e4m3_round(float(x))
 
 
 def signed_code(mode: int, u: int) -> int:

@@ -21,6 +21,9 @@
 //   * Write, INT4 with the zero point hidden in the scale -- same vLLM page,
 //     评论区精华 (zero-point steganography): the 4-bit zero point is stored in
 //     the low 4 bits of the fp32 scale, so the row needs no extra bytes.
+//   * Write, INT8 / FP8 per (token, kv_head) row -- same vLLM page, 功能与动机
+//     and 关联脉络: the INT4 mode is added on top of the INT8 / FP8
+//     per-token-head modes of the base PR #40633, one scale per token-head.
 //   * Paging -- FastDeploy PR #7718 "Optimize AppendAttention for discrete
 //     head-wise block_idx", Motivation: uniform [batch, block] table or
 //     head-wise [batch * kv_heads, block] table; PR2-only delta table and
@@ -41,6 +44,11 @@
 //   max(max, 0)]: s = (max(max, 0) - min(min, 0)) / 15 with its low 4
 //   mantissa bits cleared; zero point zp = clamp(rne(-min(min, 0) / s), 0, 15);
 //   codes clamp(rne(x / s) + zp, 0, 15); pad = bits(s) | zp; value (u - zp) * s.
+//   INT8 / FP8 per token-head: symmetric, RHT optional as for INT4; amax =
+//   max |x| of the (rotated) row; s = amax / 127 with codes clamp(rne(x / s),
+//   -127, 127), or s = amax / 448 with codes the nearest E4M3 value of x / s
+//   (ties to even, saturating at 448); row = D code bytes + fp32 s; s = 0
+//   gives all-zero codes.
 //
 // Built with -O2 -ffp-contract=off -fno-fast-math so that the fp32 write path
 // is evaluated exactly in the order written.
@@ -56,7 +64,8 @@
 
 namespace {
 
-enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2, MODE_INT4_STEGO = 3 };
+enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2, MODE_INT4_STEGO = 3, MODE_INT8_TOKEN_HEAD = 4,
+       MODE_FP8_TOKEN_HEAD = 5 };
 enum { DT_F32 = 0, DT_BF16 = 1 };
 enum { ERR_BLOCK_RANGE = 1, ERR_TABLE_RANGE = 2, ERR_SEQ_LEN = 4 };
 
@@ -122,6 +131,49 @@ uint16_t f16_saturate(float x) {
   return f16_round_nearest_even(x);
 }
 
+// ---------------------------------------------------------------------------
+// FP8 E4M3, the variant without infinities, from the format's definition:
+// 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; exponent field 0
+// encodes subnormals (fraction * 2^-9); only S.1111.111 is NaN, so the
+// largest finite magnitude is S.1111.110 = 1.75 * 2^8 = 448.
+
+double e4m3_decode(uint8_t c) {
+  const int e = (c >> 3) & 15, f = c & 7;
+  double v;
+  if (e == 15 && f == 7) v = NAN;
+  else if (e == 0) v = std::ldexp((double)f, -9);
+  else v = std::ldexp(1.0 + f / 8.0, e - 7);
+  return (c & 0x80) ? -v : v;
+}
+
+// Nearest E4M3 value of a finite float, ties to even; magnitudes that round
+// above 448 saturate to 448.  The input's sign is kept (-0 gives 0x80).
+uint8_t e4m3_round_saturate(float x) {
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs((double)x);
+  // spacing of E4M3 values around a: 2^(e-3) in binade [2^e, 2^(e+1)),
+  // e >= -6; subnormal spacing 2^-9 below 2^-6
+  double ulp;
+  if (a < std::ldexp(1.0, -6)) {
+    ulp = std::ldexp(1.0, -9);
+  } else {
+    int e2;
+    std::frexp(a, &e2);
+    ulp = std::ldexp(1.0, (e2 - 1) - 3);
+  }
+  double v = std::nearbyint(a / ulp) * ulp;  // exact: ulp is a power of two
+  if (v > 448.0) v = 448.0;
+  uint8_t mag;
+  if (v < std::ldexp(1.0, -6)) {
+    mag = (uint8_t)(v / std::ldexp(1.0, -9));
+  } else {
+    int e2;
+    const double fr = std::frexp(v, &e2);  // v = (2 fr) * 2^(e2 - 1)
+    mag = (uint8_t)(((e2 - 1 + 7) << 3) | (int)((2.0 * fr - 1.0) * 8.0));
+  }
+  return (uint8_t)(sign | mag);
+}
+
 float widen(const void* base, int dtype, size_t idx) {
   if (dtype == DT_F32) return ((const float*)base)[idx];
   uint16_t b = ((const uint16_t*)base)[idx];
@@ -132,6 +184,7 @@ float widen(const void* base, int dtype, size_t idx) {
 }
 
 int code_bits(int mode) { return (mode == MODE_INT4 || mode == MODE_INT4_STEGO) ? 4 : (mode == MODE_INT2 ? 2 : 8); }
+bool byte_token_head(int mode) { return mode == MODE_INT8_TOKEN_HEAD || mode == MODE_FP8_TOKEN_HEAD; }
 
 int row_bytes(int mode, int D) {
   if (D != 64 && D != 128) return 0;
@@ -139,6 +192,7 @@ int row_bytes(int mode, int D) {
   if (mode == MODE_INT4_STEGO) return D / 2 + 4;  // nibbles + fp32 s carrying the zero point
   if (mode == MODE_INT2) return D / 4 + 4;  // crumbs + fp16 s + fp16 m
   if (mode == MODE_INT8) return D;
+  if (byte_token_head(mode)) return D + 4;  // code bytes + fp32 s
   return 0;
 }
 
@@ -291,6 +345,37 @@ void quant_row_stego(const float* xin, int D, const int8_t* signs, uint8_t* row)
   for (int b = 0; b < 4; ++b) row[D / 2 + b] = (uint8_t)(pad >> (8 * b));
 }
 
+// One INT8 / FP8 row with a symmetric scale per (token, kv_head): RHT
+// (optional), amax = max |x|, s = amax / 127 (INT8) or amax / 448 (FP8, the
+// largest E4M3 value), code of x / s per element, pad = fp32 s.
+void quant_row_byte_token_head(int mode, const float* xin, int D, const int8_t* signs, uint8_t* row) {
+  std::vector<float> x(xin, xin + D);
+  if (signs) rht_forward_f32(x.data(), D, signs);
+  float amax = 0.0f;
+  for (int i = 0; i < D; ++i) {
+    const float a = std::fabs(x[i]);
+    if (a > amax) amax = a;
+  }
+  const float s = amax / (mode == MODE_INT8_TOKEN_HEAD ? 127.0f : 448.0f);
+  for (int i = 0; i < D; ++i) {
+    uint8_t c = 0;
+    if (s != 0.0f) {
+      const float t = x[i] / s;
+      if (mode == MODE_INT8_TOKEN_HEAD) {
+        float r = std::nearbyint(t);
+        if (r < -127.0f) r = -127.0f;
+        if (r > 127.0f) r = 127.0f;
+        c = (uint8_t)(int8_t)(int)r;
+      } else {
+        c = e4m3_round_saturate(t);
+      }
+    }
+    row[i] = c;
+  }
+  const uint32_t pad = float_to_bits(s);
+  for (int b = 0; b < 4; ++b) row[D + b] = (uint8_t)(pad >> (8 * b));
+}
+
 void quant_row_int8(const float* x, int D, const float* amax, uint8_t* row) {
   for (int c = 0; c < D; ++c) {
     float s = amax[c] / 127.0f;
@@ -318,7 +403,13 @@ void dequant_row(int mode, const uint8_t* row, int D, const int8_t* signs, const
     return;
   }
   const int data = D * code_bits(mode) / 8;
-  if (mode == MODE_INT4_STEGO) {
+  if (byte_token_head(mode)) {
+    const uint32_t pad = (uint32_t)row[D] | ((uint32_t)row[D + 1] << 8) | ((uint32_t)row[D + 2] << 16) |
+                         ((uint32_t)row[D + 3] << 24);
+    const double S = bits_to_float(pad);
+    for (int i = 0; i < D; ++i)
+      out[i] = (mode == MODE_INT8_TOKEN_HEAD ? (double)(int8_t)u[i] : e4m3_decode(u[i])) * S;
+  } else if (mode == MODE_INT4_STEGO) {
     const uint32_t pad = (uint32_t)row[data] | ((uint32_t)row[data + 1] << 8) | ((uint32_t)row[data + 2] << 16) |
                          ((uint32_t)row[data + 3] << 24);
     const int zp = (int)(pad & 15u);
@@ -373,8 +464,11 @@ int32_t orc_signed_code(int32_t mode, int32_t u) {
   // INT4 / INT2 offset encoding: stored u in [0, 2^b - 1] is q = u - 2^(b-1).
   return u - (1 << (code_bits(mode) - 1));
 }
+double orc_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
+uint8_t orc_e4m3_round(float x) { return e4m3_round_saturate(x); }
 void orc_quant_row(int32_t mode, const float* x, int32_t D, const int8_t* signs, uint8_t* row) {
   if (mode == MODE_INT4_STEGO) quant_row_stego(x, D, signs, row);
+  else if (byte_token_head(mode)) quant_row_byte_token_head(mode, x, D, signs, row);
   else quant_row_token_head(mode, x, D, signs, row);
 }
 void orc_dequant_row(int32_t mode, const uint8_t* row, int32_t D, const int8_t* signs,
@@ -444,6 +538,8 @@ int32_t orc_write(const OrcCache* c, const OrcPaging* pg, const void* k, const v
             quant_row_int8(x.data(), D, c->ch_amax + ((size_t)kv * Hkv + h) * D, dst);
           else if (mode == MODE_INT4_STEGO)
             quant_row_stego(x.data(), D, c->signs, dst);
+          else if (byte_token_head(mode))
+            quant_row_byte_token_head(mode, x.data(), D, c->signs, dst);
           else
             quant_row_token_head(mode, x.data(), D, c->signs, dst);
         }

@@ -13,6 +13,7 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import kvq_inputs as gen
@@ -20,6 +21,7 @@ import kvq_inputs as gen
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 INT4, INT2, INT8 = oracle.MODE_INT4, oracle.MODE_INT2, oracle.MODE_INT8
 STEGO = oracle.MODE_INT4_STEGO
+I8T, F8T = oracle.MODE_INT8_TOKEN_HEAD, oracle.MODE_FP8_TOKEN_HEAD
 
 
 def page_constants():
@@ -281,6 +283,105 @@ def test_stego_zero_constant_and_one_signed_rows():
     assert zp == 0 and np.max(np.abs(oracle.dequant_row(STEGO, row, D) - x)) <= st / 2 * 1.0001
 
 
+# ---------------------------------------------------------------------------
+# INT8 / FP8 with one symmetric scale per (token, kv head) (vLLM PR #40835
+# review summary, 功能与动机 and 关联脉络: the per-token-head base modes)
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = torch.arange(256, dtype=torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    nan = np.isnan(want)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_e4m3_round_matches_torch_incl_ties_subnormals_and_saturation():
+    """torch's float32 -> float8_e4m3fn conversion rounds to nearest even; it
+    agrees with the oracle wherever the result is finite (magnitudes below
+    464).  Beyond that the oracle saturates at 448 (pattern 0x7E)."""
+    vals = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])      # 0 .. 448, ascending
+    mids = (vals[:-1] + vals[1:]) / 2                                   # every tie
+    rng = np.random.default_rng(41)
+    x = np.concatenate([vals, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                        np.nextafter(mids.astype(np.float32), np.float32(1e9)),
+                        rng.uniform(0, 463.9, 4000), 2.0 ** rng.uniform(-14, 8.8, 4000)]).astype(np.float32)
+    x = np.concatenate([x, -x])
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_round(v) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, want)
+    for v, c in ((448.0, 0x7E), (463.9, 0x7E), (464.0, 0x7E), (470.0, 0x7E), (479.0, 0x7E), (1e6, 0x7E), (-500.0, 0xFE), (-0.0, 0x80)):
+        assert oracle.e4m3_round(v) == c
+
+
+def byte_pad(row, D):
+    return float(np.frombuffer(bytes(row[D:D + 4].tolist()), dtype="<f4")[0])
+
+
+def test_byte_token_head_worked_rows():
+    """Hand-worked rows (RHT off) whose amax makes the scale exactly 1."""
+    D = 64
+    x = np.zeros(D, np.float32)
+    x[:8] = [127, -63.5, 0.5, 1.5, 2.5, -2.5, -127, 3.0]
+    row = oracle.quant_row(I8T, x, None)
+    assert row[:8].view(np.int8).tolist() == [127, -64, 0, 2, 2, -2, -127, 3]   # ties to even
+    assert np.all(row[8:D] == 0)
+    assert row[D:].tolist() == [0x00, 0x00, 0x80, 0x3F]                          # fp32 1.0, little endian
+    x = np.zeros(D, np.float32)
+    x[:10] = [448, 1.0, 0.5, -2.0, 17.0, 19.0, 2.0 ** -9, 3 * 2.0 ** -10, -0.0, -448]
+    row = oracle.quant_row(F8T, x, None)
+    # 17 and 19 are ties (spacing 2 in [16, 32)): to 16 (fraction 000) and 20 (010)
+    assert row[:10].tolist() == [0x7E, 0x38, 0x30, 0xC0, 0x58, 0x5A, 0x01, 0x02, 0x80, 0xFE]
+    assert row[D:].tolist() == [0x00, 0x00, 0x80, 0x3F]
+    assert oracle.dequant_row(F8T, row, D)[:10].tolist() == [448, 1, 0.5, -2, 16, 20, 2.0 ** -9, 2.0 ** -8, 0, -448]
+
+
+@pytest.mark.parametrize("mode", [I8T, F8T])
+@pytest.mark.parametrize("rht", [False, True])
+def test_byte_token_head_error_bound(mode, rht):
+    """In the rotated domain every element is within half a code step of its
+    reconstruction: s / 2 for INT8; for FP8 half an E4M3 spacing of x / s,
+    i.e. |y| 2^-4 above 2^-6 s and s 2^-10 below."""
+    D = 128
+    rng = np.random.default_rng(51 + mode + 2 * rht)
+    signs = np.where(rng.integers(0, 2, D) == 1, 1, -1).astype(np.int8) if rht else None
+    H = sylvester(D).astype(np.float64)
+    for _ in range(200):
+        x = (rng.standard_normal(D) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+        x[rng.integers(0, D)] *= 20.0
+        row = oracle.quant_row(mode, x, signs)
+        xd = x.astype(np.float64)
+        y = H @ (signs * xd) if rht else xd
+        amax = np.abs(y).max()
+        s = byte_pad(row, D)
+        assert abs(s - amax / (127 if mode == I8T else 448)) <= 1e-6 * s
+        xh = oracle.dequant_row(mode, row, D, signs)
+        yh = H @ (signs * xh) if rht else xh
+        err = np.abs(y - yh)
+        slack = 2e-6 * amax
+        if mode == I8T:
+            assert err.max() <= s / 2 + slack
+            codes = row[:D].view(np.int8).astype(int)
+            assert np.abs(codes).max() == 127 and codes[np.argmax(np.abs(y))] == 127 * np.sign(y[np.argmax(np.abs(y))])
+        else:
+            assert np.all(err <= np.maximum(np.abs(y) * 2.0 ** -4, s * 2.0 ** -10) + slack)
+            assert np.abs(oracle.dequant_row(mode, row, D)[:D]).max() <= 448 * s
+
+
+@pytest.mark.parametrize("mode", [I8T, F8T])
+def test_byte_token_head_zero_and_constant_rows(mode):
+    D = 64
+    row = oracle.quant_row(mode, np.zeros(D, np.float32), None)
+    assert np.all(row == 0)
+    for c in (3.25, -3.25):
+        row = oracle.quant_row(mode, np.full(D, c, np.float32), None)
+        want = {(I8T, True): 0x7F, (I8T, False): 0x81, (F8T, True): 0x7E, (F8T, False): 0xFE}[(mode, c > 0)]
+        assert np.all(row[:D] == want)
+        xh = oracle.dequant_row(mode, row, D)
+        assert np.max(np.abs(xh - c)) <= abs(c) * 1e-6
+
+
 def test_signed_zero_is_canonical():
     D = 64
     x = np.zeros(D, np.float32)
@@ -345,6 +446,17 @@ def _grid_values(rng, n, D, mode):
     """Rows that INT4/INT2 (RHT off) or INT8 represent exactly."""
     if mode == INT8:
         return None
+    if mode == I8T:  # j * s with s a power of two and |j| = 127 present
+        j = rng.integers(-127, 128, size=(n, D))
+        j[:, 0] = 127 * rng.choice([-1, 1], size=n)
+        return (j * 2.0 ** rng.integers(-3, 2, size=(n, 1))).astype(np.float32)
+    if mode == F8T:  # E4M3 values times a power of two, with 448 present
+        c = rng.integers(0, 256, size=(n, D))
+        c = np.where((c & 0x7F) == 0x7F, c - 1, c)                 # no NaN patterns
+        e = np.array([oracle.e4m3_decode(i) for i in range(256)])
+        v = e[c]
+        v[:, 0] = 448 * rng.choice([-1, 1], size=n)
+        return (v * 2.0 ** rng.integers(-3, 2, size=(n, 1))).astype(np.float32)
     if mode == STEGO:  # (k - zp) * s with s a power of two, min and max pinned
         k = rng.integers(0, 16, size=(n, D))
         k[:, 0], k[:, 1] = 0, 15
@@ -369,7 +481,7 @@ def _softmax_ref(q, K, V, scale, mask):
     return p @ V
 
 
-@pytest.mark.parametrize("mode", [INT4, INT2, STEGO])
+@pytest.mark.parametrize("mode", [INT4, INT2, STEGO, I8T, F8T])
 def test_attention_brute_force_on_exact_rows(mode):
     rng = np.random.default_rng(11 + mode)
     D, bs, Hkv, Hq = 64, 16, 2, 4
