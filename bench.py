@@ -54,7 +54,8 @@ def peaks():
 
 def row_bytes(mode: int, D: int) -> int:
     """Bytes of one cache row: packed codes plus the fp16 scale / zero-point pad (INT8: codes only)."""
-    return {gen.MODE_INT4: D // 2 + 4, gen.MODE_INT2: D // 4 + 4, gen.MODE_INT8: D, gen.MODE_INT4_STEGO: D // 2 + 4}[mode]
+    return {gen.MODE_INT4: D // 2 + 4, gen.MODE_INT2: D // 4 + 4, gen.MODE_INT8: D, gen.MODE_INT4_STEGO: D // 2 + 4,
+            gen.MODE_INT8_TOKEN_HEAD: D + 4, gen.MODE_FP8_TOKEN_HEAD: D + 4}[mode]
 
 
 def recorded_units(profile: str, key: str, src_hash: str):
@@ -173,6 +174,14 @@ WORKLOADS = {
                                                   mode=gen.MODE_INT4_STEGO),
                          "INT4 (zero point in the fp32 scale) paged decode tokens/s and effective KV GB/s "
                          "(% of GB300 HBM peak)", "decode"),
+    "llama_int8_token_head": (lambda a: gen.llama_int4(seed=0, num_blocks=a.pool_blocks or 200000,
+                                                       mode=gen.MODE_INT8_TOKEN_HEAD),
+                              "INT8 per-token-head paged decode tokens/s and effective KV GB/s "
+                              "(% of GB300 HBM peak)", "decode"),
+    "llama_fp8_token_head": (lambda a: gen.llama_int4(seed=0, num_blocks=a.pool_blocks or 200000,
+                                                      mode=gen.MODE_FP8_TOKEN_HEAD),
+                             "FP8 (E4M3) per-token-head paged decode tokens/s and effective KV GB/s "
+                             "(% of GB300 HBM peak)", "decode"),
     "ernie_int2": (lambda a: gen.ernie_int2(seed=0, num_blocks=a.pool_blocks or 100000),
                    "INT2 paged decode tokens/s and effective KV GB/s (% of GB300 HBM peak)", "decode"),
     "qwen_int8_headwise": (lambda a: gen.qwen_int8_headwise(seed=0),
@@ -396,7 +405,8 @@ def run_gpu(args, rank, world, local_rank):
     hbm, tensor, peak_kind = peaks()
     cfg = {"workload": wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
-           "mode": {0: "int4", 1: "int2", 2: "int8", 3: "int4_stego"}[wl.mode], "headwise_table": bool(wl.headwise),
+           "mode": {0: "int4", 1: "int2", 2: "int8", 3: "int4_stego", 4: "int8_token_head",
+                    5: "fp8_token_head"}[wl.mode], "headwise_table": bool(wl.headwise),
            "cached_tokens": int(wl.seq_lens.sum()), "new_tokens_per_step": int(wl.n_new.sum()),
            "pool_blocks": wl.num_blocks, "rht": wl.signs is not None,
            "timing": "one CUDA graph per step (write + attention call), events around each replay; "
@@ -417,7 +427,7 @@ def run_gpu(args, rank, world, local_rank):
                 "algorithmic_bytes_per_launch": units["decode"], "traffic": traffic}
         extra = {"effective_kv_GBps": round(achieved, 1), "decode_ms": round(att, 5)}
         launches = 4  # write + (prep, stream, merge)
-        dtype = {0: "u4", 1: "u2", 2: "s8", 3: "u4"}[wl.mode] + " codes x fp16 tensor-core math, fp32 accumulate/softmax"
+        dtype = {0: "u4", 1: "u2", 2: "s8", 3: "u4", 4: "s8", 5: "e4m3"}[wl.mode] + " codes x fp16 tensor-core math, fp32 accumulate/softmax"
     else:
         achieved = units["prefill_flops"] / (att / 1e3) / 1e12
         traffic = recorded_units("prefill_tc_%s.md" % args.workload, "dram_bytes_per_prefill_call",
@@ -589,7 +599,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_int4", choices=sorted(WORKLOADS),
                     help="llama_int4 (the headline decode workload), llama_int4_d64_bs64, llama_int4_stego, "
-                         "ernie_int2, qwen_int8_headwise, prefill_int4")
+                         "llama_int8_token_head, llama_fp8_token_head, ernie_int2, qwen_int8_headwise, prefill_int4")
     ap.add_argument("--pool-blocks", type=int, default=0,
                     help="block pool size (0 = the workload's own; smaller pools only for profiling)")
     ap.add_argument("--prefill-prefixes", type=int, nargs="+", default=[0, 4096, 16384, 61440],

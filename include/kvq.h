@@ -76,12 +76,20 @@ typedef enum {
  *   (u - zp) * s holds 0, so it spans lo = min(min, 0) .. hi = max(max, 0);
  *   s = (hi - lo) / 15 with its low 4 mantissa bits cleared, zp =
  *   clamp(rne(-lo / s), 0, 15), u = clamp(rne(x / s) + zp, 0, 15), pad =
- *   bits(s) | zp, value (u - zp) * s. */
+ *   bits(s) | zp, value (u - zp) * s.
+ * INT8_TOKEN_HEAD / FP8_TOKEN_HEAD: the per-token-head INT8 / FP8 modes the
+ *   INT4 mode was built on ([vLLM-INT4] 功能与动机, 关联脉络): per row (after
+ *   the optional RHT) one symmetric fp32 scale s = amax / 127 (INT8 codes
+ *   clamp(rne(x / s), -127, 127)) or s = amax / 448 (FP8 E4M3 codes: x / s
+ *   rounded to nearest even, saturating at 448); s = 0 gives zero codes;
+ *   value code * s. */
 typedef enum {
   KVQ_INT4_TOKEN_HEAD = 0,
   KVQ_INT2_TOKEN_HEAD = 1,
   KVQ_INT8_CHANNEL = 2,
-  KVQ_INT4_STEGO = 3
+  KVQ_INT4_STEGO = 3,
+  KVQ_INT8_TOKEN_HEAD = 4,
+  KVQ_FP8_TOKEN_HEAD = 5
 } kvq_mode;
 
 /* Element type of q / k / v inputs. */
@@ -106,12 +114,15 @@ typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
  *       INT2: head_dim/4 data bytes (element 4i+j in bits 2j..2j+1 of byte i),
  *             then the same 4 pad bytes
  *       INT8: head_dim bytes of two's-complement codes (no pad)
+ *       INT8_TOKEN_HEAD / FP8_TOKEN_HEAD: head_dim code bytes (two's
+ *             complement / E4M3), then the fp32 scale (little endian)
  *   Both pools must be 16-byte aligned.
  *
  * rht_signs: int8 [head_dim] of +1/-1 (device).  Non-NULL turns the random
  *   Hadamard transform on for INT4/INT2: y = H (signs * x), H the unnormalised
- *   Sylvester Walsh-Hadamard matrix ([vLLM-INT4] 功能与动机, 实现拆解 2).  One
- *   vector per layer, shared by K, V and every head.  Must be NULL for INT8.
+ *   Sylvester Walsh-Hadamard matrix ([vLLM-INT4] 功能与动机, 实现拆解 2); the
+ *   same for INT4_STEGO and the INT8 / FP8 token-head modes.  One vector per
+ *   layer, shared by K, V and every head.  Must be NULL for INT8_CHANNEL.
  *
  * ch_amax / ch_amax_ready (INT8 only, else NULL):
  *   ch_amax: fp32 [2][num_kv_heads][head_dim] (index 0 = K, 1 = V).  The scale
@@ -177,7 +188,9 @@ int32_t kvq_row_bytes(int32_t mode, int32_t head_dim);
  * s = (max - min) / (2^b - 1) (IEEE); s, m rounded to fp16 (round to nearest
  * even, saturating at +-65504); u = clamp(rne((y - m) / s), 0, 2^b - 1), u = 0
  * when the fp16 scale is 0.  INT8: q = clamp(rne(x / (amax / 127)), -127, 127),
- * 0 when the scale is 0.
+ * 0 when the scale is 0.  INT8 / FP8 token-head: amax = max |y| of the row,
+ * s = amax / 127 or amax / 448 (IEEE), each code from y / s (IEEE division;
+ * E4M3 by round to nearest even with saturation), all 0 when s is 0.
  * num_tokens == 0 is a no-op returning KVQ_OK. */
 kvq_status kvq_write(const kvq_cache* cache, const kvq_paging* paging,
                      const void* k, const void* v, int32_t dtype,

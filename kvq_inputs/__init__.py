@@ -156,7 +156,8 @@ def llama_int4(seed: int = 0, batch: int = 64, ctx_lo: int = 1024, ctx_hi: int =
     blocks of the pool, K/V ~ N(0,1) with 1% of (head, channel) pairs x10, RHT
     on, one new token per sequence per step.  `head_dim` / `block_size` give
     the same layer at D = 64 and bs = 32 or 64; `mode` MODE_INT4_STEGO the
-    same cache with the zero point carried in the fp32 scale."""
+    same cache with the zero point carried in the fp32 scale, and
+    MODE_INT8_TOKEN_HEAD / MODE_FP8_TOKEN_HEAD the same layer in 8-bit rows."""
     rng = _structure_rng(seed)
     D, Hkv, bs = head_dim, 8, block_size
     signs = _draw_signs(rng, D)
@@ -167,8 +168,9 @@ def llama_int4(seed: int = 0, batch: int = 64, ctx_lo: int = 1024, ctx_hi: int =
     max_blocks = (ctx_hi + bs - 1) // bs
     table = _tables_from_pool(rng, seq_lens, bs, max_blocks, num_blocks)
     name = "llama_int4_decode" if (D, bs) == (128, 16) else "llama_int4_d%d_bs%d_decode" % (D, bs)
-    if mode == MODE_INT4_STEGO:
-        name = name.replace("int4", "int4_stego")
+    tag = {MODE_INT4_STEGO: "int4_stego", MODE_INT8_TOKEN_HEAD: "int8_token_head", MODE_FP8_TOKEN_HEAD: "fp8_token_head"}
+    if mode in tag:
+        name = name.replace("int4", tag[mode])
     return Workload(name, mode, 32, Hkv, D, bs, "bf16", num_blocks,
                     max_blocks, seq_lens, np.ones(batch, np.int32), table, False, None, 0,
                     signs, "decode", 1.0, ok, ov, seed)

@@ -29,6 +29,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_WORKSPACE = 0, 1, 2, 3, 4
 KVQ_INT4_TOKEN_HEAD, KVQ_INT2_TOKEN_HEAD, KVQ_INT8_CHANNEL, KVQ_INT4_STEGO = 0, 1, 2, 3
+KVQ_INT8_TOKEN_HEAD, KVQ_FP8_TOKEN_HEAD = 4, 5
 KVQ_F32, KVQ_BF16 = 0, 1
 KVQ_DEVERR_BLOCK_RANGE, KVQ_DEVERR_TABLE_RANGE, KVQ_DEVERR_SEQ_LEN, KVQ_DEVERR_TIMEOUT = 1, 2, 4, 8
 

@@ -51,7 +51,7 @@ kvq_status check_cache(const kvq_cache* c) {
   if (!aligned(c->k_pages, 16) || !aligned(c->v_pages, 16))
     return fail(KVQ_ERR_INVALID_ARG, "k_pages / v_pages must be 16-byte aligned");
   if (c->mode != KVQ_INT4_TOKEN_HEAD && c->mode != KVQ_INT2_TOKEN_HEAD && c->mode != KVQ_INT8_CHANNEL &&
-      c->mode != KVQ_INT4_STEGO)
+      c->mode != KVQ_INT4_STEGO && c->mode != KVQ_INT8_TOKEN_HEAD && c->mode != KVQ_FP8_TOKEN_HEAD)
     return fail(KVQ_ERR_UNSUPPORTED, "unknown mode");
   if (c->head_dim != 64 && c->head_dim != 128) return fail(KVQ_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (c->block_size != 16 && c->block_size != 32 && c->block_size != 64)
@@ -158,6 +158,7 @@ int32_t kvq_row_bytes(int32_t mode, int32_t head_dim) {
   if (mode == KVQ_INT4_TOKEN_HEAD || mode == KVQ_INT4_STEGO) return head_dim / 2 + 4;
   if (mode == KVQ_INT2_TOKEN_HEAD) return head_dim / 4 + 4;
   if (mode == KVQ_INT8_CHANNEL) return head_dim;
+  if (mode == KVQ_INT8_TOKEN_HEAD || mode == KVQ_FP8_TOKEN_HEAD) return head_dim + 4;
   return 0;
 }
 

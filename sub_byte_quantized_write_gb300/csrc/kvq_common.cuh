@@ -3,17 +3,30 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace kvq {
 
-enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2 };
+// Kernel code families.  The API's zero-point-in-scale INT4 mode (3) runs as
+// MODE_INT4 with the `stego` flag of the parameters; 4 and 5 are the INT8 /
+// FP8 rows with one fp32 scale per (token, kv head).
+enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2, MODE_I8T = 4, MODE_F8T = 5 };
 enum { DT_F32 = 0, DT_BF16 = 1 };
 enum { DEVERR_BLOCK_RANGE = 1, DEVERR_TABLE_RANGE = 2, DEVERR_SEQ_LEN = 4, DEVERR_TIMEOUT = 8 };
 
 __host__ __device__ constexpr int mode_bits(int mode) { return mode == MODE_INT4 ? 4 : (mode == MODE_INT2 ? 2 : 8); }
 __host__ __device__ constexpr int data_bytes(int mode, int D) { return D * mode_bits(mode) / 8; }
 __host__ __device__ constexpr int row_bytes_of(int mode, int D) { return mode == MODE_INT8 ? D : data_bytes(mode, D) + 4; }
+// INT8 / FP8 codes with a symmetric fp32 scale per row (no zero point)
+__host__ __device__ constexpr bool byte_token_head(int mode) { return mode == MODE_I8T || mode == MODE_F8T; }
+
+// Two E4M3 codes (bits 0-7 and 8-15 of `pair`) as an fp16 pair, the first in
+// the low half; exact, since every E4M3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_half2_bits(uint32_t pair) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(pair & 0xFFFFu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
 
 __device__ __forceinline__ void flag_error(int32_t* dev_error, int bit) {
   if (dev_error) atomicOr(dev_error, bit);
@@ -244,11 +257,15 @@ __device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpre
 // Scale s and the value z of the signed code 0 (stored code 2^(b-1)) from an
 // INT4 / INT2 row's 4-byte pad: fp16 s then fp16 m (z = m + 2^(b-1) s), or,
 // for zero-point-in-scale INT4 rows, an fp32 s whose low 4 bits hold the zero
-// point zp (z = (8 - zp) s, exact).
+// point zp (z = (8 - zp) s, exact).  INT8 / FP8 token-head rows: the pad is
+// the fp32 scale and z = 0.
 template <int MODE>
 __device__ __forceinline__ void pad_scale_zero(uint32_t pad, bool stego, float& s, float& z) {
   constexpr float half_range = (float)(1 << (mode_bits(MODE) - 1));
-  if (MODE == MODE_INT4 && stego) {
+  if constexpr (byte_token_head(MODE)) {
+    s = __uint_as_float(pad);
+    z = 0.0f;
+  } else if (MODE == MODE_INT4 && stego) {
     s = __uint_as_float(pad & ~15u);
     z = s * (float)(8 - (int)(pad & 15u));
   } else {

@@ -2,8 +2,8 @@
 //
 // What it computes: for every sequence b and q head hq, softmax attention of
 // the decode query (position seq_lens[b]-1) over the visible cached keys,
-// with keys and values read from INT4 / INT2 / INT8 pages, dequantised and
-// mapped back through the inverse RHT.  Sources (page title, section):
+// with keys and values read from INT4 / INT2 / INT8 / FP8 pages, dequantised
+// and mapped back through the inverse RHT.  Sources (page title, section):
 // vLLM PR #40835 review summary ("INT4 per-token-head KV cache for the Triton
 // backend"), 实现拆解 item 2 (read kernel: unpack, dequantise, attention);
 // FastDeploy PR #7718 "Optimize AppendAttention for discrete head-wise
@@ -32,7 +32,8 @@
 //   q . k_j = (s_j (q' . c_j) + z_j sum(q')) / D,   q' = H (d * q)
 //   sum_j P_j v_j = d * H( sum_j (P_j s_j) c_j + sum_j P_j z_j ) / D
 // with the signed code c = u - 2^(b-1) and z = m + 2^(b-1) s (the value of
-// code 2^(b-1)), so the hot loop multiplies codes (exact small integers in fp16) on
+// code 2^(b-1)); INT8 / FP8 token-head rows have c the stored code (an E4M3
+// value for FP8) and z = 0.  So the hot loop multiplies codes (exact small integers in fp16) on
 // the tensor cores: QK^T as m16n8k16 with M = 16 keys and N = 8 slots (4 q
 // heads of the GQA group x {hi, lo} halves of q'), and P.V as m16n8k16 with
 // M = 16 head dims, K = 16 keys, N = the same 8 slots of (P s) hi / lo.
@@ -96,7 +97,9 @@ __device__ __forceinline__ uint2 load_range(const uint8_t* tile, int kappa, int 
     else return make_uint2(lds32(p), 0u);
   } else {
     const uint8_t* row = tile + kappa * C::R;
-    if constexpr (C::BPL >= 4) {
+    if constexpr (C::BPL == 8) {  // 8-bit token-head rows: D + 4 bytes, 4-byte aligned
+      return make_uint2(lds32(row + off), lds32(row + off + 4));
+    } else if constexpr (C::BPL >= 4) {
       return make_uint2(lds32(row + off), 0u);
     } else {
       const uint32_t w = lds32(row + (off & ~3));
@@ -114,7 +117,8 @@ __host__ __device__ constexpr uint32_t magic_minus(uint32_t magic_half, int pos,
 }
 
 // Two codes of one key row as an exact fp16 pair of signed codes
-// q = u - 2^(b-1) (INT4 [-8, 7], INT2 [-2, 1], INT8 as stored).  Pair P of
+// q = u - 2^(b-1) (INT4 [-8, 7], INT2 [-2, 1], INT8 as stored, FP8 the E4M3
+// value).  Pair P of
 // word w holds head dims (d0, d1) = INT4 (8w+P, 8w+P+4), INT2 (16w+P,
 // 16w+P+8), INT8 (4w+2P, 4w+2P+1); kpair_dims gives the same map for the
 // query side.
@@ -132,6 +136,8 @@ __device__ __forceinline__ uint32_t kpair(uint32_t w) {
     constexpr uint32_t magic = q == 0 ? 0x64006400u : q == 1 ? 0x5C005C00u : q == 2 ? 0x54005400u : 0x4C004C00u;
     const uint32_t src = (P >= 4) ? (w >> 8) : w;
     return hsub2_bits(lop3_and_or(src, mask, magic), magic_minus(magic & 0xFFFF, 2 * q, 2));
+  } else if constexpr (MODE == MODE_F8T) {
+    return e4m3x2_to_half2_bits(w >> (16 * P));
   } else {
     constexpr uint32_t sel = (2 * P) | (4 << 4) | ((2 * P + 1) << 8) | (4 << 12);
     const uint32_t x = prmt(w, 0u, sel);
@@ -176,6 +182,9 @@ __device__ __forceinline__ uint32_t vpair(uint2 A, uint2 B) {
     constexpr uint32_t mask = 0x00030003u << (2 * q);
     constexpr uint32_t magic = q == 0 ? 0x64006400u : q == 1 ? 0x5C005C00u : q == 2 ? 0x54005400u : 0x4C004C00u;
     return hsub2_bits(lop3_and_or(x, mask, magic), magic_minus(magic & 0xFFFF, 2 * q, 2));
+  } else if constexpr (MODE == MODE_F8T) {
+    constexpr int b = C & 3;
+    return e4m3x2_to_half2_bits((C < 4) ? prmt(A.x, B.x, b | ((4 + b) << 4)) : prmt(A.y, B.y, b | ((4 + b) << 4)));
   } else {
     constexpr int b = C & 3;
     constexpr uint32_t sel = b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12);
@@ -257,7 +266,8 @@ __device__ __forceinline__ int worker_of(int x, int T, int nw) {
 // workloads): keys per tile, ring depth and CTAs per SM.  INT4 with GQA
 // groups up to 4 takes 64-key tiles (two independent 32-key halves per step
 // of a warp) at 3 CTAs per SM; the others 32-key tiles, NT == 1 kernels at 4
-// CTAs per SM (3 for INT8's larger rows), NT == 2 kernels at 3 (2 for INT8).
+// CTAs per SM (3 for the larger 8-bit rows), NT == 2 kernels at 3 (2 for
+// 8-bit rows).
 template <int MODE, int D, int NT>
 struct StreamCfg {
   static constexpr int KT = (MODE == MODE_INT4 && NT == 1) ? 64 : 32;
@@ -265,7 +275,8 @@ struct StreamCfg {
   static constexpr int NH2 = KT / 32;  // 32-key halves per tile
   static constexpr int NSTAGE = NT == 1 ? (MODE == MODE_INT4 ? 2 : (MODE == MODE_INT2 ? 5 : 2))
                                         : (MODE == MODE_INT4 ? 4 : (MODE == MODE_INT2 ? 3 : 3));
-  static constexpr int CTAS = NT == 1 ? (MODE == MODE_INT4 ? 3 : (MODE == MODE_INT8 ? 3 : 4)) : (MODE == MODE_INT8 ? 2 : 3);
+  static constexpr bool BYTES = MODE == MODE_INT8 || byte_token_head(MODE);
+  static constexpr int CTAS = NT == 1 ? (MODE == MODE_INT4 || BYTES ? 3 : 4) : (BYTES ? 2 : 3);
   static constexpr int TILE = KT * row_bytes_of(MODE, D);  // key rows of K (or V)
   static constexpr int STAGE = 2 * TILE;                   // K tile then V tile
 };
@@ -796,6 +807,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
             if constexpr (MODE == MODE_INT4) cdot -= kcorr[nt];
             float zz;
             if constexpr (MODE == MODE_INT8) zz = bet[nt] * cdot;
+            else if constexpr (byte_token_head(MODE)) zz = (bet[nt] * sk) * cdot;
             else zz = fmaf(bet[nt] * sk, cdot, gam[nt] * mk);
             lg[h2][m][hh][nt] = ok ? zz : -CUDART_INF_F;
           }
@@ -834,7 +846,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
             const float p = ex2(lg[h2][m][hh][nt] - muse);
             const bool ok = vk[h2][m][hh];
             tl += ok ? p : 0.0f;
-            if constexpr (MODE != MODE_INT8) tpm += ok ? p * mv_[h2][m][hh] : 0.0f;
+            if constexpr (MODE != MODE_INT8 && !byte_token_head(MODE)) tpm += ok ? p * mv_[h2][m][hh] : 0.0f;
             wv[hh] = ok ? p * sv_[h2][m][hh] : 0.0f;
           }
           const __half2 hp = __floats2half2_rn(wv[0], wv[1]);
@@ -1038,10 +1050,20 @@ size_t stream_smem_bytes() {
   return (size_t)DECODE_WARPS * NSTAGE * SC::STAGE + DECODE_WARPS * NSTAGE * 4 + DECODE_WARPS * NSTAGE * 8;
 }
 
+template <int NT>
+int ctas_per_sm_nt(int mode) {
+  switch (mode) {
+    case MODE_INT4: return StreamCfg<MODE_INT4, 128, NT>::CTAS;
+    case MODE_INT2: return StreamCfg<MODE_INT2, 128, NT>::CTAS;
+    case MODE_INT8: return StreamCfg<MODE_INT8, 128, NT>::CTAS;
+    case MODE_I8T: return StreamCfg<MODE_I8T, 128, NT>::CTAS;
+    default: return StreamCfg<MODE_F8T, 128, NT>::CTAS;
+  }
+}
+
 int decode_ctas_per_sm(int mode, int head_dim, int group) {
   (void)head_dim;
-  if (group > 4) return mode == MODE_INT8 ? StreamCfg<MODE_INT8, 128, 2>::CTAS : StreamCfg<MODE_INT4, 128, 2>::CTAS;
-  return mode == MODE_INT8 ? StreamCfg<MODE_INT8, 128, 1>::CTAS : StreamCfg<MODE_INT4, 128, 1>::CTAS;
+  return group > 4 ? ctas_per_sm_nt<2>(mode) : ctas_per_sm_nt<1>(mode);
 }
 
 template <typename Kern, typename... Args>
@@ -1100,6 +1122,10 @@ cudaError_t launch_decode(const AttnParams& P, const DecodeWs& ws, int grid, cud
     case MODE_INT2 * 1000 + 64: return launch_decode_md<MODE_INT2, 64>(P, ws, grid, stream);
     case MODE_INT8 * 1000 + 128: return launch_decode_md<MODE_INT8, 128>(P, ws, grid, stream);
     case MODE_INT8 * 1000 + 64: return launch_decode_md<MODE_INT8, 64>(P, ws, grid, stream);
+    case MODE_I8T * 1000 + 128: return launch_decode_md<MODE_I8T, 128>(P, ws, grid, stream);
+    case MODE_I8T * 1000 + 64: return launch_decode_md<MODE_I8T, 64>(P, ws, grid, stream);
+    case MODE_F8T * 1000 + 128: return launch_decode_md<MODE_F8T, 128>(P, ws, grid, stream);
+    case MODE_F8T * 1000 + 64: return launch_decode_md<MODE_F8T, 64>(P, ws, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

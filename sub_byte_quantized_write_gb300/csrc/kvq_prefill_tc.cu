@@ -4,7 +4,7 @@
 // What it computes: every query of the chunk (sequence b, position
 // seq_lens[b] - n_b + i) attends causally to all keys visible at its
 // position, the chunk's own keys included, all read back from the INT4 /
-// INT2 / INT8 pages (the chunk is written with kvq_write first).  Sources
+// INT2 / INT8 / FP8 pages (the chunk is written with kvq_write first).  Sources
 // (page title, section): FastDeploy PR #5173 "support dynamic int2
 // quantization cache kv", Usage (chunked prefill with 8192 batched tokens);
 // vLLM PR #40835 review summary ("INT4 per-token-head KV cache for the Triton
@@ -111,7 +111,8 @@ enum {
 };
 
 // Eight consecutive codes (head dims 8c .. 8c+7) of a raw row as four exact
-// fp16 pairs of signed codes u - 2^(b-1) (INT8: as stored), in dim order.
+// fp16 pairs of signed codes u - 2^(b-1) (INT8: as stored; FP8: the E4M3
+// value), in dim order.
 template <int MODE>
 __device__ __forceinline__ uint4 codes8(const uint8_t* raw_row, int c) {
   uint32_t o[4];
@@ -130,8 +131,14 @@ __device__ __forceinline__ uint4 codes8(const uint8_t* raw_row, int c) {
       o[2 * j] = hsub2_bits(lop3_and_or(x, 0x000C0003u, 0x5C006400u), 0x5C086402u);
       o[2 * j + 1] = hsub2_bits(lop3_and_or(x, 0x00C00030u, 0x4C005400u), 0x4C805420u);
     }
+  } else if constexpr (MODE == MODE_F8T) {
+    const uint2 w = make_uint2(lds32(raw_row + 8 * c), lds32(raw_row + 8 * c + 4));  // rows are D + 4 bytes
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = e4m3x2_to_half2_bits((j < 2 ? w.x : w.y) >> (16 * (j & 1)));
   } else {
-    const uint2 w = lds64(raw_row + 8 * c);
+    // INT8 channel rows (D bytes) are 8-byte aligned, token-head rows (D + 4) are not
+    const uint2 w = MODE == MODE_INT8 ? lds64(raw_row + 8 * c)
+                                      : make_uint2(lds32(raw_row + 8 * c), lds32(raw_row + 8 * c + 4));
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const uint32_t src = j < 2 ? w.x : w.y;
@@ -155,6 +162,8 @@ __device__ __forceinline__ uint32_t codes2(const uint8_t* raw_row, int d) {
     const uint32_t b = (uint32_t)raw_row[d >> 2] >> (2 * (d & 3));  // crumbs d, d+1 at bits 0-3
     const uint32_t x = b | (b << 16);
     return hsub2_bits(lop3_and_or(x, 0x000C0003u, 0x5C006400u), 0x5C086402u);
+  } else if constexpr (MODE == MODE_F8T) {
+    return e4m3x2_to_half2_bits(*reinterpret_cast<const uint16_t*>(raw_row + d));
   } else {
     const uint32_t w = *reinterpret_cast<const uint16_t*>(raw_row + d);
     const uint32_t x = prmt(w, 0u, 0 | (4 << 4) | (1 << 8) | (4 << 12));
@@ -876,6 +885,10 @@ cudaError_t launch_prefill(const AttnParams& P, cudaStream_t stream) {
     case MODE_INT2 * 1000 + 64: return launch_prefill_tc_t<MODE_INT2, 64>(P, stream);
     case MODE_INT8 * 1000 + 128: return launch_prefill_tc_t<MODE_INT8, 128>(P, stream);
     case MODE_INT8 * 1000 + 64: return launch_prefill_tc_t<MODE_INT8, 64>(P, stream);
+    case MODE_I8T * 1000 + 128: return launch_prefill_tc_t<MODE_I8T, 128>(P, stream);
+    case MODE_I8T * 1000 + 64: return launch_prefill_tc_t<MODE_I8T, 64>(P, stream);
+    case MODE_F8T * 1000 + 128: return launch_prefill_tc_t<MODE_F8T, 128>(P, stream);
+    case MODE_F8T * 1000 + 64: return launch_prefill_tc_t<MODE_F8T, 64>(P, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -10,6 +10,9 @@
 // INT8 per channel: vllm-ascend-quantized-kv-cache METADATA ("Ascend INT8 KV
 // Cache Plugin"), 运行机制 (symmetric per-channel scales along tokens, from the
 // first K/V a layer receives, separately for K and V).
+// INT8 / FP8 per (token, kv_head): the same vLLM page, 功能与动机 and 关联脉络
+// (the per-token-head INT8 / FP8 modes the INT4 mode builds on): one
+// symmetric fp32 scale per row, stored after the D code bytes.
 // Scatter through a uniform or head-wise block table with -1 sentinels:
 // FastDeploy PR #7718 "Optimize AppendAttention for discrete head-wise
 // block_idx", Motivation and PR2-only delta table.
@@ -114,53 +117,73 @@ __global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
       if (__ldg(P.signs + lane * EPL + i) < 0) x[i] = -x[i];
     wht_warp<EPL>(x, lane);
   }
-  float mn = x[0], mx = x[0];
-#pragma unroll
-  for (int i = 1; i < EPL; ++i) {
-    mn = fminf(mn, x[i]);
-    mx = fmaxf(mx, x[i]);
-  }
-  mn = __fadd_rn(warp_min(mn), 0.0f);  // canonical +0
-  mx = __fadd_rn(warp_max(mx), 0.0f);
   uint32_t bits = 0, pad;
-  if constexpr (STEGO) {
-    // the grid (u - zp) * s holds 0: it spans min(mn, 0) .. max(mx, 0); the
-    // scale's low 4 mantissa bits are cleared and carry the zero point
-    const float lo = mn < 0.0f ? mn : 0.0f, hi = mx > 0.0f ? mx : 0.0f;
-    const uint32_t sb = __float_as_uint(__fdiv_rn(__fsub_rn(hi, lo), (float)LEVELS)) & ~15u;
-    const float st = __uint_as_float(sb);
-    float zp = 0.0f;
-    if (st != 0.0f) zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, st)), 0.0f), (float)LEVELS);
+  if constexpr (byte_token_head(MODE)) {
+    // symmetric: s = amax / 127 (INT8) or amax / 448 (largest E4M3 value)
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, MODE == MODE_I8T ? 127.0f : 448.0f);
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      uint32_t u = 0;
-      if (st != 0.0f) {
-        float r = __fadd_rn(rintf(__fdiv_rn(x[i], st)), zp);
-        r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
-        u = (uint32_t)r;
+      uint32_t c = 0;
+      if (s != 0.0f) {
+        const float t = __fdiv_rn(x[i], s);
+        if constexpr (MODE == MODE_I8T) c = (uint32_t)(int)fminf(fmaxf(rintf(t), -127.0f), 127.0f) & 0xFFu;
+        else c = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);  // nearest even
       }
-      bits |= u << (i * BITS);
+      bits |= c << (8 * i);
     }
-    pad = sb | (uint32_t)zp;
+    pad = __float_as_uint(s);
   } else {
-    const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)LEVELS);
-    const uint16_t s_h = f16_sat_bits(s);
-    const uint16_t m_h = f16_sat_bits(mn);
-    const float S = __half2float(__ushort_as_half(s_h));
-    const float M = __half2float(__ushort_as_half(m_h));
+    float mn = x[0], mx = x[0];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      uint32_t u = 0;
-      if (S != 0.0f) {
-        float r = rintf(__fdiv_rn(__fsub_rn(x[i], M), S));
-        r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
-        u = (uint32_t)r;
-      }
-      bits |= u << (i * BITS);
+    for (int i = 1; i < EPL; ++i) {
+      mn = fminf(mn, x[i]);
+      mx = fmaxf(mx, x[i]);
     }
-    pad = (uint32_t)s_h | ((uint32_t)m_h << 16);
+    mn = __fadd_rn(warp_min(mn), 0.0f);  // canonical +0
+    mx = __fadd_rn(warp_max(mx), 0.0f);
+    if constexpr (STEGO) {
+      // the grid (u - zp) * s holds 0: it spans min(mn, 0) .. max(mx, 0); the
+      // scale's low 4 mantissa bits are cleared and carry the zero point
+      const float lo = mn < 0.0f ? mn : 0.0f, hi = mx > 0.0f ? mx : 0.0f;
+      const uint32_t sb = __float_as_uint(__fdiv_rn(__fsub_rn(hi, lo), (float)LEVELS)) & ~15u;
+      const float st = __uint_as_float(sb);
+      float zp = 0.0f;
+      if (st != 0.0f) zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, st)), 0.0f), (float)LEVELS);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        uint32_t u = 0;
+        if (st != 0.0f) {
+          float r = __fadd_rn(rintf(__fdiv_rn(x[i], st)), zp);
+          r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
+          u = (uint32_t)r;
+        }
+        bits |= u << (i * BITS);
+      }
+      pad = sb | (uint32_t)zp;
+    } else {
+      const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)LEVELS);
+      const uint16_t s_h = f16_sat_bits(s);
+      const uint16_t m_h = f16_sat_bits(mn);
+      const float S = __half2float(__ushort_as_half(s_h));
+      const float M = __half2float(__ushort_as_half(m_h));
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        uint32_t u = 0;
+        if (S != 0.0f) {
+          float r = rintf(__fdiv_rn(__fsub_rn(x[i], M), S));
+          r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
+          u = (uint32_t)r;
+        }
+        bits |= u << (i * BITS);
+      }
+      pad = (uint32_t)s_h | ((uint32_t)m_h << 16);
+    }
   }
-  constexpr int NBITS = EPL * BITS;        // bits per lane: 16, 8 or 4
+  constexpr int NBITS = EPL * BITS;        // bits per lane: 32, 16, 8 or 4
   const uint32_t word = gather_word<NBITS>(bits, lane);
   constexpr int LPW = 32 / NBITS;
   if (lane % LPW == 0) *reinterpret_cast<uint32_t*>(dst + 4 * (lane / LPW)) = word;
@@ -237,7 +260,13 @@ cudaError_t launch_write(const WriteParams& P, cudaStream_t stream) {
     else int8_quant_kernel<64><<<blocks, 256, 0, stream>>>(P);
     return cudaGetLastError();
   }
-  if (P.mode == MODE_INT4 && P.stego) {
+  if (P.mode == MODE_I8T) {
+    if (P.head_dim == 128) write_token_head_kernel<MODE_I8T, 128, false><<<blocks, 256, 0, stream>>>(P);
+    else write_token_head_kernel<MODE_I8T, 64, false><<<blocks, 256, 0, stream>>>(P);
+  } else if (P.mode == MODE_F8T) {
+    if (P.head_dim == 128) write_token_head_kernel<MODE_F8T, 128, false><<<blocks, 256, 0, stream>>>(P);
+    else write_token_head_kernel<MODE_F8T, 64, false><<<blocks, 256, 0, stream>>>(P);
+  } else if (P.mode == MODE_INT4 && P.stego) {
     if (P.head_dim == 128) write_token_head_kernel<MODE_INT4, 128, true><<<blocks, 256, 0, stream>>>(P);
     else write_token_head_kernel<MODE_INT4, 64, true><<<blocks, 256, 0, stream>>>(P);
   } else if (P.mode == MODE_INT4) {

@@ -50,6 +50,8 @@ def test_row_bytes(K):
     assert K.kvq_row_bytes(K.KVQ_INT2_TOKEN_HEAD, 128) == 36
     assert K.kvq_row_bytes(K.KVQ_INT8_CHANNEL, 128) == 128
     assert K.kvq_row_bytes(K.KVQ_INT4_STEGO, 128) == 68   # same row as INT4: the pad holds the fp32 scale
+    assert K.kvq_row_bytes(K.KVQ_INT8_TOKEN_HEAD, 128) == 132   # code bytes + fp32 scale
+    assert K.kvq_row_bytes(K.KVQ_FP8_TOKEN_HEAD, 64) == 68
     assert K.kvq_row_bytes(K.KVQ_INT4_TOKEN_HEAD, 80) == 0
 
 

@@ -45,7 +45,8 @@ def test_decode_qwen_int8_headwise_reduced():
     _run(gen.qwen_int8_headwise(0, batch=2, context=3000, window=700, sink=4))
 
 
-@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8, gen.MODE_INT4_STEGO])
+@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8, gen.MODE_INT4_STEGO,
+                                  gen.MODE_INT8_TOKEN_HEAD, gen.MODE_FP8_TOKEN_HEAD])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("group", [1, 2, 4, 5, 8])
 def test_decode_modes_dims_groups(mode, D, group):

@@ -29,7 +29,8 @@ def test_prefill_reduced_chunked_append():
     _run(gen.prefill_int4(0, prefixes=(0, 100, 700, 1500), chunk=130, num_blocks=1000))
 
 
-@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8, gen.MODE_INT4_STEGO])
+@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8, gen.MODE_INT4_STEGO,
+                                  gen.MODE_INT8_TOKEN_HEAD, gen.MODE_FP8_TOKEN_HEAD])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("group", [1, 4, 5])
 def test_prefill_modes_dims_groups(mode, D, group):

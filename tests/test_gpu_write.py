@@ -10,7 +10,8 @@ from harness import assert_pools_equal, build_case, write_step
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8, gen.MODE_INT4_STEGO])
+@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8, gen.MODE_INT4_STEGO,
+                                  gen.MODE_INT8_TOKEN_HEAD, gen.MODE_FP8_TOKEN_HEAD])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("bs", [16, 32, 64])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -22,7 +23,8 @@ def test_write_bit_exact(mode, D, bs, dtype):
     assert_pools_equal(c)
 
 
-@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8, gen.MODE_INT4_STEGO])
+@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8, gen.MODE_INT4_STEGO,
+                                  gen.MODE_INT8_TOKEN_HEAD, gen.MODE_FP8_TOKEN_HEAD])
 def test_write_headwise_with_sentinels(mode):
     wl = gen.custom(mode, 10, 2, 128, 16, "bf16", seq_lens=[300, 210], n_new=[300, 210], headwise=True,
                     window=[0, 64], sink=4, evict_outside_window=True, seed=11)
