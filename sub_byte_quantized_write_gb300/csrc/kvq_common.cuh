@@ -28,6 +28,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2_bits(uint32_t pair) {
   return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
+// Four E4M3 bytes with the NaN pattern S.1111.111 replaced by S.1111.110.
+// The write path never stores it, but stale bytes of masked rows may, and a
+// NaN times a zero weight still poisons a tensor-core sum.  Per byte, the low
+// 7 bits plus one carry into bit 7 only when they are all ones.
+__device__ __forceinline__ uint32_t e4m3x4_no_nan(uint32_t w) {
+  return w ^ ((((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) >> 7);
+}
+
 __device__ __forceinline__ void flag_error(int32_t* dev_error, int bit) {
   if (dev_error) atomicOr(dev_error, bit);
 }

@@ -890,6 +890,17 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
               vh[hp][e] = load_range<MODE, D>(vr, 0, 8 + gq);
             }
           }
+        if constexpr (MODE == MODE_F8T) {
+          if (!full) {  // warp-uniform; masked rows may hold stale NaN codes
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                vl[hp][e] = make_uint2(e4m3x4_no_nan(vl[hp][e].x), e4m3x4_no_nan(vl[hp][e].y));
+                vh[hp][e] = make_uint2(e4m3x4_no_nan(vh[hp][e].x), e4m3x4_no_nan(vh[hp][e].y));
+              }
+          }
+        }
         Unroll<C::MT, MODE>::run([&](auto mt_c) {
           constexpr int mt = decltype(mt_c)::value;
           const uint32_t a[4] = {vpair<MODE, mt>(vl[0][0], vl[0][1]), vpair<MODE, mt>(vh[0][0], vh[0][1]),

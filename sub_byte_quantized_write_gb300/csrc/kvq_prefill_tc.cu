@@ -163,7 +163,8 @@ __device__ __forceinline__ uint32_t codes2(const uint8_t* raw_row, int d) {
     const uint32_t x = b | (b << 16);
     return hsub2_bits(lop3_and_or(x, 0x000C0003u, 0x5C006400u), 0x5C086402u);
   } else if constexpr (MODE == MODE_F8T) {
-    return e4m3x2_to_half2_bits(*reinterpret_cast<const uint16_t*>(raw_row + d));
+    // V rows of masked keys may hold stale NaN codes (weight 0 times NaN is NaN)
+    return e4m3x2_to_half2_bits(e4m3x4_no_nan(*reinterpret_cast<const uint16_t*>(raw_row + d)));
   } else {
     const uint32_t w = *reinterpret_cast<const uint16_t*>(raw_row + d);
     const uint32_t x = prmt(w, 0u, 0 | (4 << 4) | (1 << 8) | (4 << 12));
