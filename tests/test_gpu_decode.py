@@ -245,3 +245,11 @@ def test_decode_full_size_qwen_int8_headwise_sampled():
     scales from the first write, head-wise tables with -1 outside the sink
     and window of heads 4-7."""
     _full_size_sampled(gen.qwen_int8_headwise(0), [0, 19])
+
+
+@pytest.mark.parametrize("mode", [gen.MODE_INT4_STEGO, gen.MODE_INT8_TOKEN_HEAD, gen.MODE_FP8_TOKEN_HEAD])
+def test_decode_full_size_llama_other_rows_sampled(mode):
+    """The Llama-like decode layer at full size (64 sequences, contexts up to
+    8192, 200k-block pool) in the other row formats: INT4 with the zero point
+    in the scale, INT8 and FP8 with one scale per token-head."""
+    _full_size_sampled(gen.llama_int4(0, mode=mode), [0, 33, 63])
