@@ -86,6 +86,8 @@ def lib():
             L.orc_attention.argtypes = [ctypes.POINTER(OrcCache), ctypes.POINTER(OrcPaging), P, I, I,
                                         P, I, F, P, I, P, I]
             L.orc_attention.restype = I
+            L.orc_gather.argtypes = [ctypes.POINTER(OrcCache), ctypes.POINTER(OrcPaging), P, I, P, P]
+            L.orc_gather.restype = I
             L.orc_rounding_mode_is_nearest.argtypes, L.orc_rounding_mode_is_nearest.restype = [], I
             _lib = L
     return _lib
@@ -216,6 +218,18 @@ def write(cache: Cache, paging: Paging, k: np.ndarray, v: np.ndarray, cu_new: np
     cs, ps = cache.struct(), paging.struct()
     return lib().orc_write(ctypes.byref(cs), ctypes.byref(ps), _ptr(kk), _ptr(vv), dt, _ptr(cu),
                            int(kk.shape[0]))
+
+
+def gather(cache: Cache, paging: Paging, cu_tokens: np.ndarray):
+    """Dequantised K and V (double [num_tokens, Hkv, D]) of the positions the
+    cu map names, and the error bits."""
+    cu = np.ascontiguousarray(cu_tokens, dtype=np.int32)
+    n = int(cu[-1])
+    k = np.zeros((n, cache.num_kv_heads, cache.head_dim), dtype=np.float64)
+    v = np.zeros_like(k)
+    cs, ps = cache.struct(), paging.struct()
+    err = lib().orc_gather(ctypes.byref(cs), ctypes.byref(ps), _ptr(cu), n, _ptr(k), _ptr(v))
+    return k, v, err
 
 
 def attention(cache: Cache, paging: Paging, q: np.ndarray, scale: float, cu_q=None, rows=None,

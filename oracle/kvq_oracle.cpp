@@ -29,6 +29,11 @@
 //     head-wise [batch * kv_heads, block] table; PR2-only delta table and
 //     Correctness gates: a -1 entry is an evicted sliding-window block whose
 //     keys contribute nothing and whose page is never addressed; sink_size.
+//   * Gather and dequantise -- FastDeploy PR #5173 (the review notes a new
+//     custom op dynamic_quant_get_kv_from_cache) and the Ascend INT8 plugin,
+//     运行机制 (prefill gathers and dequantises the paged cache when needed):
+//     rows of given positions read back through the table, dequantised and
+//     mapped through the inverse RHT to dense K / V.
 //   * Attention -- the textbook definition: softmax(scale * q . k_j) weights
 //     over the visible dequantised keys, output sum_j P_j v_j, in double.
 //
@@ -543,6 +548,53 @@ int32_t orc_write(const OrcCache* c, const OrcPaging* pg, const void* k, const v
           else
             quant_row_token_head(mode, x.data(), D, c->signs, dst);
         }
+      }
+    }
+  }
+  return err;
+}
+
+// Gather and dequantise the K and V rows of `num_tokens` positions.  Sequence
+// b's tokens cu[b] .. cu[b+1]-1 are its positions seq_lens[b] - n_b ..
+// seq_lens[b] - 1 (the map of orc_write).  out: double [num_tokens][Hkv][D]
+// each; a -1 table entry gives a zero row; a row that cannot be located
+// (too many tokens for the sequence, a position past the table row, a block
+// id past the pool) gives a zero row and an ERR_* bit.
+int32_t orc_gather(const OrcCache* c, const OrcPaging* pg, const int32_t* cu, int32_t num_tokens, double* k_out,
+                   double* v_out) {
+  const int D = c->head_dim, Hkv = c->num_kv_heads, bs = c->block_size, mode = c->mode;
+  const int R = row_bytes(mode, D);
+  int32_t err = 0;
+  for (size_t i = 0; i < (size_t)num_tokens * Hkv * D; ++i) k_out[i] = v_out[i] = 0.0;
+  for (int b = 0; b < pg->batch; ++b) {
+    const int n = cu[b + 1] - cu[b];
+    const int L = pg->seq_lens[b];
+    if (n == 0) continue;
+    if (L < 0 || n > L) {
+      err |= ERR_SEQ_LEN;
+      continue;
+    }
+    for (int i = 0; i < n; ++i) {
+      const int t = cu[b] + i;
+      const int p = L - n + i;
+      for (int h = 0; h < Hkv; ++h) {
+        const int lb = p / bs;
+        if (lb >= pg->max_blocks) {
+          err |= ERR_TABLE_RANGE;
+          continue;
+        }
+        const int blk = pg->table[(size_t)table_row(pg, b, h, Hkv) * pg->max_blocks + lb];
+        if (blk < 0) continue;  // evicted: a zero row
+        if (blk >= c->num_blocks) {
+          err |= ERR_BLOCK_RANGE;
+          continue;
+        }
+        const size_t off = (((size_t)blk * Hkv + h) * bs + (p % bs)) * R;
+        const size_t o = ((size_t)t * Hkv + h) * D;
+        dequant_row(mode, c->k_pages + off, D, c->signs, c->ch_amax ? c->ch_amax + (size_t)h * D : nullptr,
+                    k_out + o);
+        dequant_row(mode, c->v_pages + off, D, c->signs,
+                    c->ch_amax ? c->ch_amax + ((size_t)Hkv + h) * D : nullptr, v_out + o);
       }
     }
   }

@@ -654,3 +654,70 @@ def test_rht_attention_matches_brute_force_dequant():
     # and the quantisation error of the keys is within the half-step bound
     err_k = np.abs(Kh - kk[-L:, h].astype(np.float64)).max()
     assert err_k < 2.0
+
+
+# ---------------------------------------------------------------------------
+# gather and dequantise (FastDeploy PR #5173, the dynamic_quant_get_kv_from_cache
+# op; Ascend INT8 plugin, 运行机制: prefill gathers and dequantises the pages)
+
+def _rotated_grid_rows(rng, n, D, mode, signs):
+    """Rows x whose RHT y = H (d * x) is a grid row of `mode`, built as x =
+    d * (H y) / D with every partial sum exact in fp32, so that the write's
+    fp32 butterfly recovers y exactly and the codes reproduce it."""
+    if mode == F8T:   # E4M3 values that are multiples of 2^-3, 448 present
+        e = np.array([oracle.e4m3_decode(i) for i in range(256)])
+        ok = np.flatnonzero((np.abs(e) >= 1.0) & np.isfinite(e))
+        y = e[rng.choice(ok, size=(n, D))]
+        y[:, 0] = 448.0
+    else:
+        y = _grid_values(rng, n, D, mode).astype(np.float64)
+    if signs is None:
+        return y.astype(np.float32)
+    H = sylvester(D).astype(np.float64)
+    return ((y @ H) * signs[None, :] / D).astype(np.float32)
+
+
+@pytest.mark.parametrize("mode", [INT4, INT2, STEGO, I8T, F8T])
+@pytest.mark.parametrize("rht", [False, True])
+def test_gather_round_trips_representable_rows_exactly(mode, rht):
+    """Written then gathered, rows the mode represents exactly come back
+    exactly, through scattered pages, a -1 entry (zero rows) and the write's
+    position map (the last n_b positions of each sequence)."""
+    rng = np.random.default_rng(61 + mode + 7 * rht)
+    D, bs, Hkv = 64, 16, 2
+    signs = np.where(rng.integers(0, 2, D) == 1, 1, -1).astype(np.int8) if rht else None
+    L = [40, 23]
+    c = oracle.Cache(mode, 9, Hkv, bs, D, signs, fill=0x5A)
+    table = np.array([[6, -1, 3], [0, 8, -1]], np.int32)   # sequence 0's block 1 evicted
+    pg = oracle.Paging(table, False, np.array(L, np.int32))
+    x = [_rotated_grid_rows(rng, L[b] * Hkv, D, mode, signs).reshape(L[b], Hkv, D) for b in range(2)]
+    w = [_rotated_grid_rows(rng, L[b] * Hkv, D, mode, signs).reshape(L[b], Hkv, D) for b in range(2)]
+    assert oracle.write(c, pg, np.concatenate(x), np.concatenate(w), np.array([0, 40, 63], np.int32)) == 0
+    # the last 30 positions of sequence 0 and all 23 of sequence 1
+    k, v, err = oracle.gather(c, pg, np.array([0, 30, 53], np.int32))
+    assert err == 0
+    for b, (lo, t0) in enumerate(((10, 0), (0, 30))):
+        n = L[b] - lo
+        for i in range(n):
+            p = lo + i
+            want_k = np.zeros((Hkv, D)) if (b == 0 and 16 <= p < 32) else x[b][p].astype(np.float64)
+            want_v = np.zeros((Hkv, D)) if (b == 0 and 16 <= p < 32) else w[b][p].astype(np.float64)
+            assert np.array_equal(k[t0 + i], want_k), (b, p)
+            assert np.array_equal(v[t0 + i], want_v), (b, p)
+
+
+def test_gather_int8_channel_rows_and_errors():
+    D, T = 64, 255
+    s = 2.0 ** (np.arange(D) % 7 - 3)
+    j = np.arange(-127, 128)
+    x = (j[:, None] * s[None, :]).astype(np.float32)[:, None, :]
+    c, pg = _single_seq_paging(16, 16, T, INT8, D)
+    assert oracle.write(c, pg, x, -x, np.array([0, T], np.int32)) == 0
+    k, v, err = oracle.gather(c, pg, np.array([0, T], np.int32))
+    assert err == 0 and np.array_equal(k, x.astype(np.float64)) and np.array_equal(v, -x.astype(np.float64))
+    # more tokens than the sequence holds, and a position past the table row
+    _, _, err = oracle.gather(c, oracle.Paging(pg.table, False, np.array([3], np.int32)), np.array([0, 4], np.int32))
+    assert err == 4
+    k, _, err = oracle.gather(c, oracle.Paging(pg.table, False, np.array([T + 16], np.int32)),
+                              np.array([0, T + 16], np.int32))
+    assert err == 2 and np.all(k[T:] == 0)
