@@ -191,6 +191,10 @@ WORKLOADS = {
                                                 num_blocks=a.pool_blocks or 200000),
                      "INT4 chunked-prefill tokens/s (causal attention over the paged cache, % of tensor peak)",
                      "prefill"),
+    "gather_int4": (lambda a: gen.prefill_int4(seed=0, prefixes=tuple(a.prefill_prefixes), chunk=a.prefill_chunk,
+                                               num_blocks=a.pool_blocks or 200000),
+                    "INT4 gather-and-dequantise tokens/s (every cached position of the chunked-prefill layer "
+                    "back to dense bf16 K/V, % of GB300 HBM peak)", "gather"),
 }
 
 
@@ -206,11 +210,16 @@ def algorithmic_units(wl: gen.Workload) -> dict:
     """Decode: bytes the call must move at minimum (every visible packed K and
     V row once, the table entries of the visible pages per kv head, q in, out
     out).  Prefill: tensor FLOPs of causal attention, 4 D per visible (query,
-    key) pair per q head.  Write: bf16 K/V in, packed rows out."""
+    key) pair per q head.  Gather: every cached row read once (K and V), its
+    page-table entry once per page and kv head, bf16 K/V out.  Write: bf16
+    K/V in, packed rows out."""
     R = row_bytes(wl.mode, wl.head_dim)
     Hkv, bs, D, G = wl.num_kv_heads, wl.block_size, wl.head_dim, wl.group
     n_new = int(wl.n_new.sum())
     write = n_new * Hkv * 2 * (D * 2 + R)
+    cached = int(wl.seq_lens.sum())
+    gather_pages = sum(int((L + bs - 1) // bs) for L in wl.seq_lens) * Hkv
+    gather = {"gather": cached * Hkv * 2 * (R + 2 * D) + gather_pages * 4 + (wl.batch + 1) * 4 + wl.batch * 4}
     if wl.step == "decode":
         rows = pages = 0
         for b in range(wl.batch):
@@ -230,7 +239,7 @@ def algorithmic_units(wl: gen.Workload) -> dict:
                 pairs += n * (L - n) + n * (n + 1) // 2
             else:
                 pairs += sum(visible_keys(wl, b, h, p) for p in range(L - n, L))
-    return {"prefill_flops": 4 * D * pairs * G, "write": write}
+    return {"prefill_flops": 4 * D * pairs * G, "write": write, **gather}
 
 
 def setup_gpu(wl, device, want_splits=0):
@@ -273,6 +282,9 @@ def setup_gpu(wl, device, want_splits=0):
     }
     pag = paging(step["seq_lens"])
     step["out"] = torch.empty(tuple(step["q"].shape), dtype=torch.float32, device=device)
+    # gather: every cached position of every sequence back to dense bf16 K / V
+    step["cu_all"] = torch.from_numpy(wl.cu(wl.seq_lens)).to(device)
+    step["n_all"] = int(wl.seq_lens.sum())
     step["splits"] = 0
     if wl.step == "decode":
         nbytes, splits = K.kvq_decode_workspace_size(cache, pag, wl.num_q_heads, want_splits)
@@ -297,8 +309,15 @@ def run_gpu(args, rank, world, local_rank):
     def write_call():
         K.kvq_write(cache, pag, st["k"], st["v"], st["cu"], stream=stream)
 
+    if kind == "gather":
+        st["gk"] = torch.empty((st["n_all"], wl.num_kv_heads, wl.head_dim), dtype=torch.bfloat16, device=device)
+        st["gv"] = torch.empty_like(st["gk"])
+        st["out"] = st["gk"]  # the step's result, read back by the end-to-end run (with gv)
+
     def attn_call():
-        if kind == "decode":
+        if kind == "gather":
+            K.kvq_gather(cache, pag, st["cu_all"], st["n_all"], k_out=st["gk"], v_out=st["gv"], stream=stream)
+        elif kind == "decode":
             K.kvq_decode_attn(cache, pag, st["q"], scale, out=st["out"], workspace=st["ws"],
                               num_splits=st["splits"], stream=stream)
         else:
@@ -360,7 +379,7 @@ def run_gpu(args, rank, world, local_rank):
     att_ms = [b.elapsed_time(c) for a, b, c in ev]
     wr_ms = [a.elapsed_time(b) for a, b, c in ev]
     ms = max_over_ranks(sum(step_ms) / len(step_ms), device)
-    tokens = wl.batch if kind == "decode" else int(wl.n_new.sum())
+    tokens = {"decode": wl.batch, "prefill": int(wl.n_new.sum()), "gather": st["n_all"]}[kind]
     value = whole_job_rate(tokens, ms, world)
 
     # end to end through the C ABI with host buffers: H2D of the step's
@@ -371,18 +390,22 @@ def run_gpu(args, rank, world, local_rank):
     hcu = st["cu"].cpu().pin_memory()
     hsl = st["seq_lens"].cpu().pin_memory()
     hout = torch.empty_like(st["out"], device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hq, hcu, hsl))
-    d2h = hout.numel() * hout.element_size()
+    hout_v = torch.empty_like(st["gv"], device="cpu").pin_memory() if kind == "gather" else None
+    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hcu, hsl) + ((hq,) if kind != "gather" else ()))
+    d2h = hout.numel() * hout.element_size() + (hout_v.numel() * hout_v.element_size() if kind == "gather" else 0)
 
     def e2e_step():
         # plain library calls (no graph), inputs from pinned host memory
         st["k"].copy_(hk, non_blocking=True)
         st["v"].copy_(hv, non_blocking=True)
-        st["q"].copy_(hq, non_blocking=True)
+        if kind != "gather":
+            st["q"].copy_(hq, non_blocking=True)
         st["cu"].copy_(hcu, non_blocking=True)
         st["seq_lens"].copy_(hsl, non_blocking=True)
         step()
         hout.copy_(st["out"], non_blocking=True)
+        if kind == "gather":
+            hout_v.copy_(st["gv"], non_blocking=True)
 
     e2e_ms = []
     with torch.cuda.stream(stream):
@@ -415,7 +438,18 @@ def run_gpu(args, rank, world, local_rank):
            "parallelism": "replicas only" if world > 1 else "single GPU"}
     if args.workload.startswith("llama_int4"):
         cfg["context"] = "uniform[1024,8192]"
-    if kind == "decode":
+    if kind == "gather":
+        achieved = units["gather"] / (att / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "gather_kernel (one kvq_gather call: every cached row, dequantised, "
+                                          "inverse RHT, bf16 out)",
+                "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind + " (copy bandwidth)",
+                "unit": "GB/s", "frac": round(achieved / hbm, 4), "algorithmic_bytes_per_launch": units["gather"],
+                "traffic": recorded_units("gather_%s.md" % args.workload, "dram_bytes_per_gather_call",
+                                          kernel_source_hash(("kvq_write.cu", "kvq_common.cuh", "kvq_internal.h")))}
+        extra = {"gather_ms": round(att, 5), "gathered_tokens_per_step": st["n_all"]}
+        launches = 2  # write + gather
+        dtype = "u4 codes -> fp32 dequantise + inverse RHT -> bf16"
+    elif kind == "decode":
         cfg["decode_workers"] = st["splits"]
         achieved = units["decode"] / (att / 1e3) / 1e9
         traffic = recorded_units("decode_stream_%s.md" % args.workload, "dram_bytes_per_decode_call",
@@ -454,7 +488,7 @@ def run_gpu(args, rank, world, local_rank):
         "metric": metric, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype,
-        "data": "synthetic (seeded; K/V ~ N(0,1)%s)" % (", 1% outlier channels x10" if args.workload.startswith("llama_int4") or args.workload == "prefill_int4" else ""),
+        "data": "synthetic (seeded; K/V ~ N(0,1)%s)" % (", 1% outlier channels x10" if args.workload.startswith("llama") or args.workload in ("prefill_int4", "gather_int4") else ""),
         "config": cfg, **extra, "write_ms": round(wr, 5),
         "roofline": roof,
         "write_roofline": write_roof,
@@ -492,17 +526,22 @@ def _oracle_step_setup(wl, sample_seqs):
     return oc, nk, nv, q
 
 
-def oracle_step(wl, oc, new_k, new_v, q, sample_seqs, threads, rows=None):
+def oracle_step(wl, oc, new_k, new_v, q, sample_seqs, threads, rows=None, kind=None):
     """One step of the oracle on the sampled sequences: write their new
     tokens, then attention (decode: their one query each; prefill: the
-    sampled query rows `rows` of the chunk)."""
+    sampled query rows `rows` of the chunk) or, for the gather workload, the
+    gather of their whole contexts."""
     import oracle
     counts = np.zeros(wl.batch, np.int32)
     counts[sample_seqs] = wl.n_new[sample_seqs]
     pag = _oracle_paging(wl, wl.seq_lens)
     oracle.write(oc, pag, new_k, new_v, wl.cu(counts))
     scale = 1.0 / math.sqrt(wl.head_dim)
-    if wl.step == "decode":
+    if kind == "gather":
+        counts = np.zeros(wl.batch, np.int32)
+        counts[sample_seqs] = wl.seq_lens[sample_seqs]
+        oracle.gather(oc, pag, wl.cu(counts))
+    elif wl.step == "decode":
         oracle.attention(oc, pag, q, scale, rows=np.asarray(sample_seqs, np.int32), threads=threads)
     else:
         oracle.attention(oc, pag, q, scale, cu_q=wl.cu(wl.n_new), rows=rows, threads=threads)
@@ -520,13 +559,17 @@ def _prefill_rows(wl, per_seq):
     return np.asarray(sorted(rows), np.int32)
 
 
-def cpu_baseline(wl, budget_s=15.0):
+def cpu_baseline(wl, budget_s=15.0, kind=None):
     """The CPU oracle, as it stands, on a bounded sample of the workload,
     repeated until ~budget_s of work.  Decode: whole steps (write one token +
     attend with every q head) of a subset of the sequences.  Prefill: the
     write of the whole chunk + attention of a few query rows per sequence."""
     threads = os.cpu_count() or 1
-    if wl.step == "decode":
+    if kind == "gather":
+        sample = [0, 1, 2]  # the three shorter contexts
+        rows = None
+        per_step = int(wl.seq_lens[sample].sum())
+    elif wl.step == "decode":
         sample = list(range(0, wl.batch, 4))
         rows = None
         per_step = len(sample)
@@ -538,12 +581,17 @@ def cpu_baseline(wl, budget_s=15.0):
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle_step(wl, oc, nk, nv, q, sample, threads, rows)
+        oracle_step(wl, oc, nk, nv, q, sample, threads, rows, kind)
         n += 1
         if time.perf_counter() - t0 >= budget_s or n >= 50:
             break
     dt = time.perf_counter() - t0
-    if wl.step == "decode":
+    if kind == "gather":
+        desc = ("%d steps of: write of the chunks of sequences %s + gather of their whole contexts (%d positions, "
+                "K and V, all %d kv heads; the oracle's gather is single-threaded), %.1f s"
+                % (n, sample, per_step, wl.num_kv_heads, dt))
+        threads = 1
+    elif wl.step == "decode":
         desc = ("%d decode steps of %d of the %d sequences (every 4th; write 1 token + attention over the cached "
                 "context, all %d q heads), %.1f s" % (n, len(sample), wl.batch, wl.num_q_heads, dt))
     else:
@@ -559,7 +607,14 @@ def run_reference(args):
     factory, metric, kind = WORKLOADS[args.workload]
     wl = factory(args)
     threads = os.cpu_count() or 1
-    if kind == "decode":
+    if kind == "gather":
+        sample = [0, 1, 2]
+        rows = None
+        per_step = int(wl.seq_lens[sample].sum())
+        desc = ("sequences %s per step: write of their chunks + gather of their whole contexts (%d positions, K and "
+                "V, all %d kv heads; single-threaded oracle)" % (sample, per_step, wl.num_kv_heads))
+        threads = 1
+    elif kind == "decode":
         sample = list(range(0, wl.batch, 16))
         rows = None
         per_step = len(sample)
@@ -573,11 +628,11 @@ def run_reference(args):
                 % (int(wl.n_new.sum()), wl.num_q_heads))
     oc, nk, nv, q = _oracle_step_setup(wl, sample)
     for _ in range(args.warmup):
-        oracle_step(wl, oc, nk, nv, q, sample, threads, rows)
+        oracle_step(wl, oc, nk, nv, q, sample, threads, rows, kind)
     ts = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_step(wl, oc, nk, nv, q, sample, threads, rows)
+        oracle_step(wl, oc, nk, nv, q, sample, threads, rows, kind)
         ts.append(time.perf_counter() - t0)
     ms = 1e3 * sum(ts) / len(ts)
     value = per_step / (ms / 1e3)
@@ -599,7 +654,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="llama_int4", choices=sorted(WORKLOADS),
                     help="llama_int4 (the headline decode workload), llama_int4_d64_bs64, llama_int4_stego, "
-                         "llama_int8_token_head, llama_fp8_token_head, ernie_int2, qwen_int8_headwise, prefill_int4")
+                         "llama_int8_token_head, llama_fp8_token_head, ernie_int2, qwen_int8_headwise, prefill_int4, "
+                         "gather_int4")
     ap.add_argument("--pool-blocks", type=int, default=0,
                     help="block pool size (0 = the workload's own; smaller pools only for profiling)")
     ap.add_argument("--prefill-prefixes", type=int, nargs="+", default=[0, 4096, 16384, 61440],
@@ -621,7 +677,7 @@ def main():
     result, wl = run_gpu(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            result["cpu_baseline"] = cpu_baseline(wl)
+            result["cpu_baseline"] = cpu_baseline(wl, kind=WORKLOADS[args.workload][2])
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -197,6 +197,27 @@ kvq_status kvq_write(const kvq_cache* cache, const kvq_paging* paging,
                      const int32_t* cu_new_tokens, int32_t num_tokens,
                      int32_t* dev_error, void* stream);
 
+/* kvq_gather -- read rows of given positions back from the pages as dense,
+ * dequantised values in the input domain (inverse RHT applied): the gather
+ * and dequantise step a prefill can run before dense attention ([FD-INT2]
+ * review: the custom op dynamic_quant_get_kv_from_cache; [ASCEND-INT8]
+ * 运行机制: chunked prefill gathers and dequantises the paged cache).
+ *
+ * cu_tokens    : int32 [batch + 1], the position map of kvq_write: sequence b's
+ *                tokens cu[b] .. cu[b+1]-1 are its positions seq_lens[b] - n_b
+ *                .. seq_lens[b] - 1 (n_b = seq_lens[b] gathers the whole sequence).
+ * k_out, v_out : [num_tokens][num_kv_heads][head_dim] of out_dtype (KVQ_F32 or
+ *                KVQ_BF16, round to nearest even), caller-allocated, 16-byte aligned.
+ * Per row (fp32): INT4 / INT2 y = u * s + m; zero-point-in-scale INT4 (u -
+ * zp) * s; INT8 channel q * (amax / 127); INT8 / FP8 token-head code * s;
+ * then, with RHT signs, x = signs * (H y) / D by the same butterfly.  A row
+ * whose table entry is -1 is written as zeros; rows that cannot be located
+ * are written as zeros and set *dev_error bits as in kvq_write.  Window
+ * fields of `paging` are ignored.  num_tokens == 0 is a no-op. */
+kvq_status kvq_gather(const kvq_cache* cache, const kvq_paging* paging, const int32_t* cu_tokens,
+                      int32_t num_tokens, void* k_out, void* v_out, int32_t out_dtype, int32_t* dev_error,
+                      void* stream);
+
 /* Workspace needed by kvq_decode_attn for `num_splits` (0 = the library's
  * choice).  Writes the byte count to *bytes (host) and the split count that
  * kvq_decode_attn will use to *splits_used (host, nullable). */

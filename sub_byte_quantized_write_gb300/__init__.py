@@ -6,7 +6,7 @@ contiguity, turned into raw pointers and handed to the C ABI declared in
 library's CUDA kernels; there is no fallback.  If ``libkvq.so`` has not been
 built, importing this package raises ImportError.
 
-Names mirror the C calls: ``kvq_write``, ``kvq_decode_attn``,
+Names mirror the C calls: ``kvq_write``, ``kvq_gather``, ``kvq_decode_attn``,
 ``kvq_decode_attn_noalloc``, ``kvq_prefill_attn``, ``kvq_decode_workspace_size``,
 ``kvq_row_bytes``.
 """
@@ -57,6 +57,8 @@ _lib.kvq_status_string.argtypes, _lib.kvq_status_string.restype = [_I], ctypes.c
 _lib.kvq_last_error.argtypes, _lib.kvq_last_error.restype = [], ctypes.c_char_p
 _lib.kvq_write.argtypes = [_CP, _PP, _P, _P, _I, _P, _I, _P, _P]
 _lib.kvq_write.restype = _I
+_lib.kvq_gather.argtypes = [_CP, _PP, _P, _I, _P, _P, _I, _P, _P]
+_lib.kvq_gather.restype = _I
 _lib.kvq_decode_workspace_size.argtypes = [_CP, _PP, _I, _I, ctypes.POINTER(ctypes.c_size_t),
                                            ctypes.POINTER(ctypes.c_int32)]
 _lib.kvq_decode_workspace_size.restype = _I
@@ -182,6 +184,26 @@ def kvq_write(cache: PagedCache, paging: Paging, k: torch.Tensor, v: torch.Tenso
     _check(_lib.kvq_write(ctypes.byref(cs), ctypes.byref(ps), _dev_ptr(k, name="k"), _dev_ptr(v, name="v"),
                           _qdtype(k), _dev_ptr(cu_new_tokens, torch.int32, "cu_new_tokens"), int(k.shape[0]),
                           _dev_ptr(dev_error, torch.int32, "dev_error"), _stream_ptr(stream)))
+
+
+def kvq_gather(cache: PagedCache, paging: Paging, cu_tokens: torch.Tensor, num_tokens: int,
+               out_dtype: torch.dtype = torch.float32, k_out: Optional[torch.Tensor] = None,
+               v_out: Optional[torch.Tensor] = None, dev_error: Optional[torch.Tensor] = None, stream=None):
+    """Dense dequantised (k, v) [num_tokens, num_kv_heads, head_dim] of the
+    positions cu_tokens names (kvq_write's position map); -1 rows are zeros."""
+    shape = (num_tokens, cache.num_kv_heads, cache.head_dim)
+    dev = cache.k_pages.device
+    if k_out is None:
+        k_out = torch.empty(shape, dtype=out_dtype, device=dev)
+    if v_out is None:
+        v_out = torch.empty(shape, dtype=out_dtype, device=dev)
+    if k_out.dtype != v_out.dtype:
+        raise ValueError("k_out and v_out must have the same dtype")
+    cs, ps = cache.struct(), paging.struct()
+    _check(_lib.kvq_gather(ctypes.byref(cs), ctypes.byref(ps), _dev_ptr(cu_tokens, torch.int32, "cu_tokens"),
+                           int(num_tokens), _dev_ptr(k_out, name="k_out"), _dev_ptr(v_out, name="v_out"),
+                           _qdtype(k_out), _dev_ptr(dev_error, torch.int32, "dev_error"), _stream_ptr(stream)))
+    return k_out, v_out
 
 
 def kvq_decode_workspace_size(cache: PagedCache, paging: Paging, num_q_heads: int, num_splits: int = 0):

@@ -219,6 +219,48 @@ kvq_status kvq_write(const kvq_cache* cache, const kvq_paging* paging, const voi
   return KVQ_OK;
 }
 
+kvq_status kvq_gather(const kvq_cache* cache, const kvq_paging* paging, const int32_t* cu_tokens,
+                      int32_t num_tokens, void* k_out, void* v_out, int32_t out_dtype, int32_t* dev_error,
+                      void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
+  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "num_tokens < 0");
+  if (num_tokens == 0 || paging->batch == 0) return KVQ_OK;
+  if (!k_out || !v_out || !cu_tokens) return fail(KVQ_ERR_INVALID_ARG, "k_out / v_out / cu_tokens is NULL");
+  if (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16)
+    return fail(KVQ_ERR_UNSUPPORTED, "out_dtype must be KVQ_F32 or KVQ_BF16");
+  if (!aligned(k_out, 16) || !aligned(v_out, 16)) return fail(KVQ_ERR_INVALID_ARG, "k_out / v_out must be 16-byte aligned");
+  if ((long long)num_tokens * cache->num_kv_heads * 2 / 8 + 1 > 0x7FFFFFFFLL)
+    return fail(KVQ_ERR_UNSUPPORTED, "too many tokens for one call");
+  kvq::WriteParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.k_pages = cache->k_pages;
+  P.v_pages = cache->v_pages;
+  P.num_blocks = cache->num_blocks;
+  P.num_kv_heads = cache->num_kv_heads;
+  P.block_size = cache->block_size;
+  P.head_dim = cache->head_dim;
+  P.mode = kernel_mode(cache->mode);
+  P.stego = cache->mode == KVQ_INT4_STEGO;
+  P.signs = cache->mode == KVQ_INT8_CHANNEL ? nullptr : cache->rht_signs;
+  P.ch_amax = cache->ch_amax;
+  P.headwise = paging->block_tables_headwise != nullptr;
+  P.table = P.headwise ? paging->block_tables_headwise : paging->block_tables;
+  P.max_blocks = paging->max_blocks;
+  P.batch = paging->batch;
+  P.seq_lens = paging->seq_lens;
+  P.cu_new = cu_tokens;
+  P.num_tokens = num_tokens;
+  P.dev_error = dev_error;
+  P.out_k = k_out;
+  P.out_v = v_out;
+  P.out_dtype = out_dtype;
+  cudaError_t e = kvq::launch_gather(P, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KVQ_OK;
+}
+
 kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_paging* paging, int32_t num_q_heads,
                                      int32_t num_splits, size_t* bytes, int32_t* splits_used) {
   kvq_status st = check_cache(cache);

@@ -24,6 +24,10 @@ struct WriteParams {
   const void* v;
   int dtype, num_tokens;
   int32_t* dev_error;
+  // gather: dense outputs [num_tokens][Hkv][D] of out_dtype (DT_F32 / DT_BF16)
+  void* out_k;
+  void* out_v;
+  int out_dtype;
 };
 
 // Shared by the decode and prefill kernels.
@@ -95,6 +99,7 @@ inline DecodeLayout decode_ws_layout(int batch, int num_kv_heads, int group, int
 int decode_ctas_per_sm(int mode, int head_dim, int group);
 
 cudaError_t launch_write(const WriteParams& P, cudaStream_t stream);
+cudaError_t launch_gather(const WriteParams& P, cudaStream_t stream);
 cudaError_t launch_decode(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const AttnParams& P, cudaStream_t stream);
 

@@ -1,4 +1,5 @@
-// kvq_write.cu -- write path: rotate, quantise, pack and scatter new K/V rows.
+// kvq_write.cu -- write path: rotate, quantise, pack and scatter new K/V rows;
+// and its inverse, gathering rows back from the pages as dense values.
 //
 // INT4 / INT2 per (token, kv_head): vLLM PR #40835 review summary ("INT4
 // per-token-head KV cache for the Triton backend"), 实现拆解 item 2 (the write
@@ -247,6 +248,106 @@ __global__ void __launch_bounds__(256) int8_quant_kernel(WriteParams P) {
   const uint32_t word = gather_word<EPL * 8>(bits, lane);
   constexpr int LPW = 32 / (EPL * 8);
   if (lane % LPW == 0) *reinterpret_cast<uint32_t*>(dst + 4 * (lane / LPW)) = word;
+}
+
+// ---------------------------------------------------------------------------
+// Gather and dequantise: FastDeploy PR #5173 "support dynamic int2
+// quantization cache kv" (its review lists the new custom op
+// dynamic_quant_get_kv_from_cache) and the Ascend INT8 plugin, 运行机制
+// (chunked prefill gathers and dequantises the paged cache).  One warp per
+// (token, kv head, K|V) row with the write's position map; the lane's D/32
+// codes become fp32 values, the warp maps the row back through the inverse
+// RHT d * (H y) / D, and the row is stored densely (fp32 or bf16).  A row the
+// table marks -1, or that cannot be located, is stored as zeros.
+template <int MODE, int D, bool STEGO>
+__global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
+  constexpr int EPL = D / 32;
+  constexpr int BITS = mode_bits(MODE);
+  constexpr int DATA = data_bytes(MODE, D);
+  constexpr int LB = EPL * BITS;  // bits per lane, a divisor of 32
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int kv = (int)(wid & 1);
+  const long long th = wid >> 1;
+  const int h = (int)(th % P.num_kv_heads);
+  const long long t = th / P.num_kv_heads;
+  if (t >= P.num_tokens) return;
+  const uint8_t* src = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h, lane);
+  float y[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) y[e] = 0.0f;
+  if (src != nullptr) {  // warp-uniform
+    const int bit0 = lane * LB;
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src) + (bit0 >> 5)) >> (bit0 & 31);
+    uint32_t pad = 0;
+    if constexpr (MODE != MODE_INT8) pad = __ldg(reinterpret_cast<const uint32_t*>(src + DATA));
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const uint32_t u = (w >> (e * BITS)) & ((1u << BITS) - 1u);
+      if constexpr (MODE == MODE_INT8) {
+        const int c = lane * EPL + e;
+        const float s = __fdiv_rn(__ldg(P.ch_amax + ((size_t)kv * P.num_kv_heads + h) * D + c), 127.0f);
+        y[e] = __fmul_rn((float)(int8_t)u, s);
+      } else if constexpr (MODE == MODE_I8T) {
+        y[e] = __fmul_rn((float)(int8_t)u, __uint_as_float(pad));
+      } else if constexpr (MODE == MODE_F8T) {
+        const float c = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)u, __NV_E4M3)));
+        y[e] = __fmul_rn(c, __uint_as_float(pad));
+      } else if constexpr (STEGO) {
+        y[e] = __fmul_rn((float)((int)u - (int)(pad & 15u)), __uint_as_float(pad & ~15u));
+      } else {
+        const float S = __half2float(__ushort_as_half((unsigned short)(pad & 0xFFFFu)));
+        const float M = __half2float(__ushort_as_half((unsigned short)(pad >> 16)));
+        y[e] = __fadd_rn(__fmul_rn((float)u, S), M);
+      }
+    }
+    if (MODE != MODE_INT8 && P.signs) {
+      wht_warp<EPL>(y, lane);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        y[e] = __fmul_rn(y[e], (__ldg(P.signs + lane * EPL + e) < 0 ? -1.0f : 1.0f) / (float)D);  // exact
+    }
+  }
+  const size_t o = ((size_t)t * P.num_kv_heads + h) * D + lane * EPL;
+  void* out = kv ? P.out_v : P.out_k;
+  if (P.out_dtype == DT_F32) {
+    float* p = reinterpret_cast<float*>(out) + o;
+    if constexpr (EPL == 4) *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
+    else *reinterpret_cast<float2*>(p) = make_float2(y[0], y[1]);
+  } else {
+    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(out) + o;
+    const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]);
+    if constexpr (EPL == 4) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(y[2], y[3]);
+      *reinterpret_cast<uint2*>(p) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    } else {
+      *reinterpret_cast<__nv_bfloat162*>(p) = a;
+    }
+  }
+}
+
+template <int MODE, bool STEGO>
+void launch_gather_m(const WriteParams& P, int blocks, cudaStream_t stream) {
+  if (P.head_dim == 128) gather_kernel<MODE, 128, STEGO><<<blocks, 256, 0, stream>>>(P);
+  else gather_kernel<MODE, 64, STEGO><<<blocks, 256, 0, stream>>>(P);
+}
+
+cudaError_t launch_gather(const WriteParams& P, cudaStream_t stream) {
+  const long long warps = (long long)P.num_tokens * P.num_kv_heads * 2;
+  const int blocks = (int)((warps + 7) / 8);
+  switch (P.mode) {
+    case MODE_INT4:
+      if (P.stego) launch_gather_m<MODE_INT4, true>(P, blocks, stream);
+      else launch_gather_m<MODE_INT4, false>(P, blocks, stream);
+      break;
+    case MODE_INT2: launch_gather_m<MODE_INT2, false>(P, blocks, stream); break;
+    case MODE_INT8: launch_gather_m<MODE_INT8, false>(P, blocks, stream); break;
+    case MODE_I8T: launch_gather_m<MODE_I8T, false>(P, blocks, stream); break;
+    case MODE_F8T: launch_gather_m<MODE_F8T, false>(P, blocks, stream); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_write(const WriteParams& P, cudaStream_t stream) {

@@ -33,7 +33,8 @@ def K():
 
 def test_header_declares_the_three_calls():
     names = _declared_functions()
-    for n in ("kvq_write", "kvq_decode_attn", "kvq_prefill_attn", "kvq_decode_workspace_size", "kvq_row_bytes"):
+    for n in ("kvq_write", "kvq_decode_attn", "kvq_prefill_attn", "kvq_gather", "kvq_decode_workspace_size",
+              "kvq_row_bytes"):
         assert n in names
 
 
@@ -94,3 +95,8 @@ def test_host_validation_statuses(K):
     assert L.kvq_decode_attn(bref(_cache(K)), bref(_paging(K)), 256, 1, 18, 0.1, 256, 256, 1 << 30, 0, None, None) == K.KVQ_ERR_UNSUPPORTED
     assert L.kvq_prefill_attn(bref(_cache(K)), bref(_paging(K)), 256, 1, 8, None, 4, 4, 0.1, 256, None, None) == K.KVQ_ERR_INVALID_ARG
     assert b"cu_q" in L.kvq_last_error()
+    # gather: NULL outputs, unsupported output type, misaligned output, empty call
+    assert L.kvq_gather(bref(_cache(K)), bref(_paging(K)), 256, 4, None, 512, 0, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_gather(bref(_cache(K)), bref(_paging(K)), 256, 4, 512, 512, 7, None, None) == K.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_gather(bref(_cache(K)), bref(_paging(K)), 256, 4, 520, 512, 0, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_gather(bref(_cache(K)), bref(_paging(K)), 256, 0, None, None, 0, None, None) == K.KVQ_OK
