@@ -254,11 +254,107 @@ __global__ void __launch_bounds__(256) int8_quant_kernel(WriteParams P) {
 // Gather and dequantise: FastDeploy PR #5173 "support dynamic int2
 // quantization cache kv" (its review lists the new custom op
 // dynamic_quant_get_kv_from_cache) and the Ascend INT8 plugin, 运行机制
-// (chunked prefill gathers and dequantises the paged cache).  One warp per
-// (token, kv head, K|V) row with the write's position map; the lane's D/32
-// codes become fp32 values, the warp maps the row back through the inverse
-// RHT d * (H y) / D, and the row is stored densely (fp32 or bf16).  A row the
-// table marks -1, or that cannot be located, is stored as zeros.
+// (chunked prefill gathers and dequantises the paged cache).  The write's
+// position map; each row's codes become fp32 values, the warp maps the row
+// back through the inverse RHT d * (H y) / D, and the row is stored densely
+// (fp32 or bf16).  A row the table marks -1, or that cannot be located, is
+// stored as zeros.
+//
+// One warp per (GATHER_TOKENS consecutive tokens, kv head): lanes 0..7 locate
+// one token each (binary search of cu, then the table), the warp then issues
+// the loads of all 2 x GATHER_TOKENS rows (K and V share the lookup) before
+// it converts and stores them, so each warp keeps 16 row loads in flight
+// instead of one dependent chain per row.
+constexpr int GATHER_TOKENS = 8;
+
+// Byte offset of (token t, kv head h)'s row in a pool, or -1 (evicted or
+// invalid; invalid rows set their error bit).
+__device__ __forceinline__ long long gather_row_offset(const WriteParams& P, int t, int h) {
+  if (t >= P.num_tokens) return -1;
+  int lo = 0, hi = P.batch - 1;  // the last sequence whose first token is <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(P.cu_new + mid) <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int b = lo;
+  const int cu_b = __ldg(P.cu_new + b), cu_b1 = __ldg(P.cu_new + b + 1);
+  if (t < cu_b || t >= cu_b1) return -1;  // outside every sequence
+  const int n = cu_b1 - cu_b, L = __ldg(P.seq_lens + b);
+  if (L < 0 || n > L) {
+    flag_error(P.dev_error, DEVERR_SEQ_LEN);
+    return -1;
+  }
+  const int p = L - n + (t - cu_b);
+  const int lb = p / P.block_size;
+  if (lb >= P.max_blocks) {
+    flag_error(P.dev_error, DEVERR_TABLE_RANGE);
+    return -1;
+  }
+  const int row = P.headwise ? b * P.num_kv_heads + h : b;
+  const int blk = __ldg(P.table + (size_t)row * P.max_blocks + lb);
+  if (blk < 0) return -1;
+  if (blk >= P.num_blocks) {
+    flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
+    return -1;
+  }
+  const int R = row_bytes_of(P.mode, P.head_dim);
+  return ((long long)((size_t)blk * P.num_kv_heads + h) * P.block_size + (p % P.block_size)) * R;
+}
+
+template <int MODE, int D, bool STEGO>
+__device__ __forceinline__ void gather_dequant(const WriteParams& P, uint32_t w, uint32_t pad, int kv, int h,
+                                               int lane, float (&y)[D / 32]) {
+  constexpr int EPL = D / 32;
+  constexpr int BITS = mode_bits(MODE);
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const uint32_t u = (w >> (e * BITS)) & ((1u << BITS) - 1u);
+    if constexpr (MODE == MODE_INT8) {
+      const int c = lane * EPL + e;
+      const float s = __fdiv_rn(__ldg(P.ch_amax + ((size_t)kv * P.num_kv_heads + h) * D + c), 127.0f);
+      y[e] = __fmul_rn((float)(int8_t)u, s);
+    } else if constexpr (MODE == MODE_I8T) {
+      y[e] = __fmul_rn((float)(int8_t)u, __uint_as_float(pad));
+    } else if constexpr (MODE == MODE_F8T) {
+      const float c = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)u, __NV_E4M3)));
+      y[e] = __fmul_rn(c, __uint_as_float(pad));
+    } else if constexpr (STEGO) {
+      y[e] = __fmul_rn((float)((int)u - (int)(pad & 15u)), __uint_as_float(pad & ~15u));
+    } else {
+      const float S = __half2float(__ushort_as_half((unsigned short)(pad & 0xFFFFu)));
+      const float M = __half2float(__ushort_as_half((unsigned short)(pad >> 16)));
+      y[e] = __fadd_rn(__fmul_rn((float)u, S), M);
+    }
+  }
+  if (MODE != MODE_INT8 && P.signs) {
+    wht_warp<EPL>(y, lane);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+      y[e] = __fmul_rn(y[e], (__ldg(P.signs + lane * EPL + e) < 0 ? -1.0f : 1.0f) / (float)D);  // exact
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void gather_store(void* out, int out_dtype, size_t o, const float (&y)[D / 32]) {
+  constexpr int EPL = D / 32;
+  if (out_dtype == DT_F32) {
+    float* p = reinterpret_cast<float*>(out) + o;
+    if constexpr (EPL == 4) *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
+    else *reinterpret_cast<float2*>(p) = make_float2(y[0], y[1]);
+  } else {
+    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(out) + o;
+    const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]);
+    if constexpr (EPL == 4) {
+      const __nv_bfloat162 c = __floats2bfloat162_rn(y[2], y[3]);
+      *reinterpret_cast<uint2*>(p) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&c));
+    } else {
+      *reinterpret_cast<__nv_bfloat162*>(p) = a;
+    }
+  }
+}
+
 template <int MODE, int D, bool STEGO>
 __global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
   constexpr int EPL = D / 32;
@@ -267,64 +363,49 @@ __global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
   constexpr int LB = EPL * BITS;  // bits per lane, a divisor of 32
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int kv = (int)(wid & 1);
-  const long long th = wid >> 1;
-  const int h = (int)(th % P.num_kv_heads);
-  const long long t = th / P.num_kv_heads;
-  if (t >= P.num_tokens) return;
-  const uint8_t* src = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h, lane);
-  float y[EPL];
+  const int h = (int)(wid % P.num_kv_heads);
+  const long long t0 = (wid / P.num_kv_heads) * GATHER_TOKENS;
+  if (t0 >= P.num_tokens) return;
+  // 1. lanes 0..7 locate one token each
+  long long my_off = -1;
+  if (lane < GATHER_TOKENS) my_off = gather_row_offset(P, (int)(t0 + lane), h);
+  long long off[GATHER_TOKENS];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) y[e] = 0.0f;
-  if (src != nullptr) {  // warp-uniform
-    const int bit0 = lane * LB;
-    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src) + (bit0 >> 5)) >> (bit0 & 31);
-    uint32_t pad = 0;
-    if constexpr (MODE != MODE_INT8) pad = __ldg(reinterpret_cast<const uint32_t*>(src + DATA));
+  for (int r = 0; r < GATHER_TOKENS; ++r) off[r] = __shfl_sync(0xffffffffu, my_off, r);
+  // 2. every row's loads in flight together: the lane's code word and the pad
+  const int word = (lane * LB) >> 5, shift = (lane * LB) & 31;
+  uint32_t w[2][GATHER_TOKENS], pad[2][GATHER_TOKENS];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      const uint32_t u = (w >> (e * BITS)) & ((1u << BITS) - 1u);
-      if constexpr (MODE == MODE_INT8) {
-        const int c = lane * EPL + e;
-        const float s = __fdiv_rn(__ldg(P.ch_amax + ((size_t)kv * P.num_kv_heads + h) * D + c), 127.0f);
-        y[e] = __fmul_rn((float)(int8_t)u, s);
-      } else if constexpr (MODE == MODE_I8T) {
-        y[e] = __fmul_rn((float)(int8_t)u, __uint_as_float(pad));
-      } else if constexpr (MODE == MODE_F8T) {
-        const float c = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)u, __NV_E4M3)));
-        y[e] = __fmul_rn(c, __uint_as_float(pad));
-      } else if constexpr (STEGO) {
-        y[e] = __fmul_rn((float)((int)u - (int)(pad & 15u)), __uint_as_float(pad & ~15u));
-      } else {
-        const float S = __half2float(__ushort_as_half((unsigned short)(pad & 0xFFFFu)));
-        const float M = __half2float(__ushort_as_half((unsigned short)(pad >> 16)));
-        y[e] = __fadd_rn(__fmul_rn((float)u, S), M);
+  for (int kv = 0; kv < 2; ++kv) {
+    const uint8_t* pool = kv ? P.v_pages : P.k_pages;
+#pragma unroll
+    for (int r = 0; r < GATHER_TOKENS; ++r) {
+      w[kv][r] = 0;
+      pad[kv][r] = 0;
+      if (off[r] >= 0) {
+        const uint8_t* src = pool + off[r];
+        w[kv][r] = __ldg(reinterpret_cast<const uint32_t*>(src) + word) >> shift;
+        if constexpr (MODE != MODE_INT8) pad[kv][r] = __ldg(reinterpret_cast<const uint32_t*>(src + DATA));
       }
     }
-    if (MODE != MODE_INT8 && P.signs) {
-      wht_warp<EPL>(y, lane);
+  }
+  // 3. dequantise, inverse RHT, store
 #pragma unroll
-      for (int e = 0; e < EPL; ++e)
-        y[e] = __fmul_rn(y[e], (__ldg(P.signs + lane * EPL + e) < 0 ? -1.0f : 1.0f) / (float)D);  // exact
+  for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+    for (int r = 0; r < GATHER_TOKENS; ++r) {
+      const long long t = t0 + r;
+      if (t < P.num_tokens) {  // warp-uniform
+        float y[EPL];
+        if (off[r] >= 0) {
+          gather_dequant<MODE, D, STEGO>(P, w[kv][r], pad[kv][r], kv, h, lane, y);
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) y[e] = 0.0f;
+        }
+        gather_store<D>(kv ? P.out_v : P.out_k, P.out_dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, y);
+      }
     }
-  }
-  const size_t o = ((size_t)t * P.num_kv_heads + h) * D + lane * EPL;
-  void* out = kv ? P.out_v : P.out_k;
-  if (P.out_dtype == DT_F32) {
-    float* p = reinterpret_cast<float*>(out) + o;
-    if constexpr (EPL == 4) *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
-    else *reinterpret_cast<float2*>(p) = make_float2(y[0], y[1]);
-  } else {
-    __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(out) + o;
-    const __nv_bfloat162 a = __floats2bfloat162_rn(y[0], y[1]);
-    if constexpr (EPL == 4) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(y[2], y[3]);
-      *reinterpret_cast<uint2*>(p) =
-          make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
-    } else {
-      *reinterpret_cast<__nv_bfloat162*>(p) = a;
-    }
-  }
 }
 
 template <int MODE, bool STEGO>
@@ -334,7 +415,7 @@ void launch_gather_m(const WriteParams& P, int blocks, cudaStream_t stream) {
 }
 
 cudaError_t launch_gather(const WriteParams& P, cudaStream_t stream) {
-  const long long warps = (long long)P.num_tokens * P.num_kv_heads * 2;
+  const long long warps = (long long)((P.num_tokens + GATHER_TOKENS - 1) / GATHER_TOKENS) * P.num_kv_heads;
   const int blocks = (int)((warps + 7) / 8);
   switch (P.mode) {
     case MODE_INT4:
