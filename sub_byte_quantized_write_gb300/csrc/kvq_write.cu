@@ -302,9 +302,10 @@ __device__ __forceinline__ long long gather_row_offset(const WriteParams& P, int
   return ((long long)((size_t)blk * P.num_kv_heads + h) * P.block_size + (p % P.block_size)) * R;
 }
 
+// tsign: the lane's d_i / D factors of the inverse RHT (0 = RHT off)
 template <int MODE, int D, bool STEGO>
 __device__ __forceinline__ void gather_dequant(const WriteParams& P, uint32_t w, uint32_t pad, int kv, int h,
-                                               int lane, float (&y)[D / 32]) {
+                                               int lane, const float (&tsign)[D / 32], float (&y)[D / 32]) {
   constexpr int EPL = D / 32;
   constexpr int BITS = mode_bits(MODE);
 #pragma unroll
@@ -330,8 +331,7 @@ __device__ __forceinline__ void gather_dequant(const WriteParams& P, uint32_t w,
   if (MODE != MODE_INT8 && P.signs) {
     wht_warp<EPL>(y, lane);
 #pragma unroll
-    for (int e = 0; e < EPL; ++e)
-      y[e] = __fmul_rn(y[e], (__ldg(P.signs + lane * EPL + e) < 0 ? -1.0f : 1.0f) / (float)D);  // exact
+    for (int e = 0; e < EPL; ++e) y[e] = __fmul_rn(y[e], tsign[e]);  // exact: +-1 / D
   }
 }
 
@@ -372,6 +372,10 @@ __global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
   long long off[GATHER_TOKENS];
 #pragma unroll
   for (int r = 0; r < GATHER_TOKENS; ++r) off[r] = __shfl_sync(0xffffffffu, my_off, r);
+  float tsign[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e)
+    tsign[e] = (P.signs && __ldg(P.signs + lane * EPL + e) < 0 ? -1.0f : 1.0f) / (float)D;
   // 2. every row's loads in flight together: the lane's code word and the pad
   const int word = (lane * LB) >> 5, shift = (lane * LB) & 31;
   uint32_t w[2][GATHER_TOKENS], pad[2][GATHER_TOKENS];
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
       if (t < P.num_tokens) {  // warp-uniform
         float y[EPL];
         if (off[r] >= 0) {
-          gather_dequant<MODE, D, STEGO>(P, w[kv][r], pad[kv][r], kv, h, lane, y);
+          gather_dequant<MODE, D, STEGO>(P, w[kv][r], pad[kv][r], kv, h, lane, tsign, y);
         } else {
 #pragma unroll
           for (int e = 0; e < EPL; ++e) y[e] = 0.0f;
