@@ -84,12 +84,14 @@ __device__ __forceinline__ void wht_warp(float (&x)[EPL], int lane) {
   }
 #pragma unroll
   for (int lm = 1; lm < 32; lm <<= 1) {
-    const bool upper = (lane & lm) != 0;
+    // lower lane holds x_j: x_j + x_{j+h}; upper lane holds x_{j+h}: x_j - x_{j+h}.
+    // Both as one fma(+-1, x, o): the product is exact, so the result is the
+    // correctly rounded sum or difference, bit for bit.
+    const float sg = (lane & lm) ? -1.0f : 1.0f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const float o = __shfl_xor_sync(0xffffffffu, x[i], lm);
-      // lower lane holds x_j: x_j + x_{j+h}; upper lane holds x_{j+h}: x_j - x_{j+h}
-      x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+      x[i] = __fmaf_rn(sg, x[i], o);
     }
   }
 }

@@ -335,10 +335,10 @@ __device__ __forceinline__ void gather_dequant(const WriteParams& P, uint32_t w,
   }
 }
 
-template <int D>
-__device__ __forceinline__ void gather_store(void* out, int out_dtype, size_t o, const float (&y)[D / 32]) {
+template <int D, bool BF16>
+__device__ __forceinline__ void gather_store(void* out, size_t o, const float (&y)[D / 32]) {
   constexpr int EPL = D / 32;
-  if (out_dtype == DT_F32) {
+  if constexpr (!BF16) {
     float* p = reinterpret_cast<float*>(out) + o;
     if constexpr (EPL == 4) *reinterpret_cast<float4*>(p) = make_float4(y[0], y[1], y[2], y[3]);
     else *reinterpret_cast<float2*>(p) = make_float2(y[0], y[1]);
@@ -353,6 +353,25 @@ __device__ __forceinline__ void gather_store(void* out, int out_dtype, size_t o,
       *reinterpret_cast<__nv_bfloat162*>(p) = a;
     }
   }
+}
+
+// Dequantise, map back and store the warp's 2 x GATHER_TOKENS rows.  Rows
+// without data arrive as code word 0 and pad 0, which every mode turns into
+// zeros (scale 0, or code 0 for INT8 per channel), so no branch is needed.
+template <int MODE, int D, bool STEGO, bool BF16>
+__device__ __forceinline__ void gather_rows(const WriteParams& P, const uint32_t (&w)[2][GATHER_TOKENS],
+                                            const uint32_t (&pad)[2][GATHER_TOKENS], long long t0, int h, int lane,
+                                            const float (&tsign)[D / 32]) {
+  constexpr int EPL = D / 32;
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+    for (int r = 0; r < GATHER_TOKENS; ++r) {
+      float y[EPL];
+      gather_dequant<MODE, D, STEGO>(P, w[kv][r], pad[kv][r], kv, h, lane, tsign, y);
+      const long long t = t0 + r;
+      if (t < P.num_tokens) gather_store<D, BF16>(kv ? P.out_v : P.out_k, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, y);
+    }
 }
 
 template <int MODE, int D, bool STEGO>
@@ -394,22 +413,8 @@ __global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
     }
   }
   // 3. dequantise, inverse RHT, store
-#pragma unroll
-  for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-    for (int r = 0; r < GATHER_TOKENS; ++r) {
-      const long long t = t0 + r;
-      if (t < P.num_tokens) {  // warp-uniform
-        float y[EPL];
-        if (off[r] >= 0) {
-          gather_dequant<MODE, D, STEGO>(P, w[kv][r], pad[kv][r], kv, h, lane, tsign, y);
-        } else {
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) y[e] = 0.0f;
-        }
-        gather_store<D>(kv ? P.out_v : P.out_k, P.out_dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, y);
-      }
-    }
+  if (P.out_dtype == DT_BF16) gather_rows<MODE, D, STEGO, true>(P, w, pad, t0, h, lane, tsign);
+  else gather_rows<MODE, D, STEGO, false>(P, w, pad, t0, h, lane, tsign);
 }
 
 template <int MODE, bool STEGO>
