@@ -12,6 +12,12 @@ the dominant kernel (decode attention, HBM-bound), the end-to-end number
 through the C ABI with host buffers, the clocks seen during the timed region,
 and the CPU oracle's throughput on a bounded sample of the same workload.
 
+Other workloads (`--workload`): the same decode layer at head_dim 64 /
+block_size 64, with zero-point-in-scale INT4 rows or with INT8 / FP8
+per-token-head rows; the ERNIE-like INT2 decode; the Qwen-like INT8 head-wise
+decode with sliding windows; the INT4 chunked prefill (tcgen05); and the
+gather-and-dequantise of the chunked-prefill layer's whole cache.
+
 `--impl reference` times the CPU oracle alone (the reference arm: a plain,
 slow program), on the same workload, metric and unit.
 """
@@ -426,7 +432,7 @@ def run_gpu(args, rank, world, local_rank):
     units = algorithmic_units(wl)
     att = sum(att_ms) / len(att_ms)
     hbm, tensor, peak_kind = peaks()
-    cfg = {"workload": wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
+    cfg = {"workload": ("gather_" + wl.name) if kind == "gather" else wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
            "mode": {0: "int4", 1: "int2", 2: "int8", 3: "int4_stego", 4: "int8_token_head",
                     5: "fp8_token_head"}[wl.mode], "headwise_table": bool(wl.headwise),
