@@ -88,6 +88,9 @@ def lib():
             L.orc_attention.restype = I
             L.orc_gather.argtypes = [ctypes.POINTER(OrcCache), ctypes.POINTER(OrcPaging), P, I, P, P]
             L.orc_gather.restype = I
+            L.orc_dense_attention.argtypes = [P, P, I, P, ctypes.POINTER(OrcPaging), I, I, P, I, I, P, I, F, P, I,
+                                              P, I]
+            L.orc_dense_attention.restype = I
             L.orc_rounding_mode_is_nearest.argtypes, L.orc_rounding_mode_is_nearest.restype = [], I
             _lib = L
     return _lib
@@ -246,4 +249,28 @@ def attention(cache: Cache, paging: Paging, q: np.ndarray, scale: float, cu_q=No
     cs, ps = cache.struct(), paging.struct()
     err = lib().orc_attention(ctypes.byref(cs), ctypes.byref(ps), _ptr(qq), dt, Hq, _ptr(cu), total_q,
                               float(scale), _ptr(sel), n_rows, _ptr(out), int(threads))
+    return out, err
+
+
+def dense_attention(k: np.ndarray, v: np.ndarray, cu_kv: np.ndarray, paging: Paging, q: np.ndarray, scale: float,
+                    cu_q: np.ndarray, rows=None, threads: Optional[int] = None):
+    """Attention over dense K / V [rows, Hkv, D] (fp32 values or bf16 bits):
+    sequence b's key j is row cu_kv[b] + j.  Returns (out double
+    [n_rows, Hq, D], error bits)."""
+    kk, kdt = _input(k)
+    vv, vdt = _input(v)
+    assert kdt == vdt
+    qq, dt = _input(q)
+    total_q, Hq, D = qq.shape
+    Hkv = kk.shape[1]
+    cu = np.ascontiguousarray(cu_kv, dtype=np.int32)
+    cq = np.ascontiguousarray(cu_q, dtype=np.int32)
+    sel = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    n_rows = total_q if sel is None else sel.shape[0]
+    out = np.zeros((n_rows, Hq, D), dtype=np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    ps = paging.struct()
+    err = lib().orc_dense_attention(_ptr(kk), _ptr(vv), kdt, _ptr(cu), ctypes.byref(ps), Hkv, D, _ptr(qq), dt, Hq,
+                                    _ptr(cq), total_q, float(scale), _ptr(sel), n_rows, _ptr(out), int(threads))
     return out, err

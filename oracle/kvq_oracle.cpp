@@ -601,26 +601,26 @@ int32_t orc_gather(const OrcCache* c, const OrcPaging* pg, const int32_t* cu, in
   return err;
 }
 
-// Attention for selected query rows.  Decode (cu_q == NULL): row i is
-// sequence i's query at seq_lens[i] - 1.  Prefill: row i in [cu_q[b],
-// cu_q[b+1]) is at seq_lens[b] - n_b + (i - cu_q[b]).  `rows` lists the query
-// rows to compute (NULL = all total_q); out is double [n_rows][Hq][D].
-int32_t orc_attention(const OrcCache* c, const OrcPaging* pg, const void* q, int32_t dtype, int32_t Hq,
-                      const int32_t* cu_q, int32_t total_q, float scale, const int32_t* rows,
-                      int32_t n_rows, double* out, int32_t threads) {
-  const int D = c->head_dim, Hkv = c->num_kv_heads, bs = c->block_size, mode = c->mode;
-  const int R = row_bytes(mode, D);
-  if (Hq % Hkv) return -1;
-  const int g = Hq / Hkv;
-  std::vector<int32_t> sel;
+// Keys and values one (sequence, kv head) can see, in the input domain.
+struct Deq {
+  int b = -1, h = -1, n = 0;
+  std::vector<double> K, V;
+  std::vector<char> ok;
+};
+
+// Sequence and position of every selected query row.  Decode (cu_q == NULL):
+// row i is sequence i's query at seq_lens[i] - 1.  Prefill: row i in
+// [cu_q[b], cu_q[b+1]) is at seq_lens[b] - n_b + (i - cu_q[b]).
+static void query_rows(const OrcPaging* pg, const int32_t* cu_q, int32_t total_q, const int32_t* rows,
+                       int32_t& n_rows, std::vector<int32_t>& sel, std::vector<int32_t>& seq,
+                       std::vector<int32_t>& pos) {
   if (rows) sel.assign(rows, rows + n_rows);
   else {
     for (int i = 0; i < total_q; ++i) sel.push_back(i);
     n_rows = total_q;
   }
-  // sequence and position of every selected row
-  std::vector<int32_t> seq(n_rows), pos(n_rows);
-  int32_t err = 0;
+  seq.assign(n_rows, 0);
+  pos.assign(n_rows, 0);
   for (int r = 0; r < n_rows; ++r) {
     const int i = sel[r];
     int b = 0, p = 0;
@@ -635,19 +635,82 @@ int32_t orc_attention(const OrcCache* c, const OrcPaging* pg, const void* q, int
     seq[r] = b;
     pos[r] = p;
   }
-  // Phase 1: dequantise the keys each needed (sequence, kv head) can see.
-  struct Deq {
-    int b = -1, h = -1, n = 0;
-    std::vector<double> K, V;
-    std::vector<char> ok;
+}
+
+// Softmax attention per (selected row, q head), in double, over the keys of
+// `deq` that the row's position sees (causal, window + sink).
+static void attention_rows(const OrcPaging* pg, const std::vector<Deq>& deq, const std::vector<int32_t>& sel,
+                           const std::vector<int32_t>& seq, const std::vector<int32_t>& pos, int32_t n_rows,
+                           const void* q, int32_t dtype, int32_t Hq, int Hkv, int D, float scale, double* out,
+                           int32_t threads) {
+  const int g = Hq / Hkv;
+  std::atomic<int> next(0);
+  const int n_items = n_rows * Hq;
+  auto attn_worker = [&]() {
+    std::vector<double> z, qd(D);
+    for (;;) {
+      int w = next.fetch_add(1);
+      if (w >= n_items) break;
+      const int r = w / Hq, hq = w % Hq, h = hq / g;
+      const int b = seq[r], p = pos[r];
+      const Deq& dq = deq[(size_t)b * Hkv + h];
+      double* o = out + ((size_t)r * Hq + hq) * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      for (int d = 0; d < D; ++d) qd[d] = (double)widen(q, dtype, ((size_t)sel[r] * Hq + hq) * D + d);
+      const int W = pg->window ? pg->window[h] : 0;
+      z.assign(dq.n, -INFINITY);
+      double zmax = -INFINITY;
+      for (int j = 0; j < dq.n && j <= p; ++j) {
+        if (!dq.ok[j]) continue;
+        if (W > 0 && !(j < pg->sink || j > p - W)) continue;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += qd[d] * dq.K[(size_t)j * D + d];
+        z[j] = (double)scale * dot;
+        if (z[j] > zmax) zmax = z[j];
+      }
+      if (zmax == -INFINITY) continue;  // no visible key: output 0
+      double l = 0.0;
+      for (int j = 0; j < dq.n && j <= p; ++j) {
+        if (z[j] == -INFINITY) continue;
+        const double e = std::exp(z[j] - zmax);
+        l += e;
+        for (int d = 0; d < D; ++d) o[d] += e * dq.V[(size_t)j * D + d];
+      }
+      for (int d = 0; d < D; ++d) o[d] /= l;
+    }
   };
-  std::vector<Deq> deq((size_t)pg->batch * Hkv);
-  std::vector<int> need((size_t)pg->batch * Hkv, -1);  // max position needed
+  if (threads < 1) threads = 1;
+  std::vector<std::thread> pool;
+  for (int t = 0; t < threads; ++t) pool.emplace_back(attn_worker);
+  for (auto& th : pool) th.join();
+}
+
+// Largest position each (sequence, kv head) must provide keys up to.
+static std::vector<int> needed_keys(const OrcPaging* pg, int Hkv, const std::vector<int32_t>& seq,
+                                    const std::vector<int32_t>& pos, int32_t n_rows) {
+  std::vector<int> need((size_t)pg->batch * Hkv, -1);
   for (int r = 0; r < n_rows; ++r)
     for (int h = 0; h < Hkv; ++h) {
       int& m = need[(size_t)seq[r] * Hkv + h];
       if (pos[r] > m) m = pos[r];
     }
+  return need;
+}
+
+// Attention for selected query rows over the paged cache.  `rows` lists the
+// query rows to compute (NULL = all total_q); out is double [n_rows][Hq][D].
+int32_t orc_attention(const OrcCache* c, const OrcPaging* pg, const void* q, int32_t dtype, int32_t Hq,
+                      const int32_t* cu_q, int32_t total_q, float scale, const int32_t* rows,
+                      int32_t n_rows, double* out, int32_t threads) {
+  const int D = c->head_dim, Hkv = c->num_kv_heads, bs = c->block_size, mode = c->mode;
+  const int R = row_bytes(mode, D);
+  if (Hq % Hkv) return -1;
+  std::vector<int32_t> sel, seq, pos;
+  query_rows(pg, cu_q, total_q, rows, n_rows, sel, seq, pos);
+  int32_t err = 0;
+  // Phase 1: dequantise the keys each needed (sequence, kv head) can see.
+  std::vector<Deq> deq((size_t)pg->batch * Hkv);
+  const std::vector<int> need = needed_keys(pg, Hkv, seq, pos, n_rows);
   std::vector<int> items;
   for (size_t it = 0; it < need.size(); ++it)
     if (need[it] >= 0) items.push_back((int)it);
@@ -698,47 +761,48 @@ int32_t orc_attention(const OrcCache* c, const OrcPaging* pg, const void* q, int
     for (auto& th : pool) th.join();
   }
   // Phase 2: softmax attention per (row, q head), in double.
-  next = 0;
-  const int n_items = n_rows * Hq;
-  auto attn_worker = [&]() {
-    std::vector<double> z, qd(D);
-    for (;;) {
-      int w = next.fetch_add(1);
-      if (w >= n_items) break;
-      const int r = w / Hq, hq = w % Hq, h = hq / g;
-      const int b = seq[r], p = pos[r];
-      const Deq& dq = deq[(size_t)b * Hkv + h];
-      double* o = out + ((size_t)r * Hq + hq) * D;
-      for (int d = 0; d < D; ++d) o[d] = 0.0;
-      for (int d = 0; d < D; ++d) qd[d] = (double)widen(q, dtype, ((size_t)sel[r] * Hq + hq) * D + d);
-      const int W = pg->window ? pg->window[h] : 0;
-      z.assign(dq.n, -INFINITY);
-      double zmax = -INFINITY;
-      for (int j = 0; j < dq.n && j <= p; ++j) {
-        if (!dq.ok[j]) continue;
-        if (W > 0 && !(j < pg->sink || j > p - W)) continue;
-        double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += qd[d] * dq.K[(size_t)j * D + d];
-        z[j] = (double)scale * dot;
-        if (z[j] > zmax) zmax = z[j];
-      }
-      if (zmax == -INFINITY) continue;  // no visible key: output 0
-      double l = 0.0;
-      for (int j = 0; j < dq.n && j <= p; ++j) {
-        if (z[j] == -INFINITY) continue;
-        const double e = std::exp(z[j] - zmax);
-        l += e;
-        for (int d = 0; d < D; ++d) o[d] += e * dq.V[(size_t)j * D + d];
-      }
-      for (int d = 0; d < D; ++d) o[d] /= l;
-    }
-  };
-  {
-    std::vector<std::thread> pool;
-    for (int t = 0; t < threads; ++t) pool.emplace_back(attn_worker);
-    for (auto& th : pool) th.join();
-  }
+  attention_rows(pg, deq, sel, seq, pos, n_rows, q, dtype, Hq, Hkv, D, scale, out, threads);
   return err | aerr.load();
+}
+
+// Attention over dense K / V rows: the dense prefill that follows a gather
+// (FastDeploy PR #5173, the dynamic_quant_get_kv_from_cache op; Ascend INT8
+// plugin, 运行机制: prefill gathers and dequantises, then attends).  Sequence
+// b's key j is row cu_kv[b] + j of k, v [rows][Hkv][D] (fp32 values or bf16
+// bits, `kv_dtype`); the table fields of `pg` are not used; queries and
+// visibility as in orc_attention.
+int32_t orc_dense_attention(const void* k, const void* v, int32_t kv_dtype, const int32_t* cu_kv,
+                            const OrcPaging* pg, int32_t Hkv, int32_t D, const void* q, int32_t dtype, int32_t Hq,
+                            const int32_t* cu_q, int32_t total_q, float scale, const int32_t* rows, int32_t n_rows,
+                            double* out, int32_t threads) {
+  if (Hq % Hkv) return -1;
+  std::vector<int32_t> sel, seq, pos;
+  query_rows(pg, cu_q, total_q, rows, n_rows, sel, seq, pos);
+  std::vector<Deq> deq((size_t)pg->batch * Hkv);
+  const std::vector<int> need = needed_keys(pg, Hkv, seq, pos, n_rows);
+  int32_t err = 0;
+  for (int b = 0; b < pg->batch; ++b)
+    if (cu_kv[b + 1] - cu_kv[b] != pg->seq_lens[b]) err |= ERR_SEQ_LEN;
+  if (err) return err;
+  for (size_t it = 0; it < need.size(); ++it) {
+    if (need[it] < 0) continue;
+    const int b = (int)it / Hkv, h = (int)it % Hkv;
+    Deq& dq = deq[it];
+    dq.b = b;
+    dq.h = h;
+    dq.n = std::max(0, std::min(need[it] + 1, pg->seq_lens[b]));
+    dq.K.assign((size_t)dq.n * D, 0.0);
+    dq.V.assign((size_t)dq.n * D, 0.0);
+    dq.ok.assign(dq.n, 1);
+    for (int j = 0; j < dq.n; ++j)
+      for (int d = 0; d < D; ++d) {
+        const size_t idx = ((size_t)(cu_kv[b] + j) * Hkv + h) * D + d;
+        dq.K[(size_t)j * D + d] = widen(k, kv_dtype, idx);
+        dq.V[(size_t)j * D + d] = widen(v, kv_dtype, idx);
+      }
+  }
+  attention_rows(pg, deq, sel, seq, pos, n_rows, q, dtype, Hq, Hkv, D, scale, out, threads);
+  return 0;
 }
 
 int32_t orc_rounding_mode_is_nearest(void) { return std::fegetround() == FE_TONEAREST; }

@@ -721,3 +721,68 @@ def test_gather_int8_channel_rows_and_errors():
     k, _, err = oracle.gather(c, oracle.Paging(pg.table, False, np.array([T + 16], np.int32)),
                               np.array([0, T + 16], np.int32))
     assert err == 2 and np.all(k[T:] == 0)
+
+
+# ---------------------------------------------------------------------------
+# dense attention after a gather (the gather-then-dense-prefill strategy)
+
+def _dense_paging(seq_lens, window=None, sink=0):
+    B = len(seq_lens)
+    return oracle.Paging(np.zeros((B, 1), np.int32), False, np.asarray(seq_lens, np.int32), window, sink)
+
+
+@pytest.mark.parametrize("W,sink", [(0, 0), (9, 2)])
+def test_dense_attention_brute_force(W, sink):
+    """Causal prefill rows over dense K / V against a numpy brute force."""
+    rng = np.random.default_rng(81 + W)
+    D, Hkv, Hq = 64, 2, 4
+    L, n = np.array([30, 12], np.int32), np.array([7, 12], np.int32)
+    cu_kv = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    cu_q = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    k = rng.standard_normal((int(L.sum()), Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((int(L.sum()), Hkv, D)).astype(np.float32)
+    q = rng.standard_normal((int(n.sum()), Hq, D)).astype(np.float32)
+    win = np.array([0, W], np.int32) if W else None
+    scale = 1.0 / math.sqrt(D)
+    out, err = oracle.dense_attention(k, v, cu_kv, _dense_paging(L, win, sink), q, scale, cu_q, threads=2)
+    assert err == 0
+    for b in range(2):
+        for i in range(n[b]):
+            p = L[b] - n[b] + i
+            for hq in range(Hq):
+                h = hq // (Hq // Hkv)
+                j = np.arange(L[b])
+                mask = j <= p
+                if win is not None and win[h] > 0:
+                    mask &= (j < sink) | (j > p - win[h])
+                want = _softmax_ref(q[cu_q[b] + i, hq].astype(np.float64), k[cu_kv[b]:cu_kv[b + 1], h].astype(np.float64),
+                                    v[cu_kv[b]:cu_kv[b + 1], h].astype(np.float64), scale, mask)
+                np.testing.assert_allclose(out[cu_q[b] + i, hq], want, rtol=1e-12, atol=1e-12)
+
+
+def test_dense_attention_equals_paged_attention_on_exact_rows():
+    """Rows INT8 token-head rows hold exactly (RHT off), given once as a paged
+    cache and once as dense bf16 rows: both attentions agree."""
+    rng = np.random.default_rng(83)
+    D, bs, Hkv, Hq = 64, 16, 2, 4
+    L = [40, 23]
+    c = oracle.Cache(I8T, 9, Hkv, bs, D)
+    table = np.array([[6, 2, 3], [0, 8, 5]], np.int32)
+    pg = oracle.Paging(table, False, np.array(L, np.int32))
+    x = [_grid_values(rng, L[b] * Hkv, D, I8T).reshape(L[b], Hkv, D) for b in range(2)]
+    w = [_grid_values(rng, L[b] * Hkv, D, I8T).reshape(L[b], Hkv, D) for b in range(2)]
+    kk, vv = np.concatenate(x), np.concatenate(w)
+    assert oracle.write(c, pg, kk, vv, np.array([0, 40, 63], np.int32)) == 0
+    q = rng.standard_normal((12, Hq, D)).astype(np.float32)
+    cu_q = np.array([0, 5, 12], np.int32)
+    scale = 0.125
+    paged, err = oracle.attention(c, pg, q, scale, cu_q=cu_q, threads=2)
+    assert err == 0
+    kb, vb = gen.f32_to_bf16_bits(kk), gen.f32_to_bf16_bits(vv)   # exact: 8 significant bits suffice
+    dense, err = oracle.dense_attention(kb, vb, np.array([0, 40, 63], np.int32), _dense_paging(L), q, scale, cu_q,
+                                        threads=2)
+    assert err == 0
+    np.testing.assert_allclose(dense, paged, rtol=1e-12, atol=1e-12)
+    # a cu_kv that disagrees with seq_lens is refused
+    _, err = oracle.dense_attention(kb, vb, np.array([0, 39, 63], np.int32), _dense_paging(L), q, scale, cu_q)
+    assert err == 4
