@@ -6,7 +6,7 @@ contiguity, turned into raw pointers and handed to the C ABI declared in
 library's CUDA kernels; there is no fallback.  If ``libkvq.so`` has not been
 built, importing this package raises ImportError.
 
-Names mirror the C calls: ``kvq_write``, ``kvq_gather``, ``kvq_decode_attn``,
+Names mirror the C calls: ``kvq_write``, ``kvq_gather``, ``kvq_prefill_dense_attn``, ``kvq_decode_attn``,
 ``kvq_decode_attn_noalloc``, ``kvq_prefill_attn``, ``kvq_decode_workspace_size``,
 ``kvq_row_bytes``.
 """
@@ -68,6 +68,8 @@ _lib.kvq_decode_attn_noalloc.argtypes = [_CP, _PP, _P, _I, _I, ctypes.c_float, _
 _lib.kvq_decode_attn_noalloc.restype = _I
 _lib.kvq_prefill_attn.argtypes = [_CP, _PP, _P, _I, _I, _P, _I, _I, ctypes.c_float, _P, _P, _P]
 _lib.kvq_prefill_attn.restype = _I
+_lib.kvq_prefill_dense_attn.argtypes = [_P, _P, _P, _I, _I, _PP, _P, _I, _I, _P, _I, _I, ctypes.c_float, _P, _P, _P]
+_lib.kvq_prefill_dense_attn.restype = _I
 
 
 class KvqError(RuntimeError):
@@ -263,4 +265,28 @@ def kvq_prefill_attn(cache: PagedCache, paging: Paging, q: torch.Tensor, cu_q: t
                                  _dev_ptr(cu_q, torch.int32, "cu_q"), T, int(max_q_per_seq), float(softmax_scale),
                                  _dev_ptr(out, torch.float32, "out"), _dev_ptr(dev_error, torch.int32, "dev_error"),
                                  _stream_ptr(stream)))
+    return out
+
+
+def kvq_prefill_dense_attn(k: torch.Tensor, v: torch.Tensor, cu_kv: torch.Tensor, seq_lens: torch.Tensor,
+                           q: torch.Tensor, cu_q: torch.Tensor, max_q_per_seq: int, softmax_scale: float,
+                           window_per_kv_head: Optional[torch.Tensor] = None, sink_size: int = 0,
+                           out: Optional[torch.Tensor] = None, dev_error: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """Causal chunked-prefill attention of q [total_q, num_q_heads, head_dim]
+    over dense bf16 k, v [rows, num_kv_heads, head_dim] (sequence b's key j at
+    row cu_kv[b] + j, e.g. kvq_gather's output); returns fp32 out."""
+    if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16 or k.shape != v.shape:
+        raise ValueError("k and v must be bfloat16 tensors of one shape")
+    T, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.float32, device=q.device)
+    ps = KvqPaging(None, None, 0, int(seq_lens.shape[0]), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
+                   _dev_ptr(window_per_kv_head, torch.int32, "window_per_kv_head"), int(sink_size))
+    _check(_lib.kvq_prefill_dense_attn(_dev_ptr(k, name="k"), _dev_ptr(v, name="v"),
+                                       _dev_ptr(cu_kv, torch.int32, "cu_kv"), int(k.shape[1]), int(k.shape[2]),
+                                       ctypes.byref(ps), _dev_ptr(q, name="q"), _qdtype(q), Hq,
+                                       _dev_ptr(cu_q, torch.int32, "cu_q"), T, int(max_q_per_seq),
+                                       float(softmax_scale), _dev_ptr(out, torch.float32, "out"),
+                                       _dev_ptr(dev_error, torch.int32, "dev_error"), _stream_ptr(stream)))
     return out

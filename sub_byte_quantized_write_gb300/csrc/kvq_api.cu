@@ -343,4 +343,53 @@ kvq_status kvq_prefill_attn(const kvq_cache* cache, const kvq_paging* paging, co
   return KVQ_OK;
 }
 
+kvq_status kvq_prefill_dense_attn(const void* k, const void* v, const int32_t* cu_kv, int32_t num_kv_heads,
+                                  int32_t head_dim, const kvq_paging* paging, const void* q, int32_t dtype,
+                                  int32_t num_q_heads, const int32_t* cu_q, int32_t total_q, int32_t max_q_per_seq,
+                                  float softmax_scale, float* out, int32_t* dev_error, void* stream) {
+  if (!paging) return fail(KVQ_ERR_INVALID_ARG, "paging is NULL");
+  if (paging->block_tables || paging->block_tables_headwise)
+    return fail(KVQ_ERR_INVALID_ARG, "dense attention takes no block table");
+  if (paging->batch < 0 || total_q < 0 || max_q_per_seq < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "batch / total_q / max_q_per_seq < 0");
+  if (head_dim != 64 && head_dim != 128) return fail(KVQ_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (num_kv_heads <= 0) return fail(KVQ_ERR_INVALID_ARG, "num_kv_heads must be > 0");
+  if (paging->batch == 0 || total_q == 0 || max_q_per_seq == 0) return KVQ_OK;
+  if (!k || !v || !cu_kv || !cu_q || !paging->seq_lens) return fail(KVQ_ERR_INVALID_ARG, "k / v / cu_kv / cu_q / seq_lens is NULL");
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(KVQ_ERR_INVALID_ARG, "k / v must be 16-byte aligned");
+  if (!q || !out) return fail(KVQ_ERR_INVALID_ARG, "q / out is NULL");
+  if (dtype != KVQ_F32 && dtype != KVQ_BF16) return fail(KVQ_ERR_UNSUPPORTED, "dtype must be KVQ_F32 or KVQ_BF16");
+  if (!aligned(q, 16) || !aligned(out, 16)) return fail(KVQ_ERR_INVALID_ARG, "q / out must be 16-byte aligned");
+  if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (num_q_heads / num_kv_heads > 8) return fail(KVQ_ERR_UNSUPPORTED, "GQA group size above 8");
+  kvq::AttnParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.k_pages = static_cast<const uint8_t*>(k);
+  P.v_pages = static_cast<const uint8_t*>(v);
+  P.num_kv_heads = num_kv_heads;
+  P.block_size = 16;          // no pages: positions are bounded by cu_kv instead
+  P.max_blocks = 1 << 26;
+  P.head_dim = head_dim;
+  P.mode = kvq::MODE_DBF16;
+  P.batch = paging->batch;
+  P.seq_lens = paging->seq_lens;
+  P.window = paging->window_per_kv_head;
+  P.sink = paging->sink_size;
+  P.q = q;
+  P.dtype = dtype;
+  P.num_q_heads = num_q_heads;
+  P.group = num_q_heads / num_kv_heads;
+  P.softmax_scale = softmax_scale;
+  P.out = out;
+  P.dev_error = dev_error;
+  P.cu_q = cu_q;
+  P.total_q = total_q;
+  P.max_q_per_seq = max_q_per_seq;
+  P.cu_kv = cu_kv;
+  cudaError_t e = kvq::launch_prefill(P, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KVQ_OK;
+}
+
 }  // extern "C"

@@ -10,14 +10,19 @@ namespace kvq {
 
 // Kernel code families.  The API's zero-point-in-scale INT4 mode (3) runs as
 // MODE_INT4 with the `stego` flag of the parameters; 4 and 5 are the INT8 /
-// FP8 rows with one fp32 scale per (token, kv head).
-enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2, MODE_I8T = 4, MODE_F8T = 5 };
+// FP8 rows with one fp32 scale per (token, kv head); 6 is the dense prefill's
+// bf16 rows (no codes, no scale).
+enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2, MODE_I8T = 4, MODE_F8T = 5, MODE_DBF16 = 6 };
 enum { DT_F32 = 0, DT_BF16 = 1 };
 enum { DEVERR_BLOCK_RANGE = 1, DEVERR_TABLE_RANGE = 2, DEVERR_SEQ_LEN = 4, DEVERR_TIMEOUT = 8 };
 
-__host__ __device__ constexpr int mode_bits(int mode) { return mode == MODE_INT4 ? 4 : (mode == MODE_INT2 ? 2 : 8); }
+__host__ __device__ constexpr int mode_bits(int mode) {
+  return mode == MODE_INT4 ? 4 : (mode == MODE_INT2 ? 2 : (mode == MODE_DBF16 ? 16 : 8));
+}
 __host__ __device__ constexpr int data_bytes(int mode, int D) { return D * mode_bits(mode) / 8; }
-__host__ __device__ constexpr int row_bytes_of(int mode, int D) { return mode == MODE_INT8 ? D : data_bytes(mode, D) + 4; }
+__host__ __device__ constexpr int row_bytes_of(int mode, int D) {
+  return (mode == MODE_INT8 || mode == MODE_DBF16) ? data_bytes(mode, D) : data_bytes(mode, D) + 4;
+}
 // INT8 / FP8 codes with a symmetric fp32 scale per row (no zero point)
 __host__ __device__ constexpr bool byte_token_head(int mode) { return mode == MODE_I8T || mode == MODE_F8T; }
 

@@ -51,6 +51,8 @@ struct AttnParams {
   // prefill
   const int32_t* cu_q;
   int total_q, max_q_per_seq;
+  // dense prefill: sequence b's key j is row cu_kv[b] + j of k_pages / v_pages
+  const int32_t* cu_kv;
 };
 
 // Decode workspace (caller-owned scratch), carved by decode_ws_layout.

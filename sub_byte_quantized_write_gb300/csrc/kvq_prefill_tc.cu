@@ -110,13 +110,26 @@ enum {
   B_DRAIN = 18, B_XCH = 20, B_EPI = 28
 };
 
+// Two bf16 values (low half first) as an fp16 pair: exact for values inside
+// the fp16 range (bf16 carries 8 significant bits, fp16 11).
+__device__ __forceinline__ uint32_t bf16x2_to_half2_bits(uint32_t w) {
+  const __half2 hv = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&hv);
+}
+
 // Eight consecutive codes (head dims 8c .. 8c+7) of a raw row as four exact
 // fp16 pairs of signed codes u - 2^(b-1) (INT8: as stored; FP8: the E4M3
-// value), in dim order.
+// value; dense rows: the bf16 values), in dim order.
 template <int MODE>
 __device__ __forceinline__ uint4 codes8(const uint8_t* raw_row, int c) {
   uint32_t o[4];
-  if constexpr (MODE == MODE_INT4) {
+  if constexpr (MODE == MODE_DBF16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(raw_row + 16 * c);
+    o[0] = bf16x2_to_half2_bits(w.x);
+    o[1] = bf16x2_to_half2_bits(w.y);
+    o[2] = bf16x2_to_half2_bits(w.z);
+    o[3] = bf16x2_to_half2_bits(w.w);
+  } else if constexpr (MODE == MODE_INT4) {
     const uint32_t w = lds32(raw_row + 4 * c);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -154,7 +167,9 @@ __device__ __forceinline__ uint4 codes8(const uint8_t* raw_row, int c) {
 // pair of signed codes (low half = dim d).
 template <int MODE>
 __device__ __forceinline__ uint32_t codes2(const uint8_t* raw_row, int d) {
-  if constexpr (MODE == MODE_INT4) {
+  if constexpr (MODE == MODE_DBF16) {
+    return bf16x2_to_half2_bits(*reinterpret_cast<const uint32_t*>(raw_row + 2 * d));
+  } else if constexpr (MODE == MODE_INT4) {
     const uint32_t b = raw_row[d >> 1];
     const uint32_t x = b | (b << 16);
     return hsub2_bits(lop3_and_or(x, 0x00F0000Fu, 0x54006400u), 0x54806408u);
@@ -234,6 +249,12 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
   if (Leff > P.max_blocks * bs) {
     if (tid == 0) flag_error(P.dev_error, DEVERR_TABLE_RANGE);
     Leff = P.max_blocks * bs;
+  }
+  if constexpr (MODE == MODE_DBF16) {  // the sequence's dense rows must hold its L keys
+    if (__ldg(P.cu_kv + b + 1) - __ldg(P.cu_kv + b) < L) {
+      if (tid == 0) flag_error(P.dev_error, DEVERR_SEQ_LEN);
+      return;
+    }
   }
   const int nq = min(QB, n - q0);
   const int p_min = L - n + q0, p_max = L - n + q0 + nq - 1;
@@ -389,7 +410,38 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
     // Bulk copies of each tile's valid 16-row chunks into a ring of NRAW raw
     // stages, up to NRAW tiles ahead of the expansion; the page-table
     // entries are read two tiles ahead of the copies that use them.
-    if (lane == 0) {
+    if (MODE == MODE_DBF16 && lane == 0) {
+      // dense rows: one bulk copy per key row (rows of a head are Hkv rows apart)
+      const size_t rstride = (size_t)Hkv * C::R;
+      const uint8_t* kbase = P.k_pages + ((size_t)__ldg(P.cu_kv + b) * Hkv + h) * C::R;
+      const uint8_t* vbase = P.v_pages + ((size_t)__ldg(P.cu_kv + b) * Hkv + h) * C::R;
+      int rs = 0, rphase = 0;
+#pragma unroll 1
+      for (int v = 0; v < n_virt; ++v) {
+        if (!mbar_wait_bounded(bar + B_RAWEMPTY + rs, rphase ^ 1, TP_NAP_ISSUER) || *abort_flag) {
+          *abort_flag = 1;
+          flag_error(P.dev_error, DEVERR_TIMEOUT);
+          break;
+        }
+        const int key0 = TP_KT * tile_of(v);
+        const int nrows = max(0, min(TP_KT, Leff - key0));
+        uint8_t* rk = sm + C::OFF_RAW + rs * 2 * C::RAW;
+        uint8_t* rvp = rk + C::RAW;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) rawval[rs * 4 + c] = 16 * c < nrows ? 1 : 0;
+        mbar_arrive_expect_tx(bar + B_RAWFULL + rs, (uint32_t)(nrows * 2 * C::R));
+#pragma unroll 4
+        for (int j = 0; j < nrows; ++j) {
+          const size_t off = (size_t)(key0 + j) * rstride;
+          bulk_g2s(rk + j * C::R, kbase + off, C::R, bar + B_RAWFULL + rs);
+          bulk_g2s(rvp + j * C::R, vbase + off, C::R, bar + B_RAWFULL + rs);
+        }
+        if (++rs == C::NRAW) {
+          rs = 0;
+          rphase ^= 1;
+        }
+      }
+    } else if (MODE != MODE_DBF16 && lane == 0) {
       const int trow = P.headwise ? b * Hkv + h : b;
       const int32_t* tbl = P.table + (size_t)trow * P.max_blocks;
       const size_t blk_stride = (size_t)Hkv * bs * C::R;
@@ -497,7 +549,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
           const int key = key_0 + KSTEP * j;
-          const uint4 hv = codes8<MODE>(src + KSTEP * j * C::R, c8);
+          uint4 hv = codes8<MODE>(src + KSTEP * j * C::R, c8);
+          if (MODE == MODE_DBF16 && key0 + key >= Leff) hv = make_uint4(0u, 0u, 0u, 0u);  // not copied
           *reinterpret_cast<uint4*>(dst + tc::sw128_off(key, c8 & 7)) = hv;
         }
       }
@@ -515,6 +568,10 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
           uint32_t r4[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) r4[i] = codes2<MODE>(row, 32 * db + 8 * i + 2 * t4);
+          if (MODE == MODE_DBF16 && key0 + 8 * kb + g8 >= Leff) {  // not copied: stale bytes could be NaN
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r4[i] = 0u;
+          }
           const int mi = lane >> 3, rr = lane & 7;
           const int d = 32 * db + 8 * mi + rr;  // stored row of matrix mi
           tc::stsm_x4_t(smem_addr(vt + tc::sw128_off(d, kb)), r4[0], r4[1], r4[2], r4[3]);
@@ -529,8 +586,12 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
           const bool has = ((vmask >> (key >> 4)) & 1) && key0 + key < Leff;
           float s = 0.0f, z = 0.0f;
           if (has) {
-            const uint32_t pad = lds32((isv ? rvp : rk) + key * C::R + C::DATA);
-            pad_scale_zero<MODE>(pad, P.stego != 0, s, z);  // z: the value of the signed code 0
+            if constexpr (MODE == MODE_DBF16) {
+              s = 1.0f;  // dense values: no scale, no zero point
+            } else {
+              const uint32_t pad = lds32((isv ? rvp : rk) + key * C::R + C::DATA);
+              pad_scale_zero<MODE>(pad, P.stego != 0, s, z);  // z: the value of the signed code 0
+            }
           }
           float* scs = sc + kvs * 4 * TP_KT;
           scs[(isv ? 2 : 0) * TP_KT + key] = s;
@@ -890,6 +951,8 @@ cudaError_t launch_prefill(const AttnParams& P, cudaStream_t stream) {
     case MODE_I8T * 1000 + 64: return launch_prefill_tc_t<MODE_I8T, 64>(P, stream);
     case MODE_F8T * 1000 + 128: return launch_prefill_tc_t<MODE_F8T, 128>(P, stream);
     case MODE_F8T * 1000 + 64: return launch_prefill_tc_t<MODE_F8T, 64>(P, stream);
+    case MODE_DBF16 * 1000 + 128: return launch_prefill_tc_t<MODE_DBF16, 128>(P, stream);
+    case MODE_DBF16 * 1000 + 64: return launch_prefill_tc_t<MODE_DBF16, 64>(P, stream);
     default: return cudaErrorInvalidValue;
   }
 }
