@@ -201,6 +201,10 @@ WORKLOADS = {
                                                num_blocks=a.pool_blocks or 200000),
                     "INT4 gather-and-dequantise tokens/s (every cached position of the chunked-prefill layer "
                     "back to dense bf16 K/V, % of GB300 HBM peak)", "gather"),
+    "gather_dense_prefill_int4": (lambda a: gen.prefill_int4(seed=0, prefixes=tuple(a.prefill_prefixes),
+                                                             chunk=a.prefill_chunk, num_blocks=a.pool_blocks or 200000),
+                                  "INT4 chunked-prefill tokens/s through gather + dequantise + dense prefill "
+                                  "(% of tensor peak)", "gather_prefill"),
 }
 
 
@@ -315,13 +319,18 @@ def run_gpu(args, rank, world, local_rank):
     def write_call():
         K.kvq_write(cache, pag, st["k"], st["v"], st["cu"], stream=stream)
 
-    if kind == "gather":
+    if kind in ("gather", "gather_prefill"):
         st["gk"] = torch.empty((st["n_all"], wl.num_kv_heads, wl.head_dim), dtype=torch.bfloat16, device=device)
         st["gv"] = torch.empty_like(st["gk"])
+    if kind == "gather":
         st["out"] = st["gk"]  # the step's result, read back by the end-to-end run (with gv)
 
+    def dense_call():  # gather_prefill: the dense prefill over the gathered rows
+        K.kvq_prefill_dense_attn(st["gk"], st["gv"], st["cu_all"], st["seq_lens"], st["q"], st["cu"], max_q, scale,
+                                 out=st["out"], stream=stream)
+
     def attn_call():
-        if kind == "gather":
+        if kind in ("gather", "gather_prefill"):
             K.kvq_gather(cache, pag, st["cu_all"], st["n_all"], k_out=st["gk"], v_out=st["gv"], stream=stream)
         elif kind == "decode":
             K.kvq_decode_attn(cache, pag, st["q"], scale, out=st["out"], workspace=st["ws"],
@@ -332,6 +341,8 @@ def run_gpu(args, rank, world, local_rank):
     def step():
         write_call()
         attn_call()
+        if kind == "gather_prefill":
+            dense_call()
 
     # The step's two library calls are captured once into a CUDA graph and
     # replayed, so the timed region holds only device work (re-writing the
@@ -343,26 +354,30 @@ def run_gpu(args, rank, world, local_rank):
             step()  # first calls set the kernels' shared-memory attributes outside capture
         stream.synchronize()
         g_step, g_write, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        g_dense = torch.cuda.CUDAGraph() if kind == "gather_prefill" else None
         with torch.cuda.graph(g_step, stream=stream):
-            write_call()
-            attn_call()
+            step()
         with torch.cuda.graph(g_write, stream=stream):
             write_call()
         with torch.cuda.graph(g_attn, stream=stream):
             attn_call()
+        if g_dense is not None:
+            with torch.cuda.graph(g_dense, stream=stream):
+                dense_call()
     for _ in range(args.warmup):
         with torch.cuda.stream(stream):
             flush.fill_(1.0)
         g_step.replay()
         g_write.replay()
         g_attn.replay()
+        if g_dense is not None:
+            g_dense.replay()
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
@@ -374,18 +389,23 @@ def run_gpu(args, rank, world, local_rank):
                 c.record(stream)
             for i in range(args.steps):  # per-call breakdown, same steps replayed call by call
                 flush.fill_(float(i))
-                e0, e1, e2 = ev[i]
+                e0, e1, e2, e3 = ev[i]
                 e0.record(stream)
                 g_write.replay()
                 e1.record(stream)
                 g_attn.replay()
                 e2.record(stream)
+                if g_dense is not None:
+                    g_dense.replay()
+                e3.record(stream)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(c) for a, c in evs]
-    att_ms = [b.elapsed_time(c) for a, b, c in ev]
-    wr_ms = [a.elapsed_time(b) for a, b, c in ev]
+    att_ms = [b.elapsed_time(c) for a, b, c, d in ev]
+    wr_ms = [a.elapsed_time(b) for a, b, c, d in ev]
+    dense_ms = [c.elapsed_time(d) for a, b, c, d in ev]
     ms = max_over_ranks(sum(step_ms) / len(step_ms), device)
-    tokens = {"decode": wl.batch, "prefill": int(wl.n_new.sum()), "gather": st["n_all"]}[kind]
+    tokens = {"decode": wl.batch, "prefill": int(wl.n_new.sum()), "gather": st["n_all"],
+              "gather_prefill": int(wl.n_new.sum())}[kind]
     value = whole_job_rate(tokens, ms, world)
 
     # end to end through the C ABI with host buffers: H2D of the step's
@@ -432,7 +452,8 @@ def run_gpu(args, rank, world, local_rank):
     units = algorithmic_units(wl)
     att = sum(att_ms) / len(att_ms)
     hbm, tensor, peak_kind = peaks()
-    cfg = {"workload": ("gather_" + wl.name) if kind == "gather" else wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
+    cfg = {"workload": {"gather": "gather_", "gather_prefill": "gather_dense_"}.get(kind, "") + wl.name,
+           "batch": wl.batch, "num_q_heads": wl.num_q_heads,
            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
            "mode": {0: "int4", 1: "int2", 2: "int8", 3: "int4_stego", 4: "int8_token_head",
                     5: "fp8_token_head"}[wl.mode], "headwise_table": bool(wl.headwise),
@@ -455,6 +476,21 @@ def run_gpu(args, rank, world, local_rank):
         extra = {"gather_ms": round(att, 5), "gathered_tokens_per_step": st["n_all"]}
         launches = 2  # write + gather
         dtype = "u4 codes -> fp32 dequantise + inverse RHT -> bf16"
+    elif kind == "gather_prefill":
+        dense = sum(dense_ms) / len(dense_ms)
+        achieved = units["prefill_flops"] / (dense / 1e3) / 1e12
+        traffic = recorded_units("prefill_tc_%s.md" % args.workload, "dram_bytes_per_prefill_call",
+                                 kernel_source_hash(("kvq_prefill_tc.cu", "kvq_tc.cuh", "kvq_common.cuh",
+                                                     "kvq_internal.h")))
+        roof = {"bound": "tensor", "kernel": "prefill_tc_kernel over dense bf16 rows (one kvq_prefill_dense_attn call)",
+                "achieved": round(achieved, 2), "peak": tensor,
+                "peak_kind": peak_kind + " (cuBLAS bf16 burst; kind::f16 fp16 runs at the bf16 rate)",
+                "unit": "TFLOP/s", "frac": round(achieved / tensor, 4), "executed_tflops": round(2 * achieved, 2),
+                "algorithmic_flops_per_launch": units["prefill_flops"], "traffic": traffic}
+        extra = {"gather_ms": round(att, 5), "dense_prefill_ms": round(dense, 5),
+                 "gathered_tokens_per_step": st["n_all"]}
+        launches = 3  # write + gather + dense prefill
+        dtype = "u4 codes -> bf16 rows (gather) -> fp16 x fp16 (q hi+lo) tcgen05 math, fp32 TMEM accumulate/softmax"
     elif kind == "decode":
         cfg["decode_workers"] = st["splits"]
         achieved = units["decode"] / (att / 1e3) / 1e9
@@ -494,7 +530,7 @@ def run_gpu(args, rank, world, local_rank):
         "metric": metric, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype,
-        "data": "synthetic (seeded; K/V ~ N(0,1)%s)" % (", 1% outlier channels x10" if args.workload.startswith("llama") or args.workload in ("prefill_int4", "gather_int4") else ""),
+        "data": "synthetic (seeded; K/V ~ N(0,1)%s)" % (", 1% outlier channels x10" if args.workload.startswith("llama") or args.workload in ("prefill_int4", "gather_int4", "gather_dense_prefill_int4") else ""),
         "config": cfg, **extra, "write_ms": round(wr, 5),
         "roofline": roof,
         "write_roofline": write_roof,
@@ -547,6 +583,14 @@ def oracle_step(wl, oc, new_k, new_v, q, sample_seqs, threads, rows=None, kind=N
         counts = np.zeros(wl.batch, np.int32)
         counts[sample_seqs] = wl.seq_lens[sample_seqs]
         oracle.gather(oc, pag, wl.cu(counts))
+    elif kind == "gather_prefill":
+        lens = np.zeros(wl.batch, np.int32)
+        lens[sample_seqs] = wl.seq_lens[sample_seqs]
+        cu_kv = wl.cu(lens)
+        k, v, _ = oracle.gather(oc, pag, cu_kv)
+        kb, vb = gen.f32_to_bf16_bits(k.astype(np.float32)), gen.f32_to_bf16_bits(v.astype(np.float32))
+        dpag = oracle.Paging(np.zeros((wl.batch, 1), np.int32), False, lens, wl.window, wl.sink)
+        oracle.dense_attention(kb, vb, cu_kv, dpag, q, scale, wl.cu(wl.n_new), rows=rows, threads=threads)
     elif wl.step == "decode":
         oracle.attention(oc, pag, q, scale, rows=np.asarray(sample_seqs, np.int32), threads=threads)
     else:
@@ -579,6 +623,10 @@ def cpu_baseline(wl, budget_s=15.0, kind=None):
         sample = list(range(0, wl.batch, 4))
         rows = None
         per_step = len(sample)
+    elif kind == "gather_prefill":
+        sample = list(range(wl.batch))
+        rows = _prefill_rows(wl, 4)
+        per_step = len(rows)
     else:
         sample = list(range(wl.batch))
         rows = _prefill_rows(wl, 4)
@@ -597,6 +645,10 @@ def cpu_baseline(wl, budget_s=15.0, kind=None):
                 "K and V, all %d kv heads; the oracle's gather is single-threaded), %.1f s"
                 % (n, sample, per_step, wl.num_kv_heads, dt))
         threads = 1
+    elif kind == "gather_prefill":
+        desc = ("%d steps of: write of the %d-token chunk + gather of every cached position (single-threaded) + "
+                "dense attention of %d query rows (4 per sequence, all %d q heads), %.1f s; tokens/s counts the "
+                "attended rows" % (n, int(wl.n_new.sum()), per_step, wl.num_q_heads, dt))
     elif wl.step == "decode":
         desc = ("%d decode steps of %d of the %d sequences (every 4th; write 1 token + attention over the cached "
                 "context, all %d q heads), %.1f s" % (n, len(sample), wl.batch, wl.num_q_heads, dt))
@@ -620,6 +672,12 @@ def run_reference(args):
         desc = ("sequences %s per step: write of their chunks + gather of their whole contexts (%d positions, K and "
                 "V, all %d kv heads; single-threaded oracle)" % (sample, per_step, wl.num_kv_heads))
         threads = 1
+    elif kind == "gather_prefill":
+        sample = list(range(wl.batch))
+        rows = _prefill_rows(wl, 1)
+        per_step = len(rows)
+        desc = ("write of the %d-token chunk + gather of every cached position + dense attention of the last query "
+                "row of each sequence, all %d q heads" % (int(wl.n_new.sum()), wl.num_q_heads))
     elif kind == "decode":
         sample = list(range(0, wl.batch, 16))
         rows = None
@@ -661,7 +719,7 @@ def main():
     ap.add_argument("--workload", default="llama_int4", choices=sorted(WORKLOADS),
                     help="llama_int4 (the headline decode workload), llama_int4_d64_bs64, llama_int4_stego, "
                          "llama_int8_token_head, llama_fp8_token_head, ernie_int2, qwen_int8_headwise, prefill_int4, "
-                         "gather_int4")
+                         "gather_int4, gather_dense_prefill_int4")
     ap.add_argument("--pool-blocks", type=int, default=0,
                     help="block pool size (0 = the workload's own; smaller pools only for profiling)")
     ap.add_argument("--prefill-prefixes", type=int, nargs="+", default=[0, 4096, 16384, 61440],
