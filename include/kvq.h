@@ -307,17 +307,20 @@ int32_t kvq_abi_version(void);
  * k, v          : bf16 [rows][num_kv_heads][head_dim], 16-byte aligned; sequence
  *                 b's key j is row cu_kv[b] + j (kvq_gather with n_b = seq_lens[b]
  *                 writes exactly this layout).  Values must lie in the fp16 range.
- * cu_kv         : int32 [batch + 1]; cu_kv[b + 1] - cu_kv[b] >= seq_lens[b], else
- *                 the sequence is skipped and KVQ_DEVERR_SEQ_LEN set.
+ * cu_kv         : int32 [batch + 1] (device); cu_kv[b + 1] - cu_kv[b] >= seq_lens[b],
+ *                 else the sequence is skipped and KVQ_DEVERR_SEQ_LEN set.
+ * num_kv_rows   : rows of k and v (host); cu_kv[batch] <= num_kv_rows.  The rows
+ *                 move by tensor copies (one 64-row box of a head per tile).
  * paging        : seq_lens, batch, window_per_kv_head and sink_size as for the
  *                 paged calls; both block tables must be NULL.
  * q, dtype, num_q_heads, cu_q, total_q, max_q_per_seq, softmax_scale, out,
  * dev_error     : as in kvq_prefill_attn (queries at positions seq_lens[b] - n_b
  *                 + i, causal, window + sink per kv head). */
-kvq_status kvq_prefill_dense_attn(const void* k, const void* v, const int32_t* cu_kv, int32_t num_kv_heads,
-                                  int32_t head_dim, const kvq_paging* paging, const void* q, int32_t dtype,
-                                  int32_t num_q_heads, const int32_t* cu_q, int32_t total_q, int32_t max_q_per_seq,
-                                  float softmax_scale, float* out, int32_t* dev_error, void* stream);
+kvq_status kvq_prefill_dense_attn(const void* k, const void* v, const int32_t* cu_kv, int32_t num_kv_rows,
+                                  int32_t num_kv_heads, int32_t head_dim, const kvq_paging* paging, const void* q,
+                                  int32_t dtype, int32_t num_q_heads, const int32_t* cu_q, int32_t total_q,
+                                  int32_t max_q_per_seq, float softmax_scale, float* out, int32_t* dev_error,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

@@ -68,7 +68,8 @@ _lib.kvq_decode_attn_noalloc.argtypes = [_CP, _PP, _P, _I, _I, ctypes.c_float, _
 _lib.kvq_decode_attn_noalloc.restype = _I
 _lib.kvq_prefill_attn.argtypes = [_CP, _PP, _P, _I, _I, _P, _I, _I, ctypes.c_float, _P, _P, _P]
 _lib.kvq_prefill_attn.restype = _I
-_lib.kvq_prefill_dense_attn.argtypes = [_P, _P, _P, _I, _I, _PP, _P, _I, _I, _P, _I, _I, ctypes.c_float, _P, _P, _P]
+_lib.kvq_prefill_dense_attn.argtypes = [_P, _P, _P, _I, _I, _I, _PP, _P, _I, _I, _P, _I, _I, ctypes.c_float, _P, _P,
+                                        _P]
 _lib.kvq_prefill_dense_attn.restype = _I
 
 
@@ -284,7 +285,8 @@ def kvq_prefill_dense_attn(k: torch.Tensor, v: torch.Tensor, cu_kv: torch.Tensor
     ps = KvqPaging(None, None, 0, int(seq_lens.shape[0]), _dev_ptr(seq_lens, torch.int32, "seq_lens"),
                    _dev_ptr(window_per_kv_head, torch.int32, "window_per_kv_head"), int(sink_size))
     _check(_lib.kvq_prefill_dense_attn(_dev_ptr(k, name="k"), _dev_ptr(v, name="v"),
-                                       _dev_ptr(cu_kv, torch.int32, "cu_kv"), int(k.shape[1]), int(k.shape[2]),
+                                       _dev_ptr(cu_kv, torch.int32, "cu_kv"), int(k.shape[0]), int(k.shape[1]),
+                                       int(k.shape[2]),
                                        ctypes.byref(ps), _dev_ptr(q, name="q"), _qdtype(q), Hq,
                                        _dev_ptr(cu_q, torch.int32, "cu_q"), T, int(max_q_per_seq),
                                        float(softmax_scale), _dev_ptr(out, torch.float32, "out"),

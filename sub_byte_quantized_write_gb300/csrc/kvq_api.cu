@@ -4,6 +4,7 @@
 // its kernels on the caller's stream without synchronising.
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdio>
 #include <cstring>
@@ -343,18 +344,57 @@ kvq_status kvq_prefill_attn(const kvq_cache* cache, const kvq_paging* paging, co
   return KVQ_OK;
 }
 
-kvq_status kvq_prefill_dense_attn(const void* k, const void* v, const int32_t* cu_kv, int32_t num_kv_heads,
-                                  int32_t head_dim, const kvq_paging* paging, const void* q, int32_t dtype,
-                                  int32_t num_q_heads, const int32_t* cu_q, int32_t total_q, int32_t max_q_per_seq,
-                                  float softmax_scale, float* out, int32_t* dev_error, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [rows][Hkv][D] bf16 seen as a 3-D tensor (D, Hkv, rows) with a box of D
+// elements x 1 head x 64 rows: one box is the tile of one head.
+bool dense_rows_map(CUtensorMap* map, const void* base, int64_t rows, int Hkv, int D) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)D, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_prefill_dense_attn(const void* k, const void* v, const int32_t* cu_kv, int32_t num_kv_rows,
+                                  int32_t num_kv_heads, int32_t head_dim, const kvq_paging* paging, const void* q,
+                                  int32_t dtype, int32_t num_q_heads, const int32_t* cu_q, int32_t total_q,
+                                  int32_t max_q_per_seq, float softmax_scale, float* out, int32_t* dev_error,
+                                  void* stream) {
   if (!paging) return fail(KVQ_ERR_INVALID_ARG, "paging is NULL");
   if (paging->block_tables || paging->block_tables_headwise)
     return fail(KVQ_ERR_INVALID_ARG, "dense attention takes no block table");
   if (paging->batch < 0 || total_q < 0 || max_q_per_seq < 0)
     return fail(KVQ_ERR_INVALID_ARG, "batch / total_q / max_q_per_seq < 0");
   if (head_dim != 64 && head_dim != 128) return fail(KVQ_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
-  if (num_kv_heads <= 0) return fail(KVQ_ERR_INVALID_ARG, "num_kv_heads must be > 0");
+  if (num_kv_heads <= 0 || num_kv_rows < 0) return fail(KVQ_ERR_INVALID_ARG, "num_kv_heads <= 0 or num_kv_rows < 0");
   if (paging->batch == 0 || total_q == 0 || max_q_per_seq == 0) return KVQ_OK;
+  if (num_kv_rows == 0) return fail(KVQ_ERR_INVALID_ARG, "no K / V rows");
   if (!k || !v || !cu_kv || !cu_q || !paging->seq_lens) return fail(KVQ_ERR_INVALID_ARG, "k / v / cu_kv / cu_q / seq_lens is NULL");
   if (!aligned(k, 16) || !aligned(v, 16)) return fail(KVQ_ERR_INVALID_ARG, "k / v must be 16-byte aligned");
   if (!q || !out) return fail(KVQ_ERR_INVALID_ARG, "q / out is NULL");
@@ -387,6 +427,9 @@ kvq_status kvq_prefill_dense_attn(const void* k, const void* v, const int32_t* c
   P.total_q = total_q;
   P.max_q_per_seq = max_q_per_seq;
   P.cu_kv = cu_kv;
+  if (!dense_rows_map(&P.kv_map[0], k, num_kv_rows, num_kv_heads, head_dim) ||
+      !dense_rows_map(&P.kv_map[1], v, num_kv_rows, num_kv_heads, head_dim))
+    return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled failed for the dense K / V rows");
   cudaError_t e = kvq::launch_prefill(P, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KVQ_OK;

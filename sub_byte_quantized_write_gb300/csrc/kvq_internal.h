@@ -1,6 +1,7 @@
 // kvq_internal.h -- kernel parameter blocks and launchers behind the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,8 +52,10 @@ struct AttnParams {
   // prefill
   const int32_t* cu_q;
   int total_q, max_q_per_seq;
-  // dense prefill: sequence b's key j is row cu_kv[b] + j of k_pages / v_pages
+  // dense prefill: sequence b's key j is row cu_kv[b] + j of k_pages / v_pages;
+  // kv_map[0 | 1] view K / V as [rows][Hkv][D] bf16 with a 64-row box of one head
   const int32_t* cu_kv;
+  CUtensorMap kv_map[2];  // 128-byte aligned by its own declaration
 };
 
 // Decode workspace (caller-owned scratch), carved by decode_ws_layout.

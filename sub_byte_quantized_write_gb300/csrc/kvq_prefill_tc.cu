@@ -219,7 +219,7 @@ __device__ __forceinline__ int heavy_first_sequence(const AttnParams& P, int z) 
 }
 
 template <int MODE, int D>
-__global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P) {
+__global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_constant__ AttnParams P) {
   using C = TpCfg<MODE, D>;
   constexpr int NKV = C::NKV;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -410,44 +410,27 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(AttnParams P)
     // Bulk copies of each tile's valid 16-row chunks into a ring of NRAW raw
     // stages, up to NRAW tiles ahead of the expansion; the page-table
     // entries are read two tiles ahead of the copies that use them.
-    if (MODE == MODE_DBF16) {
-      // dense rows: one bulk copy per key row (rows of a head are Hkv rows
-      // apart), issued by the whole warp, lane l taking rows l, l + 32
-      const size_t rstride = (size_t)Hkv * C::R;
-      const uint8_t* kbase = P.k_pages + ((size_t)__ldg(P.cu_kv + b) * Hkv + h) * C::R;
-      const uint8_t* vbase = P.v_pages + ((size_t)__ldg(P.cu_kv + b) * Hkv + h) * C::R;
+    if (MODE == MODE_DBF16 && lane == 0) {
+      // dense rows: one 64-row box of this head per tensor and tile (tensor
+      // copies; rows past the array arrive as zeros, rows of the next
+      // sequence are zeroed by the producers)
+      const int row0 = __ldg(P.cu_kv + b);
       int rs = 0, rphase = 0;
 #pragma unroll 1
       for (int v = 0; v < n_virt; ++v) {
-        bool go = true;
-        if (lane == 0) go = mbar_wait_bounded(bar + B_RAWEMPTY + rs, rphase ^ 1, TP_NAP_ISSUER) && !*abort_flag;
-        go = __shfl_sync(0xffffffffu, go, 0);
-        if (!go) {
-          if (lane == 0) {
-            *abort_flag = 1;
-            flag_error(P.dev_error, DEVERR_TIMEOUT);
-          }
+        if (!mbar_wait_bounded(bar + B_RAWEMPTY + rs, rphase ^ 1, TP_NAP_ISSUER) || *abort_flag) {
+          *abort_flag = 1;
+          flag_error(P.dev_error, DEVERR_TIMEOUT);
           break;
         }
         const int key0 = TP_KT * tile_of(v);
         const int nrows = max(0, min(TP_KT, Leff - key0));
         uint8_t* rk = sm + C::OFF_RAW + rs * 2 * C::RAW;
-        uint8_t* rvp = rk + C::RAW;
-        if (lane == 0) {  // the validity flags are released by this lane's arrive
 #pragma unroll
-          for (int c = 0; c < 4; ++c) rawval[rs * 4 + c] = 16 * c < nrows ? 1 : 0;
-          mbar_arrive_expect_tx(bar + B_RAWFULL + rs, (uint32_t)(nrows * 2 * C::R));
-        }
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < TP_KT / 32; ++i) {
-          const int j = lane + 32 * i;
-          if (j < nrows) {
-            const size_t off = (size_t)(key0 + j) * rstride;
-            bulk_g2s(rk + j * C::R, kbase + off, C::R, bar + B_RAWFULL + rs);
-            bulk_g2s(rvp + j * C::R, vbase + off, C::R, bar + B_RAWFULL + rs);
-          }
-        }
+        for (int c = 0; c < 4; ++c) rawval[rs * 4 + c] = 16 * c < nrows ? 1 : 0;
+        mbar_arrive_expect_tx(bar + B_RAWFULL + rs, (uint32_t)(2 * C::RAW));
+        tma_load_3d(rk, &P.kv_map[0], 0, h, row0 + key0, bar + B_RAWFULL + rs);
+        tma_load_3d(rk + C::RAW, &P.kv_map[1], 0, h, row0 + key0, bar + B_RAWFULL + rs);
         if (++rs == C::NRAW) {
           rs = 0;
           rphase ^= 1;

@@ -101,11 +101,13 @@ def test_host_validation_statuses(K):
     assert L.kvq_gather(bref(_cache(K)), bref(_paging(K)), 256, 4, 520, 512, 0, None, None) == K.KVQ_ERR_INVALID_ARG
     assert L.kvq_gather(bref(_cache(K)), bref(_paging(K)), 256, 0, None, None, 0, None, None) == K.KVQ_OK
     # dense prefill: a block table is refused, so are a bad head_dim and a group above 8
-    assert L.kvq_prefill_dense_attn(512, 512, 256, 2, 128, bref(_paging(K)), 256, 1, 8, 256, 4, 4, 0.1, 256,
+    assert L.kvq_prefill_dense_attn(512, 512, 256, 64, 2, 128, bref(_paging(K)), 256, 1, 8, 256, 4, 4, 0.1, 256,
                                     None, None) == K.KVQ_ERR_INVALID_ARG
     none = _paging(K)
     none.block_tables = None
-    assert L.kvq_prefill_dense_attn(512, 512, 256, 2, 96, bref(none), 256, 1, 8, 256, 4, 4, 0.1, 256,
+    assert L.kvq_prefill_dense_attn(512, 512, 256, 64, 2, 96, bref(none), 256, 1, 8, 256, 4, 4, 0.1, 256,
                                     None, None) == K.KVQ_ERR_UNSUPPORTED
-    assert L.kvq_prefill_dense_attn(512, 512, 256, 2, 128, bref(none), 256, 1, 18, 256, 4, 4, 0.1, 256,
+    assert L.kvq_prefill_dense_attn(512, 512, 256, 64, 2, 128, bref(none), 256, 1, 18, 256, 4, 4, 0.1, 256,
                                     None, None) == K.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_prefill_dense_attn(512, 512, 256, 0, 2, 128, bref(none), 256, 1, 8, 256, 4, 4, 0.1, 256,
+                                    None, None) == K.KVQ_ERR_INVALID_ARG
