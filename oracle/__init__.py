@@ -88,6 +88,8 @@ def lib():
             L.orc_attention.restype = I
             L.orc_gather.argtypes = [ctypes.POINTER(OrcCache), ctypes.POINTER(OrcPaging), P, I, P, P]
             L.orc_gather.restype = I
+            L.orc_gather_chunk.argtypes = [ctypes.POINTER(OrcCache), ctypes.POINTER(OrcPaging), P, I, P, P, I, P, P, P]
+            L.orc_gather_chunk.restype = I
             L.orc_dense_attention.argtypes = [P, P, I, P, ctypes.POINTER(OrcPaging), I, I, P, I, I, P, I, F, P, I,
                                               P, I]
             L.orc_dense_attention.restype = I
@@ -232,6 +234,25 @@ def gather(cache: Cache, paging: Paging, cu_tokens: np.ndarray):
     v = np.zeros_like(k)
     cs, ps = cache.struct(), paging.struct()
     err = lib().orc_gather(ctypes.byref(cs), ctypes.byref(ps), _ptr(cu), n, _ptr(k), _ptr(v))
+    return k, v, err
+
+
+def gather_chunk(cache: Cache, paging: Paging, cu_tokens: np.ndarray, k_chunk: np.ndarray, v_chunk: np.ndarray,
+                 cu_chunk: np.ndarray):
+    """gather() with the last m_b positions of each sequence taken from the
+    full-precision chunk rows k_chunk / v_chunk (fp32 values or bf16 bits),
+    sequence b's at rows cu_chunk[b] ..; returns (k, v, error bits)."""
+    cu = np.ascontiguousarray(cu_tokens, dtype=np.int32)
+    cc = np.ascontiguousarray(cu_chunk, dtype=np.int32)
+    kk, dt = _input(k_chunk)
+    vv, dt2 = _input(v_chunk)
+    assert dt == dt2
+    n = int(cu[-1])
+    k = np.zeros((n, cache.num_kv_heads, cache.head_dim), dtype=np.float64)
+    v = np.zeros_like(k)
+    cs, ps = cache.struct(), paging.struct()
+    err = lib().orc_gather_chunk(ctypes.byref(cs), ctypes.byref(ps), _ptr(cu), n, _ptr(kk), _ptr(vv), dt, _ptr(cc),
+                                 _ptr(k), _ptr(v))
     return k, v, err
 
 

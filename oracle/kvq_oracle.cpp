@@ -560,8 +560,25 @@ int32_t orc_write(const OrcCache* c, const OrcPaging* pg, const void* k, const v
 // each; a -1 table entry gives a zero row; a row that cannot be located
 // (too many tokens for the sequence, a position past the table row, a block
 // id past the pool) gives a zero row and an ERR_* bit.
+int32_t orc_gather_chunk(const OrcCache* c, const OrcPaging* pg, const int32_t* cu, int32_t num_tokens,
+                         const void* k_chunk, const void* v_chunk, int32_t chunk_dtype, const int32_t* cu_chunk,
+                         double* k_out, double* v_out);
+
 int32_t orc_gather(const OrcCache* c, const OrcPaging* pg, const int32_t* cu, int32_t num_tokens, double* k_out,
                    double* v_out) {
+  return orc_gather_chunk(c, pg, cu, num_tokens, nullptr, nullptr, DT_F32, nullptr, k_out, v_out);
+}
+
+// The same gather where the current chunk comes in full precision (the Ascend
+// INT8 plugin's 运行机制 and FastDeploy PR #5173 attend to the chunk being
+// written; this variant takes its K / V as given, not as stored): positions
+// seq_lens[b] - m_b .. seq_lens[b] - 1, m_b = cu_chunk[b+1] - cu_chunk[b], are
+// read from rows cu_chunk[b] .. of k_chunk / v_chunk [rows][Hkv][D] (fp32 or
+// bf16 bits, the layout kvq_write reads), the earlier ones from the cache.
+// NULL k_chunk gives the plain gather.
+int32_t orc_gather_chunk(const OrcCache* c, const OrcPaging* pg, const int32_t* cu, int32_t num_tokens,
+                         const void* k_chunk, const void* v_chunk, int32_t chunk_dtype, const int32_t* cu_chunk,
+                         double* k_out, double* v_out) {
   const int D = c->head_dim, Hkv = c->num_kv_heads, bs = c->block_size, mode = c->mode;
   const int R = row_bytes(mode, D);
   int32_t err = 0;
@@ -574,10 +591,24 @@ int32_t orc_gather(const OrcCache* c, const OrcPaging* pg, const int32_t* cu, in
       err |= ERR_SEQ_LEN;
       continue;
     }
+    const int m = k_chunk ? cu_chunk[b + 1] - cu_chunk[b] : 0;
+    if (m < 0 || m > L) {
+      err |= ERR_SEQ_LEN;
+      continue;
+    }
     for (int i = 0; i < n; ++i) {
       const int t = cu[b] + i;
       const int p = L - n + i;
       for (int h = 0; h < Hkv; ++h) {
+        if (p >= L - m) {  // the current chunk, as given
+          const size_t src = ((size_t)(cu_chunk[b] + p - (L - m)) * Hkv + h) * D;
+          const size_t o = ((size_t)t * Hkv + h) * D;
+          for (int d = 0; d < D; ++d) {
+            k_out[o + d] = widen(k_chunk, chunk_dtype, src + d);
+            v_out[o + d] = widen(v_chunk, chunk_dtype, src + d);
+          }
+          continue;
+        }
         const int lb = p / bs;
         if (lb >= pg->max_blocks) {
           err |= ERR_TABLE_RANGE;

@@ -786,3 +786,30 @@ def test_dense_attention_equals_paged_attention_on_exact_rows():
     # a cu_kv that disagrees with seq_lens is refused
     _, err = oracle.dense_attention(kb, vb, np.array([0, 39, 63], np.int32), _dense_paging(L), q, scale, cu_q)
     assert err == 4
+
+
+def test_gather_with_full_precision_chunk():
+    """The chunk positions come back exactly as given (fp32 and bf16 rows);
+    the earlier positions as the plain gather gives them; a chunk longer than
+    its sequence is flagged."""
+    rng = np.random.default_rng(87)
+    D, bs, Hkv = 64, 16, 2
+    L, m = np.array([40, 23], np.int32), np.array([10, 23], np.int32)
+    signs = np.where(rng.integers(0, 2, D) == 1, 1, -1).astype(np.int8)
+    c = oracle.Cache(INT4, 9, Hkv, bs, D, signs)
+    pg = oracle.Paging(np.array([[6, 2, 3], [0, 8, 5]], np.int32), False, L)
+    x = rng.standard_normal((63, Hkv, D)).astype(np.float32)
+    assert oracle.write(c, pg, x, -x, np.array([0, 40, 63], np.int32)) == 0
+    chunk = rng.standard_normal((int(m.sum()), Hkv, D)).astype(np.float32)
+    cu_chunk = np.array([0, 10, 33], np.int32)
+    cu_all = np.array([0, 40, 63], np.int32)
+    for ck in (chunk, gen.f32_to_bf16_bits(chunk)):
+        k, v, err = oracle.gather_chunk(c, pg, cu_all, ck, ck, cu_chunk)
+        assert err == 0
+        want = chunk if ck.dtype == np.float32 else gen.bf16_bits_to_f32(ck)
+        assert np.array_equal(k[30:40], want[0:10].astype(np.float64))
+        assert np.array_equal(v[40:63], want[10:33].astype(np.float64))
+        kp, vp, _ = oracle.gather(c, pg, cu_all)
+        assert np.array_equal(k[:30], kp[:30]) and np.array_equal(v[:30], vp[:30])
+    _, _, err = oracle.gather_chunk(c, pg, cu_all, chunk, chunk, np.array([0, 10, 40], np.int32))
+    assert err == 4
