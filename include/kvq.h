@@ -218,6 +218,23 @@ kvq_status kvq_gather(const kvq_cache* cache, const kvq_paging* paging, const in
                       int32_t num_tokens, void* k_out, void* v_out, int32_t out_dtype, int32_t* dev_error,
                       void* stream);
 
+/* kvq_gather_chunk -- kvq_gather where the current chunk comes in full
+ * precision: the gather for a prefill that attends to the chunk's own K / V
+ * as given rather than as stored.
+ * k_chunk, v_chunk : [rows][num_kv_heads][head_dim] of chunk_dtype (KVQ_F32 or
+ *                    KVQ_BF16), 16-byte aligned: the rows kvq_write was given.
+ * cu_chunk         : int32 [batch + 1]: sequence b's chunk is rows cu_chunk[b] ..
+ *                    cu_chunk[b+1]-1, its positions the last m_b = cu_chunk[b+1] -
+ *                    cu_chunk[b] of the sequence (kvq_write's cu_new_tokens map).
+ * Positions before the chunk are gathered from the cache as kvq_gather does;
+ * chunk positions are copied (fp32 or bf16 out) without the RHT or any
+ * quantisation.  m_b < 0 or m_b > seq_lens[b] sets KVQ_DEVERR_SEQ_LEN and gives
+ * zero rows.  NULL k_chunk (with v_chunk and cu_chunk NULL) is kvq_gather. */
+kvq_status kvq_gather_chunk(const kvq_cache* cache, const kvq_paging* paging, const int32_t* cu_tokens,
+                            int32_t num_tokens, const void* k_chunk, const void* v_chunk, int32_t chunk_dtype,
+                            const int32_t* cu_chunk, void* k_out, void* v_out, int32_t out_dtype,
+                            int32_t* dev_error, void* stream);
+
 /* Workspace needed by kvq_decode_attn for `num_splits` (0 = the library's
  * choice).  Writes the byte count to *bytes (host) and the split count that
  * kvq_decode_attn will use to *splits_used (host, nullable). */

@@ -59,6 +59,8 @@ _lib.kvq_write.argtypes = [_CP, _PP, _P, _P, _I, _P, _I, _P, _P]
 _lib.kvq_write.restype = _I
 _lib.kvq_gather.argtypes = [_CP, _PP, _P, _I, _P, _P, _I, _P, _P]
 _lib.kvq_gather.restype = _I
+_lib.kvq_gather_chunk.argtypes = [_CP, _PP, _P, _I, _P, _P, _I, _P, _P, _P, _I, _P, _P]
+_lib.kvq_gather_chunk.restype = _I
 _lib.kvq_decode_workspace_size.argtypes = [_CP, _PP, _I, _I, ctypes.POINTER(ctypes.c_size_t),
                                            ctypes.POINTER(ctypes.c_int32)]
 _lib.kvq_decode_workspace_size.restype = _I
@@ -191,9 +193,13 @@ def kvq_write(cache: PagedCache, paging: Paging, k: torch.Tensor, v: torch.Tenso
 
 def kvq_gather(cache: PagedCache, paging: Paging, cu_tokens: torch.Tensor, num_tokens: int,
                out_dtype: torch.dtype = torch.float32, k_out: Optional[torch.Tensor] = None,
-               v_out: Optional[torch.Tensor] = None, dev_error: Optional[torch.Tensor] = None, stream=None):
+               v_out: Optional[torch.Tensor] = None, dev_error: Optional[torch.Tensor] = None, stream=None,
+               k_chunk: Optional[torch.Tensor] = None, v_chunk: Optional[torch.Tensor] = None,
+               cu_chunk: Optional[torch.Tensor] = None):
     """Dense dequantised (k, v) [num_tokens, num_kv_heads, head_dim] of the
-    positions cu_tokens names (kvq_write's position map); -1 rows are zeros."""
+    positions cu_tokens names (kvq_write's position map); -1 rows are zeros.
+    With k_chunk / v_chunk / cu_chunk (kvq_gather_chunk) the last positions
+    of each sequence come from those full-precision rows instead."""
     shape = (num_tokens, cache.num_kv_heads, cache.head_dim)
     dev = cache.k_pages.device
     if k_out is None:
@@ -203,9 +209,19 @@ def kvq_gather(cache: PagedCache, paging: Paging, cu_tokens: torch.Tensor, num_t
     if k_out.dtype != v_out.dtype:
         raise ValueError("k_out and v_out must have the same dtype")
     cs, ps = cache.struct(), paging.struct()
-    _check(_lib.kvq_gather(ctypes.byref(cs), ctypes.byref(ps), _dev_ptr(cu_tokens, torch.int32, "cu_tokens"),
-                           int(num_tokens), _dev_ptr(k_out, name="k_out"), _dev_ptr(v_out, name="v_out"),
-                           _qdtype(k_out), _dev_ptr(dev_error, torch.int32, "dev_error"), _stream_ptr(stream)))
+    if k_chunk is None:
+        _check(_lib.kvq_gather(ctypes.byref(cs), ctypes.byref(ps), _dev_ptr(cu_tokens, torch.int32, "cu_tokens"),
+                               int(num_tokens), _dev_ptr(k_out, name="k_out"), _dev_ptr(v_out, name="v_out"),
+                               _qdtype(k_out), _dev_ptr(dev_error, torch.int32, "dev_error"), _stream_ptr(stream)))
+    else:
+        if v_chunk is None or k_chunk.dtype != v_chunk.dtype:
+            raise ValueError("k_chunk and v_chunk must be given together, with one dtype")
+        _check(_lib.kvq_gather_chunk(ctypes.byref(cs), ctypes.byref(ps),
+                                     _dev_ptr(cu_tokens, torch.int32, "cu_tokens"), int(num_tokens),
+                                     _dev_ptr(k_chunk, name="k_chunk"), _dev_ptr(v_chunk, name="v_chunk"),
+                                     _qdtype(k_chunk), _dev_ptr(cu_chunk, torch.int32, "cu_chunk"),
+                                     _dev_ptr(k_out, name="k_out"), _dev_ptr(v_out, name="v_out"), _qdtype(k_out),
+                                     _dev_ptr(dev_error, torch.int32, "dev_error"), _stream_ptr(stream)))
     return k_out, v_out
 
 

@@ -223,6 +223,14 @@ kvq_status kvq_write(const kvq_cache* cache, const kvq_paging* paging, const voi
 kvq_status kvq_gather(const kvq_cache* cache, const kvq_paging* paging, const int32_t* cu_tokens,
                       int32_t num_tokens, void* k_out, void* v_out, int32_t out_dtype, int32_t* dev_error,
                       void* stream) {
+  return kvq_gather_chunk(cache, paging, cu_tokens, num_tokens, nullptr, nullptr, KVQ_F32, nullptr, k_out, v_out,
+                          out_dtype, dev_error, stream);
+}
+
+kvq_status kvq_gather_chunk(const kvq_cache* cache, const kvq_paging* paging, const int32_t* cu_tokens,
+                            int32_t num_tokens, const void* k_chunk, const void* v_chunk, int32_t chunk_dtype,
+                            const int32_t* cu_chunk, void* k_out, void* v_out, int32_t out_dtype,
+                            int32_t* dev_error, void* stream) {
   kvq_status st = check_cache(cache);
   if (st != KVQ_OK) return st;
   if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
@@ -232,6 +240,12 @@ kvq_status kvq_gather(const kvq_cache* cache, const kvq_paging* paging, const in
   if (out_dtype != KVQ_F32 && out_dtype != KVQ_BF16)
     return fail(KVQ_ERR_UNSUPPORTED, "out_dtype must be KVQ_F32 or KVQ_BF16");
   if (!aligned(k_out, 16) || !aligned(v_out, 16)) return fail(KVQ_ERR_INVALID_ARG, "k_out / v_out must be 16-byte aligned");
+  if ((k_chunk == nullptr) != (v_chunk == nullptr) || (k_chunk && !cu_chunk))
+    return fail(KVQ_ERR_INVALID_ARG, "k_chunk, v_chunk and cu_chunk go together");
+  if (k_chunk && chunk_dtype != KVQ_F32 && chunk_dtype != KVQ_BF16)
+    return fail(KVQ_ERR_UNSUPPORTED, "chunk_dtype must be KVQ_F32 or KVQ_BF16");
+  if (k_chunk && (!aligned(k_chunk, 16) || !aligned(v_chunk, 16)))
+    return fail(KVQ_ERR_INVALID_ARG, "k_chunk / v_chunk must be 16-byte aligned");
   if ((long long)num_tokens * cache->num_kv_heads * 2 / 8 + 1 > 0x7FFFFFFFLL)
     return fail(KVQ_ERR_UNSUPPORTED, "too many tokens for one call");
   kvq::WriteParams P;
@@ -257,6 +271,10 @@ kvq_status kvq_gather(const kvq_cache* cache, const kvq_paging* paging, const in
   P.out_k = k_out;
   P.out_v = v_out;
   P.out_dtype = out_dtype;
+  P.chunk_k = k_chunk;
+  P.chunk_v = v_chunk;
+  P.cu_chunk = cu_chunk;
+  P.chunk_dtype = chunk_dtype;
   cudaError_t e = kvq::launch_gather(P, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KVQ_OK;

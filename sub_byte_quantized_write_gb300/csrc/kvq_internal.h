@@ -29,6 +29,13 @@ struct WriteParams {
   void* out_k;
   void* out_v;
   int out_dtype;
+  // gather with the current chunk in full precision (NULL chunk_k: plain
+  // gather): sequence b's last cu_chunk[b+1] - cu_chunk[b] positions come
+  // from rows cu_chunk[b] .. of chunk_k / chunk_v [rows][Hkv][D] of chunk_dtype
+  const void* chunk_k;
+  const void* chunk_v;
+  const int32_t* cu_chunk;
+  int chunk_dtype;
 };
 
 // Shared by the decode and prefill kernels.

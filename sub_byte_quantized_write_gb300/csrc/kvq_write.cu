@@ -267,8 +267,9 @@ __global__ void __launch_bounds__(256) int8_quant_kernel(WriteParams P) {
 // instead of one dependent chain per row.
 constexpr int GATHER_TOKENS = 8;
 
-// Byte offset of (token t, kv head h)'s row in a pool, or -1 (evicted or
-// invalid; invalid rows set their error bit).
+// Byte offset of (token t, kv head h)'s row in a pool, -1 (evicted or
+// invalid; invalid rows set their error bit), or -2 - r for row r of the
+// full-precision chunk.
 __device__ __forceinline__ long long gather_row_offset(const WriteParams& P, int t, int h) {
   if (t >= P.num_tokens) return -1;
   int lo = 0, hi = P.batch - 1;  // the last sequence whose first token is <= t
@@ -286,6 +287,14 @@ __device__ __forceinline__ long long gather_row_offset(const WriteParams& P, int
     return -1;
   }
   const int p = L - n + (t - cu_b);
+  if (P.chunk_k) {
+    const int c0 = __ldg(P.cu_chunk + b), m = __ldg(P.cu_chunk + b + 1) - c0;
+    if (m < 0 || m > L) {
+      flag_error(P.dev_error, DEVERR_SEQ_LEN);
+      return -1;
+    }
+    if (p >= L - m) return -2 - (long long)(c0 + p - (L - m));
+  }
   const int lb = p / P.block_size;
   if (lb >= P.max_blocks) {
     flag_error(P.dev_error, DEVERR_TABLE_RANGE);
@@ -357,10 +366,12 @@ __device__ __forceinline__ void gather_store(void* out, size_t o, const float (&
 
 // Dequantise, map back and store the warp's 2 x GATHER_TOKENS rows.  Rows
 // without data arrive as code word 0 and pad 0, which every mode turns into
-// zeros (scale 0, or code 0 for INT8 per channel), so no branch is needed.
+// zeros (scale 0, or code 0 for INT8 per channel), so no branch is needed;
+// full-precision chunk rows (off <= -2, warp-uniform) are copied as given.
 template <int MODE, int D, bool STEGO, bool BF16>
 __device__ __forceinline__ void gather_rows(const WriteParams& P, const uint32_t (&w)[2][GATHER_TOKENS],
-                                            const uint32_t (&pad)[2][GATHER_TOKENS], long long t0, int h, int lane,
+                                            const uint32_t (&pad)[2][GATHER_TOKENS],
+                                            const long long (&off)[GATHER_TOKENS], long long t0, int h, int lane,
                                             const float (&tsign)[D / 32]) {
   constexpr int EPL = D / 32;
 #pragma unroll
@@ -368,7 +379,13 @@ __device__ __forceinline__ void gather_rows(const WriteParams& P, const uint32_t
 #pragma unroll
     for (int r = 0; r < GATHER_TOKENS; ++r) {
       float y[EPL];
-      gather_dequant<MODE, D, STEGO>(P, w[kv][r], pad[kv][r], kv, h, lane, tsign, y);
+      if (off[r] <= -2) {
+        const long long src = -2 - off[r];
+        load_row_elems<EPL>(kv ? P.chunk_v : P.chunk_k, P.chunk_dtype,
+                            ((size_t)src * P.num_kv_heads + h) * D + lane * EPL, y);
+      } else {
+        gather_dequant<MODE, D, STEGO>(P, w[kv][r], pad[kv][r], kv, h, lane, tsign, y);
+      }
       const long long t = t0 + r;
       if (t < P.num_tokens) gather_store<D, BF16>(kv ? P.out_v : P.out_k, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, y);
     }
@@ -413,8 +430,8 @@ __global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
     }
   }
   // 3. dequantise, inverse RHT, store
-  if (P.out_dtype == DT_BF16) gather_rows<MODE, D, STEGO, true>(P, w, pad, t0, h, lane, tsign);
-  else gather_rows<MODE, D, STEGO, false>(P, w, pad, t0, h, lane, tsign);
+  if (P.out_dtype == DT_BF16) gather_rows<MODE, D, STEGO, true>(P, w, pad, off, t0, h, lane, tsign);
+  else gather_rows<MODE, D, STEGO, false>(P, w, pad, off, t0, h, lane, tsign);
 }
 
 template <int MODE, bool STEGO>

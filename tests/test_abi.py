@@ -33,7 +33,8 @@ def K():
 
 def test_header_declares_the_three_calls():
     names = _declared_functions()
-    for n in ("kvq_write", "kvq_decode_attn", "kvq_prefill_attn", "kvq_gather", "kvq_prefill_dense_attn",
+    for n in ("kvq_write", "kvq_decode_attn", "kvq_prefill_attn", "kvq_gather", "kvq_gather_chunk",
+              "kvq_prefill_dense_attn",
               "kvq_decode_workspace_size", "kvq_row_bytes"):
         assert n in names
 
@@ -100,6 +101,11 @@ def test_host_validation_statuses(K):
     assert L.kvq_gather(bref(_cache(K)), bref(_paging(K)), 256, 4, 512, 512, 7, None, None) == K.KVQ_ERR_UNSUPPORTED
     assert L.kvq_gather(bref(_cache(K)), bref(_paging(K)), 256, 4, 520, 512, 0, None, None) == K.KVQ_ERR_INVALID_ARG
     assert L.kvq_gather(bref(_cache(K)), bref(_paging(K)), 256, 0, None, None, 0, None, None) == K.KVQ_OK
+    # gather with a chunk: k_chunk without v_chunk, and a bad chunk dtype
+    assert L.kvq_gather_chunk(bref(_cache(K)), bref(_paging(K)), 256, 4, 512, None, 0, 256, 512, 512, 0,
+                              None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_gather_chunk(bref(_cache(K)), bref(_paging(K)), 256, 4, 512, 512, 5, 256, 512, 512, 0,
+                              None, None) == K.KVQ_ERR_UNSUPPORTED
     # dense prefill: a block table is refused, so are a bad head_dim and a group above 8
     assert L.kvq_prefill_dense_attn(512, 512, 256, 64, 2, 128, bref(_paging(K)), 256, 1, 8, 256, 4, 4, 0.1, 256,
                                     None, None) == K.KVQ_ERR_INVALID_ARG

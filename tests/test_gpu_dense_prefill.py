@@ -155,3 +155,48 @@ def test_gather_then_dense_prefill_full_size_sampled():
                                      1.0 / math.sqrt(wl.head_dim), cu_q, rows=rows)
     assert oerr == 0
     assert max_err(out.cpu().numpy()[rows], o) <= ATOL
+
+
+@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT8_TOKEN_HEAD])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gather_full_precision_chunk_then_dense_prefill(mode, out_dtype):
+    """The prefill variant that attends to the current chunk as given: the
+    prefix gathered from the cache, the chunk's rows taken from the write's
+    own inputs (kvq_gather_chunk), then the dense prefill; the oracle does
+    the same on its own."""
+    K = kvq()
+    wl = gen.custom(mode, 8, 2, 128, 16, "bf16", seq_lens=[300, 150], n_new=[200, 150], step="prefill",
+                    seed=23 + mode, outlier_frac=0.02)
+    c = build_case(wl)
+    write_step(c)
+    cu_all = wl.cu(wl.seq_lens)
+    cu_new = wl.cu(wl.n_new)
+    kc, vc = to_dev_input(c.k_new, wl.dtype), to_dev_input(c.v_new, wl.dtype)
+    gk, gv = K.kvq_gather(c.gcache, c.gpag, torch.from_numpy(cu_all).cuda(), int(cu_all[-1]), out_dtype=out_dtype,
+                          dev_error=c.dev_err, k_chunk=kc, v_chunk=vc, cu_chunk=torch.from_numpy(cu_new).cuda())
+    torch.cuda.synchronize()
+    assert int(c.dev_err.cpu()[0]) == 0
+    ok_, ov, err = oracle.gather_chunk(c.ocache, c.opag, cu_all, to_orc_input(c.k_new, wl.dtype),
+                                       to_orc_input(c.v_new, wl.dtype), cu_new)
+    assert err == 0
+    # the chunk rows are copied exactly; the rest within the gather bound
+    g = gk.float().cpu().numpy().astype(np.float64)
+    for b in range(wl.batch):
+        L, m = int(wl.seq_lens[b]), int(wl.n_new[b])
+        rows = slice(int(cu_all[b]) + L - m, int(cu_all[b + 1]))
+        assert np.array_equal(g[rows], ok_[rows])
+    bound = 2.0 ** -22 * 128 * np.abs(ok_).max(axis=-1, keepdims=True) + (np.abs(ok_) * 2.0 ** -8 if out_dtype == torch.bfloat16 else 0)
+    assert np.all(np.abs(g - ok_) <= bound)
+    if out_dtype != torch.bfloat16:
+        return
+    q = gen.q_values_host(wl)
+    out = K.kvq_prefill_dense_attn(gk, gv, torch.from_numpy(cu_all).cuda(), torch.from_numpy(wl.seq_lens).cuda(),
+                                   to_dev_input(q, wl.dtype), torch.from_numpy(cu_new).cuda(), int(wl.n_new.max()),
+                                   1.0 / math.sqrt(wl.head_dim), dev_error=c.dev_err)
+    torch.cuda.synchronize()
+    kb = gen.f32_to_bf16_bits(ok_.astype(np.float32))
+    vb = gen.f32_to_bf16_bits(ov.astype(np.float32))
+    o, oerr = oracle.dense_attention(kb, vb, cu_all, _dense_paging_orc(wl.seq_lens), to_orc_input(q, wl.dtype),
+                                     1.0 / math.sqrt(wl.head_dim), cu_new)
+    assert oerr == 0
+    assert max_err(out.cpu().numpy(), o) <= ATOL
