@@ -270,6 +270,7 @@ constexpr int GATHER_TOKENS = 8;
 // Byte offset of (token t, kv head h)'s row in a pool, -1 (evicted or
 // invalid; invalid rows set their error bit), or -2 - r for row r of the
 // full-precision chunk.
+template <bool CHUNK>
 __device__ __forceinline__ long long gather_row_offset(const WriteParams& P, int t, int h) {
   if (t >= P.num_tokens) return -1;
   int lo = 0, hi = P.batch - 1;  // the last sequence whose first token is <= t
@@ -287,7 +288,7 @@ __device__ __forceinline__ long long gather_row_offset(const WriteParams& P, int
     return -1;
   }
   const int p = L - n + (t - cu_b);
-  if (P.chunk_k) {
+  if constexpr (CHUNK) {
     const int c0 = __ldg(P.cu_chunk + b), m = __ldg(P.cu_chunk + b + 1) - c0;
     if (m < 0 || m > L) {
       flag_error(P.dev_error, DEVERR_SEQ_LEN);
@@ -368,7 +369,7 @@ __device__ __forceinline__ void gather_store(void* out, size_t o, const float (&
 // without data arrive as code word 0 and pad 0, which every mode turns into
 // zeros (scale 0, or code 0 for INT8 per channel), so no branch is needed;
 // full-precision chunk rows (off <= -2, warp-uniform) are copied as given.
-template <int MODE, int D, bool STEGO, bool BF16>
+template <int MODE, int D, bool STEGO, bool BF16, bool CHUNK>
 __device__ __forceinline__ void gather_rows(const WriteParams& P, const uint32_t (&w)[2][GATHER_TOKENS],
                                             const uint32_t (&pad)[2][GATHER_TOKENS],
                                             const long long (&off)[GATHER_TOKENS], long long t0, int h, int lane,
@@ -379,7 +380,7 @@ __device__ __forceinline__ void gather_rows(const WriteParams& P, const uint32_t
 #pragma unroll
     for (int r = 0; r < GATHER_TOKENS; ++r) {
       float y[EPL];
-      if (off[r] <= -2) {
+      if (CHUNK && off[r] <= -2) {
         const long long src = -2 - off[r];
         load_row_elems<EPL>(kv ? P.chunk_v : P.chunk_k, P.chunk_dtype,
                             ((size_t)src * P.num_kv_heads + h) * D + lane * EPL, y);
@@ -391,7 +392,7 @@ __device__ __forceinline__ void gather_rows(const WriteParams& P, const uint32_t
     }
 }
 
-template <int MODE, int D, bool STEGO>
+template <int MODE, int D, bool STEGO, bool CHUNK>
 __global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
   constexpr int EPL = D / 32;
   constexpr int BITS = mode_bits(MODE);
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
   if (t0 >= P.num_tokens) return;
   // 1. lanes 0..7 locate one token each
   long long my_off = -1;
-  if (lane < GATHER_TOKENS) my_off = gather_row_offset(P, (int)(t0 + lane), h);
+  if (lane < GATHER_TOKENS) my_off = gather_row_offset<CHUNK>(P, (int)(t0 + lane), h);
   long long off[GATHER_TOKENS];
 #pragma unroll
   for (int r = 0; r < GATHER_TOKENS; ++r) off[r] = __shfl_sync(0xffffffffu, my_off, r);
@@ -430,14 +431,21 @@ __global__ void __launch_bounds__(256) gather_kernel(WriteParams P) {
     }
   }
   // 3. dequantise, inverse RHT, store
-  if (P.out_dtype == DT_BF16) gather_rows<MODE, D, STEGO, true>(P, w, pad, off, t0, h, lane, tsign);
-  else gather_rows<MODE, D, STEGO, false>(P, w, pad, off, t0, h, lane, tsign);
+  if (P.out_dtype == DT_BF16) gather_rows<MODE, D, STEGO, true, CHUNK>(P, w, pad, off, t0, h, lane, tsign);
+  else gather_rows<MODE, D, STEGO, false, CHUNK>(P, w, pad, off, t0, h, lane, tsign);
 }
 
 template <int MODE, bool STEGO>
 void launch_gather_m(const WriteParams& P, int blocks, cudaStream_t stream) {
-  if (P.head_dim == 128) gather_kernel<MODE, 128, STEGO><<<blocks, 256, 0, stream>>>(P);
-  else gather_kernel<MODE, 64, STEGO><<<blocks, 256, 0, stream>>>(P);
+  // the full-precision chunk is a separate instantiation, so the plain
+  // gather pays nothing for it
+  if (P.chunk_k) {
+    if (P.head_dim == 128) gather_kernel<MODE, 128, STEGO, true><<<blocks, 256, 0, stream>>>(P);
+    else gather_kernel<MODE, 64, STEGO, true><<<blocks, 256, 0, stream>>>(P);
+  } else {
+    if (P.head_dim == 128) gather_kernel<MODE, 128, STEGO, false><<<blocks, 256, 0, stream>>>(P);
+    else gather_kernel<MODE, 64, STEGO, false><<<blocks, 256, 0, stream>>>(P);
+  }
 }
 
 cudaError_t launch_gather(const WriteParams& P, cudaStream_t stream) {
