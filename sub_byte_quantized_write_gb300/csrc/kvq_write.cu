@@ -92,26 +92,15 @@ __device__ __forceinline__ uint32_t gather_word(uint32_t bits, int lane) {
   return v;
 }
 
+// Rotate, quantise, pack and store one row (x: the lane's D/32 elements) at
+// dst; every step is one IEEE operation in a fixed order, so the bytes match
+// any other evaluation in that order.
 template <int MODE, int D, bool STEGO>
-__global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
+__device__ __forceinline__ void quantise_store_row(const WriteParams& P, float (&x)[D / 32], uint8_t* dst, int lane) {
   constexpr int EPL = D / 32;
   constexpr int BITS = mode_bits(MODE);
   constexpr int LEVELS = (1 << BITS) - 1;
   constexpr int DATA = data_bytes(MODE, D);
-  const int lane = threadIdx.x & 31;
-  // a decode call after this write may start its query preparation now; it
-  // waits for this grid before anything reads the pages written here
-  allow_dependent_launch();
-  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int kv = (int)(wid & 1);
-  const long long th = wid >> 1;
-  const int h = (int)(th % P.num_kv_heads);
-  const long long t = th / P.num_kv_heads;
-  if (t >= P.num_tokens) return;
-  float x[EPL];  // issued before the (dependent) table lookups
-  load_row_elems<EPL>(kv ? P.v : P.k, P.dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, x);
-  uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h, lane);
-  if (dst == nullptr) return;  // warp-uniform
   if (P.signs) {
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
@@ -189,6 +178,27 @@ __global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
   constexpr int LPW = 32 / NBITS;
   if (lane % LPW == 0) *reinterpret_cast<uint32_t*>(dst + 4 * (lane / LPW)) = word;
   if (lane == 0) *reinterpret_cast<uint32_t*>(dst + DATA) = pad;
+}
+
+
+template <int MODE, int D, bool STEGO>
+__global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
+  constexpr int EPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  // a decode call after this write may start its query preparation now; it
+  // waits for this grid before anything reads the pages written here
+  allow_dependent_launch();
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int kv = (int)(wid & 1);
+  const long long th = wid >> 1;
+  const int h = (int)(th % P.num_kv_heads);
+  const long long t = th / P.num_kv_heads;
+  if (t >= P.num_tokens) return;
+  float x[EPL];  // issued before the (dependent) table lookups
+  load_row_elems<EPL>(kv ? P.v : P.k, P.dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, x);
+  uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h, lane);
+  if (dst == nullptr) return;  // warp-uniform
+  quantise_store_row<MODE, D, STEGO>(P, x, dst, lane);
 }
 
 // INT8, pass 1 (only while *ready == 0): per-channel max |x| over all tokens.
@@ -465,6 +475,60 @@ cudaError_t launch_gather(const WriteParams& P, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Long writes (a prefill chunk): one warp per WRITE_TOKENS consecutive tokens
+// of a kv head.  Lanes 0..3 locate one token each (the gather's lookup, which
+// flags the same errors as dest_row), the K and V rows of all four are loaded
+// together, then each row goes through quantise_store_row as in
+// write_token_head_kernel, so the bytes are the same.
+constexpr int WRITE_TOKENS = 4;
+constexpr int WRITE_BATCH_MIN_TOKENS = 512;
+
+template <int MODE, int D, bool STEGO>
+__global__ void __launch_bounds__(256) write_batch_kernel(WriteParams P) {
+  constexpr int EPL = D / 32;
+  const int lane = threadIdx.x & 31;
+  allow_dependent_launch();  // as in write_token_head_kernel
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int h = (int)(wid % P.num_kv_heads);
+  const long long t0 = (wid / P.num_kv_heads) * WRITE_TOKENS;
+  if (t0 >= P.num_tokens) return;
+  float x[2][WRITE_TOKENS][EPL];
+#pragma unroll
+  for (int r = 0; r < WRITE_TOKENS; ++r) {
+    if (t0 + r < P.num_tokens) {  // warp-uniform
+      const size_t e = ((size_t)(t0 + r) * P.num_kv_heads + h) * D + lane * EPL;
+      load_row_elems<EPL>(P.k, P.dtype, e, x[0][r]);
+      load_row_elems<EPL>(P.v, P.dtype, e, x[1][r]);
+    }
+  }
+  long long my_off = -1;
+  if (lane < WRITE_TOKENS) my_off = gather_row_offset<false>(P, (int)(t0 + lane), h);
+  long long off[WRITE_TOKENS];
+#pragma unroll
+  for (int r = 0; r < WRITE_TOKENS; ++r) off[r] = __shfl_sync(0xffffffffu, my_off, r);
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+    for (int r = 0; r < WRITE_TOKENS; ++r)
+      if (off[r] >= 0)  // warp-uniform: -1 is an evicted or invalid row
+        quantise_store_row<MODE, D, STEGO>(P, x[kv][r], (kv ? P.v_pages : P.k_pages) + off[r], lane);
+}
+
+template <int MODE, bool STEGO>
+void launch_write_m(const WriteParams& P, cudaStream_t stream) {
+  if (P.num_tokens >= WRITE_BATCH_MIN_TOKENS) {
+    const long long warps = (long long)((P.num_tokens + WRITE_TOKENS - 1) / WRITE_TOKENS) * P.num_kv_heads;
+    const int blocks = (int)((warps + 7) / 8);
+    if (P.head_dim == 128) write_batch_kernel<MODE, 128, STEGO><<<blocks, 256, 0, stream>>>(P);
+    else write_batch_kernel<MODE, 64, STEGO><<<blocks, 256, 0, stream>>>(P);
+  } else {
+    const long long warps = (long long)P.num_tokens * P.num_kv_heads * 2;
+    const int blocks = (int)((warps + 7) / 8);
+    if (P.head_dim == 128) write_token_head_kernel<MODE, 128, STEGO><<<blocks, 256, 0, stream>>>(P);
+    else write_token_head_kernel<MODE, 64, STEGO><<<blocks, 256, 0, stream>>>(P);
+  }
+}
+
 cudaError_t launch_write(const WriteParams& P, cudaStream_t stream) {
   const long long warps = (long long)P.num_tokens * P.num_kv_heads * 2;
   const int blocks = (int)((warps + 7) / 8);
@@ -476,22 +540,11 @@ cudaError_t launch_write(const WriteParams& P, cudaStream_t stream) {
     else int8_quant_kernel<64><<<blocks, 256, 0, stream>>>(P);
     return cudaGetLastError();
   }
-  if (P.mode == MODE_I8T) {
-    if (P.head_dim == 128) write_token_head_kernel<MODE_I8T, 128, false><<<blocks, 256, 0, stream>>>(P);
-    else write_token_head_kernel<MODE_I8T, 64, false><<<blocks, 256, 0, stream>>>(P);
-  } else if (P.mode == MODE_F8T) {
-    if (P.head_dim == 128) write_token_head_kernel<MODE_F8T, 128, false><<<blocks, 256, 0, stream>>>(P);
-    else write_token_head_kernel<MODE_F8T, 64, false><<<blocks, 256, 0, stream>>>(P);
-  } else if (P.mode == MODE_INT4 && P.stego) {
-    if (P.head_dim == 128) write_token_head_kernel<MODE_INT4, 128, true><<<blocks, 256, 0, stream>>>(P);
-    else write_token_head_kernel<MODE_INT4, 64, true><<<blocks, 256, 0, stream>>>(P);
-  } else if (P.mode == MODE_INT4) {
-    if (P.head_dim == 128) write_token_head_kernel<MODE_INT4, 128, false><<<blocks, 256, 0, stream>>>(P);
-    else write_token_head_kernel<MODE_INT4, 64, false><<<blocks, 256, 0, stream>>>(P);
-  } else {
-    if (P.head_dim == 128) write_token_head_kernel<MODE_INT2, 128, false><<<blocks, 256, 0, stream>>>(P);
-    else write_token_head_kernel<MODE_INT2, 64, false><<<blocks, 256, 0, stream>>>(P);
-  }
+  if (P.mode == MODE_I8T) launch_write_m<MODE_I8T, false>(P, stream);
+  else if (P.mode == MODE_F8T) launch_write_m<MODE_F8T, false>(P, stream);
+  else if (P.mode == MODE_INT4 && P.stego) launch_write_m<MODE_INT4, true>(P, stream);
+  else if (P.mode == MODE_INT4) launch_write_m<MODE_INT4, false>(P, stream);
+  else launch_write_m<MODE_INT2, false>(P, stream);
   return cudaGetLastError();
 }
 

@@ -95,3 +95,18 @@ def test_write_flags_bad_block_ids():
     K.kvq_write(g, pag2, x, x, torch.tensor([0, 3], dtype=torch.int32, device="cuda"), dev_error=err)
     torch.cuda.synchronize()
     assert int(err.item()) & K.KVQ_DEVERR_SEQ_LEN
+
+
+@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT4_STEGO, gen.MODE_INT8_TOKEN_HEAD,
+                                  gen.MODE_FP8_TOKEN_HEAD])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_write_long_chunk_bit_exact(mode, D, dtype):
+    """Writes of 512 tokens or more take the batched kernel (four tokens per
+    warp); a ragged count, a one-token sequence and evicted head-wise pages."""
+    wl = gen.custom(mode, 4, 2, D, 16, dtype, seq_lens=[700, 300, 5], n_new=[650, 3, 1], headwise=True,
+                    window=[0, 64], sink=4, evict_outside_window=True, seed=31 + mode + D)
+    assert int(wl.n_new.sum()) >= 512 and int(wl.n_new.sum()) % 4 != 0 and (wl.table == -1).any()
+    c = build_case(wl)
+    write_step(c)
+    assert_pools_equal(c)
