@@ -110,3 +110,89 @@ def test_write_long_chunk_bit_exact(mode, D, dtype):
     c = build_case(wl)
     write_step(c)
     assert_pools_equal(c)
+
+
+def _write_rows_both_sides(mode, x, signs=None, bs=16):
+    """Write the rows x [T, D] (one kv head, one sequence, fp32) through the
+    library and through the oracle; return both K pools after asserting they
+    are equal byte for byte (V gets -x)."""
+    import torch
+    import oracle
+    from harness import kvq, to_dev_input
+    K = kvq()
+    T, D = x.shape
+    nb = (T + bs - 1) // bs
+    table = np.arange(nb, dtype=np.int32)[None, :]
+    lens = np.array([T], np.int32)
+    g = K.PagedCache(mode, nb, 1, bs, D, None if signs is None else torch.from_numpy(signs).cuda())
+    g.k_pages.fill_(0xA5)
+    g.v_pages.fill_(0xA5)
+    o = oracle.Cache(mode, nb, 1, bs, D, signs, 0xA5)
+    pag = K.Paging(torch.from_numpy(lens).cuda(), block_tables=torch.from_numpy(table).cuda())
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    xk = np.ascontiguousarray(x[:, None, :], np.float32)
+    xv = np.ascontiguousarray(-x[:, None, :], np.float32)
+    K.kvq_write(g, pag, to_dev_input(xk, "f32"), to_dev_input(xv, "f32"),
+                torch.tensor([0, T], dtype=torch.int32, device="cuda"), dev_error=err)
+    assert oracle.write(o, oracle.Paging(table, False, lens), xk, xv, np.array([0, T], np.int32)) == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    gk, gv = g.k_pages.cpu().numpy(), g.v_pages.cpu().numpy()
+    assert np.array_equal(gk, o.k) and np.array_equal(gv, o.v)
+    if mode == gen.MODE_INT8:
+        assert np.array_equal(g.ch_amax.cpu().numpy(), o.amax)
+    return gk[:, 0].reshape(nb * bs, -1)[:T]
+
+
+@pytest.mark.parametrize("bits,D,rht", [(4, 64, False), (4, 128, True), (2, 64, False), (2, 128, True)])
+def test_write_ties_round_half_to_even_asymmetric(bits, D, rht):
+    """Elements at M + (k + 1/2) S get the even code on the GPU as in the
+    oracle (hand-worked codes in tests/tie_rows.py), RHT off and on."""
+    import oracle
+    import tie_rows
+    mode = gen.MODE_INT4 if bits == 4 else gen.MODE_INT2
+    y, codes = tie_rows.asym_row(bits, D)
+    signs = None
+    x = y
+    if rht:
+        rng = np.random.default_rng(71 + D)
+        signs = np.where(rng.integers(0, 2, D) == 1, 1, -1).astype(np.int8)
+        x = tie_rows.pre_rotate(y, signs)
+    rows = _write_rows_both_sides(mode, np.stack([x, x[::-1].copy()]), signs)
+    data = D * bits // 8
+    assert np.array_equal(oracle.unpack_codes(mode, rows[0, :data], D), codes)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_write_ties_round_half_to_even_stego(D):
+    import oracle
+    import tie_rows
+    x, codes = tie_rows.stego_row(D)
+    rows = _write_rows_both_sides(gen.MODE_INT4_STEGO, x[None, :])
+    assert rows[0, D // 2:D // 2 + 4].tolist() == tie_rows.STEGO_PAD
+    assert np.array_equal(oracle.unpack_codes(gen.MODE_INT4_STEGO, rows[0, :D // 2], D), codes)
+
+
+def test_write_ties_round_half_to_even_int8_channel():
+    import tie_rows
+    D = 64
+    x, codes = tie_rows.int8_channel_tokens(D)
+    rows = _write_rows_both_sides(gen.MODE_INT8, x)
+    assert np.array_equal(rows.view(np.int8).astype(np.int64), codes)
+
+
+def test_write_ties_round_half_to_even_byte_token_head():
+    """The 8-bit token-head rows whose scale is exactly 1: INT8 ties 0.5, 1.5,
+    2.5, -2.5 and E4M3 ties 17 and 19 (spacing 2 in [16, 32))."""
+    D = 64
+    x = np.zeros((2, D), np.float32)
+    x[0, :8] = [127, -63.5, 0.5, 1.5, 2.5, -2.5, -127, 3.0]
+    x[1, :8] = [127, -0.5, -1.5, 63.5, 64.5, 4.5, 5.5, 6.5]
+    rows = _write_rows_both_sides(gen.MODE_INT8_TOKEN_HEAD, x)
+    assert rows[0, :8].view(np.int8).tolist() == [127, -64, 0, 2, 2, -2, -127, 3]
+    assert rows[1, :8].view(np.int8).tolist() == [127, 0, -2, 64, 64, 4, 6, 6]
+    assert rows[0, D:].tolist() == [0x00, 0x00, 0x80, 0x3F]
+    x = np.zeros((1, D), np.float32)
+    x[0, :10] = [448, 1.0, 0.5, -2.0, 17.0, 19.0, 2.0 ** -9, 3 * 2.0 ** -10, -0.0, -448]
+    rows = _write_rows_both_sides(gen.MODE_FP8_TOKEN_HEAD, x)
+    assert rows[0, :10].tolist() == [0x7E, 0x38, 0x30, 0xC0, 0x58, 0x5A, 0x01, 0x02, 0x80, 0xFE]

@@ -17,6 +17,7 @@ import torch
 
 import oracle
 import kvq_inputs as gen
+import tie_rows
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 INT4, INT2, INT8 = oracle.MODE_INT4, oracle.MODE_INT2, oracle.MODE_INT8
@@ -170,6 +171,57 @@ def test_worked_grid_row_is_exact(mode, D):
     S, M = f16_of_pad(row, data)
     assert (S, M) == (s, m)
     assert np.array_equal(oracle.dequant_row(mode, row, D), x.astype(np.float64))
+
+
+@pytest.mark.parametrize("mode,D", [(INT4, 64), (INT4, 128), (INT2, 64), (INT2, 128)])
+@pytest.mark.parametrize("rht", [False, True])
+def test_ties_round_half_to_even_asymmetric(mode, D, rht):
+    """Elements at M + (k + 1/2) S take the even code (tests/tie_rows.py);
+    with the RHT on, the input is the exact pre-image of the same row."""
+    y, codes = tie_rows.asym_row(4 if mode == INT4 else 2, D)
+    signs = None
+    x = y
+    if rht:
+        rng = np.random.default_rng(61 + D)
+        signs = np.where(rng.integers(0, 2, D) == 1, 1, -1).astype(np.int8)
+        x = tie_rows.pre_rotate(y, signs)
+        assert np.array_equal(oracle.rht_forward(x, signs), y)
+    row = oracle.quant_row(mode, x, signs)
+    data = D // 2 if mode == INT4 else D // 4
+    assert f16_of_pad(row, data) == (tie_rows.S_ASYM, tie_rows.M_ASYM)
+    assert np.array_equal(oracle.unpack_codes(mode, row[:data], D), codes)
+    if mode == INT4:
+        assert row[:4].tolist() == [0xF0, 0x20, 0x42, 0x64]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_ties_round_half_to_even_stego(D):
+    """Codes at t = k + 1/2 and a zero point at -lo / s = 2.5 both go to the
+    even neighbour: zp = 2, pad 0x3E000002."""
+    x, codes = tie_rows.stego_row(D)
+    row = oracle.quant_row(STEGO, x, None)
+    assert row[D // 2:D // 2 + 4].tolist() == tie_rows.STEGO_PAD
+    assert stego_pad(row, D) == (tie_rows.S_STEGO, tie_rows.STEGO_ZP)
+    assert np.array_equal(oracle.unpack_codes(STEGO, row[:D // 2], D), codes)
+    assert row[:3].tolist() == [0xE0, 0x20, 0x42]
+
+
+def test_ties_round_half_to_even_int8_channel():
+    """Channel scales 2^(c % 7 - 3) fixed by an exact amax token; every later
+    token sits at (j + 1/2) s_c and takes the even neighbour."""
+    D = 64
+    x, codes = tie_rows.int8_channel_tokens(D)
+    T = x.shape[0]
+    assert codes[:6, 0].tolist() == tie_rows.INT8_FIRST_CODES
+    assert codes[-4:, 0].tolist() == tie_rows.INT8_LAST_CODES
+    c, pg = _single_seq_paging(16, 16, T, INT8, D)
+    assert oracle.write(c, pg, x[:, None, :], -x[:, None, :], np.array([0, T], np.int32)) == 0
+    s = tie_rows.int8_channel_scales(D)
+    assert np.array_equal(c.amax[0, 0], (127 * s).astype(np.float32))
+    got_k = np.concatenate([c.k[blk, 0] for blk in range(16)])[:T].view(np.int8).astype(np.int64)
+    got_v = np.concatenate([c.v[blk, 0] for blk in range(16)])[:T].view(np.int8).astype(np.int64)
+    assert np.array_equal(got_k, codes)
+    assert np.array_equal(got_v, -codes)      # rne is odd-symmetric: -t takes -rne(t)
 
 
 @pytest.mark.parametrize("mode", [INT4, INT2])
