@@ -120,6 +120,16 @@ kvq_status check_q(const kvq_cache* c, const void* q, int32_t dtype, int32_t hq,
   return KVQ_OK;
 }
 
+// The prefill launch's grid (query tiles, kv heads, sequences) must fit the
+// launch limits: x < 2^31, y and z <= 65535.
+kvq_status check_prefill_grid(const kvq::AttnParams& P) {
+  if (kvq::prefill_grid_x(P.max_q_per_seq, P.group) > 0x7FFFFFFFLL)
+    return fail(KVQ_ERR_UNSUPPORTED, "max_q_per_seq gives more query tiles than one launch can hold");
+  if (P.num_kv_heads > 65535) return fail(KVQ_ERR_UNSUPPORTED, "num_kv_heads > 65535 for the prefill launch");
+  if (P.batch > 65535) return fail(KVQ_ERR_UNSUPPORTED, "batch > 65535");
+  return KVQ_OK;
+}
+
 kvq::DecodeLayout decode_layout(const kvq_cache* c, const kvq_paging* p, int32_t num_q_heads) {
   const int group = num_q_heads / c->num_kv_heads;
   return kvq::decode_ws_layout(p->batch, c->num_kv_heads, group, c->head_dim, sm_count(),
@@ -355,8 +365,7 @@ kvq_status kvq_prefill_attn(const kvq_cache* cache, const kvq_paging* paging, co
   P.cu_q = cu_q;
   P.total_q = total_q;
   P.max_q_per_seq = max_q_per_seq;
-  const int qb = 64 / P.group;
-  if ((max_q_per_seq + qb - 1) / qb > 0x7FFFFFFF) return fail(KVQ_ERR_UNSUPPORTED, "too many queries");
+  if ((st = check_prefill_grid(P)) != KVQ_OK) return st;
   cudaError_t e = kvq::launch_prefill(P, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KVQ_OK;
@@ -445,6 +454,7 @@ kvq_status kvq_prefill_dense_attn(const void* k, const void* v, const int32_t* c
   P.total_q = total_q;
   P.max_q_per_seq = max_q_per_seq;
   P.cu_kv = cu_kv;
+  if (const kvq_status gs = check_prefill_grid(P); gs != KVQ_OK) return gs;
   if (!dense_rows_map(&P.kv_map[0], k, num_kv_rows, num_kv_heads, head_dim) ||
       !dense_rows_map(&P.kv_map[1], v, num_kv_rows, num_kv_heads, head_dim))
     return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled failed for the dense K / V rows");

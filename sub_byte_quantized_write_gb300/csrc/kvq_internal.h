@@ -115,4 +115,14 @@ cudaError_t launch_gather(const WriteParams& P, cudaStream_t stream);
 cudaError_t launch_decode(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const AttnParams& P, cudaStream_t stream);
 
+// The prefill grid: x = query tiles of the longest chunk (PREFILL_ROWS_PER_CTA
+// (query, q head) rows per CTA), y = kv heads, z = sequences.  Computed in 64
+// bits so that no max_q_per_seq can wrap it; the host checks it against the
+// launch limits before any launch.
+constexpr int PREFILL_ROWS_PER_CTA = 128;
+inline long long prefill_grid_x(int max_q_per_seq, int group) {
+  const long long qb = PREFILL_ROWS_PER_CTA / group;
+  return ((long long)max_q_per_seq + qb - 1) / qb;
+}
+
 }  // namespace kvq

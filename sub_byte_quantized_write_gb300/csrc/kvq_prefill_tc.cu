@@ -42,7 +42,7 @@ namespace kvq {
 
 namespace {
 
-constexpr int TP_ROWS = 128;
+constexpr int TP_ROWS = PREFILL_ROWS_PER_CTA;
 constexpr int TP_KT = 64;
 constexpr int TP_THREADS = 448;
 constexpr int TP_SOFTMAX = 256;    // warps 0-7: warp w owns rows 32 (w % 4) .. + 31, keys 32 (w / 4) .. + 31 of a tile
@@ -929,7 +929,7 @@ cudaError_t launch_prefill_tc_t(const AttnParams& P, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int QB = TP_ROWS / P.group;
-  dim3 grid((P.max_q_per_seq + QB - 1) / QB, P.num_kv_heads, P.batch);  // TP_THREADS threads each
+  dim3 grid((unsigned)prefill_grid_x(P.max_q_per_seq, P.group), P.num_kv_heads, P.batch);  // TP_THREADS threads each
   prefill_tc_kernel<MODE, D><<<grid, TP_THREADS, C::SMEM, stream>>>(P);
   return cudaGetLastError();
 }

@@ -145,19 +145,21 @@ def decode_oracle(c: Case, q32: np.ndarray, rows=None):
     return out
 
 
-def prefill_gpu(c: Case, q32: np.ndarray):
+def prefill_gpu(c: Case, q32: np.ndarray, scale: Optional[float] = None):
     K = kvq()
     wl = c.wl
     cu = torch.from_numpy(wl.cu(wl.n_new)).to("cuda")
+    scale = 1.0 / math.sqrt(wl.head_dim) if scale is None else scale
     out = K.kvq_prefill_attn(c.gcache, c.gpag, to_dev_input(q32, wl.dtype), cu, int(wl.n_new.max()),
-                             1.0 / math.sqrt(wl.head_dim), dev_error=c.dev_err)
+                             scale, dev_error=c.dev_err)
     torch.cuda.synchronize()
     return out.cpu().numpy()
 
 
-def prefill_oracle(c: Case, q32: np.ndarray, rows=None):
+def prefill_oracle(c: Case, q32: np.ndarray, rows=None, scale: Optional[float] = None):
     wl = c.wl
-    out, err = oracle.attention(c.ocache, c.opag, to_orc_input(q32, wl.dtype), 1.0 / math.sqrt(wl.head_dim),
+    scale = 1.0 / math.sqrt(wl.head_dim) if scale is None else scale
+    out, err = oracle.attention(c.ocache, c.opag, to_orc_input(q32, wl.dtype), scale,
                                 cu_q=wl.cu(wl.n_new), rows=rows)
     assert err == 0
     return out

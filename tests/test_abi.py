@@ -117,3 +117,21 @@ def test_host_validation_statuses(K):
                                     None, None) == K.KVQ_ERR_UNSUPPORTED
     assert L.kvq_prefill_dense_attn(512, 512, 256, 0, 2, 128, bref(none), 256, 1, 8, 256, 4, 4, 0.1, 256,
                                     None, None) == K.KVQ_ERR_INVALID_ARG
+
+
+def test_prefill_grid_limits_are_checked_on_the_host(K):
+    """The prefill grid is (query tiles, kv heads, sequences): a kv-head count
+    beyond the launch's y limit is refused before any launch, and the
+    query-tile count is computed in 64 bits (INT32_MAX queries per sequence
+    neither wraps nor reaches a launch here, because the kv-head check
+    fails first)."""
+    L = K.lib()
+    bref = ctypes.byref
+    big = _cache(K, num_kv_heads=70000)
+    assert L.kvq_prefill_attn(bref(big), bref(_paging(K)), 256, 1, 70000, 256, 4, 0x7FFFFFFF, 0.1, 256,
+                              None, None) == K.KVQ_ERR_UNSUPPORTED
+    assert b"num_kv_heads" in L.kvq_last_error()
+    none = _paging(K)
+    none.block_tables = None
+    assert L.kvq_prefill_dense_attn(512, 512, 256, 64, 70000, 128, bref(none), 256, 1, 70000, 256, 4, 4, 0.1, 256,
+                                    None, None) == K.KVQ_ERR_UNSUPPORTED

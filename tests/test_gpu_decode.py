@@ -253,3 +253,53 @@ def test_decode_full_size_llama_other_rows_sampled(mode):
     8192, 200k-block pool) in the other row formats: INT4 with the zero point
     in the scale, INT8 and FP8 with one scale per token-head."""
     _full_size_sampled(gen.llama_int4(0, mode=mode), [0, 33, 63])
+
+
+@pytest.mark.parametrize("group", [1, 4])
+def test_decode_int4_d64_bs64(group):
+    """INT4 decode at head_dim 64 / block_size 64: the Llama-like layer at the
+    benchmark's reduced shape (group 4), and one kv head per q head."""
+    if group == 4:
+        wl = gen.llama_int4(0, head_dim=64, block_size=64, batch=6, ctx_lo=100, ctx_hi=2100, num_blocks=4000)
+    else:
+        wl = gen.custom(gen.MODE_INT4, 4, 4, 64, 64, "bf16", seq_lens=[1, 63, 64, 65, 1500], n_new=[1] * 5,
+                        seed=19)
+    _run(wl)
+
+
+def test_decode_full_size_llama_d64_bs64_sampled():
+    """The head_dim 64 / block_size 64 decode workload exactly as benchmarked
+    (64 sequences, contexts up to 8192, 50k-block pool)."""
+    _full_size_sampled(gen.llama_int4(0, num_blocks=50000, head_dim=64, block_size=64), [0, 33, 63])
+
+
+@pytest.mark.parametrize("mode", [gen.MODE_INT4, gen.MODE_INT2, gen.MODE_INT8_TOKEN_HEAD])
+def test_decode_flags_bad_block_id_and_short_table(mode):
+    """Device-side contract violations on the decode path: a table entry past
+    the pool is skipped and sets KVQ_DEVERR_BLOCK_RANGE; a seq_len past
+    max_blocks * block_size drops the keys beyond the table and sets
+    KVQ_DEVERR_TABLE_RANGE.  The oracle skips the same keys and reports the
+    same bits; the outputs agree within the usual bound."""
+    K = kvq()
+    wl = gen.custom(mode, 8, 2, 128, 16, "bf16", seq_lens=[700, 300, 50], n_new=[1, 1, 1], seed=23 + mode)
+    c = build_case(wl)
+    write_step(c)
+    q = q_host(wl)
+    scale = 1.0 / math.sqrt(wl.head_dim)
+    bad = wl.table.copy()
+    bad[0, 5] = wl.num_blocks + 1
+    bad[1, 0] = 1 << 30
+    short = np.ascontiguousarray(wl.table[:, :wl.table.shape[1] - 3])
+    for table, bit in ((bad, K.KVQ_DEVERR_BLOCK_RANGE), (short, K.KVQ_DEVERR_TABLE_RANGE)):
+        for splits in (0, 7):
+            err = torch.zeros(1, dtype=torch.int32, device="cuda")
+            pag = K.Paging(torch.from_numpy(wl.seq_lens).cuda(), block_tables=torch.from_numpy(table).cuda())
+            g = K.kvq_decode_attn(c.gcache, pag, to_dev_input(q, wl.dtype), scale, num_splits=splits,
+                                  dev_error=err)
+            torch.cuda.synchronize()
+            o, oerr = oracle.attention(c.ocache, oracle.Paging(table, False, wl.seq_lens), to_orc_input(q, wl.dtype),
+                                       scale)
+            assert oerr == bit and int(err.item()) == bit
+            g = g.cpu().numpy()
+            assert np.all(np.isfinite(g))
+            assert max_err(g, o) <= ATOL

@@ -139,3 +139,32 @@ def test_gather_full_size_llama_sampled():
     gv = torch.cat([v[int(cu[b]):int(cu[b + 1])] for b in sample]).float().cpu().numpy().astype(np.float64)
     _assert_close(gk, ok_, True)
     _assert_close(gv, ov, True)
+
+
+def test_gather_flags_bad_block_id_and_short_table():
+    """A table entry past the pool and a position past max_blocks * block_size
+    give zero rows and KVQ_DEVERR_BLOCK_RANGE / KVQ_DEVERR_TABLE_RANGE, as in
+    the oracle; every other row is gathered as usual."""
+    K = kvq()
+    wl = gen.custom(gen.MODE_INT4, 4, 2, 64, 16, "f32", seq_lens=[100, 60], n_new=[100, 60], seed=13)
+    c = build_case(wl)
+    write_step(c)
+    cu = wl.cu(wl.seq_lens)
+    for kind, table, bit in (("block", None, K.KVQ_DEVERR_BLOCK_RANGE), ("short", None, K.KVQ_DEVERR_TABLE_RANGE)):
+        if kind == "block":
+            table = wl.table.copy()
+            table[1, 2] = wl.num_blocks + 3
+        else:
+            table = np.ascontiguousarray(wl.table[:, :wl.table.shape[1] - 2])
+        pag = K.Paging(torch.from_numpy(wl.seq_lens).cuda(), block_tables=torch.from_numpy(table).cuda())
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        k, v = K.kvq_gather(c.gcache, pag, torch.from_numpy(cu).cuda(), int(cu[-1]), dev_error=err)
+        torch.cuda.synchronize()
+        ok_, ov, oerr = oracle.gather(c.ocache, oracle.Paging(table, False, wl.seq_lens), cu)
+        assert oerr == bit and int(err.item()) == bit
+        gk = k.cpu().numpy().astype(np.float64)
+        gv = v.cpu().numpy().astype(np.float64)
+        zero = np.all(ok_ == 0.0, axis=(1, 2))
+        assert zero.sum() >= 16 and np.all(gk[zero] == 0.0) and np.all(gv[zero] == 0.0)
+        _assert_close(gk, ok_, False)
+        _assert_close(gv, ov, False)

@@ -18,11 +18,11 @@ from harness import ATOL, build_case, kvq, q_host, to_dev_input, write_step
 pytestmark = pytest.mark.gpu
 
 
-def _noalloc_via_c_abi(K, cache, paging, q, scale, out):
+def _noalloc_via_c_abi(K, cache, paging, q, scale, out, num_splits=0):
     cs, ps = cache.struct(), paging.struct()
     st = K.lib().kvq_decode_attn_noalloc(ctypes.byref(cs), ctypes.byref(ps), q.data_ptr(), K.KVQ_BF16
                                          if q.dtype == torch.bfloat16 else K.KVQ_F32, q.shape[1],
-                                         ctypes.c_float(scale), out.data_ptr(), 0, None,
+                                         ctypes.c_float(scale), out.data_ptr(), num_splits, None,
                                          torch.cuda.current_stream().cuda_stream)
     return st
 
@@ -51,6 +51,25 @@ def test_noalloc_decode_matches_workspace_decode_twice():
     assert _noalloc_via_c_abi(K, c2.gcache, c2.gpag, q2, scale, out2) == K.KVQ_OK
     torch.cuda.synchronize()
     assert float((out2 - ref2).abs().max()) <= ATOL
+
+
+def test_noalloc_forced_split_count_matches_workspace_decode():
+    """A forced split count (num_splits > 0) takes the same clamping and the
+    same partial-record layout in the static scratch as in a caller
+    workspace: two calls in a row against kvq_decode_attn with that count."""
+    K = kvq()
+    wl = gen.custom(gen.MODE_INT4, 16, 4, 128, 16, "bf16", seq_lens=[3000, 2000, 17], n_new=[1, 1, 1], seed=4)
+    c = build_case(wl)
+    write_step(c)
+    q = to_dev_input(q_host(wl), wl.dtype)
+    scale = 1.0 / math.sqrt(wl.head_dim)
+    for splits in (4, 4, 50):
+        ref = K.kvq_decode_attn(c.gcache, c.gpag, q, scale, num_splits=splits)
+        out = torch.full_like(ref, float("nan"))
+        assert _noalloc_via_c_abi(K, c.gcache, c.gpag, q, scale, out, num_splits=splits) == K.KVQ_OK
+        torch.cuda.synchronize()
+        assert torch.isfinite(out).all()
+        assert float((out - ref).abs().max()) <= ATOL
 
 
 def test_noalloc_rejects_oversized_calls():
