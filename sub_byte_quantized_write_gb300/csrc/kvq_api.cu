@@ -304,6 +304,15 @@ kvq_status kvq_decode_workspace_size(const kvq_cache* cache, const kvq_paging* p
   return KVQ_OK;
 }
 
+}  // extern "C"
+
+namespace {
+bool page_chunk_map(CUtensorMap* map, const void* pages, int num_blocks, int Hkv, int block_size, int row_bytes,
+                    int chunk_rows);
+}
+
+extern "C" {
+
 kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, const void* q, int32_t dtype,
                            int32_t num_q_heads, float softmax_scale, float* out, void* workspace,
                            size_t workspace_bytes, int32_t num_splits, int32_t* dev_error, void* stream) {
@@ -318,6 +327,15 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, con
   if (!workspace || workspace_bytes < L.total) return fail(KVQ_ERR_WORKSPACE, "workspace missing or too small");
   if (!aligned(workspace, 256)) return fail(KVQ_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   kvq::AttnParams P = attn_params(cache, paging, q, dtype, num_q_heads, softmax_scale, out, dev_error);
+  const int rpc = kvq::decode_chunk_rows(P.mode, P.head_dim, P.group);
+  if (rpc > 0) {  // the stream kernel's tensor copies: one map per pool
+    const int R = kvq_row_bytes(cache->mode, cache->head_dim);
+    if ((long long)cache->num_blocks * cache->num_kv_heads * (cache->block_size / rpc) > 0x7FFFFFFFLL)
+      return fail(KVQ_ERR_UNSUPPORTED, "pool too large for 32-bit chunk coordinates");
+    if (!page_chunk_map(&P.kv_map[0], cache->k_pages, cache->num_blocks, cache->num_kv_heads, cache->block_size, R, rpc) ||
+        !page_chunk_map(&P.kv_map[1], cache->v_pages, cache->num_blocks, cache->num_kv_heads, cache->block_size, R, rpc))
+      return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K / V pools");
+  }
   uint8_t* w = static_cast<uint8_t*>(workspace);
   kvq::DecodeWs ws;
   ws.tile_start = reinterpret_cast<int*>(w + L.off_tile_start);
@@ -400,6 +418,25 @@ bool dense_rows_map(CUtensorMap* map, const void* base, int64_t rows, int Hkv, i
   const cuuint32_t box[3] = {(cuuint32_t)D, 1, 64};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The K or V pool as a 2-D tensor of page chunks for the decode's gathers:
+// row (block * Hkv + head) * (block_size / chunk_rows) + chunk holds key rows
+// chunk * chunk_rows .. of that page, chunk_rows * row_bytes bytes (a
+// multiple of 16, at most 2048) read as 8-byte elements, one row per box.
+bool page_chunk_map(CUtensorMap* map, const void* pages, int num_blocks, int Hkv, int block_size, int row_bytes,
+                    int chunk_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t chunk = (cuuint64_t)chunk_rows * row_bytes;
+  if (chunk % 16 != 0 || chunk > 2048) return false;
+  const cuuint64_t dims[2] = {chunk / 8, (cuuint64_t)num_blocks * Hkv * (block_size / chunk_rows)};
+  const cuuint64_t strides[1] = {chunk};
+  const cuuint32_t box[2] = {(cuuint32_t)(chunk / 8), 1};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(pages), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

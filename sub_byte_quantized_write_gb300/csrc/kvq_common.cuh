@@ -272,6 +272,20 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int c0, 
       : "memory");
 }
 
+// Gather of four rows of a 2-D tensor map (`tile::gather4`): rows r0..r3
+// (each one box row of the map's width) land back to back at `dst`;
+// completion counted on `bar`.  Only lanes with `pred` set issue it.  Every
+// row coordinate passed here must lie inside the tensor.
+__device__ __forceinline__ void tma_gather4_if(bool pred, void* dst, const void* map, int r0, int r1, int r2, int r3,
+                                               uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %7, 0;\n\t"
+      "@p cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {0, %2, %3, %4, %5}], [%6];\n\t}\n" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_addr(bar)), "r"((int)pred)
+      : "memory");
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while its predecessor runs; it must call
 // grid_dependency_wait() before touching anything the predecessor writes.
@@ -301,5 +315,6 @@ __device__ __forceinline__ void pad_scale_zero(uint32_t pad, bool stego, float& 
   }
 }
 __device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ void sts128(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 }  // namespace kvq

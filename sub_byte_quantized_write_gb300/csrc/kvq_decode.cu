@@ -281,6 +281,39 @@ struct StreamCfg {
   static constexpr int STAGE = 2 * TILE;                   // K tile then V tile
 };
 
+template <int MODE, int D, int NT>
+struct TmaCfg {
+  static constexpr int R = row_bytes_of(MODE, D);
+  static constexpr bool BYTES = byte_token_head(MODE);
+  static constexpr int KT = (NT == 1 && !BYTES) ? 64 : 32;   // keys per tile
+  static constexpr int NH2 = KT / 32;                         // 32-key halves per tile
+  static constexpr int RPC = KT / 4;                          // key rows per gathered chunk
+  static constexpr int RPC_LOG2 = RPC == 16 ? 4 : 3;
+  static constexpr int TILE = KT * R;
+  static constexpr int TILE_AL = (TILE + 127) / 128 * 128;
+  static constexpr int STAGE = 2 * TILE_AL;                   // K tile then V tile
+  static constexpr int NSTAGE = STAGE >= 8000 ? 2 : (STAGE >= 4000 ? 3 : 4);
+  static constexpr int CTAS = NT == 1 ? 3 : 2;
+  static constexpr int XREG = 576;                            // exchange bytes per (half, n-tile)
+  static constexpr bool XSMEM = NH2 * NT * XREG <= TILE;
+  static_assert(RPC * R <= 2048 && (RPC * R) % 16 == 0, "a chunk must be one tensor-map box row");
+};
+
+// Rows per gathered chunk for the host's tensor maps (0: cp.async path).
+int decode_chunk_rows(int mode, int head_dim, int group) {
+  (void)head_dim;
+  if (mode == MODE_INT8) return 0;
+  const bool bytes = byte_token_head(mode);
+  return (group <= 4 && !bytes) ? 16 : 8;
+}
+
+// Keys per tile of the stream kernel that runs a configuration (the prefix
+// sum of tile counts and the slices must use the same tiles).
+template <int MODE, int D, int NT>
+__host__ __device__ constexpr int decode_tile_keys() {
+  return MODE == MODE_INT8 ? StreamCfg<MODE, D, NT>::KT : TmaCfg<MODE, D, NT>::KT;
+}
+
 // ---------------------------------------------------------------------------
 // 1. preparation
 
@@ -314,7 +347,7 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
 #pragma unroll
       for (int k = 0; k < ITEMS; ++k) {
         const int bh = first + k;
-        n[k] = bh < BH ? tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0, StreamCfg<MODE, D, NT>::KT).n_virt : 0;
+        n[k] = bh < BH ? tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0, decode_tile_keys<MODE, D, NT>()).n_virt : 0;
         tsum += n[k];
       }
       int incl = tsum;
@@ -923,6 +956,498 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
 }
 
 // ---------------------------------------------------------------------------
+// 2b. stream kernel over tensor-copied tiles (INT4 / INT2 rows, also with the
+// zero point in the scale, and INT8 / FP8 token-head rows)
+//
+// Same work split, records and arithmetic as decode_stream_kernel, with the
+// per-tile overheads taken out of the steady-state loop:
+//  * a tile's K (or V) rows arrive by ONE `tile::gather4` tensor copy: the
+//    pool is viewed as a 2-D tensor whose rows are page chunks of KT/4 key
+//    rows, so the four chunks of a tile (from up to four pages) are four row
+//    coordinates of one copy.  The four table lookups run on lanes 0-3.  A
+//    chunk with no data (a -1 entry, past the sequence) is pointed at a
+//    chunk that exists and is masked: no coordinate outside the pool is ever
+//    formed, and no -1 entry becomes an address.
+//  * tiles whose keys are all visible take a body without any mask.
+//  * the logit of key j is s_j (beta q''.c_j + kappa) + gamma m_j, with
+//    kappa = 2^(b-1) gamma - beta (key fold) per head (z = m + 2^(b-1) s).
+//  * the (P s) hi / lo weights move from the score layout to the P.V operand
+//    layout through shared memory (the consumed K tile), two 16-byte stores
+//    and four 8-byte loads per lane, bank-conflict free.
+
+template <int MODE, int D, int NT, bool STEGO>
+__global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
+    decode_tma_kernel(const __grid_constant__ AttnParams P, DecodeWs ws) {
+  using C = DecCfg<MODE, D>;
+  using TC = TmaCfg<MODE, D, NT>;
+  constexpr int NSTAGE = TC::NSTAGE, KT = TC::KT, NH2 = TC::NH2, R = TC::R;
+  constexpr int NH = 4 * NT;
+  constexpr int PER_LANE = NT * C::KSTEPS * 2;
+  constexpr uint32_t VMASK = 0xFu;  // four chunks per tile
+  constexpr float HR = (float)(1 << (mode_bits(MODE) - 1));
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int G = P.group, Hkv = P.num_kv_heads, bs = P.block_size;
+  const int BH = P.batch * Hkv;
+
+  allow_dependent_launch();  // the merge kernel may launch; it waits for this grid to finish
+  __shared__ int run_start[129];
+  const int items = (BH + 127) / 128;
+  {
+    const int first = threadIdx.x * items;
+    int tsum = 0;
+    for (int k = 0; k < items && first + k < BH; ++k) {
+      const int bh = first + k;
+      tsum += tile_list(P, bh / Hkv, bh % Hkv, false, KT).n_virt;
+    }
+    int incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    __shared__ int wtot[DECODE_WARPS];
+    if (lane == 31) wtot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += wtot[w];
+    run_start[threadIdx.x + 1] = before + incl;
+    if (threadIdx.x == 0) run_start[0] = 0;
+    __syncthreads();
+  }
+  const int T = run_start[128];
+  const int nw = stream_workers(T, gridDim.x * DECODE_WARPS, ws.fixed_workers);
+  const int gw = blockIdx.x * DECODE_WARPS + warp;
+  if (gw >= nw) return;  // whole warp; no CTA-wide barrier follows
+  const int lo = slice_lo(gw, T, nw), hi = slice_lo(gw + 1, T, nw);
+  if (lo >= hi) return;
+
+  uint8_t* ring = smem + warp * NSTAGE * TC::STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * NSTAGE * TC::STAGE) + warp * NSTAGE;
+  if (lane == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(bars + i, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  uint32_t phase_bits = 0;  // parity of the next completion to wait for, per stage
+
+  int a = 0, z = 128;
+  while (z - a > 1) {
+    const int mid = (a + z) >> 1;
+    if (run_start[mid] <= lo) a = mid;
+    else z = mid;
+  }
+  int bh0 = a * items, st0 = run_start[a];
+  for (;;) {
+    const int n0 = tile_list(P, bh0 / Hkv, bh0 % Hkv, false, KT).n_virt;
+    if (st0 + n0 > lo) break;
+    st0 += n0;
+    ++bh0;
+  }
+  Seg is;  // lookup / issue cursor
+  load_seg(P, bh0, st0, is, KT);
+  Seg cs = is;  // compute cursor
+
+  const int bs_log2 = __ffs(bs) - 1;
+  const int cpb_log2 = bs_log2 - TC::RPC_LOG2;  // chunks per page (bs >= RPC)
+
+  // The next tile to copy: lane c < 4 holds the tensor row of its chunk c
+  // (-1: no data), all lanes the mask of chunks with data.
+  int x_lookup = lo;
+  int nx_row = -1;
+  uint32_t nx_valid = 0;
+  bool nx_have = false;
+  auto lookup = [&]() {
+    nx_have = x_lookup < hi;
+    if (nx_have) {
+      while (x_lookup >= is.end) load_seg(P, is.bh + 1, is.end, is, KT);
+      const int key = KT * tile_of(is.t, x_lookup - is.start) + TC::RPC * (lane & 3);
+      int row = -1;
+      if (lane < 4 && key < is.t.Leff) {
+        const int e = __ldg(is.tbl + (key >> bs_log2));
+        if (e >= P.num_blocks) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
+        else if (e >= 0) row = ((e * Hkv + is.h) << cpb_log2) + ((key & (bs - 1)) >> TC::RPC_LOG2);
+      }
+      nx_row = row;
+      nx_valid = __ballot_sync(0xffffffffu, row >= 0) & VMASK;
+      ++x_lookup;
+    }
+  };
+
+  int st_issue = 0;
+  uint32_t vq = 0;  // chunk masks of the tiles in flight, oldest in the low bits
+  int vpos = 0;
+  auto issue = [&]() {
+    if (nx_have) {
+      int r0 = __shfl_sync(0xffffffffu, nx_row, 0);
+      int r1 = __shfl_sync(0xffffffffu, nx_row, 1);
+      int r2 = __shfl_sync(0xffffffffu, nx_row, 2);
+      int r3 = __shfl_sync(0xffffffffu, nx_row, 3);
+      // chunks without data copy an existing chunk instead (masked later)
+      const int rf = r0 >= 0 ? r0 : (r1 >= 0 ? r1 : (r2 >= 0 ? r2 : (r3 >= 0 ? r3 : 0)));
+      r0 = r0 >= 0 ? r0 : rf;
+      r1 = r1 >= 0 ? r1 : rf;
+      r2 = r2 >= 0 ? r2 : rf;
+      r3 = r3 >= 0 ? r3 : rf;
+      uint8_t* kt = ring + st_issue * TC::STAGE;
+      const bool l0 = lane == 0;
+      mbar_arrive_expect_tx_if(l0, bars + st_issue, (uint32_t)(2 * TC::TILE));
+      tma_gather4_if(l0, kt, &P.kv_map[0], r0, r1, r2, r3, bars + st_issue);
+      tma_gather4_if(l0, kt + TC::TILE_AL, &P.kv_map[1], r0, r1, r2, r3, bars + st_issue);
+      vq |= nx_valid << vpos;
+      vpos += 4;
+      st_issue = st_issue + 1 == NSTAGE ? 0 : st_issue + 1;
+    }
+    lookup();
+  };
+
+  // per-segment state
+  uint32_t bq[NT][C::KSTEPS][2];
+  float bet[NT], gam[NT], kap[NT];
+  float oacc[NT][C::MT][4];
+  float mrun[NT], lrun[NT], pmrun[NT];
+  int part_id = 0;
+
+  auto begin_seg = [&]() {
+    part_id = gw + cs.bh;  // partial record id: slice index + pair index (unique, see reduce)
+    const uint4* src = reinterpret_cast<const uint4*>(ws.qfrag + ((size_t)cs.bh * 32 + lane) * PER_LANE);
+    uint32_t tmp[PER_LANE];
+#pragma unroll
+    for (int i = 0; i < PER_LANE / 4; ++i) {
+      const uint4 v = __ldg(src + i);
+      tmp[4 * i] = v.x; tmp[4 * i + 1] = v.y; tmp[4 * i + 2] = v.z; tmp[4 * i + 3] = v.w;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int s = 0; s < C::KSTEPS; ++s) {
+        bq[nt][s][0] = tmp[(nt * C::KSTEPS + s) * 2];
+        bq[nt][s][1] = tmp[(nt * C::KSTEPS + s) * 2 + 1];
+      }
+      const float4 bg = __ldg(ws.qbg + (size_t)cs.bh * NH + 4 * nt + tq);
+      bet[nt] = bg.x;
+      gam[nt] = TC::BYTES ? 0.0f : bg.y;
+      kap[nt] = TC::BYTES ? 0.0f : fmaf(-bg.x, bg.z, HR * bg.y);  // 2^(b-1) gamma - beta fold
+      mrun[nt] = -CUDART_INF_F;
+      lrun[nt] = 0.0f;
+      pmrun[nt] = 0.0f;
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) oacc[nt][mt][r] = 0.0f;
+    }
+  };
+
+  auto flush_seg = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float l = lrun[nt], pm = pmrun[nt];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l += __shfl_xor_sync(0xffffffffu, l, o);
+        pm += __shfl_xor_sync(0xffffffffu, pm, o);
+      }
+      const int head = 4 * nt + tq;
+      if (head < G) {
+        float* po = ws.part_o + ((size_t)part_id * G + head) * D;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+          po[gq * (D / 16) + mt] = oacc[nt][mt][0] + oacc[nt][mt][1] + pm;
+          po[(8 + gq) * (D / 16) + mt] = oacc[nt][mt][2] + oacc[nt][mt][3] + pm;
+        }
+        if (gq == 0) ws.part_ml[(size_t)part_id * G + head] = make_float2(mrun[nt], l);
+      }
+    }
+  };
+
+  // per-lane shared-memory offsets (loop invariant): key rows 4gq + 2m + hh,
+  // value rows 8tq + 4m' + 2h' + e; the weight exchange writes this lane's
+  // 16 bytes at xw and reads its operand pair at xr (+ 320 for m' = 1)
+  const int koff = 4 * gq * R + 4 * tq;
+  const int poff = 4 * gq * R + C::DATA;
+  const int vrow = 8 * tq * R;
+  const int xw = 64 * (gq >> 1) + 16 * tq + 320 * (gq & 1);
+  const int xr = 64 * tq + 8 * gq;
+
+  // One tile: S = codes . q'', online softmax, O += codes^T . (P s).
+  auto tile = [&](auto full_c, const uint8_t* kt, const uint8_t* vt, uint32_t cur, int key0, int Leff, int W,
+                  int p_q) {
+    constexpr bool FULL = decltype(full_c)::value;
+    float sacc[NH2][2][NT][4];
+#pragma unroll
+    for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) sacc[h2][m][nt][r] = 0.0f;
+#pragma unroll
+    for (int wi = 0; wi < C::WPL; ++wi) {
+      uint32_t kw[NH2][2][2];
+#pragma unroll
+      for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) kw[h2][m][hh] = lds32(kt + koff + (32 * h2 + 2 * m + hh) * R + 16 * wi);
+      Unroll<C::KPW, MODE>::run([&](auto sig_c) {
+        constexpr int sig = decltype(sig_c)::value;
+        const int s = C::KPW * wi + sig;
+#pragma unroll
+        for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            uint32_t av[4];
+            if constexpr (MODE == MODE_INT4) {
+              av[0] = kpair_int4_fold<2 * sig>(kw[h2][m][0]);
+              av[1] = kpair_int4_fold<2 * sig>(kw[h2][m][1]);
+              av[2] = kpair_int4_fold<2 * sig + 1>(kw[h2][m][0]);
+              av[3] = kpair_int4_fold<2 * sig + 1>(kw[h2][m][1]);
+            } else {
+              av[0] = kpair<MODE, 2 * sig>(kw[h2][m][0]);
+              av[1] = kpair<MODE, 2 * sig>(kw[h2][m][1]);
+              av[2] = kpair<MODE, 2 * sig + 1>(kw[h2][m][0]);
+              av[3] = kpair<MODE, 2 * sig + 1>(kw[h2][m][1]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[h2][m][nt], av, bq[nt][s][0], bq[nt][s][1]);
+          }
+      });
+    }
+
+    // logits (log2 units) and the per-key value scale / zero-point value
+    float lg[NH2][2][2][NT];
+    float sv_[NH2][2][2], zv_[NH2][2][2];
+    bool vk[NH2][2][2];
+#pragma unroll
+    for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          bool ok = true;
+          if constexpr (!FULL) {
+            const int kappa = 32 * h2 + 4 * gq + 2 * m + hh;
+            const int j = key0 + kappa;
+            ok = ((cur >> (kappa / TC::RPC)) & 1) && j < Leff;
+            if (W > 0) ok = ok && (j < P.sink || j > p_q - W);
+          }
+          vk[h2][m][hh] = ok;
+          const uint32_t pk = lds32(kt + poff + (32 * h2 + 2 * m + hh) * R);
+          const uint32_t pv = lds32(vt + poff + (32 * h2 + 2 * m + hh) * R);
+          float sk, mk, zst = 0.0f;
+          if constexpr (TC::BYTES) {
+            sk = __uint_as_float(pk);
+            mk = 0.0f;
+            sv_[h2][m][hh] = __uint_as_float(pv);
+            zv_[h2][m][hh] = 0.0f;
+          } else if constexpr (STEGO) {
+            sk = __uint_as_float(pk & ~15u);
+            mk = 0.0f;
+            zst = (float)(int)(pk & 15u);
+            const float s_v = __uint_as_float(pv & ~15u);
+            sv_[h2][m][hh] = s_v;
+            zv_[h2][m][hh] = s_v * (float)(8 - (int)(pv & 15u));
+          } else {
+            const float2 fk = __half22float2(*reinterpret_cast<const __half2*>(&pk));
+            const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&pv));
+            sk = fk.x;
+            mk = fk.y;
+            sv_[h2][m][hh] = fv.x;
+            zv_[h2][m][hh] = fmaf(HR, fv.x, fv.y);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float cdot = sacc[h2][m][nt][2 * hh] + sacc[h2][m][nt][2 * hh + 1];  // hi + lo slots
+            float zz;
+            if constexpr (TC::BYTES) {
+              zz = sk * (bet[nt] * cdot);
+            } else if constexpr (STEGO) {
+              zz = sk * fmaf(-gam[nt], zst, fmaf(bet[nt], cdot, kap[nt]));
+            } else {
+              zz = fmaf(sk, fmaf(bet[nt], cdot, kap[nt]), gam[nt] * mk);
+            }
+            lg[h2][m][hh][nt] = FULL ? zz : (ok ? zz : -CUDART_INF_F);
+          }
+        }
+
+    uint32_t xh[NH2][NT][2], xl[NH2][NT][2];  // packed (P s) hi / lo per (h2, m): (key hh=0, key hh=1)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float tmax = -CUDART_INF_F;
+#pragma unroll
+      for (int h2 = 0; h2 < NH2; ++h2)
+        tmax = fmaxf(tmax, fmaxf(fmaxf(lg[h2][0][0][nt], lg[h2][0][1][nt]), fmaxf(lg[h2][1][0][nt], lg[h2][1][1][nt])));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+      const float mnew = fmaxf(mrun[nt], tmax);
+      const float muse = mnew == -CUDART_INF_F ? 0.0f : mnew;
+      const float f = ex2(mrun[nt] - muse);
+      mrun[nt] = mnew;
+      if (__any_sync(0xffffffffu, f != 1.0f)) {
+        lrun[nt] *= f;
+        pmrun[nt] *= f;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) oacc[nt][mt][r] *= f;
+      }
+      float tl = 0.0f, tpm = 0.0f;  // tile-local sums, added once per tile
+#pragma unroll
+      for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          float wv[2];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float p = ex2(lg[h2][m][hh][nt] - muse);
+            if constexpr (FULL) {
+              tl += p;
+              if constexpr (!TC::BYTES) tpm = fmaf(p, zv_[h2][m][hh], tpm);
+              wv[hh] = p * sv_[h2][m][hh];
+            } else {
+              // select after the product: a masked row's scale may be any bits
+              const bool ok = vk[h2][m][hh];
+              tl += ok ? p : 0.0f;
+              if constexpr (!TC::BYTES) tpm += ok ? p * zv_[h2][m][hh] : 0.0f;
+              wv[hh] = ok ? p * sv_[h2][m][hh] : 0.0f;
+            }
+          }
+          const __half2 hp = __floats2half2_rn(wv[0], wv[1]);
+          const float2 hf = __half22float2(hp);
+          const __half2 lp = __floats2half2_rn(wv[0] - hf.x, wv[1] - hf.y);
+          xh[h2][nt][m] = *reinterpret_cast<const uint32_t*>(&hp);
+          xl[h2][nt][m] = *reinterpret_cast<const uint32_t*>(&lp);
+        }
+      lrun[nt] += tl;
+      pmrun[nt] += tpm;
+    }
+
+    // the weights in the P.V operand layout: lane (gq, tq) takes, for keys
+    // 8tq + 4m' + {0..3}, slot gq = (head gq/2, hi or lo) from lane (2tq + m', gq/2)
+    uint32_t bw[NH2][2][NT][2];
+    if constexpr (TC::XSMEM) {
+      uint8_t* xb = const_cast<uint8_t*>(kt);  // this stage's K rows are consumed
+      __syncwarp();
+#pragma unroll
+      for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          sts128(xb + (h2 * NT + nt) * TC::XREG + xw,
+                 make_uint4(xh[h2][nt][0], xh[h2][nt][1], xl[h2][nt][0], xl[h2][nt][1]));
+      __syncwarp();
+#pragma unroll
+      for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+        for (int mp = 0; mp < 2; ++mp)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint2 b = lds64(xb + (h2 * NT + nt) * TC::XREG + xr + 320 * mp);
+            bw[h2][mp][nt][0] = b.x;
+            bw[h2][mp][nt][1] = b.y;
+          }
+    } else {
+#pragma unroll
+      for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+        for (int mp = 0; mp < 2; ++mp) {
+          const int src = ((2 * tq + mp) << 2) | (gq >> 1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t a0 = __shfl_sync(0xffffffffu, xh[h2][nt][0], src);
+            const uint32_t b0 = __shfl_sync(0xffffffffu, xl[h2][nt][0], src);
+            const uint32_t a1 = __shfl_sync(0xffffffffu, xh[h2][nt][1], src);
+            const uint32_t b1 = __shfl_sync(0xffffffffu, xl[h2][nt][1], src);
+            bw[h2][mp][nt][0] = (gq & 1) ? b0 : a0;
+            bw[h2][mp][nt][1] = (gq & 1) ? b1 : a1;
+          }
+        }
+    }
+
+    // P.V: O^T (D x slots) += U_V^T (D x 16 keys) . Wslots (16 keys x slots)
+#pragma unroll
+    for (int h2 = 0; h2 < NH2; ++h2)
+#pragma unroll
+      for (int mp = 0; mp < 2; ++mp) {
+        uint2 vl[2][2], vh[2][2];
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint8_t* vr = vt + vrow + (32 * h2 + 4 * mp + 2 * hp + e) * R;
+            vl[hp][e] = load_range<MODE, D>(vr, 0, gq);
+            vh[hp][e] = load_range<MODE, D>(vr, 0, 8 + gq);
+          }
+        if constexpr (MODE == MODE_F8T && !FULL) {  // masked rows may hold stale NaN codes
+#pragma unroll
+          for (int hp = 0; hp < 2; ++hp)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              vl[hp][e] = make_uint2(e4m3x4_no_nan(vl[hp][e].x), e4m3x4_no_nan(vl[hp][e].y));
+              vh[hp][e] = make_uint2(e4m3x4_no_nan(vh[hp][e].x), e4m3x4_no_nan(vh[hp][e].y));
+            }
+        }
+        Unroll<C::MT, MODE>::run([&](auto mt_c) {
+          constexpr int mt = decltype(mt_c)::value;
+          const uint32_t av[4] = {vpair<MODE, mt>(vl[0][0], vl[0][1]), vpair<MODE, mt>(vh[0][0], vh[0][1]),
+                                  vpair<MODE, mt>(vl[1][0], vl[1][1]), vpair<MODE, mt>(vh[1][0], vh[1][1])};
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(oacc[nt][mt], av, bw[h2][mp][nt][0], bw[h2][mp][nt][1]);
+        });
+      }
+  };
+
+  lookup();
+  // Copies wait for the kernels before: the write of this step's tokens may
+  // still run (the preparation kernel starts alongside it), and the query
+  // images and per-head constants must be ready.
+  grid_dependency_wait();
+#pragma unroll 1
+  for (int k = 0; k < NSTAGE - 1; ++k) issue();
+
+  begin_seg();
+  int st = 0;
+  bool timed_out = false;
+#pragma unroll 1
+  for (int x = lo; x < hi; ++x) {
+    if (!mbar_wait_bounded(bars + st, (phase_bits >> st) & 1)) {
+      timed_out = true;
+      break;
+    }
+    phase_bits ^= 1u << st;
+    __syncwarp();
+    issue();
+    if (x >= cs.end) {
+      flush_seg();
+      do load_seg(P, cs.bh + 1, cs.end, cs, KT);
+      while (x >= cs.end);
+      begin_seg();
+    }
+    const uint32_t cur = vq & VMASK;
+    vq >>= 4;
+    vpos -= 4;
+    const uint8_t* kt = ring + st * TC::STAGE;
+    st = st + 1 == NSTAGE ? 0 : st + 1;
+    const int key0 = KT * tile_of(cs.t, x - cs.start);
+    const int Leff = cs.t.Leff, W = cs.t.W, p_q = cs.t.L - 1;
+    const bool full = cur == VMASK && key0 + KT <= Leff && (W <= 0 || key0 > p_q - W || key0 + KT <= P.sink);
+    if (full) tile(std::true_type{}, kt, kt + TC::TILE_AL, cur, key0, Leff, W, p_q);
+    else tile(std::false_type{}, kt, kt + TC::TILE_AL, cur, key0, Leff, W, p_q);
+  }
+  if (timed_out) {
+    // a copy never arrived: report it, give the copies in flight one more
+    // bounded chance to land, and leave without writing this slice's partial
+    if (lane == 0) flag_error(P.dev_error, DEVERR_TIMEOUT);
+    for (int i = 0; i < NSTAGE; ++i) (void)mbar_wait_bounded(bars + i, (phase_bits >> i) & 1);
+    return;
+  }
+  flush_seg();
+}
+
+// ---------------------------------------------------------------------------
 // 3. merge of the partials of one (sequence, q head) + inverse RHT
 
 template <int D>
@@ -1064,11 +1589,11 @@ size_t stream_smem_bytes() {
 template <int NT>
 int ctas_per_sm_nt(int mode) {
   switch (mode) {
-    case MODE_INT4: return StreamCfg<MODE_INT4, 128, NT>::CTAS;
-    case MODE_INT2: return StreamCfg<MODE_INT2, 128, NT>::CTAS;
+    case MODE_INT4: return TmaCfg<MODE_INT4, 128, NT>::CTAS;
+    case MODE_INT2: return TmaCfg<MODE_INT2, 128, NT>::CTAS;
     case MODE_INT8: return StreamCfg<MODE_INT8, 128, NT>::CTAS;
-    case MODE_I8T: return StreamCfg<MODE_I8T, 128, NT>::CTAS;
-    default: return StreamCfg<MODE_F8T, 128, NT>::CTAS;
+    case MODE_I8T: return TmaCfg<MODE_I8T, 128, NT>::CTAS;
+    default: return TmaCfg<MODE_F8T, 128, NT>::CTAS;
   }
 }
 
@@ -1092,9 +1617,12 @@ cudaError_t launch_dependent(Kern kernel, dim3 grid, dim3 block, size_t smem, cu
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int MODE, int D, int NT>
+template <int MODE, int D, int NT, bool STEGO>
 cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream) {
-  const size_t smem = stream_smem_bytes<MODE, D, NT>();
+  constexpr bool TMA = MODE != MODE_INT8;
+  using TC = TmaCfg<MODE, D, NT>;
+  const size_t smem = TMA ? (size_t)DECODE_WARPS * TC::NSTAGE * TC::STAGE + DECODE_WARPS * TC::NSTAGE * 8
+                          : stream_smem_bytes<MODE, D, NT>();
   // the opt-in shared-memory size is set once per device (not inside later
   // calls, which may be captured into a CUDA graph)
   static bool attr_set[64] = {false};
@@ -1102,7 +1630,12 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_stream_kernel<MODE, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if constexpr (TMA)
+      e = cudaFuncSetAttribute(decode_tma_kernel<MODE, D, NT, STEGO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    else
+      e = cudaFuncSetAttribute(decode_stream_kernel<MODE, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
@@ -1113,7 +1646,10 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
   if (e != cudaSuccess) return e;
   // the stream and merge kernels launch programmatically: their CTAs become
   // resident while the previous kernel drains and wait on its completion
-  e = launch_dependent(decode_stream_kernel<MODE, D, NT>, dim3(grid), dim3(128), smem, stream, P, ws);
+  if constexpr (TMA)
+    e = launch_dependent(decode_tma_kernel<MODE, D, NT, STEGO>, dim3(grid), dim3(128), smem, stream, P, ws);
+  else
+    e = launch_dependent(decode_stream_kernel<MODE, D, NT>, dim3(grid), dim3(128), smem, stream, P, ws);
   if (e != cudaSuccess) return e;
   const long long warps = (long long)P.batch * P.num_q_heads;
   return launch_dependent(decode_reduce_kernel<D>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, P, ws);
@@ -1121,8 +1657,14 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
 
 template <int MODE, int D>
 cudaError_t launch_decode_md(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream) {
-  if (P.group <= 4) return launch_decode_t<MODE, D, 1>(P, ws, grid, stream);
-  return launch_decode_t<MODE, D, 2>(P, ws, grid, stream);
+  if constexpr (MODE == MODE_INT4) {
+    if (P.stego) {
+      if (P.group <= 4) return launch_decode_t<MODE, D, 1, true>(P, ws, grid, stream);
+      return launch_decode_t<MODE, D, 2, true>(P, ws, grid, stream);
+    }
+  }
+  if (P.group <= 4) return launch_decode_t<MODE, D, 1, false>(P, ws, grid, stream);
+  return launch_decode_t<MODE, D, 2, false>(P, ws, grid, stream);
 }
 
 cudaError_t launch_decode(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream) {

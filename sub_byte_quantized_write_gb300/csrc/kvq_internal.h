@@ -60,7 +60,9 @@ struct AttnParams {
   const int32_t* cu_q;
   int total_q, max_q_per_seq;
   // dense prefill: sequence b's key j is row cu_kv[b] + j of k_pages / v_pages;
-  // kv_map[0 | 1] view K / V as [rows][Hkv][D] bf16 with a 64-row box of one head
+  // kv_map[0 | 1] view K / V as [rows][Hkv][D] bf16 with a 64-row box of one head.
+  // decode (token-head modes): kv_map[0 | 1] view the K / V pool as 2-D tensors
+  // of page chunks (decode_chunk_rows), one chunk per box row.
   const int32_t* cu_kv;
   CUtensorMap kv_map[2];  // 128-byte aligned by its own declaration
 };
@@ -109,6 +111,11 @@ inline DecodeLayout decode_ws_layout(int batch, int num_kv_heads, int group, int
 }
 
 int decode_ctas_per_sm(int mode, int head_dim, int group);
+// Key rows per page chunk that the decode's tensor copies move (16 or 8), or 0
+// when the configuration copies its pages with cp.async (INT8 per channel).
+// The caller's tensor maps kv_map[0 | 1] view the K / V pool as 2-D tensors
+// of such chunks: row (block * Hkv + head) * (block_size / rows) + chunk.
+int decode_chunk_rows(int mode, int head_dim, int group);
 
 cudaError_t launch_write(const WriteParams& P, cudaStream_t stream);
 cudaError_t launch_gather(const WriteParams& P, cudaStream_t stream);
