@@ -332,13 +332,13 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, con
     const int R = kvq_row_bytes(cache->mode, cache->head_dim);
     if ((long long)cache->num_blocks * cache->num_kv_heads * (cache->block_size / rpc) > 0x7FFFFFFFLL)
       return fail(KVQ_ERR_UNSUPPORTED, "pool too large for 32-bit chunk coordinates");
+    P.chunk_rows_total = cache->num_blocks * cache->num_kv_heads * (cache->block_size / rpc);
     if (!page_chunk_map(&P.kv_map[0], cache->k_pages, cache->num_blocks, cache->num_kv_heads, cache->block_size, R, rpc) ||
         !page_chunk_map(&P.kv_map[1], cache->v_pages, cache->num_blocks, cache->num_kv_heads, cache->block_size, R, rpc))
       return fail(KVQ_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K / V pools");
   }
   uint8_t* w = static_cast<uint8_t*>(workspace);
   kvq::DecodeWs ws;
-  ws.tile_start = reinterpret_cast<int*>(w + L.off_tile_start);
   ws.qfrag = reinterpret_cast<uint32_t*>(w + L.off_qfrag);
   ws.qbg = reinterpret_cast<float4*>(w + L.off_qbg);
   ws.part_ml = reinterpret_cast<float2*>(w + L.off_part_ml);

@@ -299,12 +299,21 @@ struct TmaCfg {
   static_assert(RPC * R <= 2048 && (RPC * R) % 16 == 0, "a chunk must be one tensor-map box row");
 };
 
-// Rows per gathered chunk for the host's tensor maps (0: cp.async path).
+// Rows per gathered chunk for the host's tensor maps (0: cp.async path),
+// taken from the very configuration the launched kernel uses.
+template <int MODE, int D>
+int chunk_rows_md(int group) {
+  return group <= 4 ? TmaCfg<MODE, D, 1>::RPC : TmaCfg<MODE, D, 2>::RPC;
+}
 int decode_chunk_rows(int mode, int head_dim, int group) {
-  (void)head_dim;
-  if (mode == MODE_INT8) return 0;
-  const bool bytes = byte_token_head(mode);
-  return (group <= 4 && !bytes) ? 16 : 8;
+  const bool d128 = head_dim == 128;
+  switch (mode) {
+    case MODE_INT4: return d128 ? chunk_rows_md<MODE_INT4, 128>(group) : chunk_rows_md<MODE_INT4, 64>(group);
+    case MODE_INT2: return d128 ? chunk_rows_md<MODE_INT2, 128>(group) : chunk_rows_md<MODE_INT2, 64>(group);
+    case MODE_I8T: return d128 ? chunk_rows_md<MODE_I8T, 128>(group) : chunk_rows_md<MODE_I8T, 64>(group);
+    case MODE_F8T: return d128 ? chunk_rows_md<MODE_F8T, 128>(group) : chunk_rows_md<MODE_F8T, 64>(group);
+    default: return 0;
+  }
 }
 
 // Keys per tile of the stream kernel that runs a configuration (the prefix
@@ -324,56 +333,8 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
   constexpr int NH = 4 * NT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = P.num_kv_heads, G = P.group, Hq = P.num_q_heads;
-  const int BH = P.batch * Hkv;
   __shared__ __half qh[2][NH][D];
-  __shared__ int wsum[4];
   allow_dependent_launch();  // the stream kernel may launch; it waits for this grid to finish
-
-  // partial records of this call start empty (l = 0)
-  const long long nml = (long long)ws.n_partials * G;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nml; i += (long long)gridDim.x * blockDim.x)
-    ws.part_ml[i] = make_float2(-CUDART_INF_F, 0.0f);
-
-  if (blockIdx.x == 0) {
-    // exclusive prefix sum of the tile counts over (sequence, kv head): each
-    // pass covers 128 x ITEMS pairs, thread t owning ITEMS consecutive ones,
-    // so the pass's seq_lens loads are all in flight together
-    constexpr int ITEMS = 8;
-    int running = 0;
-    for (int base = 0; base < BH; base += 128 * ITEMS) {
-      const int first = base + threadIdx.x * ITEMS;
-      int n[ITEMS];
-      int tsum = 0;
-#pragma unroll
-      for (int k = 0; k < ITEMS; ++k) {
-        const int bh = first + k;
-        n[k] = bh < BH ? tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0, decode_tile_keys<MODE, D, NT>()).n_virt : 0;
-        tsum += n[k];
-      }
-      int incl = tsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (lane == 31) wsum[warp] = incl;
-      __syncthreads();
-      int before = running;
-      for (int w = 0; w < warp; ++w) before += wsum[w];
-      int x = before + incl - tsum;
-#pragma unroll
-      for (int k = 0; k < ITEMS; ++k) {
-        if (first + k < BH) ws.tile_start[first + k] = x;
-        x += n[k];
-      }
-      running += wsum[0] + wsum[1] + wsum[2] + wsum[3];
-      __syncthreads();
-    }
-    if (threadIdx.x == 0) ws.tile_start[BH] = running;
-    grid_dependency_wait();  // see below
-    return;
-  }
-
   // This kernel may start while the write kernel before it still runs
   // (programmatic launch): nothing here reads what the write produces except
   // the INT8 channel scales, so INT8 waits for the write first and the other
@@ -381,11 +342,7 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
   // grid, then also sees the new tokens.
   if (MODE == MODE_INT8) grid_dependency_wait();
   // query fragments of one (sequence, kv head)
-  const int bh = blockIdx.x - 1;
-  if (bh >= BH) {
-    grid_dependency_wait();
-    return;
-  }
+  const int bh = blockIdx.x;
   const int b = bh / Hkv, h = bh % Hkv;
   const float log2e = 1.4426950408889634f;
   const float dnorm = (MODE != MODE_INT8 && P.signs) ? (float)D : 1.0f;
@@ -956,6 +913,124 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
 }
 
 // ---------------------------------------------------------------------------
+// merge helpers (used by the merge kernel)
+
+// Merge records w0 + bh .. w0 + nrec - 1 + bh of q head i of pair bh
+// (log-sum-exp weights), apply the output transform (inverse RHT with the
+// signs tsign, or the INT8 V channel scales) and 1 / l, and store the D
+// outputs at `out`; one warp, element d = lane + 32 e in lane `lane`.
+// Records are read through L2 (they may come from other SMs of this grid).
+template <int D>
+__device__ __forceinline__ void merge_records(const AttnParams& P, const DecodeWs& ws, int bh, int i, int w0,
+                                              int nrec, const float (&tsign)[D / 32], float* out, int lane) {
+  constexpr int EPL = D / 32;
+  const int G = P.group;
+  float o[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
+  // one round trip for the first 32 records' sums and the first four
+  // records' outputs; lane j holds record w0 + j
+  float2 ml0 = make_float2(-CUDART_INF_F, 0.0f);
+  if (lane < nrec) ml0 = __ldcg(ws.part_ml + (size_t)(w0 + lane + bh) * G + i);
+  float v0[4][EPL];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float* po = ws.part_o + ((size_t)(w0 + u + bh) * G + i) * D;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v0[u][e] = u < nrec ? __ldcg(po + lane + 32 * e) : 0.0f;
+  }
+  float M = ml0.y > 0.0f ? ml0.x : -CUDART_INF_F;
+  for (int j = 32 + lane; j < nrec; j += 32) {
+    const float2 ml = __ldcg(ws.part_ml + (size_t)(w0 + j + bh) * G + i);
+    if (ml.y > 0.0f) M = fmaxf(M, ml.x);
+  }
+  M = warp_max(M);
+  if (M == -CUDART_INF_F) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = 0.0f;
+    return;
+  }
+  float l = 0.0f;
+  for (int c0 = 0; c0 < nrec; c0 += 32) {
+    float2 ml = ml0;
+    if (c0 > 0) {
+      ml = make_float2(-CUDART_INF_F, 0.0f);
+      if (c0 + lane < nrec) ml = __ldcg(ws.part_ml + (size_t)(w0 + c0 + lane + bh) * G + i);
+    }
+    const float f = (c0 + lane < nrec && ml.y > 0.0f) ? ex2(ml.x - M) : 0.0f;
+    l += f * ml.y;
+    const int n = min(32, nrec - c0);
+    // four records per round, their loads issued together (the first round's
+    // were issued with the sums above)
+    for (int k0 = 0; k0 < n; k0 += 4) {
+      float fk[4];
+      float v[4][EPL];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        fk[u] = __shfl_sync(0xffffffffu, f, (k0 + u) & 31);
+        const bool use = k0 + u < n && fk[u] != 0.0f;
+        if (c0 == 0 && k0 == 0) {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) v[u][e] = use ? v0[u][e] : 0.0f;
+        } else {
+          const float* po = ws.part_o + ((size_t)(w0 + c0 + k0 + u + bh) * G + i) * D;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) v[u][e] = use ? __ldcg(po + lane + 32 * e) : 0.0f;
+        }
+        if (!use) fk[u] = 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = fmaf(fk[u], v[u][e], o[e]);
+    }
+  }
+  l = warp_sum(l);
+  // element d = lane + 32 e: lane bits are d bits 0-4, e bits are d bits 5-6
+  if (P.mode != MODE_INT8 && P.signs) {
+#pragma unroll
+    for (int lm = 1; lm < 32; lm <<= 1) {
+      const bool upper = (lane & lm) != 0;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const float x = __shfl_xor_sync(0xffffffffu, o[e], lm);
+        o[e] = upper ? x - o[e] : o[e] + x;
+      }
+    }
+#pragma unroll
+    for (int hstep = 1; hstep < EPL; hstep <<= 1)
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        if (e & hstep) continue;
+        const float a = o[e], c = o[e + hstep];
+        o[e] = a + c;
+        o[e + hstep] = a - c;
+      }
+    const float inv = 1.0f / ((float)D * l);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = tsign[e] * o[e] * inv;
+  } else if (P.mode == MODE_INT8) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = o[e] * tsign[e] / l;
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = o[e] / l;
+  }
+}
+
+// Output transform constants of kv head h for element d = lane + 32 e: the
+// RHT signs (+-1), or the INT8 V channel scales.
+template <int D>
+__device__ __forceinline__ void output_signs(const AttnParams& P, int h, int lane, float (&tsign)[D / 32]) {
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) {
+    const int d = lane + 32 * e;
+    if (P.mode == MODE_INT8) tsign[e] = __fdiv_rn(__ldg(P.ch_amax + ((size_t)P.num_kv_heads + h) * D + d), 127.0f);
+    else tsign[e] = (P.signs && __ldg(P.signs + d) < 0) ? -1.0f : 1.0f;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // 2b. stream kernel over tensor-copied tiles (INT4 / INT2 rows, also with the
 // zero point in the scale, and INT8 / FP8 token-head rows)
 //
@@ -1023,15 +1098,8 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
   const int lo = slice_lo(gw, T, nw), hi = slice_lo(gw + 1, T, nw);
   if (lo >= hi) return;
 
-  uint8_t* ring = smem + warp * NSTAGE * TC::STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * NSTAGE * TC::STAGE) + warp * NSTAGE;
-  if (lane == 0) {
-    for (int i = 0; i < NSTAGE; ++i) mbar_init(bars + i, 1);
-    mbar_init_fence();
-  }
-  __syncwarp();
-  uint32_t phase_bits = 0;  // parity of the next completion to wait for, per stage
-
+  // first (sequence, kv head) of the slice: the run holding tile lo, then
+  // the pair inside it
   int a = 0, z = 128;
   while (z - a > 1) {
     const int mid = (a + z) >> 1;
@@ -1045,6 +1113,15 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
     st0 += n0;
     ++bh0;
   }
+  uint8_t* ring = smem + warp * NSTAGE * TC::STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * NSTAGE * TC::STAGE) + warp * NSTAGE;
+  if (lane == 0) {
+    for (int i = 0; i < NSTAGE; ++i) mbar_init(bars + i, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  uint32_t phase_bits = 0;  // parity of the next completion to wait for, per stage
+
   Seg is;  // lookup / issue cursor
   load_seg(P, bh0, st0, is, KT);
   Seg cs = is;  // compute cursor
@@ -1052,25 +1129,20 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
   const int bs_log2 = __ffs(bs) - 1;
   const int cpb_log2 = bs_log2 - TC::RPC_LOG2;  // chunks per page (bs >= RPC)
 
-  // The next tile to copy: lane c < 4 holds the tensor row of its chunk c
-  // (-1: no data), all lanes the mask of chunks with data.
+  // The next tile to copy: lane c < 4 loads the table entry of its chunk c
+  // (-1: no data) one tile before the copy, so that the load's latency
+  // overlaps a tile of work; the copy turns it into a tensor row.
   int x_lookup = lo;
-  int nx_row = -1;
-  uint32_t nx_valid = 0;
+  int nx_e = -1, nx_sub = 0, nx_h = 0;
   bool nx_have = false;
   auto lookup = [&]() {
     nx_have = x_lookup < hi;
     if (nx_have) {
       while (x_lookup >= is.end) load_seg(P, is.bh + 1, is.end, is, KT);
       const int key = KT * tile_of(is.t, x_lookup - is.start) + TC::RPC * (lane & 3);
-      int row = -1;
-      if (lane < 4 && key < is.t.Leff) {
-        const int e = __ldg(is.tbl + (key >> bs_log2));
-        if (e >= P.num_blocks) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
-        else if (e >= 0) row = ((e * Hkv + is.h) << cpb_log2) + ((key & (bs - 1)) >> TC::RPC_LOG2);
-      }
-      nx_row = row;
-      nx_valid = __ballot_sync(0xffffffffu, row >= 0) & VMASK;
+      nx_e = (lane < 4 && key < is.t.Leff) ? __ldg(is.tbl + (key >> bs_log2)) : -1;
+      nx_sub = (key & (bs - 1)) >> TC::RPC_LOG2;
+      nx_h = is.h;
       ++x_lookup;
     }
   };
@@ -1080,16 +1152,20 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
   int vpos = 0;
   auto issue = [&]() {
     if (nx_have) {
-      int r0 = __shfl_sync(0xffffffffu, nx_row, 0);
-      int r1 = __shfl_sync(0xffffffffu, nx_row, 1);
-      int r2 = __shfl_sync(0xffffffffu, nx_row, 2);
-      int r3 = __shfl_sync(0xffffffffu, nx_row, 3);
-      // chunks without data copy an existing chunk instead (masked later)
-      const int rf = r0 >= 0 ? r0 : (r1 >= 0 ? r1 : (r2 >= 0 ? r2 : (r3 >= 0 ? r3 : 0)));
-      r0 = r0 >= 0 ? r0 : rf;
-      r1 = r1 >= 0 ? r1 : rf;
-      r2 = r2 >= 0 ? r2 : rf;
-      r3 = r3 >= 0 ? r3 : rf;
+      int nx_row = -1;
+      if (nx_e >= P.num_blocks) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
+      else if (nx_e >= 0) nx_row = ((nx_e * Hkv + nx_h) << cpb_log2) + nx_sub;
+      if (nx_row >= P.chunk_rows_total) {  // a map that does not match this kernel: never copy past it
+        flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
+        nx_row = -1;
+      }
+      const uint32_t nx_valid = __ballot_sync(0xffffffffu, nx_row >= 0) & VMASK;
+      // chunks without data copy chunk row 0 of the pool instead (masked later)
+      const int rr = nx_row >= 0 ? nx_row : 0;
+      const int r0 = __shfl_sync(0xffffffffu, rr, 0);
+      const int r1 = __shfl_sync(0xffffffffu, rr, 1);
+      const int r2 = __shfl_sync(0xffffffffu, rr, 2);
+      const int r3 = __shfl_sync(0xffffffffu, rr, 3);
       uint8_t* kt = ring + st_issue * TC::STAGE;
       const bool l0 = lane == 0;
       mbar_arrive_expect_tx_if(l0, bars + st_issue, (uint32_t)(2 * TC::TILE));
@@ -1115,7 +1191,7 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
     uint32_t tmp[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE / 4; ++i) {
-      const uint4 v = __ldg(src + i);
+      const uint4 v = __ldcg(src + i);
       tmp[4 * i] = v.x; tmp[4 * i + 1] = v.y; tmp[4 * i + 2] = v.z; tmp[4 * i + 3] = v.w;
     }
 #pragma unroll
@@ -1125,7 +1201,7 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
         bq[nt][s][0] = tmp[(nt * C::KSTEPS + s) * 2];
         bq[nt][s][1] = tmp[(nt * C::KSTEPS + s) * 2 + 1];
       }
-      const float4 bg = __ldg(ws.qbg + (size_t)cs.bh * NH + 4 * nt + tq);
+      const float4 bg = __ldcg(ws.qbg + (size_t)cs.bh * NH + 4 * nt + tq);
       bet[nt] = bg.x;
       gam[nt] = TC::BYTES ? 0.0f : bg.y;
       kap[nt] = TC::BYTES ? 0.0f : fmaf(-bg.x, bg.z, HR * bg.y);  // 2^(b-1) gamma - beta fold
@@ -1401,9 +1477,8 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
   };
 
   lookup();
-  // Copies wait for the kernels before: the write of this step's tokens may
-  // still run (the preparation kernel starts alongside it), and the query
-  // images and per-head constants must be ready.
+  // Copies wait for the kernel before: the write of this step's tokens may
+  // still run (this grid starts alongside it).
   grid_dependency_wait();
 #pragma unroll 1
   for (int k = 0; k < NSTAGE - 1; ++k) issue();
@@ -1451,129 +1526,63 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
 // 3. merge of the partials of one (sequence, q head) + inverse RHT
 
 template <int D>
-__global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, DecodeWs ws) {
+__global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, DecodeWs ws, int KT) {
   constexpr int EPL = D / 32;
-  const int lane = threadIdx.x & 31;
-  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Hq = P.num_q_heads, G = P.group, Hkv = P.num_kv_heads;
+  const int BH = P.batch * Hkv;
+  // The tile ranges of the pairs (exclusive prefix sum of their tile
+  // counts, in the stream kernel's order), from the inputs alone, while the
+  // stream kernel still runs.  CTA 0 reports a negative seq_len or one past
+  // the table, once per sequence.
+  __shared__ int run_start[257];
+  __shared__ int wtot[8];
+  const int items = (BH + 255) / 256;
+  {
+    const int first = threadIdx.x * items;
+    int tsum = 0;
+    for (int k = 0; k < items && first + k < BH; ++k) {
+      const int bh = first + k;
+      tsum += tile_list(P, bh / Hkv, bh % Hkv, blockIdx.x == 0 && bh % Hkv == 0, KT).n_virt;
+    }
+    int incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wtot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += wtot[w];
+    run_start[threadIdx.x + 1] = before + incl;
+    if (threadIdx.x == 0) run_start[0] = 0;
+    __syncthreads();
+  }
+  const long long wid = (long long)blockIdx.x * 8 + warp;
   if (wid >= (long long)P.batch * Hq) return;
   const int b = (int)(wid / Hq), hq = (int)(wid % Hq);
   const int h = hq / G, i = hq % G;
   const int bh = b * Hkv + h;
-  const int BH = P.batch * Hkv;
   float* out = P.out + (size_t)wid * D;
+  const int T = run_start[256];
+  int start = run_start[bh / items];
+  for (int k = (bh / items) * items; k < bh; ++k) start += tile_list(P, k / Hkv, k % Hkv, false, KT).n_virt;
+  const int end = start + tile_list(P, b, h, false, KT).n_virt;
   // the output transform's constants do not depend on the kernels before
   float tsign[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    const int d = lane + 32 * e;
-    if (P.mode == MODE_INT8) tsign[e] = __fdiv_rn(__ldg(P.ch_amax + ((size_t)Hkv + h) * D + d), 127.0f);  // V scales
-    else tsign[e] = (P.signs && __ldg(P.signs + d) < 0) ? -1.0f : 1.0f;
-  }
+  output_signs<D>(P, h, lane, tsign);
   grid_dependency_wait();  // every partial of the stream kernel is written
-  const int T = ws.tile_start[BH];
-  const int start = ws.tile_start[bh], end = ws.tile_start[bh + 1];
-  float o[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
   if (start >= end) {
 #pragma unroll
     for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = 0.0f;
     return;
   }
   // the slices holding this pair's tiles are workers w_first .. w_last; the
-  // record of (worker w, pair bh) is w + bh
+  // record of (worker w, pair bh) is w + bh, written by this call
   const int nw = stream_workers(T, ws.nwall, ws.fixed_workers);
   const int w0 = worker_of(start, T, nw), w1 = worker_of(end - 1, T, nw);
-  const int nrec = w1 - w0 + 1;
-  // one round trip for the first 32 records' sums and the first four
-  // records' outputs; lane j holds record w0 + j
-  float2 ml0 = make_float2(-CUDART_INF_F, 0.0f);
-  if (lane < nrec) ml0 = ws.part_ml[(size_t)(w0 + lane + bh) * G + i];
-  float v0[4][EPL];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const float* po = ws.part_o + ((size_t)(w0 + u + bh) * G + i) * D;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) v0[u][e] = u < nrec ? po[lane + 32 * e] : 0.0f;
-  }
-  float M = ml0.y > 0.0f ? ml0.x : -CUDART_INF_F;
-  for (int j = 32 + lane; j < nrec; j += 32) {
-    const float2 ml = ws.part_ml[(size_t)(w0 + j + bh) * G + i];
-    if (ml.y > 0.0f) M = fmaxf(M, ml.x);
-  }
-  M = warp_max(M);
-  if (M == -CUDART_INF_F) {
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = 0.0f;
-    return;
-  }
-  float l = 0.0f;
-  for (int c0 = 0; c0 < nrec; c0 += 32) {
-    float2 ml = ml0;
-    if (c0 > 0) {
-      ml = make_float2(-CUDART_INF_F, 0.0f);
-      if (c0 + lane < nrec) ml = ws.part_ml[(size_t)(w0 + c0 + lane + bh) * G + i];
-    }
-    const float f = (c0 + lane < nrec && ml.y > 0.0f) ? ex2(ml.x - M) : 0.0f;
-    l += f * ml.y;
-    const int n = min(32, nrec - c0);
-    // four records per round, their loads issued together (the first round's
-    // were issued with the sums above)
-    for (int k0 = 0; k0 < n; k0 += 4) {
-      float fk[4];
-      float v[4][EPL];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        fk[u] = __shfl_sync(0xffffffffu, f, (k0 + u) & 31);
-        const bool use = k0 + u < n && fk[u] != 0.0f;
-        if (c0 == 0 && k0 == 0) {
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) v[u][e] = use ? v0[u][e] : 0.0f;
-        } else {
-          const float* po = ws.part_o + ((size_t)(w0 + c0 + k0 + u + bh) * G + i) * D;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) v[u][e] = use ? po[lane + 32 * e] : 0.0f;
-        }
-        if (!use) fk[u] = 0.0f;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) o[e] = fmaf(fk[u], v[u][e], o[e]);
-    }
-  }
-  l = warp_sum(l);
-  // element d = lane + 32 e: lane bits are d bits 0-4, e bits are d bits 5-6
-  if (P.mode != MODE_INT8 && P.signs) {
-#pragma unroll
-    for (int lm = 1; lm < 32; lm <<= 1) {
-      const bool upper = (lane & lm) != 0;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float x = __shfl_xor_sync(0xffffffffu, o[e], lm);
-        o[e] = upper ? x - o[e] : o[e] + x;
-      }
-    }
-#pragma unroll
-    for (int hstep = 1; hstep < EPL; hstep <<= 1)
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        if (e & hstep) continue;
-        const float a = o[e], c = o[e + hstep];
-        o[e] = a + c;
-        o[e + hstep] = a - c;
-      }
-    const float inv = 1.0f / ((float)D * l);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = tsign[e] * o[e] * inv;
-  } else if (P.mode == MODE_INT8) {
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = o[e] * tsign[e] / l;
-  } else {
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = o[e] / l;
-  }
+  merge_records<D>(P, ws, bh, i, w0, w1 - w0 + 1, tsign, out, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1640,7 +1649,7 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int BH = P.batch * P.num_kv_heads;
-  e = launch_dependent(decode_prep_kernel<MODE, D, NT>, dim3(BH + 1), dim3(128), 0, stream, P, ws);
+  e = launch_dependent(decode_prep_kernel<MODE, D, NT>, dim3(BH), dim3(128), 0, stream, P, ws);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -1652,7 +1661,8 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
     e = launch_dependent(decode_stream_kernel<MODE, D, NT>, dim3(grid), dim3(128), smem, stream, P, ws);
   if (e != cudaSuccess) return e;
   const long long warps = (long long)P.batch * P.num_q_heads;
-  return launch_dependent(decode_reduce_kernel<D>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, P, ws);
+  return launch_dependent(decode_reduce_kernel<D>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, P, ws,
+                          decode_tile_keys<MODE, D, NT>());
 }
 
 template <int MODE, int D>
