@@ -339,6 +339,7 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, con
   }
   uint8_t* w = static_cast<uint8_t*>(workspace);
   kvq::DecodeWs ws;
+  ws.tile_start = reinterpret_cast<int*>(w + L.off_tile_start);
   ws.qfrag = reinterpret_cast<uint32_t*>(w + L.off_qfrag);
   ws.qbg = reinterpret_cast<float4*>(w + L.off_qbg);
   ws.part_ml = reinterpret_cast<float2*>(w + L.off_part_ml);

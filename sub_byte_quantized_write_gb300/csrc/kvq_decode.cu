@@ -479,6 +479,17 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
     for (int w = 0; w < warp; ++w) before += wtot[w];
     run_start[threadIdx.x + 1] = before + incl;
     if (threadIdx.x == 0) run_start[0] = 0;
+    if (blockIdx.x == 0) {
+      // CTA 0 publishes every pair's first tile for the merge kernel, and
+      // reports a negative seq_len or one past the table, once per sequence
+      int x = before + incl - tsum;
+      for (int k = 0; k < items && first + k < BH; ++k) {
+        const int bh = first + k;
+        ws.tile_start[bh] = x;
+        x += tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0, KT).n_virt;
+      }
+      if (threadIdx.x == 127) ws.tile_start[BH] = before + incl;
+    }
     __syncthreads();
   }
   const int T = run_start[128];
@@ -1089,6 +1100,17 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
     for (int w = 0; w < warp; ++w) before += wtot[w];
     run_start[threadIdx.x + 1] = before + incl;
     if (threadIdx.x == 0) run_start[0] = 0;
+    if (blockIdx.x == 0) {
+      // CTA 0 publishes every pair's first tile for the merge kernel, and
+      // reports a negative seq_len or one past the table, once per sequence
+      int x = before + incl - tsum;
+      for (int k = 0; k < items && first + k < BH; ++k) {
+        const int bh = first + k;
+        ws.tile_start[bh] = x;
+        x += tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0, KT).n_virt;
+      }
+      if (threadIdx.x == 127) ws.tile_start[BH] = before + incl;
+    }
     __syncthreads();
   }
   const int T = run_start[128];
@@ -1191,7 +1213,7 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
     uint32_t tmp[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE / 4; ++i) {
-      const uint4 v = __ldcg(src + i);
+      const uint4 v = __ldg(src + i);
       tmp[4 * i] = v.x; tmp[4 * i + 1] = v.y; tmp[4 * i + 2] = v.z; tmp[4 * i + 3] = v.w;
     }
 #pragma unroll
@@ -1201,7 +1223,7 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
         bq[nt][s][0] = tmp[(nt * C::KSTEPS + s) * 2];
         bq[nt][s][1] = tmp[(nt * C::KSTEPS + s) * 2 + 1];
       }
-      const float4 bg = __ldcg(ws.qbg + (size_t)cs.bh * NH + 4 * nt + tq);
+      const float4 bg = __ldg(ws.qbg + (size_t)cs.bh * NH + 4 * nt + tq);
       bet[nt] = bg.x;
       gam[nt] = TC::BYTES ? 0.0f : bg.y;
       kap[nt] = TC::BYTES ? 0.0f : fmaf(-bg.x, bg.z, HR * bg.y);  // 2^(b-1) gamma - beta fold
@@ -1483,11 +1505,18 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
 #pragma unroll 1
   for (int k = 0; k < NSTAGE - 1; ++k) issue();
 
-  begin_seg();
   int st = 0;
   bool timed_out = false;
 #pragma unroll 1
   for (int x = lo; x < hi; ++x) {
+    if (x == lo || x >= cs.end) {  // a new (sequence, kv head): its query fragments (one code path)
+      if (x > lo) {
+        flush_seg();
+        do load_seg(P, cs.bh + 1, cs.end, cs, KT);
+        while (x >= cs.end);
+      }
+      begin_seg();
+    }
     if (!mbar_wait_bounded(bars + st, (phase_bits >> st) & 1)) {
       timed_out = true;
       break;
@@ -1495,12 +1524,6 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
     phase_bits ^= 1u << st;
     __syncwarp();
     issue();
-    if (x >= cs.end) {
-      flush_seg();
-      do load_seg(P, cs.bh + 1, cs.end, cs, KT);
-      while (x >= cs.end);
-      begin_seg();
-    }
     const uint32_t cur = vq & VMASK;
     vq >>= 4;
     vpos -= 4;
@@ -1526,53 +1549,23 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
 // 3. merge of the partials of one (sequence, q head) + inverse RHT
 
 template <int D>
-__global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, DecodeWs ws, int KT) {
+__global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, DecodeWs ws) {
   constexpr int EPL = D / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int Hq = P.num_q_heads, G = P.group, Hkv = P.num_kv_heads;
-  const int BH = P.batch * Hkv;
-  // The tile ranges of the pairs (exclusive prefix sum of their tile
-  // counts, in the stream kernel's order), from the inputs alone, while the
-  // stream kernel still runs.  CTA 0 reports a negative seq_len or one past
-  // the table, once per sequence.
-  __shared__ int run_start[257];
-  __shared__ int wtot[8];
-  const int items = (BH + 255) / 256;
-  {
-    const int first = threadIdx.x * items;
-    int tsum = 0;
-    for (int k = 0; k < items && first + k < BH; ++k) {
-      const int bh = first + k;
-      tsum += tile_list(P, bh / Hkv, bh % Hkv, blockIdx.x == 0 && bh % Hkv == 0, KT).n_virt;
-    }
-    int incl = tsum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) wtot[warp] = incl;
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp; ++w) before += wtot[w];
-    run_start[threadIdx.x + 1] = before + incl;
-    if (threadIdx.x == 0) run_start[0] = 0;
-    __syncthreads();
-  }
-  const long long wid = (long long)blockIdx.x * 8 + warp;
   if (wid >= (long long)P.batch * Hq) return;
   const int b = (int)(wid / Hq), hq = (int)(wid % Hq);
   const int h = hq / G, i = hq % G;
   const int bh = b * Hkv + h;
+  const int BH = P.batch * Hkv;
   float* out = P.out + (size_t)wid * D;
-  const int T = run_start[256];
-  int start = run_start[bh / items];
-  for (int k = (bh / items) * items; k < bh; ++k) start += tile_list(P, k / Hkv, k % Hkv, false, KT).n_virt;
-  const int end = start + tile_list(P, b, h, false, KT).n_virt;
   // the output transform's constants do not depend on the kernels before
   float tsign[EPL];
   output_signs<D>(P, h, lane, tsign);
   grid_dependency_wait();  // every partial of the stream kernel is written
+  const int T = ws.tile_start[BH];
+  const int start = ws.tile_start[bh], end = ws.tile_start[bh + 1];
   if (start >= end) {
 #pragma unroll
     for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = 0.0f;
@@ -1661,8 +1654,7 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
     e = launch_dependent(decode_stream_kernel<MODE, D, NT>, dim3(grid), dim3(128), smem, stream, P, ws);
   if (e != cudaSuccess) return e;
   const long long warps = (long long)P.batch * P.num_q_heads;
-  return launch_dependent(decode_reduce_kernel<D>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, P, ws,
-                          decode_tile_keys<MODE, D, NT>());
+  return launch_dependent(decode_reduce_kernel<D>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, P, ws);
 }
 
 template <int MODE, int D>

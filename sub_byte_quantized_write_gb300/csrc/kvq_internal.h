@@ -70,6 +70,7 @@ struct AttnParams {
 
 // Decode workspace (caller-owned scratch), carved by decode_ws_layout.
 struct DecodeWs {
+  int* tile_start;     // [B*Hkv + 1] first stream tile of each pair (written by the stream kernel's CTA 0)
   uint32_t* qfrag;     // [B*Hkv][32 lanes][NT * D/16 * 2] query B-operand images
   float4* qbg;         // [B*Hkv][4*NT] per-head logit constants (beta, gamma, key fold, 0)
   float2* part_ml;     // [n_partials][G] (running max in log2 units, sum of weights)
@@ -85,7 +86,7 @@ constexpr int DECODE_WARPS = 4;
 constexpr int DECODE_MIN_TILES_PER_WARP = 8;
 
 struct DecodeLayout {
-  size_t off_qfrag, off_qbg, off_part_ml, off_part_o, total;
+  size_t off_tile_start, off_qfrag, off_qbg, off_part_ml, off_part_o, total;
   int grid, nwall, n_partials;
 };
 
@@ -101,6 +102,7 @@ inline DecodeLayout decode_ws_layout(int batch, int num_kv_heads, int group, int
   L.nwall = L.grid * DECODE_WARPS;
   L.n_partials = L.nwall + BH;
   size_t o = 0;
+  L.off_tile_start = o; o = align256(o + (size_t)(BH + 1) * 4);
   L.off_qfrag = o;      o = align256(o + (size_t)BH * 32 * NT * (head_dim / 16) * 2 * 4);
   L.off_qbg = o;        o = align256(o + (size_t)BH * 4 * NT * 16);
   L.off_part_ml = o;    o = align256(o + (size_t)L.n_partials * group * 8);
