@@ -45,21 +45,36 @@ __device__ __forceinline__ void flag_error(int32_t* dev_error, int bit) {
   if (dev_error) atomicOr(dev_error, bit);
 }
 
-// Load EPL consecutive input elements (fp32 or bf16) as fp32.
+// Load EPL consecutive input elements (fp32 or bf16) as fp32 (EPL = 2, 4, 8
+// or 16; elem_off a multiple of EPL, so the vector loads are aligned).
 template <int EPL>
 __device__ __forceinline__ void load_row_elems(const void* base, int dtype, size_t elem_off, float (&x)[EPL]) {
   if (dtype == DT_F32) {
     const float* p = reinterpret_cast<const float*>(base) + elem_off;
-    if constexpr (EPL == 4) {
-      float4 v = __ldg(reinterpret_cast<const float4*>(p));
-      x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    if constexpr (EPL >= 4) {
+#pragma unroll
+      for (int c = 0; c < EPL / 4; ++c) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(p) + c);
+        x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
+      }
     } else {
       float2 v = __ldg(reinterpret_cast<const float2*>(p));
       x[0] = v.x; x[1] = v.y;
     }
   } else {
     const uint16_t* p = reinterpret_cast<const uint16_t*>(base) + elem_off;
-    if constexpr (EPL == 4) {
+    if constexpr (EPL >= 8) {
+#pragma unroll
+      for (int c = 0; c < EPL / 8; ++c) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          x[8 * c + 2 * k] = __uint_as_float(w[k] << 16);
+          x[8 * c + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+      }
+    } else if constexpr (EPL == 4) {
       uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
       x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xFFFF0000u);
       x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xFFFF0000u);

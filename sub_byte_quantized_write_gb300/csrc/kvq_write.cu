@@ -92,28 +92,65 @@ __device__ __forceinline__ uint32_t gather_word(uint32_t bits, int lane) {
   return v;
 }
 
-// Rotate, quantise, pack and store one row (x: the lane's D/32 elements) at
-// dst; every step is one IEEE operation in a fixed order, so the bytes match
-// any other evaluation in that order.
-template <int MODE, int D, bool STEGO>
-__device__ __forceinline__ void quantise_store_row(const WriteParams& P, float (&x)[D / 32], uint8_t* dst, int lane) {
-  constexpr int EPL = D / 32;
+// Rotate, quantise, pack and store one row at dst.  The row is held by LPR
+// consecutive lanes (32: a warp per row; 8: four rows per warp), lane `sub`
+// of the group holding elements sub * EPL .. + EPL - 1 (EPL = D / LPR).
+// Every step is one IEEE operation in a fixed order (butterfly stages
+// h = 1, 2, ..., D/2, exact min / max, one division for the scale, fp16 RNE,
+// one subtract and one divide per element, round-half-even), so the bytes
+// match any other evaluation in that order, whatever LPR.  Every lane of
+// the warp must call this (the shuffles span the warp); `store` is false
+// for a group whose row is not written.
+template <int MODE, int D, bool STEGO, int LPR>
+__device__ __forceinline__ void quantise_store_row(const WriteParams& P, float (&x)[D / LPR], uint8_t* dst, int lane,
+                                                   bool store) {
+  constexpr int EPL = D / LPR;
   constexpr int BITS = mode_bits(MODE);
   constexpr int LEVELS = (1 << BITS) - 1;
   constexpr int DATA = data_bytes(MODE, D);
+  const int sub = lane & (LPR - 1);
   if (P.signs) {
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
-      if (__ldg(P.signs + lane * EPL + i) < 0) x[i] = -x[i];
-    wht_warp<EPL>(x, lane);
+      if (__ldg(P.signs + sub * EPL + i) < 0) x[i] = -x[i];
+    // stages h = 1 .. EPL/2 in lane, then h = EPL .. D/2 over the group's lanes
+#pragma unroll
+    for (int h = 1; h < EPL; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        if (i & h) continue;
+        const float a = x[i], c = x[i + h];
+        x[i] = __fadd_rn(a, c);
+        x[i + h] = __fsub_rn(a, c);
+      }
+    }
+#pragma unroll
+    for (int lm = 1; lm < LPR; lm <<= 1) {
+      // lower lane holds x_j: x_j + x_{j+h}; upper lane holds x_{j+h}: x_j - x_{j+h},
+      // both as one exact fma(+-1, x, o)
+      const float sg = (sub & lm) ? -1.0f : 1.0f;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, x[i], lm);
+        x[i] = __fmaf_rn(sg, x[i], o);
+      }
+    }
   }
-  uint32_t bits = 0, pad;
+  // codes: NBITS = EPL * BITS bits per lane, in NW words (at least one)
+  constexpr int NBITS = EPL * BITS;
+  constexpr int NW = NBITS >= 32 ? NBITS / 32 : 1;
+  constexpr int CPW = 32 / BITS;  // codes per word
+  uint32_t bits[NW];
+#pragma unroll
+  for (int k = 0; k < NW; ++k) bits[k] = 0;
+  uint32_t pad;
   if constexpr (byte_token_head(MODE)) {
     // symmetric: s = amax / 127 (INT8) or amax / 448 (largest E4M3 value)
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = warp_max(amax);
+#pragma unroll
+    for (int lm = 1; lm < LPR; lm <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, lm));
     const float s = __fdiv_rn(amax, MODE == MODE_I8T ? 127.0f : 448.0f);
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
@@ -123,7 +160,7 @@ __device__ __forceinline__ void quantise_store_row(const WriteParams& P, float (
         if constexpr (MODE == MODE_I8T) c = (uint32_t)(int)fminf(fmaxf(rintf(t), -127.0f), 127.0f) & 0xFFu;
         else c = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);  // nearest even
       }
-      bits |= c << (8 * i);
+      bits[i / CPW] |= c << ((i % CPW) * BITS);
     }
     pad = __float_as_uint(s);
   } else {
@@ -133,8 +170,13 @@ __device__ __forceinline__ void quantise_store_row(const WriteParams& P, float (
       mn = fminf(mn, x[i]);
       mx = fmaxf(mx, x[i]);
     }
-    mn = __fadd_rn(warp_min(mn), 0.0f);  // canonical +0
-    mx = __fadd_rn(warp_max(mx), 0.0f);
+#pragma unroll
+    for (int lm = 1; lm < LPR; lm <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, lm));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, lm));
+    }
+    mn = __fadd_rn(mn, 0.0f);  // canonical +0
+    mx = __fadd_rn(mx, 0.0f);
     if constexpr (STEGO) {
       // the grid (u - zp) * s holds 0: it spans min(mn, 0) .. max(mx, 0); the
       // scale's low 4 mantissa bits are cleared and carry the zero point
@@ -151,7 +193,7 @@ __device__ __forceinline__ void quantise_store_row(const WriteParams& P, float (
           r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
           u = (uint32_t)r;
         }
-        bits |= u << (i * BITS);
+        bits[i / CPW] |= u << ((i % CPW) * BITS);
       }
       pad = sb | (uint32_t)zp;
     } else {
@@ -168,18 +210,27 @@ __device__ __forceinline__ void quantise_store_row(const WriteParams& P, float (
           r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
           u = (uint32_t)r;
         }
-        bits |= u << (i * BITS);
+        bits[i / CPW] |= u << ((i % CPW) * BITS);
       }
       pad = (uint32_t)s_h | ((uint32_t)m_h << 16);
     }
   }
-  constexpr int NBITS = EPL * BITS;        // bits per lane: 32, 16, 8 or 4
-  const uint32_t word = gather_word<NBITS>(bits, lane);
-  constexpr int LPW = 32 / NBITS;
-  if (lane % LPW == 0) *reinterpret_cast<uint32_t*>(dst + 4 * (lane / LPW)) = word;
-  if (lane == 0) *reinterpret_cast<uint32_t*>(dst + DATA) = pad;
+  if constexpr (NBITS >= 32) {
+    // this lane's bytes sub * NBITS/8 ..: whole words (rows are 4-byte aligned)
+    if (store) {
+#pragma unroll
+      for (int k = 0; k < NW; ++k) *reinterpret_cast<uint32_t*>(dst + sub * (NBITS / 8) + 4 * k) = bits[k];
+    }
+  } else {
+    // 32 / NBITS lanes share a word: OR their bits into the group's first lane
+    constexpr int LPW = 32 / NBITS;
+    uint32_t v = bits[0] << ((sub % LPW) * NBITS);
+#pragma unroll
+    for (int o = 1; o < LPW; o <<= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+    if (store && sub % LPW == 0) *reinterpret_cast<uint32_t*>(dst + 4 * (sub / LPW)) = v;
+  }
+  if (store && sub == 0) *reinterpret_cast<uint32_t*>(dst + DATA) = pad;
 }
-
 
 template <int MODE, int D, bool STEGO>
 __global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
@@ -198,7 +249,7 @@ __global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
   load_row_elems<EPL>(kv ? P.v : P.k, P.dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, x);
   uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h, lane);
   if (dst == nullptr) return;  // warp-uniform
-  quantise_store_row<MODE, D, STEGO>(P, x, dst, lane);
+  quantise_store_row<MODE, D, STEGO, 32>(P, x, dst, lane, true);
 }
 
 // INT8, pass 1 (only while *ready == 0): per-channel max |x| over all tokens.
@@ -475,43 +526,46 @@ cudaError_t launch_gather(const WriteParams& P, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// Long writes (a prefill chunk): one warp per WRITE_TOKENS consecutive tokens
-// of a kv head.  Lanes 0..3 locate one token each (the gather's lookup, which
-// flags the same errors as dest_row), the K and V rows of all four are loaded
-// together, then each row goes through quantise_store_row as in
-// write_token_head_kernel, so the bytes are the same.
+// Long writes (a prefill chunk): one warp per WRITE_TOKENS = 4 consecutive
+// tokens of a kv head, eight lanes per row: lane group g (lanes 8g .. 8g+7)
+// takes token t0 + g, first its K row, then its V row.  With D/8 elements per
+// lane the butterfly's first log2(D/8) stages and most of the min / max run
+// in registers and the packed bytes form in lane (no word gather).  Lanes
+// 0..3 locate one token each (the gather's lookup, which flags the same
+// errors as dest_row).  The row arithmetic is quantise_store_row's, so the
+// bytes are those of write_token_head_kernel.
 constexpr int WRITE_TOKENS = 4;
+constexpr int WRITE_LPR = 32 / WRITE_TOKENS;  // lanes per row
 constexpr int WRITE_BATCH_MIN_TOKENS = 512;
 
 template <int MODE, int D, bool STEGO>
 __global__ void __launch_bounds__(256) write_batch_kernel(WriteParams P) {
-  constexpr int EPL = D / 32;
+  constexpr int EPL = D / WRITE_LPR;
   const int lane = threadIdx.x & 31;
+  const int g = lane / WRITE_LPR, sub = lane % WRITE_LPR;
   allow_dependent_launch();  // as in write_token_head_kernel
   const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int h = (int)(wid % P.num_kv_heads);
   const long long t0 = (wid / P.num_kv_heads) * WRITE_TOKENS;
-  if (t0 >= P.num_tokens) return;
-  float x[2][WRITE_TOKENS][EPL];
+  if (t0 >= P.num_tokens) return;  // warp-uniform
+  const long long t = t0 + g;
+  const bool have = t < P.num_tokens;
+  float x[2][EPL];
+  if (have) {
+    const size_t e = ((size_t)t * P.num_kv_heads + h) * D + sub * EPL;
+    load_row_elems<EPL>(P.k, P.dtype, e, x[0]);
+    load_row_elems<EPL>(P.v, P.dtype, e, x[1]);
+  } else {
 #pragma unroll
-  for (int r = 0; r < WRITE_TOKENS; ++r) {
-    if (t0 + r < P.num_tokens) {  // warp-uniform
-      const size_t e = ((size_t)(t0 + r) * P.num_kv_heads + h) * D + lane * EPL;
-      load_row_elems<EPL>(P.k, P.dtype, e, x[0][r]);
-      load_row_elems<EPL>(P.v, P.dtype, e, x[1][r]);
-    }
+    for (int i = 0; i < EPL; ++i) x[0][i] = x[1][i] = 0.0f;
   }
   long long my_off = -1;
   if (lane < WRITE_TOKENS) my_off = gather_row_offset<false>(P, (int)(t0 + lane), h);
-  long long off[WRITE_TOKENS];
-#pragma unroll
-  for (int r = 0; r < WRITE_TOKENS; ++r) off[r] = __shfl_sync(0xffffffffu, my_off, r);
+  const long long off = __shfl_sync(0xffffffffu, my_off, g);  // -1: an evicted, invalid or absent row
 #pragma unroll
   for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-    for (int r = 0; r < WRITE_TOKENS; ++r)
-      if (off[r] >= 0)  // warp-uniform: -1 is an evicted or invalid row
-        quantise_store_row<MODE, D, STEGO>(P, x[kv][r], (kv ? P.v_pages : P.k_pages) + off[r], lane);
+    quantise_store_row<MODE, D, STEGO, WRITE_LPR>(P, x[kv], (kv ? P.v_pages : P.k_pages) + (off >= 0 ? off : 0), lane,
+                                                  off >= 0);
 }
 
 template <int MODE, bool STEGO>
