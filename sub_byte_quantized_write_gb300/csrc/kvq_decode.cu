@@ -377,18 +377,16 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
     amx = warp_max(amx);
     const int ex = amx > 0.0f ? ilogbf(amx) : 0;
     const float sc = ldexpf(1.0f, 10 - ex);  // max |q''| in [1024, 2048)
+    float opsum = 0.0f;  // sum of the exact operand values (hi + lo) for the folded key offset
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
       const float v = x[e] * sc;
       const __half hi = __float2half_rn(v);
+      const __half lo = __float2half_rn(v - __half2float(hi));
       qh[0][i][lane * EPL + e] = hi;
-      qh[1][i][lane * EPL + e] = __float2half_rn(v - __half2float(hi));
+      qh[1][i][lane * EPL + e] = lo;
+      opsum += __half2float(hi) + __half2float(lo);
     }
-    // sum of the exact operand values (hi + lo) for the folded key offset
-    float opsum = 0.0f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e)
-      opsum += __half2float(qh[0][i][lane * EPL + e]) + __half2float(qh[1][i][lane * EPL + e]);
     opsum = warp_sum(opsum);
     if (lane == 0) {
       const float beta = i < G ? P.softmax_scale * log2e / (dnorm * sc) : 0.0f;
@@ -402,17 +400,24 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
   // 4 nt + gq/2, half gq & 1; the register pairs head dims in the order the
   // key-side unpack produces them (kpair_dims).
   constexpr int PER_LANE = NT * C::KSTEPS * 2;
-  uint32_t* dst = ws.qfrag + (size_t)bh * 32 * PER_LANE;
-  for (int idx = threadIdx.x; idx < 32 * PER_LANE; idx += blockDim.x) {
-    const int ln = idx / PER_LANE, rest = idx % PER_LANE;
-    const int nt = rest / (C::KSTEPS * 2), s = (rest / 2) % C::KSTEPS, r = rest & 1;
-    const int g_ = ln >> 2, t_ = ln & 3;
-    const int head = 4 * nt + (g_ >> 1), hl = g_ & 1;
-    const int w = 4 * (s / C::KPW) + t_, sig = s % C::KPW;
-    int d0, d1;
-    kpair_dims<MODE>(w, 2 * sig + r, d0, d1);
-    const __half2 pr = __halves2half2(qh[hl][head][d0], qh[hl][head][d1]);
-    dst[idx] = *reinterpret_cast<const uint32_t*>(&pr);
+  uint4* dst = reinterpret_cast<uint4*>(ws.qfrag + (size_t)bh * 32 * PER_LANE);
+  // four consecutive image words per thread and 16-byte store
+  for (int q4 = threadIdx.x; q4 < 32 * PER_LANE / 4; q4 += blockDim.x) {
+    uint32_t wv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = 4 * q4 + k;
+      const int ln = idx / PER_LANE, rest = idx % PER_LANE;
+      const int nt = rest / (C::KSTEPS * 2), s = (rest / 2) % C::KSTEPS, r = rest & 1;
+      const int g_ = ln >> 2, t_ = ln & 3;
+      const int head = 4 * nt + (g_ >> 1), hl = g_ & 1;
+      const int w = 4 * (s / C::KPW) + t_, sig = s % C::KPW;
+      int d0, d1;
+      kpair_dims<MODE>(w, 2 * sig + r, d0, d1);
+      const __half2 pr = __halves2half2(qh[hl][head][d0], qh[hl][head][d1]);
+      wv[k] = *reinterpret_cast<const uint32_t*>(&pr);
+    }
+    dst[q4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
   if (MODE != MODE_INT8) grid_dependency_wait();
 }
@@ -943,9 +948,10 @@ __device__ __forceinline__ void merge_records(const AttnParams& P, const DecodeW
   // records' outputs; lane j holds record w0 + j
   float2 ml0 = make_float2(-CUDART_INF_F, 0.0f);
   if (lane < nrec) ml0 = __ldcg(ws.part_ml + (size_t)(w0 + lane + bh) * G + i);
-  float v0[4][EPL];
+  constexpr int V0 = 8;  // records whose outputs load in the first round trip
+  float v0[V0][EPL];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
+  for (int u = 0; u < V0; ++u) {
     const float* po = ws.part_o + ((size_t)(w0 + u + bh) * G + i) * D;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) v0[u][e] = u < nrec ? __ldcg(po + lane + 32 * e) : 0.0f;
@@ -971,23 +977,28 @@ __device__ __forceinline__ void merge_records(const AttnParams& P, const DecodeW
     const float f = (c0 + lane < nrec && ml.y > 0.0f) ? ex2(ml.x - M) : 0.0f;
     l += f * ml.y;
     const int n = min(32, nrec - c0);
-    // four records per round, their loads issued together (the first round's
-    // were issued with the sums above)
-    for (int k0 = 0; k0 < n; k0 += 4) {
+    int kfirst = 0;
+    if (c0 == 0) {  // the first V0 records: outputs loaded with the sums above
+#pragma unroll
+      for (int u = 0; u < V0; ++u) {
+        const float fk = __shfl_sync(0xffffffffu, f, u);
+        const bool use = u < n && fk != 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = fmaf(use ? fk : 0.0f, use ? v0[u][e] : 0.0f, o[e]);
+      }
+      kfirst = V0;
+    }
+    // then four records per round, their loads issued together
+    for (int k0 = kfirst; k0 < n; k0 += 4) {
       float fk[4];
       float v[4][EPL];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         fk[u] = __shfl_sync(0xffffffffu, f, (k0 + u) & 31);
         const bool use = k0 + u < n && fk[u] != 0.0f;
-        if (c0 == 0 && k0 == 0) {
+        const float* po = ws.part_o + ((size_t)(w0 + c0 + k0 + u + bh) * G + i) * D;
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) v[u][e] = use ? v0[u][e] : 0.0f;
-        } else {
-          const float* po = ws.part_o + ((size_t)(w0 + c0 + k0 + u + bh) * G + i) * D;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) v[u][e] = use ? __ldcg(po + lane + 32 * e) : 0.0f;
-        }
+        for (int e = 0; e < EPL; ++e) v[u][e] = use ? __ldcg(po + lane + 32 * e) : 0.0f;
         if (!use) fk[u] = 0.0f;
       }
 #pragma unroll
