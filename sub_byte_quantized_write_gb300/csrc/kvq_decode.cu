@@ -1183,15 +1183,15 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
   int st_issue = 0;
   uint32_t vq = 0;  // chunk masks of the tiles in flight, oldest in the low bits
   int vpos = 0;
+  int err_bits = 0;  // error bits of this lane, published once after the loop
   auto issue = [&]() {
     if (nx_have) {
-      int nx_row = -1;
-      if (nx_e >= P.num_blocks) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
-      else if (nx_e >= 0) nx_row = ((nx_e * Hkv + nx_h) << cpb_log2) + nx_sub;
-      if (nx_row >= P.chunk_rows_total) {  // a map that does not match this kernel: never copy past it
-        flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
-        nx_row = -1;
-      }
+      const bool out_of_pool = nx_e >= P.num_blocks;
+      int nx_row = (nx_e >= 0 && !out_of_pool) ? ((nx_e * Hkv + nx_h) << cpb_log2) + nx_sub : -1;
+      // a row at or past the tensor map's end (a map that does not match this kernel) is never copied
+      const bool past_map = nx_row >= P.chunk_rows_total;
+      nx_row = past_map ? -1 : nx_row;
+      err_bits |= (out_of_pool || past_map) ? DEVERR_BLOCK_RANGE : 0;
       const uint32_t nx_valid = __ballot_sync(0xffffffffu, nx_row >= 0) & VMASK;
       // chunks without data copy chunk row 0 of the pool instead (masked later)
       const int rr = nx_row >= 0 ? nx_row : 0;
@@ -1546,6 +1546,8 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
     if (full) tile(std::true_type{}, kt, kt + TC::TILE_AL, cur, key0, Leff, W, p_q);
     else tile(std::false_type{}, kt, kt + TC::TILE_AL, cur, key0, Leff, W, p_q);
   }
+  err_bits = __reduce_or_sync(0xffffffffu, err_bits);
+  if (err_bits && lane == 0) flag_error(P.dev_error, err_bits);
   if (timed_out) {
     // a copy never arrived: report it, give the copies in flight one more
     // bounded chance to land, and leave without writing this slice's partial
