@@ -354,6 +354,14 @@ def run_gpu(args, rank, world, local_rank):
         if kind == "gather_prefill":
             dense_call()
 
+    # decode, token-head modes: the same step as one kvq_write_decode_attn
+    # call (the write done by the decode's query-preparation kernel)
+    fused = kind == "decode" and wl.mode != gen.MODE_INT8
+
+    def fused_call():
+        K.kvq_write_decode_attn(cache, pag, st["k"], st["v"], st["cu"], st["q"], scale, out=st["out"],
+                                workspace=st["ws"], num_splits=st["splits"], stream=stream)
+
     # The step's two library calls are captured once into a CUDA graph and
     # replayed, so the timed region holds only device work (re-writing the
     # same new tokens at the same positions is idempotent).  One graph holds
@@ -362,6 +370,8 @@ def run_gpu(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         for _ in range(2):
             step()  # first calls set the kernels' shared-memory attributes outside capture
+            if fused:
+                fused_call()
         stream.synchronize()
         g_step, g_write, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         g_dense = torch.cuda.CUDAGraph() if kind == "gather_prefill" else None
@@ -374,6 +384,10 @@ def run_gpu(args, rank, world, local_rank):
         if g_dense is not None:
             with torch.cuda.graph(g_dense, stream=stream):
                 dense_call()
+        g_fused = torch.cuda.CUDAGraph() if fused else None
+        if g_fused is not None:
+            with torch.cuda.graph(g_fused, stream=stream):
+                fused_call()
     for _ in range(args.warmup):
         with torch.cuda.stream(stream):
             flush_l2(1)
@@ -382,12 +396,17 @@ def run_gpu(args, rank, world, local_rank):
         g_attn.replay()
         if g_dense is not None:
             g_dense.replay()
+        if g_fused is not None:
+            with torch.cuda.stream(stream):
+                flush_l2(1)
+            g_fused.replay()
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
+    evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
@@ -408,11 +427,18 @@ def run_gpu(args, rank, world, local_rank):
                 if g_dense is not None:
                     g_dense.replay()
                 e3.record(stream)
+            for i in range(args.steps if g_fused is not None else 0):  # the step as one fused call
+                flush_l2(i)
+                a, c = evf[i]
+                a.record(stream)
+                g_fused.replay()
+                c.record(stream)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(c) for a, c in evs]
     att_ms = [b.elapsed_time(c) for a, b, c, d in ev]
     wr_ms = [a.elapsed_time(b) for a, b, c, d in ev]
     dense_ms = [c.elapsed_time(d) for a, b, c, d in ev]
+    fused_ms = [a.elapsed_time(c) for a, c in evf] if g_fused is not None else []
     ms = max_over_ranks(sum(step_ms) / len(step_ms), device)
     tokens = {"decode": wl.batch, "prefill": int(wl.n_new.sum()), "gather": st["n_all"],
               "gather_prefill": int(wl.n_new.sum())}[kind]
@@ -512,6 +538,8 @@ def run_gpu(args, rank, world, local_rank):
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "frac_of_nominal_8000": round(achieved / 8000.0, 4),
                 "algorithmic_bytes_per_launch": units["decode"], "traffic": traffic}
         extra = {"effective_kv_GBps": round(achieved, 1), "decode_ms": round(att, 5)}
+        if fused_ms:
+            extra["fused_write_decode_step_ms"] = round(sum(fused_ms) / len(fused_ms), 5)
         launches = 4  # write + (prep, stream, merge)
         dtype = {0: "u4", 1: "u2", 2: "s8", 3: "u4", 4: "s8", 5: "e4m3"}[wl.mode] + " codes x fp16 tensor-core math, fp32 accumulate/softmax"
     else:

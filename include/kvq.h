@@ -263,6 +263,31 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging,
                            void* workspace, size_t workspace_bytes, int32_t num_splits,
                            int32_t* dev_error, void* stream);
 
+/* kvq_write_decode_attn -- one decode step in one call: kvq_write of the
+ * step's new tokens, then kvq_decode_attn, with the write done by the
+ * decode's query-preparation kernel instead of a launch of its own.
+ * ([vLLM-INT4] 关键源码片段 get_kv_cache_shape: the row the write produces
+ * and the decode reads; 实现拆解 2: the write and read kernels.)
+ *
+ * k, v, kv_dtype, cu_new_tokens, num_tokens : as kvq_write (new rows
+ *       [num_tokens][num_kv_heads][head_dim]; sequence b's new tokens are at
+ *       positions seq_lens[b] - n_b .. seq_lens[b] - 1).
+ * q, q_dtype, num_q_heads, softmax_scale, out, workspace, workspace_bytes,
+ * num_splits : as kvq_decode_attn.
+ * The pages and error bits are exactly those of kvq_write followed by
+ * kvq_decode_attn: the rows come from the same row arithmetic.  Meant for
+ * decode steps (a few new tokens per sequence: each (sequence, kv head)
+ * writes its rows with one CTA).  KVQ_INT8_CHANNEL is not supported (its
+ * first write takes the channel maxima over every token first):
+ * KVQ_ERR_UNSUPPORTED. */
+kvq_status kvq_write_decode_attn(const kvq_cache* cache, const kvq_paging* paging,
+                                 const void* k, const void* v, int32_t kv_dtype,
+                                 const int32_t* cu_new_tokens, int32_t num_tokens,
+                                 const void* q, int32_t q_dtype, int32_t num_q_heads,
+                                 float softmax_scale, float* out,
+                                 void* workspace, size_t workspace_bytes, int32_t num_splits,
+                                 int32_t* dev_error, void* stream);
+
 /* kvq_prefill_attn -- causal chunked-prefill attention of a chunk of queries
  * against everything in the cache, the chunk itself included (write the chunk
  * with kvq_write first).  ([FD-INT2] Usage: chunked prefill; [vLLM-INT4]

@@ -7,6 +7,7 @@ library's CUDA kernels; there is no fallback.  If ``libkvq.so`` has not been
 built, importing this package raises ImportError.
 
 Names mirror the C calls: ``kvq_write``, ``kvq_gather``, ``kvq_prefill_dense_attn``, ``kvq_decode_attn``,
+``kvq_write_decode_attn``,
 ``kvq_decode_attn_noalloc``, ``kvq_prefill_attn``, ``kvq_decode_workspace_size``,
 ``kvq_row_bytes``.
 """
@@ -66,6 +67,9 @@ _lib.kvq_decode_workspace_size.argtypes = [_CP, _PP, _I, _I, ctypes.POINTER(ctyp
 _lib.kvq_decode_workspace_size.restype = _I
 _lib.kvq_decode_attn.argtypes = [_CP, _PP, _P, _I, _I, ctypes.c_float, _P, _P, ctypes.c_size_t, _I, _P, _P]
 _lib.kvq_decode_attn.restype = _I
+_lib.kvq_write_decode_attn.argtypes = [_CP, _PP, _P, _P, _I, _P, _I, _P, _I, _I, ctypes.c_float, _P, _P,
+                                       ctypes.c_size_t, _I, _P, _P]
+_lib.kvq_write_decode_attn.restype = _I
 _lib.kvq_decode_attn_noalloc.argtypes = [_CP, _PP, _P, _I, _I, ctypes.c_float, _P, _I, _P, _P]
 _lib.kvq_decode_attn_noalloc.restype = _I
 _lib.kvq_prefill_attn.argtypes = [_CP, _PP, _P, _I, _I, _P, _I, _I, ctypes.c_float, _P, _P, _P]
@@ -249,6 +253,31 @@ def kvq_decode_attn(cache: PagedCache, paging: Paging, q: torch.Tensor, softmax_
                                 float(softmax_scale), _dev_ptr(out, torch.float32, "out"),
                                 _dev_ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
                                 num_splits, _dev_ptr(dev_error, torch.int32, "dev_error"), _stream_ptr(stream)))
+    return out
+
+
+def kvq_write_decode_attn(cache: PagedCache, paging: Paging, k: torch.Tensor, v: torch.Tensor,
+                          cu_new_tokens: torch.Tensor, q: torch.Tensor, softmax_scale: float,
+                          out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                          num_splits: int = 0, dev_error: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step in one call: kvq_write of k, v [num_tokens, num_kv_heads, head_dim] (the step's new
+    tokens), then decode attention of q [batch, num_q_heads, head_dim]; returns fp32 out.  The pages and
+    the output are those of kvq_write followed by kvq_decode_attn."""
+    if k.shape != v.shape or k.dtype != v.dtype:
+        raise ValueError("k and v must have the same shape and dtype")
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes, _ = kvq_decode_workspace_size(cache, paging, Hq, num_splits)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    cs, ps = cache.struct(), paging.struct()
+    _check(_lib.kvq_write_decode_attn(ctypes.byref(cs), ctypes.byref(ps), _dev_ptr(k, name="k"), _dev_ptr(v, name="v"),
+                                      _qdtype(k), _dev_ptr(cu_new_tokens, torch.int32, "cu_new_tokens"),
+                                      int(k.shape[0]), _dev_ptr(q, name="q"), _qdtype(q), Hq, float(softmax_scale),
+                                      _dev_ptr(out, torch.float32, "out"), _dev_ptr(workspace, torch.uint8, "workspace"),
+                                      workspace.numel(), int(num_splits), _dev_ptr(dev_error, torch.int32, "dev_error"),
+                                      _stream_ptr(stream)))
     return out
 
 

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
 SOURCES = ["kvq_api.cu", "kvq_write.cu", "kvq_decode.cu", "kvq_prefill_tc.cu"]
-HEADERS = ["kvq_common.cuh", "kvq_internal.h", "kvq_tc.cuh"]
+HEADERS = ["kvq_common.cuh", "kvq_internal.h", "kvq_tc.cuh", "kvq_row.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -313,9 +313,22 @@ bool page_chunk_map(CUtensorMap* map, const void* pages, int num_blocks, int Hkv
 
 extern "C" {
 
-kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, const void* q, int32_t dtype,
-                           int32_t num_q_heads, float softmax_scale, float* out, void* workspace,
-                           size_t workspace_bytes, int32_t num_splits, int32_t* dev_error, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Fields of the step's write for the fused call (new_k == nullptr: none).
+struct FusedWrite {
+  const void* k = nullptr;
+  const void* v = nullptr;
+  int32_t dtype = 0;
+  const int32_t* cu_new = nullptr;
+  int32_t num_tokens = 0;
+};
+
+kvq_status decode_call(const kvq_cache* cache, const kvq_paging* paging, const void* q, int32_t dtype,
+                       int32_t num_q_heads, float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                       int32_t num_splits, int32_t* dev_error, void* stream, const FusedWrite& fw) {
   kvq_status st = check_cache(cache);
   if (st != KVQ_OK) return st;
   if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
@@ -347,9 +360,52 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, con
   ws.n_partials = L.n_partials;
   ws.nwall = L.nwall;
   ws.fixed_workers = num_splits > 0 ? num_splits : 0;
+  P.new_k = fw.k;
+  P.new_v = fw.v;
+  P.new_dtype = fw.dtype;
+  P.cu_new = fw.cu_new;
+  P.num_new = fw.num_tokens;
   cudaError_t e = kvq::launch_decode(P, ws, L.grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_paging* paging, const void* q, int32_t dtype,
+                           int32_t num_q_heads, float softmax_scale, float* out, void* workspace,
+                           size_t workspace_bytes, int32_t num_splits, int32_t* dev_error, void* stream) {
+  return decode_call(cache, paging, q, dtype, num_q_heads, softmax_scale, out, workspace, workspace_bytes, num_splits,
+                     dev_error, stream, FusedWrite());
+}
+
+kvq_status kvq_write_decode_attn(const kvq_cache* cache, const kvq_paging* paging, const void* k, const void* v,
+                                 int32_t kv_dtype, const int32_t* cu_new_tokens, int32_t num_tokens, const void* q,
+                                 int32_t q_dtype, int32_t num_q_heads, float softmax_scale, float* out,
+                                 void* workspace, size_t workspace_bytes, int32_t num_splits, int32_t* dev_error,
+                                 void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (cache->mode == KVQ_INT8_CHANNEL)
+    return fail(KVQ_ERR_UNSUPPORTED, "the fused write + decode does not take INT8 per-channel caches");
+  if ((st = check_paging(paging, cache->num_kv_heads)) != KVQ_OK) return st;
+  if (num_tokens < 0) return fail(KVQ_ERR_INVALID_ARG, "num_tokens < 0");
+  FusedWrite fw;
+  if (num_tokens > 0 && paging->batch > 0) {
+    if (!k || !v || !cu_new_tokens) return fail(KVQ_ERR_INVALID_ARG, "k / v / cu_new_tokens is NULL");
+    if (kv_dtype != KVQ_F32 && kv_dtype != KVQ_BF16)
+      return fail(KVQ_ERR_UNSUPPORTED, "kv_dtype must be KVQ_F32 or KVQ_BF16");
+    if (!aligned(k, 16) || !aligned(v, 16)) return fail(KVQ_ERR_INVALID_ARG, "k / v must be 16-byte aligned");
+    fw.k = k;
+    fw.v = v;
+    fw.dtype = kv_dtype;
+    fw.cu_new = cu_new_tokens;
+    fw.num_tokens = num_tokens;
+  }
+  return decode_call(cache, paging, q, q_dtype, num_q_heads, softmax_scale, out, workspace, workspace_bytes,
+                     num_splits, dev_error, stream, fw);
 }
 
 kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_paging* paging, const void* q,

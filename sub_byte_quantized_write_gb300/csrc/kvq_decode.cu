@@ -48,6 +48,7 @@
 #include <type_traits>
 
 #include "kvq_internal.h"
+#include "kvq_row.cuh"
 
 namespace kvq {
 
@@ -326,7 +327,48 @@ __host__ __device__ constexpr int decode_tile_keys() {
 // ---------------------------------------------------------------------------
 // 1. preparation
 
-template <int MODE, int D, int NT>
+// The new tokens' K and V rows of pair (b, h), written as kvq_write writes
+// them (the same row function, so the same bytes; a -1 destination is
+// skipped, errors set the same bits): the step's write fused into the
+// decode.  One warp per row, the CTA's four warps in turn.
+template <int MODE, int D, bool STEGO>
+__device__ __forceinline__ void fused_write_pair(const AttnParams& P, int b, int h) {
+  constexpr int EPL = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = P.num_kv_heads, bs = P.block_size;
+  const int t0 = __ldg(P.cu_new + b), n = __ldg(P.cu_new + b + 1) - t0;
+  if (n <= 0) return;
+  const int L = __ldg(P.seq_lens + b);
+  if (L < 0 || n > L) {
+    if (threadIdx.x == 0) flag_error(P.dev_error, DEVERR_SEQ_LEN);
+    return;
+  }
+  const int R = row_bytes_of(MODE, D);
+  const int32_t* tbl = P.table + (size_t)(P.headwise ? b * Hkv + h : b) * P.max_blocks;
+  for (int r = warp; r < 2 * n; r += 4) {
+    const int i = r >> 1, kv = r & 1;
+    if (t0 + i < 0 || t0 + i >= P.num_new) continue;  // as the write: rows 0 .. num_tokens - 1 only
+    const int p = L - n + i;
+    const int lb = p / bs;
+    if (lb >= P.max_blocks) {
+      if (lane == 0) flag_error(P.dev_error, DEVERR_TABLE_RANGE);
+      continue;
+    }
+    const int blk = __ldg(tbl + lb);
+    if (blk < 0) continue;  // evicted slot: nothing is written
+    if (blk >= P.num_blocks) {
+      if (lane == 0) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
+      continue;
+    }
+    float x[EPL];
+    load_row_elems<EPL>(kv ? P.new_v : P.new_k, P.new_dtype, ((size_t)(t0 + i) * Hkv + h) * D + lane * EPL, x);
+    uint8_t* pages = const_cast<uint8_t*>(kv ? P.v_pages : P.k_pages);
+    quantise_store_row<MODE, D, STEGO, 32>(P.signs, x, pages + (((size_t)blk * Hkv + h) * bs + p % bs) * R, lane,
+                                           true);
+  }
+}
+
+template <int MODE, int D, int NT, bool STEGO>
 __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs ws) {
   using C = DecCfg<MODE, D>;
   constexpr int EPL = D / 32;
@@ -420,6 +462,10 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
     dst[q4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
   if (MODE != MODE_INT8) grid_dependency_wait();
+  if constexpr (MODE != MODE_INT8) {
+    // the step's write, after the kernels before it are done with the pools
+    if (P.new_k) fused_write_pair<MODE, D, STEGO>(P, b, h);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1655,7 +1701,7 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int BH = P.batch * P.num_kv_heads;
-  e = launch_dependent(decode_prep_kernel<MODE, D, NT>, dim3(BH), dim3(128), 0, stream, P, ws);
+  e = launch_dependent(decode_prep_kernel<MODE, D, NT, STEGO>, dim3(BH), dim3(128), 0, stream, P, ws);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -65,6 +65,14 @@ struct AttnParams {
   // of page chunks (decode_chunk_rows), one chunk per box row.
   const int32_t* cu_kv;
   int chunk_rows_total;   // decode: rows of the kv_map tensors (the kernel copies no row at or past it)
+  // decode with the step's write (kvq_write_decode_attn): the preparation
+  // kernel quantises and stores the new K / V rows [num_new][Hkv][D] of
+  // new_dtype; sequence b's are rows cu_new[b] .. cu_new[b+1] - 1 (NULL new_k:
+  // no write)
+  const void* new_k;
+  const void* new_v;
+  int new_dtype, num_new;
+  const int32_t* cu_new;
   CUtensorMap kv_map[2];  // 128-byte aligned by its own declaration
 };
 

@@ -135,3 +135,17 @@ def test_prefill_grid_limits_are_checked_on_the_host(K):
     none.block_tables = None
     assert L.kvq_prefill_dense_attn(512, 512, 256, 64, 70000, 128, bref(none), 256, 1, 70000, 256, 4, 4, 0.1, 256,
                                     None, None) == K.KVQ_ERR_UNSUPPORTED
+
+
+def test_fused_write_decode_host_validation(K):
+    """kvq_write_decode_attn refuses INT8 per-channel caches (their first
+    write takes channel maxima over every token) and NULL write inputs."""
+    L = K.lib()
+    bref = ctypes.byref
+    int8 = _cache(K, mode=K.KVQ_INT8_CHANNEL, ch_amax=4096, ch_amax_ready=4096)
+    assert L.kvq_write_decode_attn(bref(int8), bref(_paging(K)), 4096, 4096, 1, 4096, 2, 256, 1, 8, 0.1, 256,
+                                   256, 1 << 20, 0, None, None) == K.KVQ_ERR_UNSUPPORTED
+    assert L.kvq_write_decode_attn(bref(_cache(K)), bref(_paging(K)), None, 4096, 1, 4096, 2, 256, 1, 8, 0.1, 256,
+                                   256, 1 << 20, 0, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert L.kvq_write_decode_attn(bref(_cache(K)), bref(_paging(K)), 4096, 4096, 7, 4096, 2, 256, 1, 8, 0.1, 256,
+                                   256, 1 << 20, 0, None, None) == K.KVQ_ERR_UNSUPPORTED
