@@ -157,6 +157,24 @@ __device__ __forceinline__ uint32_t kpair_int4_fold(uint32_t w) {
 }
 constexpr float KFOLD_INT4 = 72.0f;
 
+// INT2 key pairs without the subtraction: crumb P of each half goes to bit 4,
+// 6 or 8 of the half (from w << 4, w or w >> 6) and is OR-ed into 64, 16 or 4,
+// the value whose unit in the last place puts weight 1 on that bit: M_P + u
+// exactly, with M_P at most 64 so that the folded constant stays small next
+// to the products.  Pair P holds head dims 16w+P and 16w+P+8 (as kpair).
+template <int P>
+__device__ __forceinline__ uint32_t kpair_int2_fold(uint32_t w) {
+  constexpr int pos = (P == 0 || P == 2 || P == 5) ? 4 : (P == 1 || P == 3 || P == 6) ? 6 : 8;
+  constexpr uint32_t magic = pos == 4 ? 0x54005400u : pos == 6 ? 0x4C004C00u : 0x44004400u;  // 64, 16, 4
+  const uint32_t src = P <= 1 ? (w << 4) : P <= 4 ? w : (w >> 6);
+  return lop3_and_or(src, 0x00030003u << pos, magic);
+}
+// M_P + 2 for the head dim d (P = d mod 8): what the folded INT2 key value
+// adds to the signed code u - 2.
+__host__ __device__ constexpr float kfold_int2(int d) {
+  return (d & 7) == 4 || (d & 7) == 7 ? 6.0f : ((d & 7) == 1 || (d & 7) == 3 || (d & 7) == 6) ? 18.0f : 66.0f;
+}
+
 template <int MODE>
 __device__ __forceinline__ void kpair_dims(int w, int P, int& d0, int& d1) {
   if (MODE == MODE_INT4) { d0 = 8 * w + P; d1 = d0 + 4; }
@@ -419,7 +437,9 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
     amx = warp_max(amx);
     const int ex = amx > 0.0f ? ilogbf(amx) : 0;
     const float sc = ldexpf(1.0f, 10 - ex);  // max |q''| in [1024, 2048)
-    float opsum = 0.0f;  // sum of the exact operand values (hi + lo) for the folded key offset
+    // the folded key offset: sum over dims of the exact operand value (hi +
+    // lo) times the constant the folded key unpack adds to the signed code
+    float opsum = 0.0f;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
       const float v = x[e] * sc;
@@ -427,13 +447,14 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(AttnParams P, DecodeWs
       const __half lo = __float2half_rn(v - __half2float(hi));
       qh[0][i][lane * EPL + e] = hi;
       qh[1][i][lane * EPL + e] = lo;
-      opsum += __half2float(hi) + __half2float(lo);
+      const float kc = MODE == MODE_INT4 ? KFOLD_INT4 : MODE == MODE_INT2 ? kfold_int2(lane * EPL + e) : 0.0f;
+      opsum = fmaf(kc, __half2float(hi) + __half2float(lo), opsum);
     }
     opsum = warp_sum(opsum);
     if (lane == 0) {
       const float beta = i < G ? P.softmax_scale * log2e / (dnorm * sc) : 0.0f;
       const float gamma = i < G ? P.softmax_scale * log2e * sum / dnorm : 0.0f;
-      const float corr = MODE == MODE_INT4 ? KFOLD_INT4 * opsum : 0.0f;
+      const float corr = opsum;
       ws.qbg[(size_t)bh * NH + i] = make_float4(beta, gamma, corr, 0.0f);
     }
   }
@@ -1360,6 +1381,11 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
               av[1] = kpair_int4_fold<2 * sig>(kw[h2][m][1]);
               av[2] = kpair_int4_fold<2 * sig + 1>(kw[h2][m][0]);
               av[3] = kpair_int4_fold<2 * sig + 1>(kw[h2][m][1]);
+            } else if constexpr (MODE == MODE_INT2) {
+              av[0] = kpair_int2_fold<2 * sig>(kw[h2][m][0]);
+              av[1] = kpair_int2_fold<2 * sig>(kw[h2][m][1]);
+              av[2] = kpair_int2_fold<2 * sig + 1>(kw[h2][m][0]);
+              av[3] = kpair_int2_fold<2 * sig + 1>(kw[h2][m][1]);
             } else {
               av[0] = kpair<MODE, 2 * sig>(kw[h2][m][0]);
               av[1] = kpair<MODE, 2 * sig>(kw[h2][m][1]);
