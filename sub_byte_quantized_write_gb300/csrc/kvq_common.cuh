@@ -330,6 +330,7 @@ __device__ __forceinline__ void pad_scale_zero(uint32_t pad, bool stego, float& 
   }
 }
 __device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ void sts128(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 }  // namespace kvq

@@ -363,6 +363,7 @@ __device__ __forceinline__ void fused_write_pair(const AttnParams& P, int b, int
   }
   const int R = row_bytes_of(MODE, D);
   const int32_t* tbl = P.table + (size_t)(P.headwise ? b * Hkv + h : b) * P.max_blocks;
+  const RowSigns<EPL> sg = load_row_signs<EPL>(P.signs, lane);
   for (int r = warp; r < 2 * n; r += 4) {
     const int i = r >> 1, kv = r & 1;
     if (t0 + i < 0 || t0 + i >= P.num_new) continue;  // as the write: rows 0 .. num_tokens - 1 only
@@ -381,7 +382,7 @@ __device__ __forceinline__ void fused_write_pair(const AttnParams& P, int b, int
     float x[EPL];
     load_row_elems<EPL>(kv ? P.new_v : P.new_k, P.new_dtype, ((size_t)(t0 + i) * Hkv + h) * D + lane * EPL, x);
     uint8_t* pages = const_cast<uint8_t*>(kv ? P.v_pages : P.k_pages);
-    quantise_store_row<MODE, D, STEGO, 32>(P.signs, x, pages + (((size_t)blk * Hkv + h) * bs + p % bs) * R, lane,
+    quantise_store_row<MODE, D, STEGO, 32>(sg, x, pages + (((size_t)blk * Hkv + h) * bs + p % bs) * R, lane,
                                            true);
   }
 }

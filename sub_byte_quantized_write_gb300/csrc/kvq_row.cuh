@@ -13,27 +13,89 @@
 
 namespace kvq {
 
+// The quantiser's code before clamping is rint(RN(d / s)).  It is first
+// taken as the nearest integer k of t = RN(d r), r = RN(1 / s):
+// t = (d / s)(1 + e1)(1 + e2) with |e1|, |e2| <= 2^-24, so |t - d/s| <=
+// |d/s| 2^-22.99, below 2^-14.9 while |t| < 256.  Where t is farther than
+// 2^-14 from every half-integer, the exact quotient and its correctly rounded
+// value lie on the same side of the same half-integer as t and round to k;
+// where |t| >= 256 every code in use (at most 127 in size) clamps to the same
+// end either way.  near_half marks the elements within 2^-14 of a
+// half-integer (ties among them; for |t| >= 2^22 possibly more, which only
+// costs time); a lane with one of them, or whose 1 / s is not a finite
+// float, recomputes its codes with the correctly rounded division.  k comes from adding and
+// removing 1.5 * 2^23 (round-half-even for |t| < 2^22; a larger |t| keeps its
+// sign and size, which is all the clamp needs).
+__device__ __forceinline__ float quotient_rint_fast(float d, float r, bool& near_half) {
+  const float t = __fmul_rn(d, r);
+  const float k = __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
+  near_half |= fabsf(__fsub_rn(t, k)) >= 0.49993896484375f;  // 0.5 - 2^-14
+  return k;
+}
+
+// The RHT signs of a lane's EPL elements as float sign-bit masks (0 or
+// 0x80000000): x XOR mask is the exact product with the +-1 sign.  Loaded
+// once and reused for every row the lane rotates.
+template <int EPL>
+struct RowSigns {
+  uint32_t m[EPL];
+  bool on;
+};
+template <int EPL>
+__device__ __forceinline__ RowSigns<EPL> load_row_signs(const int8_t* signs, int sub) {
+  RowSigns<EPL> r;
+  r.on = signs != nullptr;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) r.m[i] = 0;
+  if (!r.on) return r;
+  const int8_t* p = signs + sub * EPL;
+  if constexpr (EPL % 4 == 0) {
+    if ((reinterpret_cast<uintptr_t>(signs) & (EPL >= 16 ? 15 : EPL - 1)) == 0) {  // whole words
+      uint32_t w[EPL / 4];
+      if constexpr (EPL >= 16) {
+#pragma unroll
+        for (int v = 0; v < EPL / 16; ++v) {
+          const uint4 q = __ldg(reinterpret_cast<const uint4*>(p) + v);
+          w[4 * v] = q.x; w[4 * v + 1] = q.y; w[4 * v + 2] = q.z; w[4 * v + 3] = q.w;
+        }
+      } else if constexpr (EPL == 8) {
+        const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+        w[0] = q.x; w[1] = q.y;
+      } else {
+        w[0] = __ldg(reinterpret_cast<const unsigned int*>(p));
+      }
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) r.m[i] = (w[i / 4] << (24 - 8 * (i % 4))) & 0x80000000u;
+      return r;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) r.m[i] = (uint32_t)(__ldg(p + i) & 0x80) << 24;
+  return r;
+}
+
 // Rotate, quantise, pack and store one row at dst.  The row is held by LPR
 // consecutive lanes (32: a warp per row; 8: four rows per warp), lane `sub`
 // of the group holding elements sub * EPL .. + EPL - 1 (EPL = D / LPR).
 // Every step is one IEEE operation in a fixed order (butterfly stages
 // h = 1, 2, ..., D/2, exact min / max, one division for the scale, fp16 RNE,
-// one subtract and one divide per element, round-half-even), so the bytes
+// one subtract and one correctly rounded divide per element (reached through
+// a multiply wherever that provably gives the same integer),
+// round-half-even), so the bytes
 // match any other evaluation in that order, whatever LPR.  Every lane of
 // the warp must call this (the shuffles span the warp); `store` is false
 // for a group whose row is not written.
 template <int MODE, int D, bool STEGO, int LPR>
-__device__ __forceinline__ void quantise_store_row(const int8_t* signs, float (&x)[D / LPR], uint8_t* dst, int lane,
-                                                   bool store) {
+__device__ __forceinline__ void quantise_store_row(const RowSigns<D / LPR>& sg, float (&x)[D / LPR], uint8_t* dst,
+                                                   int lane, bool store) {
   constexpr int EPL = D / LPR;
   constexpr int BITS = mode_bits(MODE);
   constexpr int LEVELS = (1 << BITS) - 1;
   constexpr int DATA = data_bytes(MODE, D);
   const int sub = lane & (LPR - 1);
-  if (signs) {
+  if (sg.on) {
 #pragma unroll
-    for (int i = 0; i < EPL; ++i)
-      if (__ldg(signs + sub * EPL + i) < 0) x[i] = -x[i];
+    for (int i = 0; i < EPL; ++i) x[i] = __uint_as_float(__float_as_uint(x[i]) ^ sg.m[i]);
     // stages h = 1 .. EPL/2 in lane, then h = EPL .. D/2 over the group's lanes
 #pragma unroll
     for (int h = 1; h < EPL; h <<= 1) {
@@ -73,15 +135,31 @@ __device__ __forceinline__ void quantise_store_row(const int8_t* signs, float (&
 #pragma unroll
     for (int lm = 1; lm < LPR; lm <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, lm));
     const float s = __fdiv_rn(amax, MODE == MODE_I8T ? 127.0f : 448.0f);
+    if (s != 0.0f) {
+      if constexpr (MODE == MODE_I8T) {
+        const float rs = __frcp_rn(s);
+        bool exact = !(rs <= 3.402823466e38f);
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      uint32_t c = 0;
-      if (s != 0.0f) {
-        const float t = __fdiv_rn(x[i], s);
-        if constexpr (MODE == MODE_I8T) c = (uint32_t)(int)fminf(fmaxf(rintf(t), -127.0f), 127.0f) & 0xFFu;
-        else c = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);  // nearest even
+        for (int i = 0; i < EPL; ++i) {
+          const float k = quotient_rint_fast(x[i], rs, exact);
+          bits[i / CPW] |= ((uint32_t)(int)fminf(fmaxf(k, -127.0f), 127.0f) & 0xFFu) << ((i % CPW) * BITS);
+        }
+        if (exact) {  // rare: recompute this lane's codes with the division
+#pragma unroll
+          for (int k = 0; k < NW; ++k) bits[k] = 0;
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) {
+            const float k = rintf(__fdiv_rn(x[i], s));
+            bits[i / CPW] |= ((uint32_t)(int)fminf(fmaxf(k, -127.0f), 127.0f) & 0xFFu) << ((i % CPW) * BITS);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const uint32_t c = __nv_cvt_float_to_fp8(__fdiv_rn(x[i], s), __NV_SATFINITE, __NV_E4M3);  // nearest even
+          bits[i / CPW] |= c << ((i % CPW) * BITS);
+        }
       }
-      bits[i / CPW] |= c << ((i % CPW) * BITS);
     }
     pad = __float_as_uint(s);
   } else {
@@ -106,15 +184,23 @@ __device__ __forceinline__ void quantise_store_row(const int8_t* signs, float (&
       const float st = __uint_as_float(sb);
       float zp = 0.0f;
       if (st != 0.0f) zp = fminf(fmaxf(rintf(__fdiv_rn(-lo, st)), 0.0f), (float)LEVELS);
+      if (st != 0.0f) {
+        const float rst = __frcp_rn(st);
+        bool exact = !(rst <= 3.402823466e38f);
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        uint32_t u = 0;
-        if (st != 0.0f) {
-          float r = __fadd_rn(rintf(__fdiv_rn(x[i], st)), zp);
-          r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
-          u = (uint32_t)r;
+        for (int i = 0; i < EPL; ++i) {
+          const float r = __fadd_rn(quotient_rint_fast(x[i], rst, exact), zp);
+          bits[i / CPW] |= (uint32_t)fminf(fmaxf(r, 0.0f), (float)LEVELS) << ((i % CPW) * BITS);
         }
-        bits[i / CPW] |= u << ((i % CPW) * BITS);
+        if (exact) {  // rare: recompute this lane's codes with the division
+#pragma unroll
+          for (int k = 0; k < NW; ++k) bits[k] = 0;
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) {
+            const float r = __fadd_rn(rintf(__fdiv_rn(x[i], st)), zp);
+            bits[i / CPW] |= (uint32_t)fminf(fmaxf(r, 0.0f), (float)LEVELS) << ((i % CPW) * BITS);
+          }
+        }
       }
       pad = sb | (uint32_t)zp;
     } else {
@@ -123,15 +209,23 @@ __device__ __forceinline__ void quantise_store_row(const int8_t* signs, float (&
       const uint16_t m_h = f16_sat_bits(mn);
       const float S = __half2float(__ushort_as_half(s_h));
       const float M = __half2float(__ushort_as_half(m_h));
+      if (S != 0.0f) {
+        const float rS = __frcp_rn(S);
+        bool exact = !(rS <= 3.402823466e38f);
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        uint32_t u = 0;
-        if (S != 0.0f) {
-          float r = rintf(__fdiv_rn(__fsub_rn(x[i], M), S));
-          r = fminf(fmaxf(r, 0.0f), (float)LEVELS);
-          u = (uint32_t)r;
+        for (int i = 0; i < EPL; ++i) {
+          const float k = quotient_rint_fast(__fsub_rn(x[i], M), rS, exact);
+          bits[i / CPW] |= (uint32_t)fminf(fmaxf(k, 0.0f), (float)LEVELS) << ((i % CPW) * BITS);
         }
-        bits[i / CPW] |= u << ((i % CPW) * BITS);
+        if (exact) {  // rare: recompute this lane's codes with the division
+#pragma unroll
+          for (int k = 0; k < NW; ++k) bits[k] = 0;
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) {
+            const float k = rintf(__fdiv_rn(__fsub_rn(x[i], M), S));
+            bits[i / CPW] |= (uint32_t)fminf(fmaxf(k, 0.0f), (float)LEVELS) << ((i % CPW) * BITS);
+          }
+        }
       }
       pad = (uint32_t)s_h | ((uint32_t)m_h << 16);
     }

@@ -24,6 +24,8 @@
 // one subtract and one divide per element, round-half-even), so the packed
 // bytes are identical to any other evaluation in the same order.
 
+#include <algorithm>
+
 #include "kvq_internal.h"
 #include "kvq_row.cuh"
 
@@ -108,9 +110,10 @@ __global__ void __launch_bounds__(256) write_token_head_kernel(WriteParams P) {
   if (t >= P.num_tokens) return;
   float x[EPL];  // issued before the (dependent) table lookups
   load_row_elems<EPL>(kv ? P.v : P.k, P.dtype, ((size_t)t * P.num_kv_heads + h) * D + lane * EPL, x);
+  const RowSigns<EPL> sg = load_row_signs<EPL>(P.signs, lane);
   uint8_t* dst = dest_row(P, kv ? P.v_pages : P.k_pages, (int)t, h, lane);
   if (dst == nullptr) return;  // warp-uniform
-  quantise_store_row<MODE, D, STEGO, 32>(P.signs, x, dst, lane, true);
+  quantise_store_row<MODE, D, STEGO, 32>(sg, x, dst, lane, true);
 }
 
 // INT8, pass 1 (only while *ready == 0): per-channel max |x| over all tokens.
@@ -387,61 +390,164 @@ cudaError_t launch_gather(const WriteParams& P, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// Long writes (a prefill chunk): one warp per WRITE_TOKENS = 4 consecutive
-// tokens of a kv head, eight lanes per row: lane group g (lanes 8g .. 8g+7)
-// takes token t0 + g, first its K row, then its V row.  With D/8 elements per
+// The write of a long chunk: persistent warps, each taking units of four
+// tokens of one kv head in turn (unit u: tokens 4 (u / Hkv) .. + 3, head
+// u % Hkv).  Eight lanes per row: lane group g (lanes 8g .. 8g+7) takes token
+// 4 (u / Hkv) + g, first its K row, then its V row.  With D/8 elements per
 // lane the butterfly's first log2(D/8) stages and most of the min / max run
-// in registers and the packed bytes form in lane (no word gather).  Lanes
-// 0..3 locate one token each (the gather's lookup, which flags the same
-// errors as dest_row).  The row arithmetic is quantise_store_row's, so the
-// bytes are those of write_token_head_kernel.
+// in registers and the packed bytes form in lane (no word gather).  While a
+// unit is quantised, the warp's next unit's input rows are already on their
+// way into its shared-memory stage (cp.async) and lanes 0..3 have looked up
+// its destinations (the gather's lookup, which flags the same errors as
+// dest_row).  The row arithmetic is quantise_store_row's, so the bytes are
+// those of write_token_head_kernel.
 constexpr int WRITE_TOKENS = 4;
 constexpr int WRITE_LPR = 32 / WRITE_TOKENS;  // lanes per row
 constexpr int WRITE_BATCH_MIN_TOKENS = 512;
+constexpr int WRITE_WARPS = 8;   // per CTA
+constexpr int WRITE_STAGES = 2;  // input stages per warp
+constexpr int WRITE_CTAS_PER_SM = 3;
 
-template <int MODE, int D, bool STEGO>
-__global__ void __launch_bounds__(256) write_batch_kernel(WriteParams P) {
+// Shared memory of write_batch_kernel: per warp and stage, the unit's K rows
+// then V rows as they are in the input ([4][D] of the input dtype each).
+inline size_t write_batch_smem(int head_dim, int dtype) {
+  return (size_t)WRITE_WARPS * WRITE_STAGES * 2 * WRITE_TOKENS * head_dim * (dtype == DT_F32 ? 4 : 2);
+}
+
+template <int MODE, int D, bool STEGO, bool F32>
+__global__ void __launch_bounds__(WRITE_WARPS * 32, WRITE_CTAS_PER_SM) write_batch_kernel(WriteParams P) {
   constexpr int EPL = D / WRITE_LPR;
-  const int lane = threadIdx.x & 31;
+  constexpr int ESZ = F32 ? 4 : 2;
+  constexpr int IN_ROW = D * ESZ;                        // bytes of one input row
+  constexpr int UNIT = 2 * WRITE_TOKENS * IN_ROW;        // K rows, then V rows
+  constexpr int CPR = IN_ROW / 16;                       // 16-byte pieces per row
+  static_assert((UNIT / 16) % 32 == 0, "whole pieces per lane");
+  extern __shared__ __align__(16) uint8_t wsm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane / WRITE_LPR, sub = lane % WRITE_LPR;
   allow_dependent_launch();  // as in write_token_head_kernel
-  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int h = (int)(wid % P.num_kv_heads);
-  const long long t0 = (wid / P.num_kv_heads) * WRITE_TOKENS;
-  if (t0 >= P.num_tokens) return;  // warp-uniform
-  const long long t = t0 + g;
-  const bool have = t < P.num_tokens;
-  float x[2][EPL];
-  if (have) {
-    const size_t e = ((size_t)t * P.num_kv_heads + h) * D + sub * EPL;
-    load_row_elems<EPL>(P.k, P.dtype, e, x[0]);
-    load_row_elems<EPL>(P.v, P.dtype, e, x[1]);
-  } else {
+  const int Hkv = P.num_kv_heads;
+  const int groups = (P.num_tokens + WRITE_TOKENS - 1) / WRITE_TOKENS;
+  uint8_t* buf = wsm + (size_t)warp * WRITE_STAGES * UNIT;
+  const RowSigns<EPL> sg = load_row_signs<EPL>(P.signs, sub);  // shared by every row of this lane
+  // unit u = grp * Hkv + h, taken by warps u, u + nw, u + 2 nw, ...
+  const int nw = gridDim.x * WRITE_WARPS;
+  const int step_g = nw / Hkv, step_h = nw % Hkv;
+  const int w0 = blockIdx.x * WRITE_WARPS + warp;
+  int grp = w0 / Hkv, h = w0 % Hkv;
+
+  // input rows of unit (gg, hh) into stage st (rows past the input are not read)
+  auto issue = [&](int gg, int hh, int st) {
+    if (gg < groups) {
+      uint8_t* dst = buf + st * UNIT;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) x[0][i] = x[1][i] = 0.0f;
+      for (int k = 0; k < UNIT / 16 / 32; ++k) {
+        const int c = lane + 32 * k;
+        const int row = c / CPR, part = c % CPR;
+        const int t = gg * WRITE_TOKENS + row % WRITE_TOKENS;
+        if (t < P.num_tokens)
+          cp_async16(dst + 16 * c,
+                     static_cast<const uint8_t*>(row < WRITE_TOKENS ? P.k : P.v) + ((size_t)t * Hkv + hh) * IN_ROW +
+                         16 * part,
+                     16);
+      }
+    }
+    cp_async_commit();
+  };
+  // destination byte offset of token WRITE_TOKENS gg + lane (lanes 0..3), -1: none
+  auto lookup = [&](int gg, int hh) -> long long {
+    if (gg >= groups || lane >= WRITE_TOKENS) return -1;
+    return gather_row_offset<false>(P, gg * WRITE_TOKENS + lane, hh);
+  };
+
+  issue(grp, h, 0);
+  long long my_off = lookup(grp, h);
+  int st = 0;
+  while (grp < groups) {
+    int ng = grp + step_g, nh = h + step_h;
+    if (nh >= Hkv) {
+      nh -= Hkv;
+      ++ng;
+    }
+    issue(ng, nh, st ^ 1);
+    const long long next_off = lookup(ng, nh);
+    cp_async_wait<1>();  // this unit's rows have landed
+    __syncwarp();
+    float x[2][EPL];
+    const uint8_t* src = buf + st * UNIT + g * IN_ROW + sub * EPL * ESZ;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint8_t* r = src + kv * WRITE_TOKENS * IN_ROW;
+#pragma unroll
+      for (int c = 0; c < EPL * ESZ / 16; ++c) {
+        const uint4 v = lds128(r + 16 * c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if constexpr (F32) {
+            x[kv][4 * c + k] = __uint_as_float(w[k]);
+          } else {
+            x[kv][8 * c + 2 * k] = __uint_as_float(w[k] << 16);
+            x[kv][8 * c + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane has read this stage before it is filled again
+    const long long off = __shfl_sync(0xffffffffu, my_off, g);  // -1: an evicted, invalid or absent row
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv)
+      quantise_store_row<MODE, D, STEGO, WRITE_LPR>(sg, x[kv], (kv ? P.v_pages : P.k_pages) + (off >= 0 ? off : 0),
+                                                    lane, off >= 0);
+    my_off = next_off;
+    grp = ng;
+    h = nh;
+    st ^= 1;
   }
-  long long my_off = -1;
-  if (lane < WRITE_TOKENS) my_off = gather_row_offset<false>(P, (int)(t0 + lane), h);
-  const long long off = __shfl_sync(0xffffffffu, my_off, g);  // -1: an evicted, invalid or absent row
-#pragma unroll
-  for (int kv = 0; kv < 2; ++kv)
-    quantise_store_row<MODE, D, STEGO, WRITE_LPR>(P.signs, x[kv], (kv ? P.v_pages : P.k_pages) + (off >= 0 ? off : 0), lane,
-                                                  off >= 0);
+  cp_async_wait<0>();
 }
 
 template <int MODE, bool STEGO>
-void launch_write_m(const WriteParams& P, cudaStream_t stream) {
+cudaError_t launch_write_m(const WriteParams& P, cudaStream_t stream) {
   if (P.num_tokens >= WRITE_BATCH_MIN_TOKENS) {
-    const long long warps = (long long)((P.num_tokens + WRITE_TOKENS - 1) / WRITE_TOKENS) * P.num_kv_heads;
-    const int blocks = (int)((warps + 7) / 8);
-    if (P.head_dim == 128) write_batch_kernel<MODE, 128, STEGO><<<blocks, 256, 0, stream>>>(P);
-    else write_batch_kernel<MODE, 64, STEGO><<<blocks, 256, 0, stream>>>(P);
+    // one CTA of eight persistent warps per unit group, at most
+    // WRITE_CTAS_PER_SM per SM; the opt-in shared-memory size is set once per
+    // device (not inside later calls, which may be captured into a graph)
+    static bool attr_set[64] = {false};
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const size_t smem = write_batch_smem(P.head_dim, P.dtype);
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+      const int mx = (int)write_batch_smem(128, DT_F32);
+      const void* fns[4] = {(const void*)write_batch_kernel<MODE, 128, STEGO, false>,
+                            (const void*)write_batch_kernel<MODE, 128, STEGO, true>,
+                            (const void*)write_batch_kernel<MODE, 64, STEGO, false>,
+                            (const void*)write_batch_kernel<MODE, 64, STEGO, true>};
+      for (const void* f : fns)
+        if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)) != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    // units of four tokens of one kv head; the kernel counts them in 32 bits
+    const long long units = (long long)((P.num_tokens + WRITE_TOKENS - 1) / WRITE_TOKENS) * P.num_kv_heads;
+    const int blocks = (int)std::min<long long>((units + WRITE_WARPS - 1) / WRITE_WARPS, (long long)sms * WRITE_CTAS_PER_SM);
+    const dim3 grid(blocks), block(WRITE_WARPS * 32);
+    const bool f32 = P.dtype == DT_F32;
+    if (P.head_dim == 128) {
+      if (f32) write_batch_kernel<MODE, 128, STEGO, true><<<grid, block, smem, stream>>>(P);
+      else write_batch_kernel<MODE, 128, STEGO, false><<<grid, block, smem, stream>>>(P);
+    } else {
+      if (f32) write_batch_kernel<MODE, 64, STEGO, true><<<grid, block, smem, stream>>>(P);
+      else write_batch_kernel<MODE, 64, STEGO, false><<<grid, block, smem, stream>>>(P);
+    }
   } else {
     const long long warps = (long long)P.num_tokens * P.num_kv_heads * 2;
     const int blocks = (int)((warps + 7) / 8);
     if (P.head_dim == 128) write_token_head_kernel<MODE, 128, STEGO><<<blocks, 256, 0, stream>>>(P);
     else write_token_head_kernel<MODE, 64, STEGO><<<blocks, 256, 0, stream>>>(P);
   }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_write(const WriteParams& P, cudaStream_t stream) {
@@ -455,12 +561,11 @@ cudaError_t launch_write(const WriteParams& P, cudaStream_t stream) {
     else int8_quant_kernel<64><<<blocks, 256, 0, stream>>>(P);
     return cudaGetLastError();
   }
-  if (P.mode == MODE_I8T) launch_write_m<MODE_I8T, false>(P, stream);
-  else if (P.mode == MODE_F8T) launch_write_m<MODE_F8T, false>(P, stream);
-  else if (P.mode == MODE_INT4 && P.stego) launch_write_m<MODE_INT4, true>(P, stream);
-  else if (P.mode == MODE_INT4) launch_write_m<MODE_INT4, false>(P, stream);
-  else launch_write_m<MODE_INT2, false>(P, stream);
-  return cudaGetLastError();
+  if (P.mode == MODE_I8T) return launch_write_m<MODE_I8T, false>(P, stream);
+  if (P.mode == MODE_F8T) return launch_write_m<MODE_F8T, false>(P, stream);
+  if (P.mode == MODE_INT4 && P.stego) return launch_write_m<MODE_INT4, true>(P, stream);
+  if (P.mode == MODE_INT4) return launch_write_m<MODE_INT4, false>(P, stream);
+  return launch_write_m<MODE_INT2, false>(P, stream);
 }
 
 }  // namespace kvq
