@@ -348,7 +348,10 @@ int32_t kvq_abi_version(void);
  *
  * k, v          : bf16 [rows][num_kv_heads][head_dim], 16-byte aligned; sequence
  *                 b's key j is row cu_kv[b] + j (kvq_gather with n_b = seq_lens[b]
- *                 writes exactly this layout).  Values must lie in the fp16 range.
+ *                 writes exactly this layout).  The kernel converts the rows to
+ *                 fp16 (round to nearest): exact for 0 and 2^-17 <= |x| <= 65504;
+ *                 smaller magnitudes round to a multiple of 2^-24, larger ones
+ *                 become 65504 or infinity, so keep the rows inside that range.
  * cu_kv         : int32 [batch + 1] (device); cu_kv[b + 1] - cu_kv[b] >= seq_lens[b],
  *                 else the sequence is skipped and KVQ_DEVERR_SEQ_LEN set.
  * num_kv_rows   : rows of k and v (host); cu_kv[batch] <= num_kv_rows.  The rows

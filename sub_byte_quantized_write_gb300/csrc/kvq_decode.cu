@@ -12,22 +12,34 @@
 // vllm-ascend-quantized-kv-cache METADATA ("Ascend INT8 KV Cache Plugin"),
 // 运行机制 (decode dequantises inside the attention kernel).
 //
-// Design (GB300), three kernels per call:
-//  1. decode_prep_kernel: per (sequence, kv head) the count of 32-key tiles
-//     it must visit (sliding-window heads: sink tiles + window tiles) and its
-//     exclusive prefix sum over all (sequence, kv head) pairs; per pair the
-//     query fragments (q' split hi / lo, in the lane order of the MMA operand)
-//     and the per-head logit constants (for INT4 also the constant that the
-//     folded key unpack adds: 72 * sum of the query operand).
-//  2. decode_stream_kernel: persistent warps.  The concatenated tile lists of
-//     all pairs are cut into one contiguous, equal slice per warp
-//     ("stream-K"), so the work is balanced to within a tile whatever the
-//     context lengths.  Each warp streams its 32-key tiles (two 16-row page
-//     chunks each of K and V) through its own cp.async ring in shared memory,
-//     keeps its own online softmax, and writes one partial per pair its slice
-//     touches (no CTA-wide barrier in the loop).
+// Design (GB300), three kernels per call, chained by programmatic dependent
+// launch:
+//  1. decode_prep_kernel: one CTA per (sequence, kv head) pair: the query
+//     operand images (q' = H (d * q) split fp16 hi / lo, in the lane order of
+//     the MMA operand) and the per-head logit constants, including the
+//     constant the folded key unpack adds (INT4: 72 per dim; INT2: 66, 18 or
+//     6 by the dim's crumb position).  With kvq_write_decode_attn it also
+//     quantises and stores the step's new K / V rows of its pair, after the
+//     kernels before it are done with the pools.
+//  2. decode_tma_kernel (INT4 / INT2 / 8-bit token-head rows): persistent
+//     warps, 3 CTAs of 4 warps per SM for GQA groups up to 4 (2 for groups up
+//     to 8).  The concatenated tile lists of all pairs (64-key tiles for the
+//     4-bit and 2-bit rows at groups up to 4, else 32) are cut into one
+//     contiguous, equal slice per warp ("stream-K"), balanced to within a tile
+//     whatever the context lengths.  Each tile's K and V rows arrive by one
+//     cp.async.bulk.tensor ... tile::gather4 copy each: the pool is viewed as
+//     a 2-D tensor whose rows are page chunks of KT/4 key rows, so the tile's
+//     four chunks (from four pages anywhere in the pool) are four row
+//     coordinates of one copy, into the warp's ring of mbarrier-tracked
+//     stages.  Lanes 0-3 look up the next tile's table entries one tile ahead;
+//     a -1 entry or a chunk past the sequence points the copy at row 0 and is
+//     masked, never turned into the page's own address.  Full tiles run a
+//     body without masks.  CTA 0 publishes each pair's first tile for the
+//     merge.  decode_stream_kernel (INT8 per channel) is the same algorithm
+//     over 16-byte cp.async pieces with XOR-swizzled rows and its own scan.
 //  3. decode_reduce_kernel: per (sequence, q head) the log-sum-exp merge of
-//     the partials, the inverse RHT and 1 / l.
+//     the partials of the warps whose slices cover the pair, the inverse RHT
+//     and 1 / l.
 // The RHT and the dequantisation are folded into the query and the weights:
 //   q . k_j = (s_j (q' . c_j) + z_j sum(q')) / D,   q' = H (d * q)
 //   sum_j P_j v_j = d * H( sum_j (P_j s_j) c_j + sum_j P_j z_j ) / D

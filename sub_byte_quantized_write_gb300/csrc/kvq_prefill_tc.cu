@@ -110,8 +110,11 @@ enum {
   B_DRAIN = 18, B_XCH = 20, B_EPI = 28
 };
 
-// Two bf16 values (low half first) as an fp16 pair: exact for values inside
-// the fp16 range (bf16 carries 8 significant bits, fp16 11).
+// Two bf16 values (low half first) as an fp16 pair, rounded to nearest.  A
+// bf16 value carries 8 significant bits, so the conversion is exact for 0 and
+// for 2^-17 <= |x| <= 65504 (fp16 normals, and the subnormals that are
+// multiples of 2^-24).  Smaller magnitudes round to a multiple of 2^-24
+// (error at most 2^-25); magnitudes above 65504 become 65504 or infinity.
 __device__ __forceinline__ uint32_t bf16x2_to_half2_bits(uint32_t w) {
   const __half2 hv = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
   return *reinterpret_cast<const uint32_t*>(&hv);
