@@ -100,6 +100,9 @@ typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1 } kvq_dtype;
 #define KVQ_DEVERR_TABLE_RANGE 2 /* position / block_size >= max_blocks: row skipped */
 #define KVQ_DEVERR_SEQ_LEN 4     /* negative seq_len, or more new tokens than seq_len */
 #define KVQ_DEVERR_TIMEOUT 8     /* a bounded wait for an asynchronous copy gave up (never expected) */
+#define KVQ_DEVERR_BOUNDS 16     /* debug library only (libkvq_debug.so, built with -DKVQ_BOUNDS_CHECK):
+                                     an index computed on the device fell outside its buffer; the access
+                                     was skipped (never expected) */
 
 /* One layer's paged cache (caller-allocated; store it as torch.uint8, cf.
  * [FD-UINT8] 修复).

@@ -20,11 +20,15 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvq.so")
+# KVQ_BOUNDS_CHECK=1 loads the debug library: the same kernels with device-side
+# bounds checks on their computed indices (a failure sets KVQ_DEVERR_BOUNDS).
+BOUNDS_CHECK = os.environ.get("KVQ_BOUNDS_CHECK", "0") == "1"
+LIB_NAME = "libkvq_debug.so" if BOUNDS_CHECK else "libkvq.so"
+LIB_PATH = os.path.join(_HERE, LIB_NAME)
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("libkvq.so is not built: run `python sub_byte_quantized_write_gb300/build_lib.py` "
-                      "(or __graft_entry__.build()) first")
+    raise ImportError("%s is not built: run `python sub_byte_quantized_write_gb300/build_lib.py` "
+                      "(or __graft_entry__.build()) first" % LIB_NAME)
 
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -33,6 +37,7 @@ KVQ_INT4_TOKEN_HEAD, KVQ_INT2_TOKEN_HEAD, KVQ_INT8_CHANNEL, KVQ_INT4_STEGO = 0, 
 KVQ_INT8_TOKEN_HEAD, KVQ_FP8_TOKEN_HEAD = 4, 5
 KVQ_F32, KVQ_BF16 = 0, 1
 KVQ_DEVERR_BLOCK_RANGE, KVQ_DEVERR_TABLE_RANGE, KVQ_DEVERR_SEQ_LEN, KVQ_DEVERR_TIMEOUT = 1, 2, 4, 8
+KVQ_DEVERR_BOUNDS = 16  # debug library only
 
 
 class KvqCache(ctypes.Structure):

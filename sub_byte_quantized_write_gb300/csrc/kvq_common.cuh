@@ -14,7 +14,7 @@ namespace kvq {
 // bf16 rows (no codes, no scale).
 enum { MODE_INT4 = 0, MODE_INT2 = 1, MODE_INT8 = 2, MODE_I8T = 4, MODE_F8T = 5, MODE_DBF16 = 6 };
 enum { DT_F32 = 0, DT_BF16 = 1 };
-enum { DEVERR_BLOCK_RANGE = 1, DEVERR_TABLE_RANGE = 2, DEVERR_SEQ_LEN = 4, DEVERR_TIMEOUT = 8 };
+enum { DEVERR_BLOCK_RANGE = 1, DEVERR_TABLE_RANGE = 2, DEVERR_SEQ_LEN = 4, DEVERR_TIMEOUT = 8, DEVERR_BOUNDS = 16 };
 
 __host__ __device__ constexpr int mode_bits(int mode) {
   return mode == MODE_INT4 ? 4 : (mode == MODE_INT2 ? 2 : (mode == MODE_DBF16 ? 16 : 8));
@@ -44,6 +44,20 @@ __device__ __forceinline__ uint32_t e4m3x4_no_nan(uint32_t w) {
 __device__ __forceinline__ void flag_error(int32_t* dev_error, int bit) {
   if (dev_error) atomicOr(dev_error, bit);
 }
+
+// Debug builds (-DKVQ_BOUNDS_CHECK, libkvq_debug.so): indices that a kernel
+// computes are checked against their buffers before the access; a failed
+// check sets DEVERR_BOUNDS and the access is skipped.  Release builds compile
+// the checks away: there the conditions hold by construction.
+#ifdef KVQ_BOUNDS_CHECK
+__device__ __forceinline__ bool in_bounds(bool ok, int32_t* dev_error) {
+  if (!ok) flag_error(dev_error, DEVERR_BOUNDS);
+  return ok;
+}
+#define KVQ_IN_BOUNDS(ok, err) ::kvq::in_bounds((ok), (err))
+#else
+#define KVQ_IN_BOUNDS(ok, err) true
+#endif
 
 // Load EPL consecutive input elements (fp32 or bf16) as fp32 (EPL = 2, 4, 8
 // or 16; elem_off a multiple of EPL, so the vector loads are aligned).

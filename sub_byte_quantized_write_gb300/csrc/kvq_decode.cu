@@ -391,6 +391,7 @@ __device__ __forceinline__ void fused_write_pair(const AttnParams& P, int b, int
       if (lane == 0) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
       continue;
     }
+    if (!KVQ_IN_BOUNDS(((size_t)blk * Hkv + h) * bs + p % bs < (size_t)P.num_blocks * Hkv * bs, P.dev_error)) continue;
     float x[EPL];
     load_row_elems<EPL>(kv ? P.new_v : P.new_k, P.new_dtype, ((size_t)(t0 + i) * Hkv + h) * D + lane * EPL, x);
     uint8_t* pages = const_cast<uint8_t*>(kv ? P.v_pages : P.k_pages);
@@ -641,7 +642,9 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const int key = nx_key + 16 * c;
-        nx_blk[c] = key < nx_leff ? __ldg(is.tbl + (key >> bs_log2)) : -1;
+        nx_blk[c] = (key < nx_leff && KVQ_IN_BOUNDS((key >> bs_log2) < P.max_blocks, P.dev_error))
+                        ? __ldg(is.tbl + (key >> bs_log2))
+                        : -1;
       }
       ++x_lookup;
     }
@@ -666,6 +669,13 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
           if (lane == 0) flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
         }
         off[c] = ok ? (size_t)blk * blk_stride + (size_t)(key & (bs - 1)) * C::R : 0;
+        // the chunk's 16 rows lie inside the pool (kbase is head h's first page)
+        if (ok && !KVQ_IN_BOUNDS((size_t)nx_h * bs * C::R + off[c] + (size_t)C::CHUNK <=
+                                     (size_t)P.num_blocks * Hkv * bs * C::R,
+                                 P.dev_error)) {
+          ok = false;
+          off[c] = 0;
+        }
         valid |= (ok ? 1 : 0) << c;
       }
       if constexpr (BULK) {
@@ -714,7 +724,8 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
   auto begin_seg = [&](int x) {
     // partial record id: slice index + pair index (unique, see reduce)
     part_id = gw + cs.bh;
-    const uint4* src = reinterpret_cast<const uint4*>(ws.qfrag + ((size_t)cs.bh * 32 + lane) * PER_LANE);
+    const int qbh = KVQ_IN_BOUNDS(cs.bh >= 0 && cs.bh < BH, P.dev_error) ? cs.bh : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(ws.qfrag + ((size_t)qbh * 32 + lane) * PER_LANE);
     uint32_t tmp[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE / 4; ++i) {
@@ -728,7 +739,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
         bq[nt][s][0] = tmp[(nt * C::KSTEPS + s) * 2];
         bq[nt][s][1] = tmp[(nt * C::KSTEPS + s) * 2 + 1];
       }
-      const float4 bg = __ldg(ws.qbg + (size_t)cs.bh * NH + 4 * nt + tq);
+      const float4 bg = __ldg(ws.qbg + (size_t)qbh * NH + 4 * nt + tq);
       bet[nt] = bg.x;
       gam[nt] = bg.y;
       kcorr[nt] = bg.z;
@@ -752,7 +763,7 @@ __global__ void __launch_bounds__(128, (StreamCfg<MODE, D, NT>::CTAS)) decode_st
         pm += __shfl_xor_sync(0xffffffffu, pm, o);
       }
       const int head = 4 * nt + tq;
-      if (head < G) {
+      if (head < G && KVQ_IN_BOUNDS(part_id >= 0 && part_id < ws.n_partials, P.dev_error)) {
         float* po = ws.part_o + ((size_t)part_id * G + head) * D;
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
@@ -1026,13 +1037,15 @@ __device__ __forceinline__ void merge_records(const AttnParams& P, const DecodeW
   for (int e = 0; e < EPL; ++e) o[e] = 0.0f;
   // one round trip for the first 32 records' sums and the first four
   // records' outputs; lane j holds record w0 + j
+  // every record index w0 + r + bh must lie in the workspace
+  if (!KVQ_IN_BOUNDS(w0 >= 0 && nrec >= 1 && w0 + nrec - 1 + bh < ws.n_partials, P.dev_error)) nrec = 0;
   float2 ml0 = make_float2(-CUDART_INF_F, 0.0f);
   if (lane < nrec) ml0 = __ldcg(ws.part_ml + (size_t)(w0 + lane + bh) * G + i);
   constexpr int V0 = 8;  // records whose outputs load in the first round trip
   float v0[V0][EPL];
 #pragma unroll
   for (int u = 0; u < V0; ++u) {
-    const float* po = ws.part_o + ((size_t)(w0 + u + bh) * G + i) * D;
+    const float* po = ws.part_o + ((size_t)(u < nrec ? w0 + u + bh : 0) * G + i) * D;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) v0[u][e] = u < nrec ? __ldcg(po + lane + 32 * e) : 0.0f;
   }
@@ -1253,7 +1266,9 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
     if (nx_have) {
       while (x_lookup >= is.end) load_seg(P, is.bh + 1, is.end, is, KT);
       const int key = KT * tile_of(is.t, x_lookup - is.start) + TC::RPC * (lane & 3);
-      nx_e = (lane < 4 && key < is.t.Leff) ? __ldg(is.tbl + (key >> bs_log2)) : -1;
+      nx_e = (lane < 4 && key < is.t.Leff && KVQ_IN_BOUNDS((key >> bs_log2) < P.max_blocks, P.dev_error))
+                 ? __ldg(is.tbl + (key >> bs_log2))
+                 : -1;
       nx_sub = (key & (bs - 1)) >> TC::RPC_LOG2;
       nx_h = is.h;
       ++x_lookup;
@@ -1300,7 +1315,8 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
 
   auto begin_seg = [&]() {
     part_id = gw + cs.bh;  // partial record id: slice index + pair index (unique, see reduce)
-    const uint4* src = reinterpret_cast<const uint4*>(ws.qfrag + ((size_t)cs.bh * 32 + lane) * PER_LANE);
+    const int qbh = KVQ_IN_BOUNDS(cs.bh >= 0 && cs.bh < BH, P.dev_error) ? cs.bh : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(ws.qfrag + ((size_t)qbh * 32 + lane) * PER_LANE);
     uint32_t tmp[PER_LANE];
 #pragma unroll
     for (int i = 0; i < PER_LANE / 4; ++i) {
@@ -1314,7 +1330,7 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
         bq[nt][s][0] = tmp[(nt * C::KSTEPS + s) * 2];
         bq[nt][s][1] = tmp[(nt * C::KSTEPS + s) * 2 + 1];
       }
-      const float4 bg = __ldg(ws.qbg + (size_t)cs.bh * NH + 4 * nt + tq);
+      const float4 bg = __ldg(ws.qbg + (size_t)qbh * NH + 4 * nt + tq);
       bet[nt] = bg.x;
       gam[nt] = TC::BYTES ? 0.0f : bg.y;
       kap[nt] = TC::BYTES ? 0.0f : fmaf(-bg.x, bg.z, HR * bg.y);  // 2^(b-1) gamma - beta fold
@@ -1338,7 +1354,7 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
         pm += __shfl_xor_sync(0xffffffffu, pm, o);
       }
       const int head = 4 * nt + tq;
-      if (head < G) {
+      if (head < G && KVQ_IN_BOUNDS(part_id >= 0 && part_id < ws.n_partials, P.dev_error)) {
         float* po = ws.part_o + ((size_t)part_id * G + head) * D;
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
@@ -1664,7 +1680,7 @@ __global__ void __launch_bounds__(256) decode_reduce_kernel(AttnParams P, Decode
   grid_dependency_wait();  // every partial of the stream kernel is written
   const int T = ws.tile_start[BH];
   const int start = ws.tile_start[bh], end = ws.tile_start[bh + 1];
-  if (start >= end) {
+  if (start >= end || !KVQ_IN_BOUNDS(start >= 0 && end <= T, P.dev_error)) {
 #pragma unroll
     for (int e = 0; e < EPL; ++e) out[lane + 32 * e] = 0.0f;
     return;

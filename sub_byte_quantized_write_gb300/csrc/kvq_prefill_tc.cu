@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
     uint8_t* qlo = sm + C::OFF_K + TP_ROWS * C::QROW;  // [128 rows][QROW] fp16 lo
     for (int r = warp; r < TP_ROWS; r += TP_THREADS / 32) {
       const int ql = r / G, i = r % G;
-      const bool rv = ql < nq;
+      const bool rv = ql < nq && KVQ_IN_BOUNDS(cq0 + q0 + ql < P.total_q, P.dev_error);  // warp-uniform
       float x[EPL];
       if (rv) {
         load_row_elems<EPL>(P.q, P.dtype, ((size_t)(cq0 + q0 + ql) * Hq + h * G + i) * D + lane * EPL, x);
@@ -484,6 +484,13 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
             flag_error(P.dev_error, DEVERR_BLOCK_RANGE);
             ids0[c] = -1;
           }
+          // the chunk's 16 rows lie inside the pool (kbase is head h's first page)
+          if (ids0[c] >= 0 &&
+              !KVQ_IN_BOUNDS((size_t)h * bs * C::R + (size_t)ids0[c] * blk_stride +
+                                     (size_t)((key0 + 16 * c) & (bs - 1)) * C::R + C::CHUNK <=
+                                 (size_t)P.num_blocks * P.num_kv_heads * bs * C::R,
+                             P.dev_error))
+            ids0[c] = -1;
           if (ids0[c] >= 0) valid |= 1 << c;
           rawval[rs * 4 + c] = ids0[c] >= 0 ? 1 : 0;
         }
@@ -902,10 +909,12 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
           for (int e = 0; e < EPL; ++e) o[e] = o[e] * __fdiv_rn(am[e], 127.0f) / lr;
         }
         float* orow = P.out + ((size_t)(cq0 + q0 + ql) * Hq + h * G + i) * D + lane * EPL;
-        if constexpr (EPL == 4) {
-          *reinterpret_cast<float4*>(orow) = make_float4(o[0], o[1], o[2], o[3]);
-        } else {
-          *reinterpret_cast<float2*>(orow) = make_float2(o[0], o[1]);
+        if (KVQ_IN_BOUNDS(cq0 + q0 + ql < P.total_q, P.dev_error)) {
+          if constexpr (EPL == 4) {
+            *reinterpret_cast<float4*>(orow) = make_float4(o[0], o[1], o[2], o[3]);
+          } else {
+            *reinterpret_cast<float2*>(orow) = make_float2(o[0], o[1]);
+          }
         }
       }
     }

@@ -81,7 +81,9 @@ __device__ __forceinline__ uint8_t* dest_row(const WriteParams& P, uint8_t* page
     return nullptr;
   }
   const int R = row_bytes_of(P.mode, P.head_dim);
-  return pages + (((size_t)blk * P.num_kv_heads + h) * P.block_size + (p % P.block_size)) * R;
+  const size_t slot = ((size_t)blk * P.num_kv_heads + h) * P.block_size + (p % P.block_size);
+  if (!KVQ_IN_BOUNDS(slot < (size_t)P.num_blocks * P.num_kv_heads * P.block_size, P.dev_error)) return nullptr;
+  return pages + slot * R;
 }
 
 // OR-combine `bits` (nbits per lane) of groups of 32/nbits lanes into one
@@ -234,7 +236,9 @@ __device__ __forceinline__ long long gather_row_offset(const WriteParams& P, int
     return -1;
   }
   const int R = row_bytes_of(P.mode, P.head_dim);
-  return ((long long)((size_t)blk * P.num_kv_heads + h) * P.block_size + (p % P.block_size)) * R;
+  const size_t slot = ((size_t)blk * P.num_kv_heads + h) * P.block_size + (p % P.block_size);
+  if (!KVQ_IN_BOUNDS(slot < (size_t)P.num_blocks * P.num_kv_heads * P.block_size, P.dev_error)) return -1;
+  return (long long)slot * R;
 }
 
 // tsign: the lane's d_i / D factors of the inverse RHT (0 = RHT off)
@@ -306,7 +310,8 @@ __device__ __forceinline__ void gather_rows(const WriteParams& P, const uint32_t
     for (int r = 0; r < GATHER_TOKENS; ++r) {
       float y[EPL];
       if (CHUNK && off[r] <= -2) {
-        const long long src = -2 - off[r];
+        long long src = -2 - off[r];
+        if (!KVQ_IN_BOUNDS(src < (long long)__ldg(P.cu_chunk + P.batch), P.dev_error)) src = 0;
         load_row_elems<EPL>(kv ? P.chunk_v : P.chunk_k, P.chunk_dtype,
                             ((size_t)src * P.num_kv_heads + h) * D + lane * EPL, y);
       } else {

@@ -46,6 +46,18 @@ def test_library_exports_every_declared_symbol(K):
     assert lib.kvq_abi_version() == 1
 
 
+def test_debug_library_exports_every_declared_symbol(K):
+    """libkvq_debug.so (the -DKVQ_BOUNDS_CHECK build of the same sources)
+    loads and exports the same calls."""
+    path = os.path.join(os.path.dirname(K.LIB_PATH), "libkvq_debug.so")
+    if not os.path.exists(path):
+        pytest.skip("libkvq_debug.so not built")
+    lib = ctypes.CDLL(path)
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+    assert lib.kvq_abi_version() == 1
+
+
 def test_row_bytes(K):
     assert K.kvq_row_bytes(K.KVQ_INT4_TOKEN_HEAD, 128) == 68
     assert K.kvq_row_bytes(K.KVQ_INT4_TOKEN_HEAD, 64) == 36
