@@ -680,11 +680,12 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
     // ======================= softmax =======================
     // Row r is shared by warps r / 32 (keys 0-31 of each tile) and r / 32 + 4
     // (keys 32-63), which may both read TMEM lanes 32 (w % 4) ...  Per tile
-    // each half makes two passes over its 32 logits in 16-key chunks: pass 1
-    // forms y = s c.q'' + rho z (rho = gamma / beta), masks it, writes it back
-    // over S in TMEM and takes the half's maximum; the pair combines the two
-    // maxima through shared memory; pass 2 re-reads y, forms
-    // p = 2^(beta y - m) and writes (p s) hi / lo of its 32 keys to P.
+    // each half makes two passes over its 32 logits (two 16-key chunks, kept
+    // in registers between the passes): pass 1 forms y = s c.q'' + rho z
+    // (rho = gamma / beta), masks it and takes the half's maximum; the pair
+    // combines the two maxima through shared memory; pass 2 forms
+    // p = 2^(beta y - m) and writes (p s) hi / lo of its 32 keys to P, over
+    // the tile's S columns.
     const int quad = warp & 3, hf = warp >> 2;
     const int r = quad * 32 + lane;
     const float rb = rbeta[r];
@@ -713,11 +714,16 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
       const bool all_full = __all_sync(0xffffffffu, full);
       const uint32_t s_col = tmem + lane_base + st * TP_KT;
       float ymax = -CUDART_INF_F;
-#pragma unroll 1
-      for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
-        uint32_t rr[16];
-        tc::ld16(s_col + 16 * c, rr);
-        tc::wait_ld();
+      uint32_t yy[2][16];  // this half's 32 logits y, kept for pass 2
+      tc::ld16(s_col + 16 * (2 * hf), yy[0]);
+      tc::ld16(s_col + 16 * (2 * hf + 1), yy[1]);
+      tc::wait_ld();
+      tc::regs_after_wait(yy[0]);
+      tc::regs_after_wait(yy[1]);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hf + cc;
+        uint32_t (&rr)[16] = yy[cc];
 #pragma unroll
         for (int j4 = 0; j4 < 4; ++j4) {
           float4 ks = make_float4(0.f, 0.f, 0.f, 0.f), kz = ks;
@@ -744,7 +750,6 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
         }
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) ymax = fmaxf(ymax, __uint_as_float(rr[jj]));
-        tc::st16(s_col + 16 * c, rr);
       }
       // the pair's maxima meet in shared memory (bounded wait: a partner
       // that left the loop turns into an error, not a hang)
@@ -755,14 +760,14 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
         break;
       }
       ymax = fmaxf(ymax, xmax[(st * 2 + (hf ^ 1)) * TP_ROWS + r]);
-      tc::wait_st();
       // lazy rescale: keep the reference maximum until a row's maximum
       // passes it by more than 2^TP_SLACK (both halves decide alike)
       const float tmax = rb * ymax;
       const bool grow = tmax > mrow + TP_SLACK;
       const float mref = grow ? tmax : mrow;
       const float muse = mref == -CUDART_INF_F ? 0.0f : mref;
-      // the previous P.V must be done before P is overwritten or O rescaled
+      // the previous P.V must be done before O is rescaled (this wait also
+      // keeps the softmax within one tile of the MMA warp's P barrier)
       if (v >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_ODONE, (v - 1) & 1, TP_NAP_SOFTMAX))) {
         ok = false;
         break;
@@ -777,6 +782,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
           tc::ld16(tmem_o + lane_base + c0, ra);
           tc::ld16(tmem_o + lane_base + c0 + 16, rb2);
           tc::wait_ld();
+          tc::regs_after_wait(ra);
+          tc::regs_after_wait(rb2);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             ra[j] = __float_as_uint(__uint_as_float(ra[j]) * f);
@@ -791,11 +798,10 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
       }
       mrow = mref;
       float tl = 0.0f, tpz = 0.0f;
-#pragma unroll 1
-      for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
-        uint32_t rr[16];
-        tc::ld16(s_col + 16 * c, rr);
-        tc::wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * hf + cc;
+        const uint32_t (&rr)[16] = yy[cc];
         uint32_t pw[16];  // P hi (8 columns) then P lo (8 columns) of these 16 keys
 #pragma unroll
         for (int j4 = 0; j4 < 4; ++j4) {
@@ -856,6 +862,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
           tc::ld16(tmem_o + lane_base + c0, ra);
           tc::ld16(tmem_o + lane_base + c0 + 16, rb2);
           tc::wait_ld();
+          tc::regs_after_wait(ra);
+          tc::regs_after_wait(rb2);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             stage[r * P4 + ((c0 / 4 + j) ^ (r & 7))] =

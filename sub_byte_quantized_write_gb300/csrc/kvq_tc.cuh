@@ -89,6 +89,14 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
       : "memory");
 }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The registers a tcgen05.ld filled are final only after wait_ld: passing
+// them through an empty volatile asm placed after the wait keeps the compiler
+// from moving their uses above it.
+template <int N>
+__device__ __forceinline__ void regs_after_wait(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Four 8x8 fp16 matrices from registers to shared memory, transposed: lane
