@@ -133,7 +133,7 @@ kvq_status check_prefill_grid(const kvq::AttnParams& P) {
 kvq::DecodeLayout decode_layout(const kvq_cache* c, const kvq_paging* p, int32_t num_q_heads) {
   const int group = num_q_heads / c->num_kv_heads;
   return kvq::decode_ws_layout(p->batch, c->num_kv_heads, group, c->head_dim, sm_count(),
-                               kvq::decode_ctas_per_sm(kernel_mode(c->mode), c->head_dim, group));
+                               kvq::decode_shape(kernel_mode(c->mode), c->head_dim, group));
 }
 
 // Scratch of kvq_decode_attn_noalloc: one static device array per GPU that

@@ -22,8 +22,8 @@
 //     quantises and stores the step's new K / V rows of its pair, after the
 //     kernels before it are done with the pools.
 //  2. decode_tma_kernel (INT4 / INT2 / 8-bit token-head rows): persistent
-//     warps, 3 CTAs of 4 warps per SM for GQA groups up to 4 (2 for groups up
-//     to 8).  The concatenated tile lists of all pairs (64-key tiles for the
+//     warps, one CTA of 12 warps per SM for GQA groups up to 4 (two CTAs of 4
+//     for groups up to 8).  The concatenated tile lists of all pairs (64-key tiles for the
 //     4-bit and 2-bit rows at groups up to 4, else 32) are cut into one
 //     contiguous, equal slice per warp ("stream-K"), balanced to within a tile
 //     whatever the context lengths.  Each tile's K and V rows arrive by one
@@ -324,10 +324,17 @@ struct TmaCfg {
   static constexpr int TILE_AL = (TILE + 127) / 128 * 128;
   static constexpr int STAGE = 2 * TILE_AL;                   // K tile then V tile
   static constexpr int NSTAGE = STAGE >= 8000 ? 2 : (STAGE >= 4000 ? 3 : 4);
-  static constexpr int CTAS = NT == 1 ? 3 : 2;
+  // one n-tile: one CTA of 12 warps per SM, so that the SM's warps are not
+  // ranked by the age of the CTA they belong to (three CTAs of 4 warps finish
+  // in the order they started); two n-tiles: two CTAs of 4 warps, which
+  // measured faster there than one CTA of 8
+  static constexpr int WARPS = NT == 1 ? 3 * DECODE_WARPS : DECODE_WARPS;
+  static constexpr int CTAS = NT == 1 ? 1 : 2;
   static constexpr int XREG = 576;                            // exchange bytes per (half, n-tile)
   static constexpr bool XSMEM = NH2 * NT * XREG <= TILE;
   static_assert(RPC * R <= 2048 && (RPC * R) % 16 == 0, "a chunk must be one tensor-map box row");
+  static_assert(MODE == MODE_INT8 || WARPS * NSTAGE * (STAGE + 8) + 1024 <= 227 * 1024,
+                "the warps' rings must fit one SM");  // (INT8 per channel streams with cp.async instead)
 };
 
 // Rows per gathered chunk for the host's tensor maps (0: cp.async path),
@@ -1166,7 +1173,7 @@ __device__ __forceinline__ void output_signs(const AttnParams& P, int h, int lan
 //    and four 8-byte loads per lane, bank-conflict free.
 
 template <int MODE, int D, int NT, bool STEGO>
-__global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
+__global__ void __launch_bounds__(TmaCfg<MODE, D, NT>::WARPS * 32, (TmaCfg<MODE, D, NT>::CTAS))
     decode_tma_kernel(const __grid_constant__ AttnParams P, DecodeWs ws) {
   using C = DecCfg<MODE, D>;
   using TC = TmaCfg<MODE, D, NT>;
@@ -1185,41 +1192,47 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
   __shared__ int run_start[129];
   const int items = (BH + 127) / 128;
   {
+    // the first 128 threads scan: thread t owns pairs t * items ..
+    const bool scanner = threadIdx.x < 128;
     const int first = threadIdx.x * items;
-    int tsum = 0;
-    for (int k = 0; k < items && first + k < BH; ++k) {
-      const int bh = first + k;
-      tsum += tile_list(P, bh / Hkv, bh % Hkv, false, KT).n_virt;
-    }
-    int incl = tsum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    __shared__ int wtot[DECODE_WARPS];
-    if (lane == 31) wtot[warp] = incl;
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp; ++w) before += wtot[w];
-    run_start[threadIdx.x + 1] = before + incl;
-    if (threadIdx.x == 0) run_start[0] = 0;
-    if (blockIdx.x == 0) {
-      // CTA 0 publishes every pair's first tile for the merge kernel, and
-      // reports a negative seq_len or one past the table, once per sequence
-      int x = before + incl - tsum;
+    int tsum = 0, incl = 0;
+    __shared__ int wtot[4];
+    if (scanner) {
       for (int k = 0; k < items && first + k < BH; ++k) {
         const int bh = first + k;
-        ws.tile_start[bh] = x;
-        x += tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0, KT).n_virt;
+        tsum += tile_list(P, bh / Hkv, bh % Hkv, false, KT).n_virt;
       }
-      if (threadIdx.x == 127) ws.tile_start[BH] = before + incl;
+      incl = tsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) wtot[warp] = incl;
+    }
+    __syncthreads();
+    if (scanner) {
+      int before = 0;
+      for (int w = 0; w < warp; ++w) before += wtot[w];
+      run_start[threadIdx.x + 1] = before + incl;
+      if (threadIdx.x == 0) run_start[0] = 0;
+      if (blockIdx.x == 0) {
+        // CTA 0 publishes every pair's first tile for the merge kernel, and
+        // reports a negative seq_len or one past the table, once per sequence
+        int x = before + incl - tsum;
+        for (int k = 0; k < items && first + k < BH; ++k) {
+          const int bh = first + k;
+          ws.tile_start[bh] = x;
+          x += tile_list(P, bh / Hkv, bh % Hkv, bh % Hkv == 0, KT).n_virt;
+        }
+        if (threadIdx.x == 127) ws.tile_start[BH] = before + incl;
+      }
     }
     __syncthreads();
   }
   const int T = run_start[128];
-  const int nw = stream_workers(T, gridDim.x * DECODE_WARPS, ws.fixed_workers);
-  const int gw = blockIdx.x * DECODE_WARPS + warp;
+  const int nw = stream_workers(T, gridDim.x * TC::WARPS, ws.fixed_workers);
+  const int gw = blockIdx.x * TC::WARPS + warp;
   if (gw >= nw) return;  // whole warp; no CTA-wide barrier follows
   const int lo = slice_lo(gw, T, nw), hi = slice_lo(gw + 1, T, nw);
   if (lo >= hi) return;
@@ -1240,7 +1253,7 @@ __global__ void __launch_bounds__(128, (TmaCfg<MODE, D, NT>::CTAS))
     ++bh0;
   }
   uint8_t* ring = smem + warp * NSTAGE * TC::STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DECODE_WARPS * NSTAGE * TC::STAGE) + warp * NSTAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TC::WARPS * NSTAGE * TC::STAGE) + warp * NSTAGE;
   if (lane == 0) {
     for (int i = 0; i < NSTAGE; ++i) mbar_init(bars + i, 1);
     mbar_init_fence();
@@ -1702,20 +1715,21 @@ size_t stream_smem_bytes() {
   return (size_t)DECODE_WARPS * NSTAGE * SC::STAGE + DECODE_WARPS * NSTAGE * 4 + DECODE_WARPS * NSTAGE * 8;
 }
 
-template <int NT>
-int ctas_per_sm_nt(int mode) {
+// CTAs per SM and warps per CTA of the stream kernel one configuration launches
+template <int D, int NT>
+DecodeShape decode_shape_dnt(int mode) {
   switch (mode) {
-    case MODE_INT4: return TmaCfg<MODE_INT4, 128, NT>::CTAS;
-    case MODE_INT2: return TmaCfg<MODE_INT2, 128, NT>::CTAS;
-    case MODE_INT8: return StreamCfg<MODE_INT8, 128, NT>::CTAS;
-    case MODE_I8T: return TmaCfg<MODE_I8T, 128, NT>::CTAS;
-    default: return TmaCfg<MODE_F8T, 128, NT>::CTAS;
+    case MODE_INT4: return {TmaCfg<MODE_INT4, D, NT>::CTAS, TmaCfg<MODE_INT4, D, NT>::WARPS};
+    case MODE_INT2: return {TmaCfg<MODE_INT2, D, NT>::CTAS, TmaCfg<MODE_INT2, D, NT>::WARPS};
+    case MODE_INT8: return {StreamCfg<MODE_INT8, D, NT>::CTAS, DECODE_WARPS};
+    case MODE_I8T: return {TmaCfg<MODE_I8T, D, NT>::CTAS, TmaCfg<MODE_I8T, D, NT>::WARPS};
+    default: return {TmaCfg<MODE_F8T, D, NT>::CTAS, TmaCfg<MODE_F8T, D, NT>::WARPS};
   }
 }
 
-int decode_ctas_per_sm(int mode, int head_dim, int group) {
-  (void)head_dim;
-  return group > 4 ? ctas_per_sm_nt<2>(mode) : ctas_per_sm_nt<1>(mode);
+DecodeShape decode_shape(int mode, int head_dim, int group) {
+  if (head_dim == 64) return group > 4 ? decode_shape_dnt<64, 2>(mode) : decode_shape_dnt<64, 1>(mode);
+  return group > 4 ? decode_shape_dnt<128, 2>(mode) : decode_shape_dnt<128, 1>(mode);
 }
 
 template <typename Kern, typename... Args>
@@ -1737,7 +1751,7 @@ template <int MODE, int D, int NT, bool STEGO>
 cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, cudaStream_t stream) {
   constexpr bool TMA = MODE != MODE_INT8;
   using TC = TmaCfg<MODE, D, NT>;
-  const size_t smem = TMA ? (size_t)DECODE_WARPS * TC::NSTAGE * TC::STAGE + DECODE_WARPS * TC::NSTAGE * 8
+  const size_t smem = TMA ? (size_t)TC::WARPS * TC::NSTAGE * TC::STAGE + TC::WARPS * TC::NSTAGE * 8
                           : stream_smem_bytes<MODE, D, NT>();
   // the opt-in shared-memory size is set once per device (not inside later
   // calls, which may be captured into a CUDA graph)
@@ -1763,7 +1777,8 @@ cudaError_t launch_decode_t(const AttnParams& P, const DecodeWs& ws, int grid, c
   // the stream and merge kernels launch programmatically: their CTAs become
   // resident while the previous kernel drains and wait on its completion
   if constexpr (TMA)
-    e = launch_dependent(decode_tma_kernel<MODE, D, NT, STEGO>, dim3(grid), dim3(128), smem, stream, P, ws);
+    e = launch_dependent(decode_tma_kernel<MODE, D, NT, STEGO>, dim3(grid), dim3(TC::WARPS * 32), smem, stream, P,
+                         ws);
   else
     e = launch_dependent(decode_stream_kernel<MODE, D, NT>, dim3(grid), dim3(128), smem, stream, P, ws);
   if (e != cudaSuccess) return e;

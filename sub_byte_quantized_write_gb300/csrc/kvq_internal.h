@@ -93,6 +93,12 @@ constexpr int DECODE_KEYS_PER_TILE = 32;
 constexpr int DECODE_WARPS = 4;
 constexpr int DECODE_MIN_TILES_PER_WARP = 8;
 
+// How the stream kernel of one configuration is launched: CTAs per SM and
+// warps per CTA.
+struct DecodeShape {
+  int ctas_per_sm, warps_per_cta;
+};
+
 struct DecodeLayout {
   size_t off_tile_start, off_qfrag, off_qbg, off_part_ml, off_part_o, total;
   int grid, nwall, n_partials;
@@ -100,14 +106,15 @@ struct DecodeLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace layout for one decode call; sm_count * ctas_per_sm CTAs of 4 warps.
+// Workspace layout for one decode call; sm_count * ctas_per_sm CTAs of
+// warps_per_cta warps.
 inline DecodeLayout decode_ws_layout(int batch, int num_kv_heads, int group, int head_dim, int sm_count,
-                                     int ctas_per_sm) {
+                                     DecodeShape shape) {
   DecodeLayout L;
   const int BH = batch * num_kv_heads;
   const int NT = group <= 4 ? 1 : 2;
-  L.grid = sm_count * ctas_per_sm;
-  L.nwall = L.grid * DECODE_WARPS;
+  L.grid = sm_count * shape.ctas_per_sm;
+  L.nwall = L.grid * shape.warps_per_cta;
   L.n_partials = L.nwall + BH;
   size_t o = 0;
   L.off_tile_start = o; o = align256(o + (size_t)(BH + 1) * 4);
@@ -119,7 +126,7 @@ inline DecodeLayout decode_ws_layout(int batch, int num_kv_heads, int group, int
   return L;
 }
 
-int decode_ctas_per_sm(int mode, int head_dim, int group);
+DecodeShape decode_shape(int mode, int head_dim, int group);
 // Key rows per page chunk that the decode's tensor copies move (16 or 8), or 0
 // when the configuration copies its pages with cp.async (INT8 per channel).
 // The caller's tensor maps kv_map[0 | 1] view the K / V pool as 2-D tensors
