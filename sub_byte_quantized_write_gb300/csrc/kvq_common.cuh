@@ -315,6 +315,27 @@ __device__ __forceinline__ void tma_gather4_if(bool pred, void* dst, const void*
       : "memory");
 }
 
+// Same copy with an L2 cache policy (`policy` from l2_evict_first_policy()).
+__device__ __forceinline__ void tma_gather4_hint_if(bool pred, void* dst, const void* map, int r0, int r1, int r2,
+                                                    int r3, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %7, 0;\n\t"
+      "@p cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {0, %2, %3, %4, %5}], [%6], %8;\n\t}\n" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_addr(bar)), "r"((int)pred),
+      "l"(policy)
+      : "memory");
+}
+
+// An L2 policy under which the lines a load brings in are the first to be
+// evicted: for data read once, so that it does not push out data written
+// for a later kernel.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while its predecessor runs; it must call
 // grid_dependency_wait() before touching anything the predecessor writes.
