@@ -14,20 +14,25 @@
 // PR #7718 "Optimize AppendAttention for discrete head-wise block_idx"
 // (head-wise rows, -1 sentinel, sink tokens).
 //
-// Design: one CTA of 8 warps per (128 rows, kv head, sequence); the 128
+// Design: one CTA of 14 warps per (128 rows, kv head, sequence); the 128
 // rows are (query, q head of the GQA group) pairs, so every key tile is
 // expanded once for the whole group.  Roles:
-//   warps 0-3  softmax: thread r owns row r; reads its row of S from TMEM,
-//              applies masks, online softmax, writes (P s) hi / lo rows to
-//              shared memory, rescales its O row in TMEM when the max grows,
-//              and in the end applies the zero-point term, the inverse RHT and
-//              1 / l to its O row.
-//   warp 4     TMEM allocation; lane 0 issues every tcgen05.mma:
+//   warps 0-7  softmax: row r belongs to warps r / 32 (keys 0-31 of each
+//              tile) and r / 32 + 4 (keys 32-63).  Each half keeps its own
+//              running maximum, sum and O accumulator (O0, O1 in TMEM), so
+//              the two never wait for each other inside the key loop; it
+//              reads its logits from TMEM, masks them, writes (P s) hi / lo
+//              over them and rescales its O when its maximum grows.  In the
+//              end the halves merge (log-sum-exp weights) and the row gets
+//              the zero-point term, the inverse RHT and 1 / l.
+//   warp 8     TMEM allocation; lane 0 issues every tcgen05.mma:
 //              S_b = Q_hi K^T + Q_lo K^T (M=128, N=64, K=D) into one of two
-//              TMEM buffers, then O += P_hi V + P_lo V (M=128, N=D, K=64).
-//   warps 5-7  producers: cp.async of the raw page chunks (double-buffered),
-//              expansion of the codes into fp16 K (K-major) and V^T (K-major,
-//              transposed with stmatrix) tiles in the 128-byte swizzle layout.
+//              TMEM buffers, then O0 += P_hi V + P_lo V over keys 0-31 and
+//              O1 over keys 32-63 (M=128, N=D).
+//   warps 9-12 producers: expansion of the codes into fp16 K (K-major) and
+//              V^T (K-major, transposed with stmatrix) tiles in the 128-byte
+//              swizzle layout.
+//   warp 13    copy issuer: bulk copies of the raw page chunks.
 // Codes enter the tensor cores as signed integers (exact in fp16); the
 // query and (P s) are split into fp16 hi + lo terms so fp16 does not limit
 // accuracy.  Every wait on an mbarrier is bounded; on a timeout the CTA
@@ -79,18 +84,19 @@ struct TpCfg {
   static constexpr int OFF_SC = OFF_RAW + NRAW * 2 * RAW;              // [NKV][ks, kz, vs, vz][64] f32
   static constexpr int OFF_KVAL = OFF_SC + NKV * 4 * TP_KT * 4;        // [NKV][4] chunk validity of the expanded tiles
   static constexpr int OFF_RAWVAL = OFF_KVAL + 64;                     // [NRAW][4] chunk validity of the raw tiles
-  static constexpr int OFF_XMAX = OFF_RAWVAL + 64;                     // [2 tile parity][2 key halves][128] f32
+  static constexpr int OFF_XMAX = OFF_RAWVAL + 64;                     // [2 key halves][128] f32 (epilogue)
   static constexpr int OFF_ROW = OFF_XMAX + 2 * 2 * TP_ROWS * 4;       // beta, gamma [128] f32, pos [128] int
   static constexpr int OFF_BAR = OFF_ROW + 3 * TP_ROWS * 4;            // mbarriers
   static constexpr int NBAR = 32;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;                  // tmem slot, abort flag, sequence
   static constexpr int SMEM = OFF_MISC + 16 + 1024;                    // + alignment slack
-  // TMEM columns: S[2] (64 fp32 each; P hi / lo overwrite them), O (D fp32),
-  // Q hi and Q lo (D / 2 columns each: two fp16 per column)
+  // TMEM columns: S[2] (64 fp32 each; P hi / lo overwrite them), O0 (D fp32),
+  // Q hi and Q lo (D / 2 columns each: two fp16 per column), O1 (D fp32)
   static constexpr int TM_O = 2 * TP_KT;
   static constexpr int TM_QHI = TM_O + D;
   static constexpr int TM_QLO = TM_QHI + D / 2;
-  static constexpr int TMEM_COLS = TM_QLO + D / 2 <= 256 ? 256 : 512;
+  static constexpr int TM_O1 = TM_QLO + D / 2;  // O of the second key half
+  static constexpr int TMEM_COLS = TM_O1 + D <= 256 ? 256 : 512;
   // the query rows are staged (fp16 hi / lo, rows padded by 16 bytes) in the
   // K / V^T stages before they are moved to TMEM
   static constexpr int QROW = 2 * D + 16;
@@ -104,10 +110,10 @@ struct TpCfg {
 
 // barriers: raw stage full [3] / empty [3], K/V stage full [3] / empty [3],
 // S full [2] / empty [2], P full, O done, drain, and per row quad the
-// exchange between its two softmax warps [4][tile parity] and at the end [4]
+// epilogue's meeting of its two softmax warps [4]
 enum {
   B_RAWFULL = 0, B_RAWEMPTY = 3, B_KVFULL = 6, B_KVEMPTY = 9, B_SFULL = 12, B_SEMPTY = 14, B_PFULL = 16, B_ODONE = 17,
-  B_DRAIN = 18, B_XCH = 20, B_EPI = 28
+  B_DRAIN = 18, B_EPI = 28
 };
 
 // Two bf16 values (low half first) as an fp16 pair, rounded to nearest.  A
@@ -304,7 +310,6 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
     mbar_init(bar + B_PFULL, TP_SOFTMAX);
     mbar_init(bar + B_ODONE, 1);
     mbar_init(bar + B_DRAIN, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(bar + B_XCH + i, 64);
     for (int i = 0; i < 4; ++i) mbar_init(bar + B_EPI + i, 64);
     *abort_flag = 0;
     mbar_init_fence();
@@ -406,7 +411,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
   __syncthreads();  // the query rows are in TMEM; the staging area is free again
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + C::TM_O;
+  const uint32_t tmem_o = tmem + C::TM_O;    // O of keys 0-31 of every tile
+  const uint32_t tmem_o1 = tmem + C::TM_O1;  // O of keys 32-63
 
   if (warp == TP_ISSUE_WARP) {
     // ======================= raw page copies (one lane) =======================
@@ -620,8 +626,9 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
     if (lane == 0) {
       const uint32_t idesc_qk = tc::idesc_f16(TP_ROWS, TP_KT);
       const uint32_t idesc_pv = tc::idesc_f16(TP_ROWS, D);
-      // O += P V with P (hi / lo interleaved per 16 keys, where the tile's S
-      // was) from TMEM and V^T from shared memory
+      // O0 += P V over the tile's keys 0-31 and O1 over keys 32-63, with P
+      // (hi / lo interleaved per 16 keys, where the tile's S was) from TMEM
+      // and V^T from shared memory
       auto pv = [&](int i, int kvs_i) -> bool {
         if (!mbar_wait_bounded(bar + B_PFULL, i & 1, TP_NAP_MMA)) return false;
         tc::fence_after();
@@ -630,8 +637,9 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
         for (int kk = 0; kk < TP_KT / 16; ++kk) {
           const uint64_t bdesc = tc::sw128_desc(a_vt + 32 * kk);
-          tc::mma_f16_ts(tmem_o, p_tm + 16 * kk, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_f16_ts(tmem_o, p_tm + 16 * kk + 8, bdesc, idesc_pv, 1u);
+          const uint32_t o_tm = kk < TP_KT / 32 ? tmem_o : tmem_o1;
+          tc::mma_f16_ts(o_tm, p_tm + 16 * kk, bdesc, idesc_pv, (i > 0 || (kk % (TP_KT / 32)) > 0) ? 1u : 0u);
+          tc::mma_f16_ts(o_tm, p_tm + 16 * kk + 8, bdesc, idesc_pv, 1u);
         }
         tc::commit(bar + B_ODONE);
         tc::commit(bar + B_KVEMPTY + kvs_i);
@@ -679,19 +687,20 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
   } else {
     // ======================= softmax =======================
     // Row r is shared by warps r / 32 (keys 0-31 of each tile) and r / 32 + 4
-    // (keys 32-63), which may both read TMEM lanes 32 (w % 4) ...  Per tile
-    // each half makes two passes over its 32 logits (two 16-key chunks, kept
-    // in registers between the passes): pass 1 forms y = s c.q'' + rho z
-    // (rho = gamma / beta), masks it and takes the half's maximum; the pair
-    // combines the two maxima through shared memory; pass 2 forms
-    // p = 2^(beta y - m) and writes (p s) hi / lo of its 32 keys to P, over
-    // the tile's S columns.
+    // (keys 32-63), which may both read TMEM lanes 32 (w % 4) ...  Each half
+    // is an online softmax of its own over its keys, with its own maximum,
+    // sums and O accumulator.  Per tile it makes two passes over its 32
+    // logits (two 16-key chunks, kept in registers between the passes):
+    // pass 1 forms y = s c.q'' + rho z (rho = gamma / beta), masks it and
+    // takes the maximum; pass 2 forms p = 2^(beta y - m) and writes (p s)
+    // hi / lo of its 32 keys to P, over the tile's S columns.
     const int quad = warp & 3, hf = warp >> 2;
     const int r = quad * 32 + lane;
     const float rb = rbeta[r];
     const float rho = rgamma[r] / rb;
     const int rp = rpos[r];
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tmem_oh = hf ? tmem_o1 : tmem_o;  // this half's O
     float* xmax = reinterpret_cast<float*>(sm + C::OFF_XMAX);
     float mrow = -CUDART_INF_F, lrow = 0.0f, pzrow = 0.0f;  // lrow, pzrow: this half's keys
     bool ok = true;
@@ -751,17 +760,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) ymax = fmaxf(ymax, __uint_as_float(rr[jj]));
       }
-      // the pair's maxima meet in shared memory (bounded wait: a partner
-      // that left the loop turns into an error, not a hang)
-      xmax[(st * 2 + hf) * TP_ROWS + r] = ymax;
-      tc::mbar_arrive(bar + B_XCH + quad * 2 + st);
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_XCH + quad * 2 + st, (v >> 1) & 1, TP_NAP_SOFTMAX))) {
-        ok = false;
-        break;
-      }
-      ymax = fmaxf(ymax, xmax[(st * 2 + (hf ^ 1)) * TP_ROWS + r]);
-      // lazy rescale: keep the reference maximum until a row's maximum
-      // passes it by more than 2^TP_SLACK (both halves decide alike)
+      // lazy rescale: keep the reference maximum until the row's maximum
+      // over this half's keys passes it by more than 2^TP_SLACK
       const float tmax = rb * ymax;
       const bool grow = tmax > mrow + TP_SLACK;
       const float mref = grow ? tmax : mrow;
@@ -773,14 +773,14 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
         break;
       }
       const bool resc = v >= 1 && grow && mrow != -CUDART_INF_F;
-      if (__any_sync(0xffffffffu, resc)) {  // this half's O columns; rows keeping their reference scale by 1
+      if (__any_sync(0xffffffffu, resc)) {  // this half's O; rows keeping their reference scale by 1
         tc::fence_after();
         const float f = resc ? ex2(mrow - muse) : 1.0f;
 #pragma unroll 1
-        for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t ra[16], rb2[16];
-          tc::ld16(tmem_o + lane_base + c0, ra);
-          tc::ld16(tmem_o + lane_base + c0 + 16, rb2);
+          tc::ld16(tmem_oh + lane_base + c0, ra);
+          tc::ld16(tmem_oh + lane_base + c0 + 16, rb2);
           tc::wait_ld();
           tc::regs_after_wait(ra);
           tc::regs_after_wait(rb2);
@@ -789,8 +789,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
             ra[j] = __float_as_uint(__uint_as_float(ra[j]) * f);
             rb2[j] = __float_as_uint(__uint_as_float(rb2[j]) * f);
           }
-          tc::st16(tmem_o + lane_base + c0, ra);
-          tc::st16(tmem_o + lane_base + c0 + 16, rb2);
+          tc::st16(tmem_oh + lane_base + c0, ra);
+          tc::st16(tmem_oh + lane_base + c0 + 16, rb2);
         }
         tc::wait_st();
         lrow *= f;
@@ -842,47 +842,57 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
         break;
       }
     }
-    // ---- epilogue: each half stages its O columns in shared memory, the
-    // pair adds up its l and zero-point sums, then per row a warp applies
-    // the zero-point term, the inverse RHT (or the INT8 V channel scales) and
-    // 1 / l and stores the row with coalesced writes
+    // ---- epilogue: the pair's two halves merge (each weighted by 2^(its
+    // maximum - the row's), half 0 staging its O in shared memory and half 1
+    // adding its own), then per row a warp applies the zero-point term, the
+    // inverse RHT (or the INT8 V channel scales) and 1 / l and stores the row
+    // with coalesced writes.  Both warps of a pair pass the same three phases
+    // of B_EPI + quad, whatever their status, so neither waits on a partner
+    // that left; every wait is bounded.
     if (ok && n_virt >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar + B_ODONE, (n_virt - 1) & 1)))
       ok = false;
     float4* stage = reinterpret_cast<float4*>(sm + C::OFF_K);  // [128 rows][D / 4], piece j at j ^ (row & 7)
-    float* xsum = reinterpret_cast<float*>(sm + C::OFF_RAW);    // [2 halves][l, pz, ok][128]
+    float* xsum = reinterpret_cast<float*>(sm + C::OFF_RAW);    // [l, pz, ok half 0, ok half 1][128]
     constexpr int P4 = D / 4;
-    if (ok) {  // every P.V is done: the K / V^T stages are free for staging
-      xsum[(hf * 3 + 0) * TP_ROWS + r] = lrow;
-      xsum[(hf * 3 + 1) * TP_ROWS + r] = MODE != MODE_INT8 ? pzrow : 0.0f;
-      if (n_virt >= 1) {  // whole warp reads its 32 TMEM rows, valid or not
-        tc::fence_after();
+    xmax[hf * TP_ROWS + r] = mrow;
+    xsum[(2 + hf) * TP_ROWS + r] = ok ? 1.0f : 0.0f;
+    tc::mbar_arrive(bar + B_EPI + quad);
+    bool good = mbar_wait_bounded(bar + B_EPI + quad, 0);
+    good = __all_sync(0xffffffffu, ok && good && xsum[(2 + (hf ^ 1)) * TP_ROWS + r] != 0.0f);
+    const float mrr = fmaxf(mrow, xmax[(hf ^ 1) * TP_ROWS + r]);
+    const float fw = mrow == -CUDART_INF_F ? 0.0f : ex2(mrow - mrr);  // 0 for a half without visible keys
 #pragma unroll 1
-        for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
-          uint32_t ra[16], rb2[16];
-          tc::ld16(tmem_o + lane_base + c0, ra);
-          tc::ld16(tmem_o + lane_base + c0 + 16, rb2);
-          tc::wait_ld();
-          tc::regs_after_wait(ra);
-          tc::regs_after_wait(rb2);
+    for (int ph = 0; ph < 2; ++ph) {
+      if (good && hf == ph) {  // every P.V is done: the K / V^T stages are free for staging
+        xsum[0 * TP_ROWS + r] = (ph ? xsum[0 * TP_ROWS + r] : 0.0f) + fw * lrow;
+        xsum[1 * TP_ROWS + r] = (ph ? xsum[1 * TP_ROWS + r] : 0.0f) + (MODE != MODE_INT8 ? fw * pzrow : 0.0f);
+        if (n_virt >= 1) {  // whole warp reads its 32 TMEM rows, valid or not
+          tc::fence_after();
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t ra[16], rb2[16];
+            tc::ld16(tmem_oh + lane_base + c0, ra);
+            tc::ld16(tmem_oh + lane_base + c0 + 16, rb2);
+            tc::wait_ld();
+            tc::regs_after_wait(ra);
+            tc::regs_after_wait(rb2);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            stage[r * P4 + ((c0 / 4 + j) ^ (r & 7))] =
-                make_float4(__uint_as_float(ra[4 * j]), __uint_as_float(ra[4 * j + 1]), __uint_as_float(ra[4 * j + 2]),
-                            __uint_as_float(ra[4 * j + 3]));
-            stage[r * P4 + ((c0 / 4 + 4 + j) ^ (r & 7))] =
-                make_float4(__uint_as_float(rb2[4 * j]), __uint_as_float(rb2[4 * j + 1]),
-                            __uint_as_float(rb2[4 * j + 2]), __uint_as_float(rb2[4 * j + 3]));
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t* w = j < 4 ? ra + 4 * j : rb2 + 4 * (j - 4);
+              float4& dst = stage[r * P4 + ((c0 / 4 + j) ^ (r & 7))];
+              const float4 prev = ph ? dst : make_float4(0.f, 0.f, 0.f, 0.f);
+              dst = make_float4(fmaf(fw, __uint_as_float(w[0]), prev.x), fmaf(fw, __uint_as_float(w[1]), prev.y),
+                                fmaf(fw, __uint_as_float(w[2]), prev.z), fmaf(fw, __uint_as_float(w[3]), prev.w));
+            }
           }
+        } else if (ph == 0) {
+          for (int j = 0; j < P4; ++j) stage[r * P4 + j] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      } else {
-        for (int j = hf * (P4 / 2); j < (hf + 1) * (P4 / 2); ++j) stage[r * P4 + j] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      tc::mbar_arrive(bar + B_EPI + quad);  // half ph has staged (or failed)
+      good = __all_sync(0xffffffffu, mbar_wait_bounded(bar + B_EPI + quad, (ph + 1) & 1) && good);
     }
-    xsum[(hf * 3 + 2) * TP_ROWS + r] = ok ? 1.0f : 0.0f;
-    tc::mbar_arrive(bar + B_EPI + quad);  // both halves of these 32 rows are staged (or failed)
-    const bool met = mbar_wait_bounded(bar + B_EPI + quad, 0);
-    const bool pair_ok = __all_sync(0xffffffffu, ok && met && xsum[((hf ^ 1) * 3 + 2) * TP_ROWS + r] != 0.0f);
-    if (!pair_ok) {
+    if (!good) {
       *abort_flag = 1;
       if (lane == 0) flag_error(P.dev_error, DEVERR_TIMEOUT);
     } else {
@@ -891,8 +901,8 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
         const int row = quad * 32 + k;
         const int ql = row / G, i = row % G;
         if (ql >= nq) continue;  // warp-uniform
-        const float lr = xsum[0 * TP_ROWS + row] + xsum[3 * TP_ROWS + row];
-        const float pz = xsum[1 * TP_ROWS + row] + xsum[4 * TP_ROWS + row];
+        const float lr = xsum[0 * TP_ROWS + row];
+        const float pz = xsum[1 * TP_ROWS + row];
         float o[EPL];
         const float* src = reinterpret_cast<const float*>(stage + row * P4 + ((lane * EPL / 4) ^ (row & 7))) +
                            (lane * EPL) % 4;
