@@ -112,6 +112,17 @@ def test_decode_evicted_pages_never_read():
     assert np.array_equal(g0, g1)
 
 
+@pytest.mark.parametrize("batch", [17, 20])
+def test_decode_pair_count_not_a_multiple_of_the_scan_width(batch):
+    """136 or 160 (sequence, kv head) pairs: the stream kernel's prefix scan of
+    the pairs' tile counts runs on 128 threads, so each scanning thread owns two
+    pairs and the last ones own none.  Parity with the oracle, and a second call
+    on the same inputs returns the same bits (the slices and the merge order are
+    fixed, not scheduled)."""
+    c, q, g, _ = _run(gen.llama_int4(0, batch=batch, ctx_lo=100, ctx_hi=1500, num_blocks=4000))
+    assert np.array_equal(g, decode_gpu(c, q))
+
+
 def test_decode_empty_and_zero_length():
     wl = gen.custom(gen.MODE_INT4, 4, 2, 64, 16, "f32", seq_lens=[5, 9], n_new=[1, 1], seed=2)
     c = build_case(wl)
