@@ -465,17 +465,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// [rows][Hkv][D] bf16 seen as a 3-D tensor (D, Hkv, rows) with a box of D
-// elements x 1 head x 64 rows: one box is the tile of one head.
+// [rows][Hkv][D] bf16 seen as a 4-D tensor (64, D / 64, Hkv, rows): a box of
+// 64 elements x 1 half x 1 head x 64 rows is one 64-dim half of the tile of
+// one head, 64 lines of 128 bytes whose 16-byte pieces land XOR-swizzled by
+// the line index (128-byte swizzle), so that the expansion's reads of one
+// column across eight rows fall in eight different banks.
 bool dense_rows_map(CUtensorMap* map, const void* base, int64_t rows, int Hkv, int D) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)D, 1, 64};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  if (!enc || D % 64 != 0) return false;
+  const cuuint64_t dims[4] = {64, (cuuint64_t)D / 64, (cuuint64_t)Hkv, (cuuint64_t)rows};
+  const cuuint64_t strides[3] = {128, (cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+  const cuuint32_t box[4] = {64, 1, 1, 64};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

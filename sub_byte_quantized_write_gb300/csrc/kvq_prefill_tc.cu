@@ -172,6 +172,22 @@ __device__ __forceinline__ uint4 codes8(const uint8_t* raw_row, int c) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Dense raw tiles: D / 64 halves of DENSE_HALF bytes, each 64 rows of 128
+// bytes (64 bf16 dims) with the 128-byte swizzle of the tensor copy.
+constexpr int DENSE_HALF = 64 * 128;
+// Dims 8c .. 8c+7 of row `row` as four fp16 pairs.
+__device__ __forceinline__ uint4 dense_codes8(const uint8_t* raw, int row, int c) {
+  const uint4 w = *reinterpret_cast<const uint4*>(raw + (c >> 3) * DENSE_HALF + tc::sw128_off(row, c & 7));
+  return make_uint4(bf16x2_to_half2_bits(w.x), bf16x2_to_half2_bits(w.y), bf16x2_to_half2_bits(w.z),
+                    bf16x2_to_half2_bits(w.w));
+}
+// Dims d, d+1 (d even) of row `row` as an fp16 pair (low half = dim d).
+__device__ __forceinline__ uint32_t dense_codes2(const uint8_t* raw, int row, int d) {
+  const int c = (d & 63) >> 3;
+  return bf16x2_to_half2_bits(*reinterpret_cast<const uint32_t*>(raw + (d >> 6) * DENSE_HALF +
+                                                                 tc::sw128_off(row, c) + 2 * (d & 7)));
+}
+
 // The two codes of head dims (d, d+1), d even, of a raw row as an exact fp16
 // pair of signed codes (low half = dim d).
 template <int MODE>
@@ -420,9 +436,10 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
     // stages, up to NRAW tiles ahead of the expansion; the page-table
     // entries are read two tiles ahead of the copies that use them.
     if (MODE == MODE_DBF16 && lane == 0) {
-      // dense rows: one 64-row box of this head per tensor and tile (tensor
-      // copies; rows past the array arrive as zeros, rows of the next
-      // sequence are zeroed by the producers)
+      // dense rows: the 64-row tile of this head per tensor, as D / 64
+      // 128-byte-swizzled boxes of one 64-dim half each (tensor copies; rows
+      // past the array arrive as zeros, rows of the next sequence are zeroed
+      // by the producers)
       const int row0 = __ldg(P.cu_kv + b);
       int rs = 0, rphase = 0;
 #pragma unroll 1
@@ -438,8 +455,11 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
         for (int c = 0; c < 4; ++c) rawval[rs * 4 + c] = 16 * c < nrows ? 1 : 0;
         mbar_arrive_expect_tx(bar + B_RAWFULL + rs, (uint32_t)(2 * C::RAW));
-        tma_load_3d(rk, &P.kv_map[0], 0, h, row0 + key0, bar + B_RAWFULL + rs);
-        tma_load_3d(rk + C::RAW, &P.kv_map[1], 0, h, row0 + key0, bar + B_RAWFULL + rs);
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh) {  // one 64-dim half (64 swizzled lines of 128 B) per copy
+          tc::tma_load_4d(rk + hh * DENSE_HALF, &P.kv_map[0], 0, hh, h, row0 + key0, bar + B_RAWFULL + rs);
+          tc::tma_load_4d(rk + C::RAW + hh * DENSE_HALF, &P.kv_map[1], 0, hh, h, row0 + key0, bar + B_RAWFULL + rs);
+        }
         if (++rs == C::NRAW) {
           rs = 0;
           rphase ^= 1;
@@ -560,7 +580,9 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
           const int key = key_0 + KSTEP * j;
-          uint4 hv = codes8<MODE>(src + KSTEP * j * C::R, c8);
+          uint4 hv;
+          if constexpr (MODE == MODE_DBF16) hv = dense_codes8(rk, key, c8);
+          else hv = codes8<MODE>(src + KSTEP * j * C::R, c8);
           if (MODE == MODE_DBF16 && key0 + key >= Leff) hv = make_uint4(0u, 0u, 0u, 0u);  // not copied
           *reinterpret_cast<uint4*>(dst + tc::sw128_off(key, c8 & 7)) = hv;
         }
@@ -578,7 +600,10 @@ __global__ void __launch_bounds__(TP_THREADS, 1) prefill_tc_kernel(const __grid_
           const uint8_t* row = rvp + (8 * kb + g8) * C::R;
           uint32_t r4[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) r4[i] = codes2<MODE>(row, 32 * db + 8 * i + 2 * t4);
+          for (int i = 0; i < 4; ++i) {
+            if constexpr (MODE == MODE_DBF16) r4[i] = dense_codes2(rvp, 8 * kb + g8, 32 * db + 8 * i + 2 * t4);
+            else r4[i] = codes2<MODE>(row, 32 * db + 8 * i + 2 * t4);
+          }
           if (MODE == MODE_DBF16 && key0 + 8 * kb + g8 >= Leff) {  // not copied: stale bytes could be NaN
 #pragma unroll
             for (int i = 0; i < 4; ++i) r4[i] = 0u;

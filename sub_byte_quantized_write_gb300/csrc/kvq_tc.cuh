@@ -10,6 +10,18 @@
 namespace kvq {
 namespace tc {
 
+// 4-D tensor copy (box coordinates c0..c3) into shared memory, completion
+// counted on `bar`; the innermost coordinate times the element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand stored in the
 // canonical 128-byte-swizzle layout: rows of 128 bytes (64 fp16 along K),
 // 8-row groups 1024 bytes apart, 16-byte chunk c of row r stored at chunk

@@ -16,6 +16,11 @@ key k + 1 lands in the bank of the first code word of key k, so each of its
 scale reads (the same 16 bytes in every lane) are conflict-free under the
 rule.  The measured counts, and how they compare, are in the prefill profile
 summary.
+
+For the dense bf16 rows of the same kernel the value expansion reads one
+column of eight 256-byte rows at a time, all in one bank (8-way); the tensor
+copies therefore land each 64-dim half with the 128-byte swizzle, which the
+model shows conflict-free for both expansions.
 """
 from collections import defaultdict
 
@@ -106,6 +111,31 @@ def softmax_scale_loads():
     return out
 
 
+def dense_vt_loads(swizzled):
+    """Dense rows (bf16, 2 D bytes), value expansion: producer job (kb, db),
+    lane (g8, t4) reads the 4 bytes of dims 32 db + 8 i + 2 t4 and + 1 of key
+    row 8 kb + g8, i = 0..3.  Unswizzled the rows are 256 bytes apart; the
+    kernel's tensor copies instead land each 64-dim half as 64 lines of 128
+    bytes with 16-byte piece c of line r at piece c ^ (r & 7)."""
+    out = []
+    for kb in range(TP_KT // 8):
+        for db in range(D // 32):
+            for i in range(4):
+                addrs = []
+                for lane in range(32):
+                    g8, t4 = lane >> 2, lane & 3
+                    addrs.append(dense_addr(8 * kb + g8, 32 * db + 8 * i + 2 * t4, swizzled))
+                out.append((addrs, 4))
+    return out
+
+
+def dense_addr(row, d, swizzled):
+    if not swizzled:
+        return row * 2 * D + 2 * d
+    c = (d % 64) // 8
+    return (d // 64) * 64 * 128 + row * 128 + 16 * (c ^ (row & 7)) + 2 * (d % 8)
+
+
 def role_totals(loads):
     waves = phases = instr = 0
     for addrs, width in loads:
@@ -144,3 +174,31 @@ def test_wavefront_rule_on_textbook_patterns():
     assert wavefronts([0] * 32, 4) == (1, 1)                              # broadcast
     assert wavefronts([16 * l for l in range(32)], 16) == (4, 4)          # 512 contiguous bytes
     assert wavefronts([8 * (l % 16) * 2 for l in range(32)], 8) == (4, 2)  # 2-way in each half
+
+
+def test_dense_value_expansion_swizzle():
+    # 256-byte rows put one column of eight rows in one bank: every load 8-way
+    instr, waves, excess = role_totals(dense_vt_loads(False))
+    assert instr == 128 and excess == 7 * instr
+    # the 128-byte swizzle of the tensor copies spreads them over all banks
+    assert role_totals(dense_vt_loads(True)) == (128, 128, 0)
+    # and the swizzled layout is still one place per (row, dim pair): a
+    # permutation of the tile's 4-byte words
+    words = {dense_addr(r, d, True) // 4 for r in range(TP_KT) for d in range(0, D, 2)}
+    assert words == set(range(TP_KT * D // 2))
+
+
+def test_dense_key_expansion_swizzled_reads_conflict_free():
+    # producer thread pt reads 16 bytes (dims 8 c8 .. 8 c8 + 7) of key row
+    # pt / (D/8) + KSTEP j: whole pieces, so the piece index is swizzled
+    loads = []
+    for pw in range(4):
+        for j in range(TP_KT * (D // 8) // TP_PRODUCERS):
+            addrs = []
+            for lane in range(32):
+                pt = 32 * pw + lane
+                c8, key = pt % (D // 8), pt // (D // 8) + KSTEP * j
+                addrs.append(dense_addr(key, 8 * c8, True))
+            loads.append((addrs, 16))
+    instr, waves, excess = role_totals(loads)
+    assert excess == 0
