@@ -289,18 +289,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                : "memory");
 }
 
-// 3-D tensor copy (TMA) of one box of `map` at coordinates (c0, c1, c2) into
-// shared memory, completion counted on `bar`.  `map` must live in the kernel
-// parameter space (a __grid_constant__ parameter) or global memory; c0 times
-// the element size must be a multiple of 16 bytes; rows outside the tensor
-// arrive as zeros and still count as transaction bytes.
-__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int c0, int c1, int c2, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
-      : "memory");
-}
-
 // Gather of four rows of a 2-D tensor map (`tile::gather4`): rows r0..r3
 // (each one box row of the map's width) land back to back at `dst`;
 // completion counted on `bar`.  Only lanes with `pred` set issue it.  Every

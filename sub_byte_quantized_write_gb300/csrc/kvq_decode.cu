@@ -1470,7 +1470,8 @@ __global__ void __launch_bounds__(TmaCfg<MODE, D, NT>::WARPS * 32, (TmaCfg<MODE,
           vk[h2][m][hh] = ok;
           const uint32_t pk = lds32(kt + poff + (32 * h2 + 2 * m + hh) * R);
           const uint32_t pv = lds32(vt + poff + (32 * h2 + 2 * m + hh) * R);
-          float sk, mk, zst = 0.0f;
+          float sk, mk;
+          [[maybe_unused]] float zst = 0.0f;  // STEGO: the key's zero point
           if constexpr (TC::BYTES) {
             sk = __uint_as_float(pk);
             mk = 0.0f;

@@ -60,7 +60,8 @@ struct AttnParams {
   const int32_t* cu_q;
   int total_q, max_q_per_seq;
   // dense prefill: sequence b's key j is row cu_kv[b] + j of k_pages / v_pages;
-  // kv_map[0 | 1] view K / V as [rows][Hkv][D] bf16 with a 64-row box of one head.
+  // kv_map[0 | 1] view K / V as [rows][Hkv][D] bf16 in boxes of one 64-dim half
+  // of 64 rows of one head, 128-byte swizzled.
   // decode (token-head modes): kv_map[0 | 1] view the K / V pool as 2-D tensors
   // of page chunks (decode_chunk_rows), one chunk per box row.
   const int32_t* cu_kv;

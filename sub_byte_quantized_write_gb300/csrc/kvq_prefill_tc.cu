@@ -65,8 +65,8 @@ constexpr uint32_t TP_NAP_SOFTMAX = 20, TP_NAP_MMA = 20, TP_NAP_PRODUCER = 100, 
 
 template <int MODE, int D>
 struct TpCfg {
-  static constexpr int BITS = mode_bits(MODE);
-  static constexpr int DATA = data_bytes(MODE, D);
+  static constexpr int DATA = data_bytes(MODE, D);  // code bytes before the pad (dense rows: D * 2, no pad)
+  static_assert(DATA <= row_bytes_of(MODE, D), "the pad follows the codes");
   static constexpr int R = row_bytes_of(MODE, D);
   static constexpr int CHUNK = 16 * R;          // one 16-row chunk of a page (contiguous)
   static constexpr int RAW = TP_KT * R;         // raw bytes of one tensor per tile
@@ -983,7 +983,6 @@ cudaError_t launch_prefill_tc_t(const AttnParams& P, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  const int QB = TP_ROWS / P.group;
   dim3 grid((unsigned)prefill_grid_x(P.max_q_per_seq, P.group), P.num_kv_heads, P.batch);  // TP_THREADS threads each
   prefill_tc_kernel<MODE, D><<<grid, TP_THREADS, C::SMEM, stream>>>(P);
   return cudaGetLastError();

@@ -10,9 +10,11 @@
 namespace kvq {
 namespace tc {
 
-// 4-D tensor copy (box coordinates c0..c3) into shared memory, completion
-// counted on `bar`; the innermost coordinate times the element size must be a
-// multiple of 16 bytes.
+// 4-D tensor copy (TMA) of one box of `map` at coordinates (c0..c3) into
+// shared memory, completion counted on `bar`.  `map` must live in the kernel
+// parameter space (a __grid_constant__ parameter) or global memory; c0 times
+// the element size must be a multiple of 16 bytes; rows outside the tensor
+// arrive as zeros and still count as transaction bytes.
 __device__ __forceinline__ void tma_load_4d(void* dst, const void* map, int c0, int c1, int c2, int c3,
                                             uint64_t* bar) {
   asm volatile(
