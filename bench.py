@@ -290,6 +290,21 @@ def setup_gpu(wl, device, want_splits=0):
         "cu": torch.from_numpy(wl.cu(wl.n_new)).to(device),
         "seq_lens": torch.from_numpy(wl.seq_lens).to(device),
     }
+    # The inputs a serving step receives from the host live in one device
+    # buffer (256-byte aligned parts, the step's tensors rebound as views into
+    # it), so that the end-to-end run moves them with one copy per step; q is
+    # last, so that a step without queries copies the prefix before it.
+    parts, off = [], 0
+    for n in ("k", "v", "cu", "seq_lens", "q"):
+        nb = step[n].numel() * step[n].element_size()
+        parts.append((n, off, nb))
+        off = (off + nb + 255) // 256 * 256
+    inbuf = torch.empty(off, dtype=torch.uint8, device=device)
+    for n, o, nb in parts:
+        view = inbuf[o:o + nb].view(step[n].dtype).view(step[n].shape)
+        view.copy_(step[n])
+        step[n] = view
+    step["inbuf"], step["q_off"] = inbuf, parts[-1][1]
     pag = paging(step["seq_lens"])
     step["out"] = torch.empty(tuple(step["q"].shape), dtype=torch.float32, device=device)
     # gather: every cached position of every sequence back to dense bf16 K / V
@@ -445,25 +460,18 @@ def run_gpu(args, rank, world, local_rank):
     value = whole_job_rate(tokens, ms, world)
 
     # end to end through the C ABI with host buffers: H2D of the step's
-    # inputs from pinned memory, write + attention, D2H of the output
-    hk = st["k"].cpu().pin_memory()
-    hv = st["v"].cpu().pin_memory()
-    hq = st["q"].cpu().pin_memory()
-    hcu = st["cu"].cpu().pin_memory()
-    hsl = st["seq_lens"].cpu().pin_memory()
+    # inputs (new K / V rows, their positions, the lengths and the queries)
+    # from one pinned buffer, write + attention, D2H of the output
+    nin = st["q_off"] if kind == "gather" else st["inbuf"].numel()  # the gather step takes no queries
+    hin = st["inbuf"][:nin].cpu().pin_memory()
     hout = torch.empty_like(st["out"], device="cpu").pin_memory()
     hout_v = torch.empty_like(st["gv"], device="cpu").pin_memory() if kind == "gather" else None
-    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hcu, hsl) + ((hq,) if kind != "gather" else ()))
+    h2d = nin
     d2h = hout.numel() * hout.element_size() + (hout_v.numel() * hout_v.element_size() if kind == "gather" else 0)
 
     def e2e_step():
         # plain library calls (no graph), inputs from pinned host memory
-        st["k"].copy_(hk, non_blocking=True)
-        st["v"].copy_(hv, non_blocking=True)
-        if kind != "gather":
-            st["q"].copy_(hq, non_blocking=True)
-        st["cu"].copy_(hcu, non_blocking=True)
-        st["seq_lens"].copy_(hsl, non_blocking=True)
+        st["inbuf"][:nin].copy_(hin, non_blocking=True)
         step()
         hout.copy_(st["out"], non_blocking=True)
         if kind == "gather":
