@@ -516,7 +516,7 @@ def run_gpu(args, rank, world, local_rank):
                 "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind + " (copy bandwidth)",
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "algorithmic_bytes_per_launch": units["gather"],
                 "traffic": recorded_units("gather_%s.md" % args.workload, "dram_bytes_per_gather_call",
-                                          kernel_source_hash(("kvq_write.cu", "kvq_common.cuh", "kvq_internal.h")))}
+                                          kernel_source_hash(("kvq_write.cu", "kvq_common.cuh", "kvq_internal.h", "kvq_api.cu")))}
         extra = {"gather_ms": round(att, 5), "gathered_tokens_per_step": st["n_all"]}
         launches = 2  # write + gather
         dtype = "u4 codes -> fp32 dequantise + inverse RHT -> bf16"
@@ -525,7 +525,7 @@ def run_gpu(args, rank, world, local_rank):
         achieved = units["prefill_flops"] / (dense / 1e3) / 1e12
         traffic = recorded_units("prefill_tc_%s.md" % args.workload, "dram_bytes_per_prefill_call",
                                  kernel_source_hash(("kvq_prefill_tc.cu", "kvq_tc.cuh", "kvq_common.cuh",
-                                                     "kvq_internal.h")))
+                                                     "kvq_internal.h", "kvq_api.cu")))
         roof = {"bound": "tensor", "kernel": "prefill_tc_kernel over dense bf16 rows (one kvq_prefill_dense_attn call)",
                 "achieved": round(achieved, 2), "peak": tensor,
                 "peak_kind": peak_kind + " (cuBLAS bf16 burst; kind::f16 fp16 runs at the bf16 rate)",
@@ -539,7 +539,7 @@ def run_gpu(args, rank, world, local_rank):
         cfg["decode_workers"] = st["splits"]
         achieved = units["decode"] / (att / 1e3) / 1e9
         traffic = recorded_units("decode_stream_%s.md" % args.workload, "dram_bytes_per_decode_call",
-                                 kernel_source_hash(("kvq_decode.cu", "kvq_common.cuh", "kvq_internal.h")))
+                                 kernel_source_hash(("kvq_decode.cu", "kvq_common.cuh", "kvq_internal.h", "kvq_api.cu")))
         roof = {"bound": "hbm", "kernel": "decode attention (query prep + stream-K split-KV + merge, "
                                           "one kvq_decode_attn call)",
                 "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind + " (copy bandwidth)",
@@ -554,7 +554,7 @@ def run_gpu(args, rank, world, local_rank):
         achieved = units["prefill_flops"] / (att / 1e3) / 1e12
         traffic = recorded_units("prefill_tc_%s.md" % args.workload, "dram_bytes_per_prefill_call",
                                  kernel_source_hash(("kvq_prefill_tc.cu", "kvq_tc.cuh", "kvq_common.cuh",
-                                                     "kvq_internal.h")))
+                                                     "kvq_internal.h", "kvq_api.cu")))
         roof = {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05, one kvq_prefill_attn call)",
                 "achieved": round(achieved, 2), "peak": tensor,
                 "peak_kind": peak_kind + " (cuBLAS bf16 burst; kind::f16 fp16 runs at the bf16 rate)",
