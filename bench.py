@@ -113,6 +113,12 @@ class ClockSampler:
             self.thread.start()
         except (FileNotFoundError, OSError):
             self.proc = None
+            return self
+        # The timed region starts once nvidia-smi samples (its start-up
+        # otherwise overlaps the first timed steps); at most 5 s.
+        t0 = time.time()
+        while not self.lines and self.proc.poll() is None and time.time() - t0 < 5.0:
+            time.sleep(0.01)
         return self
 
     def _read(self):
@@ -370,14 +376,15 @@ def run_gpu(args, rank, world, local_rank):
             dense_call()
 
     # decode, token-head modes: the same step as one kvq_write_decode_attn
-    # call (the write done by the decode's query-preparation kernel)
+    # call (the write done by the decode's query-preparation kernel; pools
+    # and output identical to the two calls), timed beside the step
     fused = kind == "decode" and wl.mode != gen.MODE_INT8
 
     def fused_call():
         K.kvq_write_decode_attn(cache, pag, st["k"], st["v"], st["cu"], st["q"], scale, out=st["out"],
                                 workspace=st["ws"], num_splits=st["splits"], stream=stream)
 
-    # The step's two library calls are captured once into a CUDA graph and
+    # The step's library calls are captured once into a CUDA graph and
     # replayed, so the timed region holds only device work (re-writing the
     # same new tokens at the same positions is idempotent).  One graph holds
     # the whole step (its kernels chain with programmatic dependent launch);
@@ -403,34 +410,44 @@ def run_gpu(args, rank, world, local_rank):
         if g_fused is not None:
             with torch.cuda.graph(g_fused, stream=stream):
                 fused_call()
-    for _ in range(args.warmup):
-        with torch.cuda.stream(stream):
-            flush_l2(1)
-        g_step.replay()
-        g_write.replay()
-        g_attn.replay()
-        if g_dense is not None:
-            g_dense.replay()
-        if g_fused is not None:
-            with torch.cuda.stream(stream):
-                flush_l2(1)
-            g_fused.replay()
-    torch.cuda.synchronize()
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
     evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
+        # the warm-up replays run right before the timed steps (a GPU left
+        # idle before them had made the first timed replays slower)
+        for _ in range(args.warmup):
+            with torch.cuda.stream(stream):
+                flush_l2(1)
+            g_step.replay()
+            g_write.replay()
+            g_attn.replay()
+            if g_dense is not None:
+                g_dense.replay()
+            if g_fused is not None:
+                with torch.cuda.stream(stream):
+                    flush_l2(1)
+                g_fused.replay()
         torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
         with torch.cuda.stream(stream):
-            for i in range(args.steps):  # the K timed steps
+            # the K timed steps, each followed, where it exists, by the same
+            # step as one fused call (both whole-step variants under the same
+            # conditions)
+            for i in range(args.steps):
                 flush_l2(i)
                 a, c = evs[i]
                 a.record(stream)
                 g_step.replay()
                 c.record(stream)
+                if g_fused is not None:
+                    flush_l2(i)
+                    a, c = evf[i]
+                    a.record(stream)
+                    g_fused.replay()
+                    c.record(stream)
             for i in range(args.steps):  # per-call breakdown, same steps replayed call by call
                 flush_l2(i)
                 e0, e1, e2, e3 = ev[i]
@@ -442,12 +459,6 @@ def run_gpu(args, rank, world, local_rank):
                 if g_dense is not None:
                     g_dense.replay()
                 e3.record(stream)
-            for i in range(args.steps if g_fused is not None else 0):  # the step as one fused call
-                flush_l2(i)
-                a, c = evf[i]
-                a.record(stream)
-                g_fused.replay()
-                c.record(stream)
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(c) for a, c in evs]
     att_ms = [b.elapsed_time(c) for a, b, c, d in ev]
